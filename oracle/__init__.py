@@ -1,0 +1,206 @@
+"""ctypes wrapper of the plain CPU oracle (oracle/sdv_oracle.c, oracle/exact.c).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  It shares no
+code with the CUDA library; both take their inputs from
+``draft_verification_row_gb300.workloads``.
+
+Every function takes numpy arrays (or CPU torch tensors) laid out exactly as
+the CUDA library's arguments and returns numpy arrays.
+"""
+import ctypes
+import numpy as np
+
+from . import build as _build
+
+MODE = {"token": 0, "greedy": 1, "block": 2, "multidraft": 3}
+F32, BF16 = 0, 1
+REQ_BAD_LENGTH, REQ_BAD_TOKEN, REQ_NONFINITE = 1, 2, 4
+MAX_K = 16
+MAX_L = 16
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("K", ctypes.c_int), ("L", ctypes.c_int), ("V", ctypes.c_int),
+        ("row_stride", ctypes.c_longlong), ("dtype", ctypes.c_int),
+        ("temperature", ctypes.c_double),
+        ("target", ctypes.c_void_p), ("draft", ctypes.c_void_p),
+        ("tokens", ctypes.c_void_p), ("lengths", ctypes.c_void_p),
+        ("accept_u", ctypes.c_void_p), ("sample_u", ctypes.c_void_p),
+    ]
+
+
+class _TraceEntry(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("index", ctypes.c_int),
+                ("lo", ctypes.c_double), ("hi", ctypes.c_double)]
+
+
+class _Trace(ctypes.Structure):
+    _fields_ = [("e", ctypes.POINTER(_TraceEntry)), ("cap", ctypes.c_int), ("n", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(_build.build())
+        _lib.sdvo_verify.restype = ctypes.c_int
+        _lib.sdvo_exact_outcomes.restype = ctypes.c_int
+        _lib.sdvo_exact_streams.restype = ctypes.c_int
+        _lib.sdvo_prefix_index.restype = ctypes.c_longlong
+    return _lib
+
+
+def _np(a):
+    """numpy view of a numpy array or CPU torch tensor (bf16 -> uint16 bits)."""
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        import torch
+        t = a.detach()
+        if t.device.type != "cpu":
+            raise ValueError("oracle inputs must be host tensors")
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        a = t.contiguous().numpy()
+    return np.ascontiguousarray(a)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Problem:
+    """One batch in the CUDA library's layout, held as numpy arrays."""
+
+    def __init__(self, target, draft, tokens, lengths, accept_u, sample_u, temperature,
+                 V=None):
+        self.target = _np(target)
+        self.draft = _np(draft)
+        self.tokens = np.ascontiguousarray(_np(tokens), dtype=np.int32)
+        self.lengths = None if lengths is None else np.ascontiguousarray(_np(lengths), dtype=np.int32)
+        # uniforms are passed to the oracle as doubles (exact widening of fp32)
+        self.accept_u = None if accept_u is None else np.ascontiguousarray(_np(accept_u), dtype=np.float64)
+        self.sample_u = None if sample_u is None else np.ascontiguousarray(_np(sample_u), dtype=np.float64)
+        self.temperature = float(temperature)
+        t = self.target
+        self.B, self.K = t.shape[0], t.shape[1]
+        self.L = t.shape[2] - 1
+        self.row_stride = t.shape[3]
+        self.V = self.row_stride if V is None else int(V)
+        if t.dtype in (np.uint16, np.int16):
+            self.dtype = BF16
+        elif t.dtype == np.float32:
+            self.dtype = F32
+        else:
+            raise TypeError(f"unsupported logit dtype {t.dtype}")
+
+    def struct(self):
+        s = _Problem()
+        s.B, s.K, s.L, s.V = self.B, self.K, self.L, self.V
+        s.row_stride = self.row_stride
+        s.dtype = self.dtype
+        s.temperature = self.temperature
+        s.target, s.draft = _ptr(self.target), _ptr(self.draft)
+        s.tokens, s.lengths = _ptr(self.tokens), _ptr(self.lengths)
+        s.accept_u, s.sample_u = _ptr(self.accept_u), _ptr(self.sample_u)
+        return s
+
+    def request(self, b):
+        """The same problem restricted to request b (a contiguous slab)."""
+        sub = object.__new__(Problem)
+        sub.__dict__.update(self.__dict__)
+        sl = slice(b, b + 1)
+        sub.target = self.target[sl]
+        sub.draft = None if self.draft is None else self.draft[sl]
+        sub.tokens = self.tokens[sl]
+        sub.lengths = None if self.lengths is None else self.lengths[sl]
+        sub.accept_u = None if self.accept_u is None else self.accept_u[sl]
+        sub.sample_u = None if self.sample_u is None else self.sample_u[sl]
+        sub.B = 1
+        return sub
+
+
+def verify(mode, prob: Problem, residual_out=False, trace_cap=0):
+    """Run the oracle; returns a dict of numpy arrays (and 'trace' if asked)."""
+    B, K, L, V = prob.B, prob.K, prob.L, prob.V
+    out = {
+        "accept_len": np.zeros(B, np.int32),
+        "accept_draft": np.zeros(B, np.int32),
+        "out_token": np.zeros(B, np.int32),
+        "accept_prob": np.zeros((B, K, L), np.float32),
+        "residual_mass": np.zeros(B, np.float64),
+        "margin": np.zeros(B, np.float64),
+        "req_status": np.zeros(B, np.int32),
+    }
+    ro = np.zeros((B, V), np.float64) if residual_out else None
+    tr = None
+    entries = None
+    if trace_cap:
+        entries = (_TraceEntry * trace_cap)()
+        tr = _Trace(ctypes.cast(entries, ctypes.POINTER(_TraceEntry)), trace_cap, 0)
+    s = prob.struct()
+    rc = lib().sdvo_verify(
+        ctypes.c_int(MODE[mode]), ctypes.byref(s),
+        _ptr(out["accept_len"]), _ptr(out["accept_draft"]), _ptr(out["out_token"]),
+        _ptr(out["accept_prob"]), _ptr(out["residual_mass"]), _ptr(out["margin"]),
+        _ptr(ro), _ptr(out["req_status"]), ctypes.byref(tr) if tr is not None else None)
+    out["rc"] = rc
+    if ro is not None:
+        out["residual_out"] = ro
+    if tr is not None:
+        out["trace"] = [(entries[i].kind, entries[i].index, entries[i].lo, entries[i].hi)
+                        for i in range(min(tr.n, trace_cap))]
+    return out
+
+
+def exact_outcomes(mode, prob: Problem):
+    """Exact P(tau, k*, token) of a one-request problem: array [L+1][K][V]."""
+    assert prob.B == 1
+    out = np.zeros((prob.L + 1, prob.K, prob.V), np.float64)
+    s = prob.struct()
+    rc = lib().sdvo_exact_outcomes(ctypes.c_int(MODE[mode]), ctypes.byref(s), _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"sdvo_exact_outcomes failed: {rc}")
+    return out
+
+
+def prefix_index(tokens, V):
+    """Index of a prefix in the toy-model tables (all shorter prefixes first)."""
+    off, pw = 0, 1
+    for _ in range(len(tokens)):
+        off += pw
+        pw *= V
+    num = 0
+    for t in tokens:
+        num = num * V + int(t)
+    return off + num
+
+
+def n_prefixes(n, V):
+    """Number of prefixes of length 0..n."""
+    return sum(V ** i for i in range(n + 1))
+
+
+def exact_streams(mode, V, K, L, temperature, tgt_tab, dft_tab, q_tab):
+    """Exact distribution of the emitted stream over all draft tuples.
+
+    Tables hold one row per prefix of length 0..L (prefix_index order):
+    f32 logits for target and draft, and the draft's sampling probabilities.
+    Returns (stream_prob indexed by prefix_index over lengths 0..L+1,
+    tau_prob[L+1]).
+    """
+    tgt = np.ascontiguousarray(tgt_tab, np.float32)
+    dft = np.ascontiguousarray(dft_tab, np.float32)
+    q = np.ascontiguousarray(q_tab, np.float64)
+    sp = np.zeros(n_prefixes(L + 1, V), np.float64)
+    tp = np.zeros(L + 1, np.float64)
+    rc = lib().sdvo_exact_streams(ctypes.c_int(MODE[mode]), ctypes.c_int(V), ctypes.c_int(K),
+                                  ctypes.c_int(L), ctypes.c_double(temperature),
+                                  _ptr(tgt), _ptr(dft), _ptr(q), _ptr(sp), _ptr(tp))
+    if rc != 0:
+        raise RuntimeError(f"sdvo_exact_streams failed: {rc}")
+    return sp, tp
