@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Throughput of batched speculative-decoding verification on one GB300.
+
+Metric: verified draft positions per second (positions = sum over requests
+of K * L_b) on the mixed batch B=256, K=8 drafts, ragged L_b in 1..8,
+V=151936 bf16, T=0.7 (SpecTr-GBV multi-draft block verification; the
+token-level rule on the same batch is reported beside it).  A step is one
+verification call over the whole batch, inputs resident in HBM; the inputs
+(about 10.6 GB) are far larger than L2, so no flush is needed between
+steps.
+
+The JSON line also carries the roofline of the dominant kernel (the node
+kernel: vocabulary-row work), timed live with CUDA events recorded by the
+library around those launches, the end-to-end figure through the C-ABI with
+host buffers, the oracle timed on host cores, the launch count and the SM
+clocks sampled during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 it runs under torch.distributed (one process per GPU): every
+rank verifies its own batch (weak scaling) with no collective on the data
+path; the time is the maximum over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "verified draft positions/sec at V=151936, B=256; achieved HBM GB/s vs GB300 peak"
+UNIT = "positions/s"
+KERNEL_SRC = os.path.join(ROOT, "draft_verification_row_gb300", "csrc", "sdv_kernels.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "node_kernel_traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", choices=["multidraft", "token"], default="multidraft")
+    ap.add_argument("--workload", default=None, help="workload name (default: the mixed B=256 batch)")
+    ap.add_argument("--B", type=int, default=None, help="override the batch size (profiling runs)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-extras", action="store_true", help="skip e2e, token mode and CPU baseline")
+    ap.add_argument("--cpu-requests", type=int, default=8, help="requests in the oracle's timed sample")
+    return ap.parse_args()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def trie_rows(tokens, lengths, K):
+    """(target rows, draft rows) the method reads: one per distinct draft
+    prefix (node) of each request; leaves (depth L_b) read no draft row."""
+    tok = tokens.cpu().numpy()
+    lens = lengths.cpu().numpy()
+    nt = nd = 0
+    for b in range(tok.shape[0]):
+        Lb = int(lens[b])
+        for j in range(Lb + 1):
+            n = len({tuple(tok[b, k, :j]) for k in range(K)})
+            nt += n
+            if j < Lb:
+                nd += n
+    return nt, nd
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per call of the node kernels from a committed ncu capture,
+    valid only while the kernel source is unchanged."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        with open(KERNEL_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if d.get("kernel_source_sha256") != sha:
+            return None
+        return float(d["dram_bytes_per_call"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons (200 ms)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_calls(fn, steps, stream, prof=None):
+    """Total ms of `steps` calls between CUDA events on `stream`, and the
+    summed ms between the library's profiling events (row kernels only)."""
+    import draft_verification_row_gb300 as sdv
+    pairs = []
+    if prof:
+        for _ in range(steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            b.record(stream)
+            pairs.append((a, b))
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        if prof:
+            sdv.set_profile_events(*pairs[i])
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    sdv.set_profile_events(None, None)
+    total = start.elapsed_time(end)
+    rows = sum(a.elapsed_time(b) for a, b in pairs) if prof else None
+    return total, rows
+
+
+def oracle_sample(batch, mode, requests):
+    """Time the oracle, as it stands, on the given requests (host copies)."""
+    import oracle
+    sel = torch.as_tensor(requests, dtype=torch.long, device=batch.target.device)
+
+    def take(t):
+        return t.index_select(0, sel).cpu()
+
+    prob = oracle.Problem(take(batch.target), take(batch.draft), take(batch.tokens), take(batch.lengths),
+                          take(batch.accept_u), take(batch.sample_u), batch.temperature, V=batch.V)
+    positions = int(take(batch.lengths).sum().item()) * batch.K
+    t0 = time.perf_counter()
+    out = oracle.verify(mode, prob)
+    dt = time.perf_counter() - t0
+    assert out["rc"] == 0
+    return positions, dt
+
+
+def config_of(batch, mode, world):
+    return {"workload": batch.name, "mode": mode, "B": batch.B, "K": batch.K, "L": batch.L,
+            "L_b": "uniform 1..L" if batch.meta.get("ragged") else "L", "V": batch.V,
+            "logits": batch.dtype, "temperature": batch.temperature, "seed": batch.meta.get("seed"),
+            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
+
+
+def run_reference(args, world, rank):
+    """The oracle on the host cores: each step times a bounded sample."""
+    from draft_verification_row_gb300 import workloads as W
+    if rank != 0:
+        return
+    name = args.workload or W.HEADLINE
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    batch = W.make(name, dev, B=args.B)
+    n = max(1, min(args.cpu_requests // 4 or 1, batch.B))
+    rng = np.random.default_rng(0)
+    times, positions = [], []
+    for i in range(args.warmup + args.steps):
+        req = sorted(rng.choice(batch.B, size=n, replace=False).tolist())
+        p, dt = oracle_sample(batch, args.mode, req)
+        if i >= args.warmup:
+            times.append(dt)
+            positions.append(p)
+    value = sum(positions) / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(batch, args.mode, world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{n} random requests of the batch per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import draft_verification_row_gb300 as sdv
+    from draft_verification_row_gb300 import binding, workloads as W
+
+    dev = torch.device(f"cuda:{local}")
+    name = args.workload or W.HEADLINE
+    seed = W.WORKLOADS[name]["seed"] + 7919 * rank
+    batch = W.make(name, dev, seed=seed, B=args.B)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    esz = 2 if batch.dtype == "bf16" else 4
+    nt, nd = trie_rows(batch.tokens, batch.lengths, batch.K)
+    alg_bytes = (nt + nd) * batch.V * esz
+    positions = batch.positions
+
+    def make_call(mode, out):
+        def call():
+            sdv.verify(mode, batch.target, batch.draft, batch.tokens, batch.lengths, batch.accept_u,
+                       batch.sample_u, batch.temperature, V=batch.V, out=out, stream=stream)
+        return call
+
+    out = binding.Outputs(args.mode, batch.B, batch.K, batch.L, batch.V, dev)
+    call = make_call(args.mode, out)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device())
+    barrier(world)
+    clocks.start()
+    total_ms, row_ms = time_calls(call, args.steps, stream, prof=True)
+    clk = clocks.stop()
+    st = int(out.device_status.item())
+    if st:
+        raise RuntimeError(f"device status {st}")
+    total_ms = max_over_ranks(total_ms, world)
+    row_ms = max_over_ranks(row_ms, world)
+    all_positions = sum_over_ranks(positions, world)
+    ms_step = total_ms / args.steps
+    value = all_positions / (ms_step / 1000.0)
+    row_launches = 1 if args.mode == "token" else batch.L + 1
+    launches = (2 + row_launches) * args.steps
+
+    peak, peak_kind = measured_peaks()
+    row_step_s = row_ms / args.steps / 1000.0
+    achieved = alg_bytes / row_step_s / 1e9
+    traffic = recorded_traffic()
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_of(batch, args.mode, world),
+            "positions_per_step": all_positions,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                         "traffic": traffic, "kernel": "node_kernel",
+                         "algorithmic_bytes_per_step": alg_bytes,
+                         "kernel_ms_per_step": row_ms / args.steps,
+                         "rows_read_per_step": {"target": nt, "draft": nd}},
+            "gpu_launches": launches,
+            "clocks": clk}
+
+    if not args.no_extras:
+        # the token-level rule on the same batch
+        other = "token" if args.mode == "multidraft" else "multidraft"
+        out2 = binding.Outputs(other, batch.B, batch.K, batch.L, batch.V, dev)
+        call2 = make_call(other, out2)
+        for _ in range(max(2, args.warmup // 2)):
+            call2()
+        t2, r2 = time_calls(call2, args.steps, stream, prof=True)
+        t2 = max_over_ranks(t2, world)
+        r2 = max_over_ranks(r2, world)
+        line["modes"] = {other: {"value": all_positions / (t2 / args.steps / 1000.0), "unit": UNIT,
+                                 "ms_per_step": t2 / args.steps,
+                                 "hbm_gbs": alg_bytes / (r2 / args.steps / 1000.0) / 1e9}}
+        # end to end through the C-ABI with host buffers: H2D of every input,
+        # the call, D2H of the per-request results
+        names = ["target", "draft", "tokens", "lengths", "accept_u", "sample_u"]
+        host = {n: getattr(batch, n).cpu().pin_memory() for n in names}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        res_host = [torch.empty(batch.B, dtype=torch.int32).pin_memory() for _ in range(3)]
+        d2h = 3 * 4 * batch.B
+        dev_in = {n: getattr(batch, n) for n in names}
+
+        def e2e_step():
+            for n in names:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            call()
+            res_host[0].copy_(out.accept_len, non_blocking=True)
+            res_host[1].copy_(out.accept_draft, non_blocking=True)
+            res_host[2].copy_(out.out_token, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        te, _ = time_calls(e2e_step, args.e2e_steps, stream)
+        te = max_over_ranks(te, world)
+        line["e2e"] = {"value": all_positions / (te / args.e2e_steps / 1000.0), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": te / args.e2e_steps}
+        del host
+        if rank == 0:
+            rng = np.random.default_rng(1)
+            req = sorted(rng.choice(batch.B, size=min(args.cpu_requests, batch.B), replace=False).tolist())
+            p, dt = oracle_sample(batch, args.mode, req)
+            line["cpu_baseline"] = {"value": p / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                    "sample": f"{len(req)} random requests of the batch ({p} positions, "
+                                              f"{dt:.1f} s, single thread)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,22 @@
+"""Batched speculative-decoding verification on GB300 (sm_103a).
+
+A thin ctypes binding of the C-ABI in include/sdv.h (libsdv.so, built
+in-tree by ``draft_verification_row_gb300.build``).  Every step of the
+verification runs in the library's CUDA kernels; this module only checks
+tensor shapes, takes pointers and the current stream, and allocates the
+workspace and outputs with torch.  There is no CPU fallback: without the
+compiled library every call raises.
+"""
+from .binding import (  # noqa: F401
+    MODES,
+    SDVError,
+    launch_shape,
+    lib,
+    set_profile_events,
+    verify,
+    verify_block,
+    verify_greedy,
+    verify_multidraft,
+    verify_token,
+    workspace_bytes,
+)

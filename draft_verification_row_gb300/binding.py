@@ -1,0 +1,173 @@
+"""ctypes binding of libsdv.so (include/sdv.h).  Argument marshalling only."""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsdv.so")
+
+MODES = {"token": 0, "greedy": 1, "block": 2, "multidraft": 3}
+_ENTRY = {"token": "sdv_verify_token", "greedy": "sdv_verify_greedy",
+          "block": "sdv_verify_block", "multidraft": "sdv_verify_multidraft"}
+SDV_F32, SDV_BF16 = 0, 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "timeout",
+          5: "workspace"}
+REQ_BAD_LENGTH, REQ_BAD_TOKEN, REQ_NONFINITE, DEV_TIMEOUT = 1, 2, 4, 8
+
+_VERIFY_ARGTYPES = [
+    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, ctypes.c_int,
+    ctypes.c_float,
+    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+    ctypes.c_void_p,
+    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+]
+
+EXPORTS = list(_ENTRY.values()) + ["sdv_workspace_bytes", "sdv_status_string", "sdv_launch_shape",
+                                   "sdv_set_profile_events"]
+
+
+class SDVError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+_lib = None
+
+
+def lib(path: str = LIB_PATH):
+    """Load libsdv.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    h = ctypes.CDLL(path)
+    for name in _ENTRY.values():
+        fn = getattr(h, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = _VERIFY_ARGTYPES
+    h.sdv_workspace_bytes.restype = ctypes.c_size_t
+    h.sdv_workspace_bytes.argtypes = [ctypes.c_int] * 5
+    h.sdv_status_string.restype = ctypes.c_char_p
+    h.sdv_status_string.argtypes = [ctypes.c_int]
+    h.sdv_launch_shape.restype = ctypes.c_int
+    h.sdv_launch_shape.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.POINTER(ctypes.c_int)] * 3
+    h.sdv_set_profile_events.restype = ctypes.c_int
+    h.sdv_set_profile_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    _lib = h
+    return h
+
+
+def workspace_bytes(mode, B, K, L, V):
+    return int(lib().sdv_workspace_bytes(MODES[mode], B, K, L, V))
+
+
+def launch_shape(V, dtype="bf16"):
+    c, t, s = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = lib().sdv_launch_shape(V, SDV_BF16 if dtype == "bf16" else SDV_F32,
+                                ctypes.byref(c), ctypes.byref(t), ctypes.byref(s))
+    if rc:
+        raise SDVError(rc, "sdv_launch_shape")
+    return {"cluster": c.value, "threads": t.value, "smem_bytes": s.value}
+
+
+def set_profile_events(start=None, stop=None):
+    """Record two torch.cuda.Events around the vocabulary-row kernels of each
+    later call from this thread (None, None turns it off).  The events must
+    have been recorded once so that they exist."""
+    hs = None if start is None else ctypes.c_void_p(start.cuda_event)
+    he = None if stop is None else ctypes.c_void_p(stop.cuda_event)
+    rc = lib().sdv_set_profile_events(hs, he)
+    if rc:
+        raise SDVError(rc, "sdv_set_profile_events")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return SDV_BF16
+    if t.dtype == torch.float32:
+        return SDV_F32
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+class Outputs:
+    """Preallocated outputs (and workspace) for repeated calls of one shape."""
+
+    def __init__(self, mode, B, K, L, V, device, accept_prob=True, residual_mass=True):
+        self.accept_len = torch.empty(B, dtype=torch.int32, device=device)
+        self.accept_draft = torch.empty(B, dtype=torch.int32, device=device)
+        self.out_token = torch.empty(B, dtype=torch.int32, device=device)
+        self.accept_prob = torch.empty((B, K, L), dtype=torch.float32, device=device) if accept_prob else None
+        self.residual_mass = torch.empty(B, dtype=torch.float32, device=device) if residual_mass else None
+        self.device_status = torch.empty(1, dtype=torch.int32, device=device)
+        nbytes = max(workspace_bytes(mode, B, K, L, V), 256)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k in ("accept_len", "accept_draft", "out_token", "accept_prob",
+                                              "residual_mass", "device_status")}
+
+
+def verify(mode, target, draft, tokens, lengths, accept_u, sample_u, temperature, *, V=None,
+           out: Outputs = None, stream=None, accept_prob=True, residual_mass=True):
+    """Run one verification call on the current CUDA stream.
+
+    target [B][K][L+1][stride], draft [B][K][L][stride] (float32 or bfloat16),
+    tokens [B][K][L] int32, lengths [B] int32 or None, accept_u [B][K][L],
+    sample_u [B][K][L+1] float32.  Returns a dict of output tensors; the call
+    is asynchronous (read them after a synchronize).
+    """
+    if mode not in _ENTRY:
+        raise ValueError(f"unknown mode {mode!r}")
+    h = lib()
+    if target.dim() != 4:
+        raise ValueError("target must be [B][K][L+1][stride]")
+    B, K, Lp1, stride = target.shape
+    L = Lp1 - 1
+    V = stride if V is None else int(V)
+    for name, t in (("target", target), ("draft", draft)):
+        if t is not None and (not t.is_contiguous() or not t.is_cuda):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if draft is not None and draft.dtype != target.dtype:
+        raise TypeError("target and draft logits must have the same dtype")
+    for name, t, dt in (("tokens", tokens, torch.int32), ("lengths", lengths, torch.int32),
+                        ("accept_u", accept_u, torch.float32), ("sample_u", sample_u, torch.float32)):
+        if t is not None and (t.dtype != dt or not t.is_contiguous() or not t.is_cuda):
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    if out is None:
+        out = Outputs(mode, B, K, L, V, target.device, accept_prob, residual_mass)
+    if stream is None:
+        stream = torch.cuda.current_stream(target.device)
+    rc = getattr(h, _ENTRY[mode])(
+        B, K, L, V, stride, _dtype_code(target), float(temperature),
+        _ptr(target), _ptr(draft), _ptr(tokens), _ptr(lengths), _ptr(accept_u), _ptr(sample_u),
+        _ptr(out.accept_len), _ptr(out.accept_draft), _ptr(out.out_token), _ptr(out.accept_prob),
+        _ptr(out.residual_mass), _ptr(out.device_status), _ptr(out.workspace),
+        out.workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SDVError(rc, _ENTRY[mode])
+    return out.as_dict()
+
+
+def verify_token(*args, **kw):
+    return verify("token", *args, **kw)
+
+
+def verify_greedy(*args, **kw):
+    return verify("greedy", *args, **kw)
+
+
+def verify_block(*args, **kw):
+    return verify("block", *args, **kw)
+
+
+def verify_multidraft(*args, **kw):
+    return verify("multidraft", *args, **kw)

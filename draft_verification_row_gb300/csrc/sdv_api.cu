@@ -1,0 +1,259 @@
+// sdv_api.cu -- the C-ABI of include/sdv.h: argument checks, workspace
+// layout and the launch sequence of each verification rule.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "sdv_internal.h"
+
+namespace sdv {
+
+size_t node_smem_bytes(int units_per_cta);
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kSmemTarget = 110 * 1024;    // two CTAs per SM
+constexpr int kSmemMax = 227 * 1024;
+
+size_t align_up(size_t n) { return (n + kAlign - 1) / kAlign * kAlign; }
+
+bool sizes_ok(int B, int K, int L, int V)
+{
+    return B >= 0 && K >= 1 && K <= SDV_MAX_K && L >= 0 && L <= SDV_MAX_L && V >= 1 && V <= SDV_MAX_V;
+}
+
+size_t workspace_size(int B, int K, int L)
+{
+    const size_t n = slot_count(B, K, L);
+    return 6 * align_up(n * 4) + align_up(n) + align_up((size_t)B * 4);
+}
+
+Workspace carve(void* base, int B, int K, int L)
+{
+    const size_t n = slot_count(B, K, L);
+    char* p = static_cast<char*>(base);
+    Workspace w;
+    w.a = reinterpret_cast<float*>(p);
+    p += align_up(n * 4);
+    w.h = reinterpret_cast<float*>(p);
+    p += align_up(n * 4);
+    w.S = reinterpret_cast<float*>(p);
+    p += align_up(n * 4);
+    w.p = reinterpret_cast<float*>(p);
+    p += align_up(n * 4);
+    w.tok = reinterpret_cast<int*>(p);
+    p += align_up(n * 4);
+    w.am = reinterpret_cast<int*>(p);
+    p += align_up(n * 4);
+    w.owner = reinterpret_cast<unsigned char*>(p);
+    p += align_up(n);
+    w.req = reinterpret_cast<int*>(p);
+    return w;
+}
+
+// Device memory of the current device, managed memory, or host memory
+// mapped into the device's address space.
+bool device_accessible(const void* ptr)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type == cudaMemoryTypeDevice) return a.device == dev;
+    if (a.type == cudaMemoryTypeManaged) return true;
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer == ptr;
+    return false;
+}
+
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+// profiling hook (sdv_set_profile_events): per host thread
+thread_local cudaEvent_t g_prof_start = nullptr;
+thread_local cudaEvent_t g_prof_stop = nullptr;
+
+bool prof_record(cudaEvent_t e, cudaStream_t st) { return !e || cudaEventRecord(e, st) == cudaSuccess; }
+
+int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype, float temperature,
+           const void* target_logits, const void* draft_logits, const int* draft_tokens, const int* lengths,
+           const float* accept_u, const float* sample_u, int* accept_len, int* accept_draft, int* out_token,
+           float* accept_prob, float* residual_mass, int* device_status, void* workspace,
+           size_t workspace_bytes, void* cuda_stream)
+{
+    if (!sizes_ok(B, K, L, V)) return SDV_ERR_INVALID;
+    if (row_stride < V || row_stride % 8 != 0) return SDV_ERR_INVALID;
+    if (dtype != SDV_F32 && dtype != SDV_BF16) return SDV_ERR_INVALID;
+    if (!(temperature >= 0.f) || std::isinf(temperature)) return SDV_ERR_INVALID;
+    if (mode == SDV_MODE_BLOCK && K != 1) return SDV_ERR_INVALID;
+    const bool greedy = mode == SDV_MODE_GREEDY || temperature == 0.f;
+    const float c = greedy ? 0.f : (float)(1.4426950408889634 / (double)temperature);
+    if (!greedy && !std::isfinite(c)) return SDV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+
+    if (device_status && !device_accessible(device_status)) return SDV_ERR_INVALID;
+    if (B == 0) {
+        if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+        return SDV_OK;
+    }
+
+    // required pointers
+    const bool need_draft = !greedy && L > 0;
+    if (!target_logits || (L > 0 && !draft_tokens) || !accept_len || !accept_draft || !out_token)
+        return SDV_ERR_INVALID;
+    if (need_draft && (!draft_logits || !accept_u)) return SDV_ERR_INVALID;
+    if (!greedy && !sample_u) return SDV_ERR_INVALID;
+    if (!aligned(target_logits, 16) || (need_draft && !aligned(draft_logits, 16))) return SDV_ERR_INVALID;
+    const void* ptrs[] = {target_logits,  need_draft ? draft_logits : nullptr,
+                          L > 0 ? draft_tokens : nullptr, lengths,
+                          need_draft ? accept_u : nullptr, greedy ? nullptr : sample_u,
+                          accept_len, accept_draft, out_token, accept_prob, residual_mass};
+    for (const void* q : ptrs)
+        if (q && !device_accessible(q)) return SDV_ERR_INVALID;
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < workspace_size(B, K, L))
+        return SDV_ERR_WORKSPACE;
+    if (!device_accessible(workspace)) return SDV_ERR_WORKSPACE;
+
+    Problem pb;
+    std::memset(&pb, 0, sizeof pb);
+    pb.B = B;
+    pb.K = K;
+    pb.L = L;
+    pb.V = V;
+    pb.stride = row_stride;
+    pb.dtype = dtype;
+    pb.mode = greedy ? SDV_MODE_GREEDY : mode;
+    pb.c = c;
+    pb.target = target_logits;
+    pb.draft = draft_logits;
+    pb.tokens = draft_tokens;
+    pb.lengths = lengths;
+    pb.accept_u = accept_u;
+    pb.sample_u = sample_u;
+    pb.accept_len = accept_len;
+    pb.accept_draft = accept_draft;
+    pb.out_token = out_token;
+    pb.accept_prob = accept_prob;
+    pb.residual_mass = residual_mass;
+    pb.device_status = device_status;
+    pb.ws = carve(workspace, B, K, L);
+
+    Shape sh;
+    if (!greedy) {
+        const int rc = choose_shape(V, dtype, &sh);
+        if (rc != SDV_OK) return rc;
+        if (prepare_node_kernel(sh, dtype) != cudaSuccess) {
+            cudaGetLastError();
+            return SDV_ERR_UNSUPPORTED;
+        }
+    }
+    if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_prep(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (!prof_record(g_prof_start, st)) return SDV_ERR_CUDA;
+    if (greedy) {
+        if (launch_argmax(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
+    } else if (mode == SDV_MODE_TOKEN) {
+        // node weights are all 1: every node of every depth at once
+        if (launch_nodes(pb, sh, 0, L, st) != cudaSuccess) return SDV_ERR_CUDA;
+    } else {
+        // a node's weight comes from its parent: one depth at a time
+        for (int j = 0; j <= L; ++j)
+            if (launch_nodes(pb, sh, j, j, st) != cudaSuccess) return SDV_ERR_CUDA;
+    }
+    if (!prof_record(g_prof_stop, st)) return SDV_ERR_CUDA;
+    if (launch_decide(pb, greedy, st) != cudaSuccess) return SDV_ERR_CUDA;
+    return SDV_OK;
+}
+
+}  // namespace
+
+int choose_shape(int V, int dtype, Shape* s)
+{
+    if (V < 1 || V > SDV_MAX_V || (dtype != SDV_F32 && dtype != SDV_BF16)) return SDV_ERR_INVALID;
+    const int epu = dtype == SDV_BF16 ? 8 : 4;
+    const int n_units = (V + epu - 1) / epu;
+    int C = 1;
+    const char* env = std::getenv("SDV_CLUSTER");
+    if (env && *env) {
+        C = std::atoi(env);
+        if (C != 1 && C != 2 && C != 4 && C != 8 && C != 16) return SDV_ERR_INVALID;
+    } else {
+        while (C < 16 && (size_t)(n_units + C - 1) / C * 32 > (size_t)kSmemTarget) C *= 2;
+    }
+    for (;; C *= 2) {
+        if (C > 16) return SDV_ERR_UNSUPPORTED;
+        const int upc = (n_units + C - 1) / C;
+        const int threads = upc >= 1024 ? 512 : (upc >= 256 ? 256 : 128);
+        int eu = (upc + threads - 1) / threads;
+        if (eu % 2 == 0) ++eu;  // odd: 16-byte loads of a warp hit distinct banks
+        const size_t smem = node_smem_bytes(upc);
+        if (smem > (size_t)kSmemMax) continue;
+        s->cluster = C;
+        s->threads = threads;
+        s->units_per_cta = upc;
+        s->units_per_thr = eu;
+        s->smem = (int)smem;
+        return SDV_OK;
+    }
+}
+
+}  // namespace sdv
+
+extern "C" {
+
+#define SDV_FORWARD(mode)                                                                                    \
+    sdv::verify(mode, B, K, L, V, row_stride, dtype, temperature, target_logits, draft_logits, draft_tokens, \
+                lengths, accept_u, sample_u, accept_len, accept_draft, out_token, accept_prob, residual_mass, \
+                device_status, workspace, workspace_bytes, cuda_stream)
+
+int sdv_verify_token(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_TOKEN); }
+int sdv_verify_greedy(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_GREEDY); }
+int sdv_verify_block(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_BLOCK); }
+int sdv_verify_multidraft(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_MULTIDRAFT); }
+
+size_t sdv_workspace_bytes(int mode, int B, int K, int L, int V)
+{
+    if (mode < SDV_MODE_TOKEN || mode > SDV_MODE_MULTIDRAFT || !sdv::sizes_ok(B, K, L, V)) return 0;
+    if (mode == SDV_MODE_BLOCK && K != 1) return 0;
+    return sdv::workspace_size(B, K, L);
+}
+
+const char* sdv_status_string(int status)
+{
+    switch (status) {
+    case SDV_OK: return "ok";
+    case SDV_ERR_INVALID: return "invalid argument";
+    case SDV_ERR_UNSUPPORTED: return "unsupported on this build or device";
+    case SDV_ERR_CUDA: return "CUDA runtime or launch error";
+    case SDV_ERR_TIMEOUT: return "device wait timed out";
+    case SDV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+    }
+}
+
+int sdv_set_profile_events(void* start, void* stop)
+{
+    if ((start == nullptr) != (stop == nullptr)) return SDV_ERR_INVALID;
+    sdv::g_prof_start = static_cast<cudaEvent_t>(start);
+    sdv::g_prof_stop = static_cast<cudaEvent_t>(stop);
+    return SDV_OK;
+}
+
+int sdv_launch_shape(int V, int dtype, int* cluster, int* threads, int* smem_bytes)
+{
+    sdv::Shape s;
+    const int rc = sdv::choose_shape(V, dtype, &s);
+    if (rc != SDV_OK) return rc;
+    if (cluster) *cluster = s.cluster;
+    if (threads) *threads = s.threads;
+    if (smem_bytes) *smem_bytes = s.smem;
+    return SDV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// sdv_internal.h -- declarations shared by the host API (sdv_api.cu) and
+// the kernels (sdv_kernels.cu).  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "sdv.h"
+
+namespace sdv {
+
+// Per-call scratch, carved out of the caller's workspace.  Node and draw
+// records are indexed by slot s = (b * (L + 1) + j) * K + k: the node of
+// depth j owned by draft k (valid when k is the lowest draft with that
+// prefix), and the draw of draft k at depth j.
+struct Workspace {
+    float* a;              // draw acceptance probability a (token / multidraft)
+    float* h;              // node block acceptance probability h_v
+    float* S;              // node residual mass S_n
+    float* p;              // node weight p_v
+    int* tok;              // node candidate correction token
+    int* am;               // node argmax (greedy)
+    unsigned char* owner;  // lowest draft sharing draft k's first j tokens
+    int* req;              // [B] request status bits
+};
+
+struct Problem {
+    int B, K, L, V;
+    long long stride;
+    int dtype;
+    int mode;       // SDV_MODE_*; greedy when temperature == 0
+    float c;        // log2(e) / T
+    const void* target;
+    const void* draft;
+    const int* tokens;
+    const int* lengths;
+    const float* accept_u;
+    const float* sample_u;
+    int* accept_len;
+    int* accept_draft;
+    int* out_token;
+    float* accept_prob;
+    float* residual_mass;
+    int* device_status;
+    Workspace ws;
+};
+
+// Launch shape of the node kernel for rows of V elements.
+struct Shape {
+    int cluster;       // CTAs sharing one node's rows (vocabulary split)
+    int threads;       // threads per CTA
+    int units_per_cta; // 16-byte units of one row held by each CTA
+    int units_per_thr; // contiguous units per thread (odd: conflict-free)
+    int smem;          // dynamic shared memory bytes per CTA
+};
+
+constexpr int kSlotRecordBytes = 6 * 4 + 1;
+
+inline size_t slot_count(int B, int K, int L) { return (size_t)B * (size_t)(L + 1) * (size_t)K; }
+
+int choose_shape(int V, int dtype, Shape* s);
+
+// Kernel launchers (sdv_kernels.cu); each returns a cudaError_t.
+cudaError_t launch_prep(const Problem& pb, cudaStream_t st);
+cudaError_t launch_nodes(const Problem& pb, const Shape& sh, int j_lo, int j_hi, cudaStream_t st);
+cudaError_t launch_argmax(const Problem& pb, cudaStream_t st);
+cudaError_t launch_decide(const Problem& pb, bool greedy, cudaStream_t st);
+cudaError_t prepare_node_kernel(const Shape& sh, int dtype);
+
+}  // namespace sdv

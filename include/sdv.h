@@ -1,0 +1,196 @@
+/*
+ * sdv.h -- batched speculative-decoding verification on GB300 (sm_103a).
+ *
+ * Given, for a batch of B requests, the target and draft logits of every
+ * draft position, the drafted tokens and per-position uniforms, each call
+ * returns per request the accepted prefix length tau, the index k* of the
+ * draft whose prefix was accepted, and the correction (or bonus) token.
+ *
+ * The four entry points are the verification rules named on the source
+ * pages:
+ *   sdv_verify_token       standard token-level speculative sampling;
+ *                          with K > 1 drafts, per-position multi-draft
+ *                          verification (recursive rejection sampling over
+ *                          the draft trie).  "SpecTr-GBV: Multi-Draft Block
+ *                          Verification Accelerating Speculative Decoding",
+ *                          section 1 (problem definition, the single-draft
+ *                          and SpecTr-style multi-draft bullets);
+ *                          "MineDraft: A Framework for Batch Parallel
+ *                          Speculative Decoding", section 1.
+ *   sdv_verify_greedy      temperature-0 argmax matching (the T = 0 limit
+ *                          of every sampling rule).
+ *   sdv_verify_block       greedy block verification (GBV) of one draft.
+ *                          SpecTr-GBV page, section 1 (block verification
+ *                          bullet).
+ *   sdv_verify_multidraft  SpecTr-GBV: K i.i.d. drafts verified as blocks,
+ *                          acceptance probabilities h_ik, rejected set H,
+ *                          residual correction and target adjustment.
+ *                          SpecTr-GBV page, section 2 (algorithmic
+ *                          procedure, steps 1-5).
+ *
+ * The pages print none of the formulas; the rules computed are:
+ *   P_v = softmax(target_row / T), Q_v = softmax(draft_row / T) at a trie
+ *   node v (drafts sharing a prefix share the node and the rows of the
+ *   lowest-index draft through it).  At a node of weight p (p = 1 for
+ *   sdv_verify_token, and at the root) with draws y_1..y_n (the next tokens
+ *   of the drafts through v, in index order):
+ *     R_0 = p P_v, D_0 = 1,
+ *     a_j = min(R_{j-1}(y_j) / (D_{j-1} Q_v(y_j)), 1)     (1 if D Q = 0)
+ *     R_j = max(R_{j-1} - D_{j-1} Q_v, 0), S_j = sum R_j, D_j = 1 - p + S_j
+ *   A child first reached by draw j has weight a_j; h_v = S_n / D_n (1 if
+ *   D_n = 0) is the block acceptance probability of the sub-block ending
+ *   at v; the correction is drawn from R_n / S_n (P_v if S_n = 0).
+ *   token:      walk from the root; at each node try the draws in order,
+ *               draw j accepted iff accept_u[b][k_j][depth] <= a_j; the
+ *               first accepted draw moves to its child; stop when all are
+ *               rejected or at depth L_b.
+ *   block/multidraft: depth-first over the trie (children in order of first
+ *               appearance); a node v at depth d >= 1 is accepted iff
+ *               accept_u[b][owner(v)][d-1] <= h_v, tried after its whole
+ *               subtree failed; the first accepted node ends the search
+ *               (the root if none).  K = 1 gives GBV exactly.
+ *   greedy:     a draft position matches iff its token is the row's argmax
+ *               (lowest index on ties); the longest matching draft wins
+ *               (lowest k on ties); the correction is the argmax of the
+ *               row after the accepted prefix.
+ *   Sampling:   the correction is the first token x (index order) whose
+ *               running sum of the distribution exceeds u * S with
+ *               u = sample_u[b][k*][tau] (else the last token of nonzero
+ *               mass).  T = 0 in any sampling rule gives the greedy result.
+ *
+ * Memory and ownership.  Every pointer argument is a device pointer (or
+ * host memory registered with CUDA and mapped into the device's address
+ * space) owned by the caller; the library allocates nothing and keeps no
+ * pointer after the call returns.  Calls are asynchronous on cuda_stream
+ * (a cudaStream_t; NULL = the legacy default stream); the caller must keep
+ * every buffer alive until the stream has passed the call.  Two calls that
+ * share a workspace must not overlap on the GPU.
+ *
+ * Errors.  The return value reports argument validation and launch errors
+ * only (SDV_OK or an SDV_ERR_* code; nothing is launched on error).  Data
+ * errors are found on the device: for each request whose length is outside
+ * 0..L, whose used tokens are outside [0, V), or one of whose used rows
+ * holds NaN or +Inf or no finite value, the outputs are accept_len = 0,
+ * accept_draft = 0, out_token = -1, residual_mass = 0 and accept_prob = 0,
+ * and the request's SDV_REQ_* bit is OR-ed into *device_status.  Other
+ * requests are unaffected.  Kernels never trap.
+ */
+#ifndef SDV_H
+#define SDV_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SDV_MAX_K 16      /* drafts per request */
+#define SDV_MAX_L 16      /* draft tokens per draft */
+#define SDV_MAX_V 262144  /* vocabulary size */
+
+/* logit element types */
+enum { SDV_F32 = 0, SDV_BF16 = 1 };
+
+/* modes, for sdv_workspace_bytes */
+enum { SDV_MODE_TOKEN = 0, SDV_MODE_GREEDY = 1, SDV_MODE_BLOCK = 2, SDV_MODE_MULTIDRAFT = 3 };
+
+/* return codes */
+enum {
+    SDV_OK = 0,
+    SDV_ERR_INVALID = 1,     /* an argument is out of range, misaligned or not device memory */
+    SDV_ERR_UNSUPPORTED = 2, /* valid, but this build or this GPU cannot run it */
+    SDV_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    SDV_ERR_TIMEOUT = 4,     /* reserved: a device wait ran out (reported in device_status) */
+    SDV_ERR_WORKSPACE = 5    /* workspace NULL, misaligned or smaller than sdv_workspace_bytes */
+};
+
+/* *device_status bits (OR of all requests) */
+enum {
+    SDV_REQ_BAD_LENGTH = 1, /* lengths[b] outside 0..L */
+    SDV_REQ_BAD_TOKEN = 2,  /* a used draft token outside [0, V) */
+    SDV_REQ_NONFINITE = 4,  /* a used row holds NaN or +Inf, or no finite value */
+    SDV_DEV_TIMEOUT = 8     /* a bounded device wait gave up; outputs are not valid */
+};
+
+/*
+ * Arguments shared by the four entry points.
+ *   B, K, L, V   batch size (>= 0), drafts per request (1..SDV_MAX_K), draft
+ *                length (0..SDV_MAX_L), vocabulary size (1..SDV_MAX_V).
+ *   row_stride   elements between consecutive rows; >= V and a multiple
+ *                of 8.  Elements V..row_stride-1 of a row are never read.
+ *   dtype        SDV_F32 or SDV_BF16 (both logit tensors).
+ *   temperature  T >= 0 and finite; the same T applies to target and draft.
+ *   target_logits [B][K][L+1][row_stride], 16-byte aligned.  Row (b,k,j) is
+ *                conditioned on draft k's first j tokens.  Only the rows of
+ *                trie nodes are read: row (b,k,j) with j <= lengths[b] and k
+ *                the lowest-index draft with that prefix (row 0: k = 0).
+ *   draft_logits [B][K][L][row_stride], 16-byte aligned; same rule with
+ *                j < lengths[b].  May be NULL when L = 0 or for greedy.
+ *   draft_tokens [B][K][L] int32; positions j >= lengths[b] are ignored.
+ *   lengths      [B] int32 in 0..L, or NULL for L everywhere.
+ *   accept_u     [B][K][L] fp32 uniforms in [0,1); NULL for greedy.
+ *   sample_u     [B][K][L+1] fp32 uniforms in [0,1); NULL for greedy.
+ * Outputs:
+ *   accept_len   [B] int32: tau in 0..lengths[b].
+ *   accept_draft [B] int32: k*, the lowest-index draft whose first tau
+ *                tokens were accepted (0 when tau = 0).
+ *   out_token    [B] int32: correction token (bonus when tau = lengths[b]).
+ *   accept_prob  [B][K][L] fp32 or NULL: the threshold each draft position
+ *                was (or would have been) tested against -- token: a of
+ *                draft k's draw at depth j; block/multidraft: h of the node
+ *                ending draft k's first j+1 tokens; greedy: 1 if the token
+ *                is its row's argmax else 0.  0 past lengths[b].
+ *   residual_mass [B] fp32 or NULL: S_n of the end node, the mass of the
+ *                unnormalised distribution the correction was drawn from
+ *                (a leaf's is its weight p); 1 for greedy.
+ *   device_status [1] int32 or NULL: cleared by the call, then OR of the
+ *                SDV_REQ_* / SDV_DEV_* bits.
+ *   workspace    device scratch of at least sdv_workspace_bytes(mode, B, K,
+ *                L, V) bytes, 256-byte aligned; contents need no
+ *                initialisation and are meaningless after the call.
+ *   cuda_stream  cudaStream_t to launch on.
+ */
+#define SDV_VERIFY_ARGS                                                                              \
+    int B, int K, int L, int V, long long row_stride, int dtype, float temperature,                  \
+        const void *target_logits, const void *draft_logits, const int *draft_tokens,                \
+        const int *lengths, const float *accept_u, const float *sample_u, int *accept_len,           \
+        int *accept_draft, int *out_token, float *accept_prob, float *residual_mass,                 \
+        int *device_status, void *workspace, size_t workspace_bytes, void *cuda_stream
+
+/* Token-level speculative sampling; K > 1: per-position multi-draft. */
+int sdv_verify_token(SDV_VERIFY_ARGS);
+
+/* Temperature-0 argmax matching; temperature, draft_logits, accept_u and
+ * sample_u are ignored and may be NULL. */
+int sdv_verify_greedy(SDV_VERIFY_ARGS);
+
+/* Greedy block verification; requires K == 1 (else SDV_ERR_INVALID). */
+int sdv_verify_block(SDV_VERIFY_ARGS);
+
+/* SpecTr-GBV multi-draft block verification. */
+int sdv_verify_multidraft(SDV_VERIFY_ARGS);
+
+/* Workspace bytes a call of `mode` with these sizes needs (0 if the sizes
+ * are invalid). */
+size_t sdv_workspace_bytes(int mode, int B, int K, int L, int V);
+
+/* Static description of a return code (not of device status bits). */
+const char *sdv_status_string(int status);
+
+/* Launch shape the library picks for rows of V elements of dtype: cluster
+ * size (CTAs sharing one vocabulary row), threads per CTA and dynamic
+ * shared memory per CTA.  Returns SDV_OK or SDV_ERR_INVALID. */
+int sdv_launch_shape(int V, int dtype, int *cluster, int *threads, int *smem_bytes);
+
+/* Profiling hook.  With start and stop both cudaEvent_t handles, every
+ * later call made from the calling host thread records `start` on its
+ * stream just before its first vocabulary-row kernel and `stop` just after
+ * its last one, so that cudaEventElapsedTime gives the time of those
+ * kernels alone; NULL, NULL turns it off.  The events stay owned by the
+ * caller.  Returns SDV_OK, or SDV_ERR_INVALID if exactly one is NULL. */
+int sdv_set_profile_events(void *start, void *stop);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

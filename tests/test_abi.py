@@ -1,0 +1,91 @@
+"""The C-ABI library on the host: it loads, exports what include/sdv.h
+declares, and rejects invalid arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from draft_verification_row_gb300 import build
+    build.build()
+    import draft_verification_row_gb300 as sdv
+    return sdv.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "sdv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdv_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert "sdv_verify_multidraft" in names and len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_bytes(lib):
+    import draft_verification_row_gb300 as sdv
+    assert sdv.workspace_bytes("multidraft", 256, 8, 8, 151936) > 256 * 8 * 9 * 24
+    assert sdv.workspace_bytes("token", 0, 1, 0, 1) >= 0
+    assert lib.sdv_workspace_bytes(2, 4, 2, 4, 100) == 0      # block needs K = 1
+    assert lib.sdv_workspace_bytes(0, 4, 0, 4, 100) == 0      # K = 0
+    assert lib.sdv_workspace_bytes(0, 4, 1, 17, 100) == 0     # L > 16
+    assert lib.sdv_workspace_bytes(0, 4, 1, 4, 262145) == 0   # V > max
+    assert lib.sdv_workspace_bytes(7, 4, 1, 4, 100) == 0      # unknown mode
+
+
+@pytest.mark.parametrize("V,dtype,C", [(1024, "f32", 1), (32000, "bf16", 2), (32000, "f32", 4),
+                                       (128256, "bf16", 8), (151936, "bf16", 8), (262144, "f32", 16)])
+def test_launch_shape(lib, V, dtype, C):
+    import draft_verification_row_gb300 as sdv
+    s = sdv.launch_shape(V, dtype)
+    assert s["cluster"] == C
+    assert s["smem_bytes"] <= 227 * 1024
+    assert s["threads"] in (128, 256, 512)
+
+
+def test_status_strings(lib):
+    assert lib.sdv_status_string(0) == b"ok"
+    assert b"workspace" in lib.sdv_status_string(5)
+
+
+def _call(lib, name, **over):
+    a = dict(B=2, K=1, L=2, V=16, stride=16, dtype=0, T=1.0)
+    a.update(over)
+    fn = getattr(lib, name)
+    return fn(a["B"], a["K"], a["L"], a["V"], a["stride"], a["dtype"], a["T"],
+              None, None, None, None, None, None, None, None, None, None, None, None, None, 0, None)
+
+
+@pytest.mark.parametrize("over", [dict(K=0), dict(K=17), dict(L=-1), dict(L=17), dict(V=0),
+                                  dict(V=262145, stride=262152), dict(stride=12), dict(stride=8),
+                                  dict(dtype=2), dict(T=-1.0), dict(T=float("nan")), dict(T=float("inf")),
+                                  dict(B=-1)])
+def test_invalid_sizes_rejected_without_gpu(lib, over):
+    assert _call(lib, "sdv_verify_token", **over) == 1
+
+
+def test_block_rejects_multiple_drafts(lib):
+    assert _call(lib, "sdv_verify_block", K=2) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _call(lib, "sdv_verify_multidraft", B=0) == 0
+
+
+def test_package_fails_loudly_without_library(tmp_path):
+    from draft_verification_row_gb300 import binding
+    saved = binding._lib
+    binding._lib = None
+    try:
+        with pytest.raises(ImportError):
+            binding.lib(str(tmp_path / "missing.so"))
+    finally:
+        binding._lib = saved

@@ -1,0 +1,202 @@
+"""CUDA path against the oracle through the C-ABI (needs a GB300)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from draft_verification_row_gb300 import workloads as W
+from tests import goldens
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+MODES_K1 = ["token", "block", "multidraft", "greedy"]
+MODES_K = ["token", "multidraft", "greedy"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _modes(batch):
+    return MODES_K1 if batch.K == 1 else MODES_K
+
+
+GOLDEN = goldens.cases()
+
+
+@pytest.mark.parametrize("case", GOLDEN, ids=[c["name"] for c in GOLDEN])
+def test_worked_examples(case):
+    dev = torch.device(DEV)
+    t = lambda a: None if a is None else torch.as_tensor(a).to(dev)
+    out = P.sdv.verify(case["mode"], t(P.pad8(case["target"])), t(P.pad8(case["draft"])), t(case["tokens"]),
+                       t(case["lengths"]), t(case["accept_u"]), t(case["sample_u"]), case["T"],
+                       V=case["V"])
+    torch.cuda.synchronize()
+    e = case["expected"]
+    assert int(out["device_status"][0]) == 0
+    assert int(out["accept_len"][0]) == e["accept_len"]
+    assert int(out["accept_draft"][0]) == e["accept_draft"]
+    assert int(out["out_token"][0]) == e["out_token"]
+    np.testing.assert_allclose(out["accept_prob"][0].cpu().numpy(), np.asarray(e["accept_prob"]), atol=1e-6)
+    assert abs(float(out["residual_mass"][0]) - e["residual_mass"]) < 1e-6
+
+
+# small shapes of every workload: several tiles, a ragged vocabulary tail
+SMALL = [
+    ("token-B4-K1-L4-V1024-f32", dict(B=6, V=1021), None),
+    ("token-greedy-B64-K1-L5-V32000-bf16", dict(B=6, V=3001), 1.0),
+    ("token-greedy-B64-K1-L5-V32000-bf16", dict(B=6, V=3001), 0.0),
+    ("block-B128-K1-L5-V128256-bf16", dict(B=6, V=12829), None),
+    ("multidraft-B32-K4-L4-V32000-f32", dict(B=6, V=3203), 0.1),
+    ("multidraft-B32-K4-L4-V32000-f32", dict(B=6, V=3203), 0.7),
+    ("mixed-B256-K8-L8-V151936-bf16", dict(B=6, V=15197), None),
+]
+
+
+@pytest.mark.parametrize("name,kw,T", SMALL)
+def test_small_parity(name, kw, T):
+    batch = W.make(name, DEV, temperature=T, **kw)
+    for mode in _modes(batch):
+        P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"{name}/{mode}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [1, 2, 7, 8, 9, 33, 1000, 4097])
+def test_vocabulary_edges(dtype, V):
+    batch = W.make("multidraft-B32-K4-L4-V32000-f32", DEV, B=4, K=3, L=3, V=V, dtype=dtype, temperature=0.9)
+    for mode in MODES_K:
+        P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"V={V}/{mode}")
+
+
+def test_max_drafts_and_length():
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=3, K=16, L=16, V=2053, temperature=1.5)
+    for mode in MODES_K:
+        P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"K16L16/{mode}")
+
+
+@pytest.mark.parametrize("lengths", [[0, 0, 0], [0, 3, 1], [3, 3, 3]])
+def test_ragged_and_empty_lengths(lengths):
+    batch = W.make("multidraft-B32-K4-L4-V32000-f32", DEV, B=3, K=4, L=3, V=999, lengths=lengths,
+                   temperature=0.7)
+    for mode in MODES_K:
+        P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"{lengths}/{mode}")
+
+
+def test_empty_draft_dimension():
+    batch = W.make("token-B4-K1-L4-V1024-f32", DEV, B=5, L=0, V=777)
+    for mode in MODES_K1:
+        P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"L=0/{mode}")
+
+
+def test_empty_batch():
+    batch = W.make("token-B4-K1-L4-V1024-f32", DEV, B=0)
+    out = P.gpu_run("token", batch)
+    assert out["accept_len"].shape == (0,)
+    assert int(out["device_status"][0]) == 0
+
+
+@pytest.mark.parametrize("name", ["mixed-B256-K8-L8-V151936-bf16", "multidraft-B32-K4-L4-V32000-f32"])
+def test_unread_rows_are_never_read(name):
+    """Rows past a request's length, duplicate-prefix copies, stride padding
+    and padding tokens hold NaN / -1: the outputs must not change."""
+    kw = dict(B=5, V=4001, stride_pad=8)
+    clean = W.make(name, DEV, **kw)
+    dirty = W.make(name, DEV, poison_unread=True, **kw)
+    for mode in MODES_K:
+        a, b = P.gpu_run(mode, clean), P.gpu_run(mode, dirty)
+        assert int(b["device_status"][0]) == 0
+        for key in ("accept_len", "accept_draft", "out_token", "accept_prob", "residual_mass"):
+            np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_invalid_requests_are_isolated():
+    batch = W.make("multidraft-B32-K4-L4-V32000-f32", DEV, B=6, K=3, L=3, V=1500, temperature=0.7)
+    batch.target[1, 0, 0, 17] = float("nan")          # used row of request 1
+    batch.draft[2, 0, 0, 3] = float("inf")            # used draft row of request 2
+    batch.tokens[3, 1, 0] = batch.V                   # used token out of range
+    batch.lengths[4] = 4                              # length > L
+    batch.target[5, 0, 0, :] = float("-inf")          # no finite value
+    for mode in MODES_K:
+        gpu = P.gpu_run(mode, batch)
+        ref = P.oracle_run(mode, batch)
+        P.compare(gpu, ref, f"invalid/{mode}")
+        st = ref["req_status"]
+        assert st[0] == 0 and st[3] == 2 and st[4] == 1
+        assert st[1] == 4 and st[5] == 4
+        assert st[2] == (0 if mode == "greedy" else 4)
+
+
+def test_deterministic():
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=8, V=30011)
+    for mode in ("token", "multidraft"):
+        a, b = P.gpu_run(mode, batch), P.gpu_run(mode, batch)
+        for key in a:
+            if a[key] is not None:
+                np.testing.assert_array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("C", ["1", "2", "4", "8", "16"])
+def test_every_cluster_size(C, monkeypatch):
+    monkeypatch.setenv("SDV_CLUSTER", C)
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=4, K=4, L=4, V=20011)
+    for mode in ("token", "multidraft"):
+        P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"C={C}/{mode}")
+
+
+@pytest.mark.parametrize("mode,K", [("token", 1), ("token", 2), ("block", 1), ("multidraft", 2)])
+def test_sampled_outputs_follow_exact_law(mode, K):
+    """Chi-square of the GPU's (tau, k*, token) over many requests sharing
+    logits and drafts but not uniforms, against the exact law the oracle
+    integrates (tiny vocabulary)."""
+    from scipy.stats import chi2
+    import oracle
+    V, L, N = 4, 2, 200000
+    rng = np.random.default_rng(17)
+    tgt = rng.normal(0, 1.2, (1, K, L + 1, V)).astype(np.float32)
+    dft = (tgt[:, :, :L] + rng.normal(0, 1.0, (1, K, L, V))).astype(np.float32)
+    tok = rng.integers(0, V, (1, K, L)).astype(np.int32)
+    if K > 1:
+        tgt[:, 1:, 0] = tgt[:, :1, 0]
+        dft[:, 1:, 0] = dft[:, :1, 0]
+    law = oracle.exact_outcomes(mode, oracle.Problem(tgt, dft, tok, None, np.zeros((1, K, L)),
+                                                     np.zeros((1, K, L + 1)), 1.0)).ravel()
+    dev = torch.device(DEV)
+    rep = lambda a: torch.as_tensor(a).to(dev).expand((N,) + a.shape[1:]).contiguous()
+    g = torch.Generator(device=dev).manual_seed(5)
+    out = P.sdv.verify(mode, rep(P.pad8(tgt)), rep(P.pad8(dft)), rep(tok), None,
+                       torch.rand((N, K, L), generator=g, device=dev),
+                       torch.rand((N, K, L + 1), generator=g, device=dev), 1.0, V=V)
+    torch.cuda.synchronize()
+    code = ((out["accept_len"].long() * K + out["accept_draft"].long()) * V + out["out_token"].long())
+    counts = torch.bincount(code, minlength=law.size).cpu().numpy()
+    keep = law * N >= 5
+    assert counts[~keep].sum() <= max(10, 3 * law[~keep].sum() * N + 3)
+    exp = law[keep] * N
+    stat = float(((counts[keep] - exp) ** 2 / exp).sum())
+    assert chi2.sf(stat, keep.sum() - 1) > 1e-3, (stat, keep.sum())
+
+
+FULL = [
+    ("token-B4-K1-L4-V1024-f32", [None], None),
+    ("token-greedy-B64-K1-L5-V32000-bf16", [0.0, 1.0], None),
+    ("block-B128-K1-L5-V128256-bf16", [None], list(range(0, 128, 8))),
+    ("multidraft-B32-K4-L4-V32000-f32", [0.1, 0.4, 0.7], None),
+    ("mixed-B256-K8-L8-V151936-bf16", [None], [0, 1, 37, 101, 190, 255]),
+]
+
+
+@pytest.mark.parametrize("name,temps,sample", FULL)
+def test_full_size_parity(name, temps, sample):
+    """The workloads at their full sizes, in the launch configuration the
+    bench times; the oracle checks every request or a fixed sample."""
+    for T in temps:
+        batch = W.make(name, DEV, temperature=T)
+        for mode in _modes(batch):
+            P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch, sample), f"{name}/T={T}/{mode}")
+        del batch
+        torch.cuda.empty_cache()
