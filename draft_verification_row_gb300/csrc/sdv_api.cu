@@ -41,7 +41,7 @@ Workspace carve(void* base, int B, int K, int L)
     p += align_up(n * 4);
     w.S = reinterpret_cast<float*>(p);
     p += align_up(n * 4);
-    w.p = reinterpret_cast<float*>(p);
+    w.pbar = reinterpret_cast<float*>(p);
     p += align_up(n * 4);
     w.tok = reinterpret_cast<int*>(p);
     p += align_up(n * 4);

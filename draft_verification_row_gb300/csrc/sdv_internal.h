@@ -19,7 +19,7 @@ struct Workspace {
     float* a;              // draw acceptance probability a (token / multidraft)
     float* h;              // node block acceptance probability h_v
     float* S;              // node residual mass S_n
-    float* p;              // node weight p_v
+    float* pbar;           // node weight complement 1 - p_v
     int* tok;              // node candidate correction token
     int* am;               // node argmax (greedy)
     unsigned char* owner;  // lowest draft sharing draft k's first j tokens

@@ -246,16 +246,44 @@ __device__ void block_max2(float& a, float& b, float* red)
     __syncthreads();
 }
 
+// Softmax of one row in fp64, from the fp32 sweep results.  The row
+// maximum is excluded from `zrest`, so that P and 1 - P of a dominant
+// token are both exact to fp64 rounding of fp32-accurate addends.
+struct RowD {
+    double z;      // sum of e(x) = 2^(x c - m c) over the row
+    double zrest;  // the same without the elements equal to the maximum
+    float emax;    // e at the maximum
+    float neg;     // -(m c)
+    int n;         // elements equal to the maximum
+    int ux;        // index of the unique maximum, or -1
+};
+
+struct ProbD {
+    double P, Pbar;
+};
+
 // Shared-memory layout of the node kernel (after the two row slices).
 struct NodeSmem {
-    float part[kMaxThreads];              // per-thread partial mass of the last sweep
-    float partT[kMaxThreads];             // per-thread partial target mass (stats sweep)
-    float xbuf[2][kMaxCluster][4];        // cluster exchange, double-buffered
-    float totT[kMaxCluster];              // per-CTA target mass
-    float red[64];                        // block reductions
-    uint64_t bar[2];                      // row-slice mbarriers
-    int pick[2];                          // sampling: chosen thread, found flag
-    float pick_base;                      // sampling: mass before the chosen thread
+    float part[kMaxThreads];          // per-thread partial mass of the last residual sweep
+    float partT[kMaxThreads];         // per-thread partial target mass (normaliser sweep)
+    float xbuf[2][kMaxCluster][8];    // cluster exchange, double-buffered
+    float red[64];                    // block reductions
+    int ired[4][32];                  // block reductions of counts / indices
+    uint64_t bar[2];                  // row-slice mbarriers
+    // scalar state, written by thread 0 and read by every thread
+    float aT, aD;                     // sweep weights p / Z_T and C_j / Z_D
+    float tot[kMaxCluster];           // per-CTA mass of the sampled distribution
+    float thr;                        // u * total mass
+    int use_res;                      // sample the residual (else P)
+    int rstar;                        // CTA holding the sample
+    float base;                       // mass before CTA rstar
+    int spec_x[2];                    // indices whose residual weight is exact (or -1)
+    float spec_w[2];                  // their exact weights
+    int bad;                          // a used row is not finite
+    int pick;                         // sampling: chosen thread
+    float pick_base;                  // sampling: mass before the chosen thread
+    RowD rT, rD;                      // fp64 row state (thread 0)
+    double S, D, cbar;                // residual recursion state (thread 0)
 };
 
 }  // namespace
@@ -307,13 +335,13 @@ __global__ void prep_kernel(Problem pb)
             own[j * K + k] = (unsigned char)o;
         }
     }
-    pb.ws.p[(size_t)b * (L + 1) * K] = 1.f;
+    pb.ws.pbar[(size_t)b * (L + 1) * K] = 0.f;  // root weight 1
 }
 
 // ------------------------------------------------------------------------
 // node kernel
 
-// Cluster-wide exchange: thread 0 of every CTA publishes n (<= 4) values
+// Cluster-wide exchange: thread 0 of every CTA publishes n (<= 8) words
 // into slot [rank] of buffer `par` of every CTA; after the cluster barrier
 // each CTA reads all slots locally.
 __device__ __forceinline__ void cluster_publish(cg::cluster_group& cl, NodeSmem* sm, int par, int rank, int C,
@@ -326,6 +354,64 @@ __device__ __forceinline__ void cluster_publish(cg::cluster_group& cl, NodeSmem*
         }
     }
     cl.sync();
+}
+
+// Block-wide sum of two ints and minimum of two ints (thread 0's result).
+__device__ void block_int4(int& s0, int& s1, int& m0, int& m1, int (*ired)[32])
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        m0 = min(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+        m1 = min(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
+    if (lane == 0) {
+        ired[0][warp] = s0;
+        ired[1][warp] = s1;
+        ired[2][warp] = m0;
+        ired[3][warp] = m1;
+    }
+    __syncthreads();
+    s0 = s1 = 0;
+    m0 = m1 = 0x7fffffff;
+    for (int w = 0; w < nw; ++w) {
+        s0 += ired[0][w];
+        s1 += ired[1][w];
+        m0 = min(m0, ired[2][w]);
+        m1 = min(m1, ired[3][w]);
+    }
+    __syncthreads();
+}
+
+// The residual term of one element as every sweep computes it, in fp32.
+__device__ __forceinline__ float res_term(float eT, float eD, float aT, float aD)
+{
+    return fmaxf(__fmaf_rn(eT, aT, -__fmul_rn(eD, aD)), 0.f);
+}
+
+template <int DT>
+__device__ ProbD row_prob(const RowD& r, const char* g, int x, float c)
+{
+    ProbD o;
+    if (x == r.ux) {
+        o.P = (double)r.emax / r.z;
+        o.Pbar = r.zrest / r.z;
+    } else {
+        const float e = ex2(fmaf(Elem<DT>::load(g, x), c, r.neg));
+        o.P = (double)e / r.z;
+        o.Pbar = 1.0 - o.P;
+    }
+    return o;
+}
+
+// alpha P(x) - beta Q(x) with alpha = 1 - pbar and beta = 1 + cbar, written
+// with complements so that nothing of order one cancels when P and Q are
+// both close to 1.
+__device__ __forceinline__ double g_diff(const ProbD& P, const ProbD& Q, double pbar, double cbar)
+{
+    return Q.Pbar - P.Pbar + pbar * P.Pbar + cbar * Q.Pbar - pbar - cbar;
 }
 
 template <int DT>
@@ -393,16 +479,16 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
 
     bool timed_out = false;
     // ---- row maxima (NaN-propagating) ----
-    float mT = -INFINITY, mD = -INFINITY;
+    float mlT = -INFINITY, mlD = -INFINITY;
     if (nU > 0) {
         if (!mbar_wait_bounded(&sm->bar[0], 0)) timed_out = true;
         for (int u = cu0; u < cu1; ++u) {
             if ((u_base + u + 1) * EPU > V) {
                 float v[EPU];
                 unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, v);
-                for (int e = 0; e < EPU; ++e) mT = max_nan(mT, v[e]);
+                for (int e = 0; e < EPU; ++e) mlT = max_nan(mlT, v[e]);
             } else {
-                mT = E::unit_max(smT[u], mT);
+                mlT = E::unit_max(smT[u], mlT);
             }
         }
         if (!leaf) {
@@ -411,13 +497,14 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                 if ((u_base + u + 1) * EPU > V) {
                     float v[EPU];
                     unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, v);
-                    for (int e = 0; e < EPU; ++e) mD = max_nan(mD, v[e]);
+                    for (int e = 0; e < EPU; ++e) mlD = max_nan(mlD, v[e]);
                 } else {
-                    mD = E::unit_max(smD[u], mD);
+                    mlD = E::unit_max(smD[u], mlD);
                 }
             }
         }
     }
+    float mT = mlT, mD = mlD;
     block_max2(mT, mD, sm->red);
     {
         float v[2] = {mT, mD};
@@ -434,136 +521,247 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
     // whole row and cancels in e(x) / sum e.
     const float negT = -(mT * c);
     const float negD = -(mD * c);
+    const float emaxT = ex2(fmaf(mT, c, negT));
+    const float emaxD = ex2(fmaf(mD, c, negD));
 
-    // ---- softmax normalisers ----
+    // ---- softmax normalisers, the maxima counted apart ----
     float zT = 0.f, zD = 0.f;
-    for (int u = cu0; u < cu1; ++u) {
-        float t[EPU];
-        unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, t);
-#pragma unroll
-        for (int e = 0; e < EPU; ++e) zT += ex2(fmaf(t[e], c, negT));
-    }
-    if (!leaf) {
+    int cntT = 0, cntD = 0, firstT = 0x7fffffff, firstD = 0x7fffffff;
+    if (mlT == mT) {  // this thread holds the target maximum
         for (int u = cu0; u < cu1; ++u) {
-            float d[EPU];
-            unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, d);
+            float t[EPU];
+            unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, t);
+            for (int e = 0; e < EPU; ++e) {
+                if (t[e] == mT) {
+                    ++cntT;
+                    firstT = min(firstT, (u_base + u) * EPU + e);
+                } else {
+                    zT += ex2(fmaf(t[e], c, negT));
+                }
+            }
+        }
+    } else {
+        for (int u = cu0; u < cu1; ++u) {
+            float t[EPU];
+            unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, t);
 #pragma unroll
-            for (int e = 0; e < EPU; ++e) zD += ex2(fmaf(d[e], c, negD));
+            for (int e = 0; e < EPU; ++e) zT += ex2(fmaf(t[e], c, negT));
         }
     }
-    sm->partT[tid] = zT;
+    if (!leaf) {
+        if (mlD == mD) {
+            for (int u = cu0; u < cu1; ++u) {
+                float d[EPU];
+                unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, d);
+                for (int e = 0; e < EPU; ++e) {
+                    if (d[e] == mD) {
+                        ++cntD;
+                        firstD = min(firstD, (u_base + u) * EPU + e);
+                    } else {
+                        zD += ex2(fmaf(d[e], c, negD));
+                    }
+                }
+            }
+        } else {
+            for (int u = cu0; u < cu1; ++u) {
+                float d[EPU];
+                unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, d);
+#pragma unroll
+                for (int e = 0; e < EPU; ++e) zD += ex2(fmaf(d[e], c, negD));
+            }
+        }
+    }
+    sm->partT[tid] = zT + (float)cntT * emaxT;
     block_sum2(zT, zD, sm->red);
+    block_int4(cntT, cntD, firstT, firstD, sm->ired);
     {
-        float v[2] = {zT, zD};
-        cluster_publish(cl, sm, 1, rank, C, v, 2);
+        float v[6] = {zT, zD, __int_as_float(cntT), __int_as_float(cntD), __int_as_float(firstT),
+                      __int_as_float(firstD)};
+        cluster_publish(cl, sm, 1, rank, C, v, 6);
     }
-    zT = 0.f;
-    zD = 0.f;
-    for (int r = 0; r < C; ++r) {
-        sm->totT[r] = sm->xbuf[1][r][0];  // read by this thread only after the barrier below
-        zT += sm->xbuf[1][r][0];
-        zD += sm->xbuf[1][r][1];
+
+    // ---- scalar state (thread 0, fp64, kept in shared memory) ----
+    RowD& rT = sm->rT;
+    RowD& rD = sm->rD;
+    const double p_in = (j == 0 || pb.mode == SDV_MODE_TOKEN) ? 0.0 : (double)pb.ws.pbar[s];
+    const double pbar = p_in;
+    const double p = 1.0 - pbar;
+    if (tid == 0) {
+        rT.zrest = rD.zrest = 0.0;
+        rT.n = rD.n = 0;
+        int fT = 0x7fffffff, fD = 0x7fffffff;
+        for (int r = 0; r < C; ++r) {
+            rT.zrest += (double)sm->xbuf[1][r][0];
+            rD.zrest += (double)sm->xbuf[1][r][1];
+            rT.n += __float_as_int(sm->xbuf[1][r][2]);
+            rD.n += __float_as_int(sm->xbuf[1][r][3]);
+            fT = min(fT, __float_as_int(sm->xbuf[1][r][4]));
+            fD = min(fD, __float_as_int(sm->xbuf[1][r][5]));
+        }
+        rT.emax = emaxT;
+        rD.emax = emaxD;
+        rT.neg = negT;
+        rD.neg = negD;
+        rT.z = rT.n * (double)emaxT + rT.zrest;
+        rD.z = rD.n * (double)emaxD + rD.zrest;
+        rT.ux = rT.n == 1 ? fT : -1;
+        rD.ux = rD.n == 1 ? fD : -1;
+        const bool bad = !(isfinite(mT) && isfinite(rT.z) && rT.z > 0.0) ||
+                         (!leaf && !(isfinite(mD) && isfinite(rD.z) && rD.z > 0.0));
+        sm->bad = bad;
+        if (bad && rank == 0) {
+            atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
+            if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
+        }
+        sm->spec_x[0] = leaf ? -1 : rT.ux;
+        sm->spec_x[1] = (leaf || rD.ux == rT.ux) ? -1 : rD.ux;
+        sm->spec_w[0] = sm->spec_w[1] = 0.f;
+        for (int r = 0; r < C; ++r)
+            sm->tot[r] = sm->xbuf[1][r][0] + (float)__float_as_int(sm->xbuf[1][r][2]) * emaxT;
+        sm->use_res = 0;
     }
-    const bool bad_row = !(isfinite(mT) && isfinite(zT) && zT > 0.f) ||
-                         (!leaf && !(isfinite(mD) && isfinite(zD) && zD > 0.f));
-    if (bad_row && rank == 0 && tid == 0) {
-        atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
-        if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
-    }
-    const float invZT = 1.f / zT;
-    const float invZD = 1.f / zD;
 
     // ---- residual recursion over the draws of the drafts through the node ----
-    const float p = (j == 0 || pb.mode == SDV_MODE_TOKEN) ? 1.f : pb.ws.p[s];
-    float S = p;        // S_0 = sum p P = p
-    float D = 1.f;      // D_0
-    float Csum = 0.f;   // C_j = D_0 + ... + D_{j-1}
-    int par = 0;
-    bool have_part = false;
+    // R_j = max(p P - C_j Q, 0), S_j = sum R_j, D_j = 1 - p + S_j,
+    // C_1 = 1, C_{j+1} = C_j + D_j.  Thread 0 keeps the scalars in fp64 as
+    // pbar = 1 - p and cbar = C_j - 1.
+    double& S = sm->S;
+    double& D = sm->D;
+    double& cbar = sm->cbar;
+    if (tid == 0) {
+        S = p;
+        D = 1.0;
+        cbar = 0.0;
+    }
+    int par = 1;
+    bool first = true;
     if (!leaf) {
         for (int k2 = k; k2 < K; ++k2) {
             if (pb.ws.owner[((size_t)b * (L + 1) + j) * K + k2] != k) continue;
-            const int y = pb.tokens[((size_t)b * K + k2) * L + j];
-            const float Py = ex2(fmaf(E::load(gT, y), c, negT)) * invZT;
-            const float Qy = ex2(fmaf(E::load(gD, y), c, negD)) * invZD;
-            const float Rprev = fmaxf(p * Py - Csum * Qy, 0.f);
-            const float denom = D * Qy;
-            const float a = denom > 0.f ? fminf(Rprev / denom, 1.f) : 1.f;
-            if (rank == 0 && tid == 0) {
-                pb.ws.a[((size_t)b * (L + 1) + j) * K + k2] = a;
-                if (pb.mode != SDV_MODE_TOKEN) {
-                    const size_t sc = ((size_t)b * (L + 1) + j + 1) * K + k2;
-                    if (pb.ws.owner[sc] == k2) pb.ws.p[sc] = a;  // child first reached by this draw
+            if (tid == 0) {
+                const int y = pb.tokens[((size_t)b * K + k2) * L + j];
+                const ProbD Py = row_prob<DT>(rT, gT, y, c);
+                const ProbD Qy = row_prob<DT>(rD, gD, y, c);
+                // R_{j-1}(y): C_0 = 0 for the first draw
+                const double R = first ? p * Py.P : fmax(g_diff(Py, Qy, pbar, cbar), 0.0);
+                const double cnew = first ? 0.0 : cbar + D;
+                const double denom = D * Qy.P;
+                double a, abar;
+                if (!(denom > 0.0) || R >= denom) {
+                    a = 1.0;
+                    abar = 0.0;
+                } else if (!(R > 0.0)) {
+                    a = 0.0;
+                    abar = 1.0;
+                } else {
+                    a = R / denom;
+                    // 1 - a = (C_j Q(y) - p P(y)) / (D Q(y))
+                    abar = fmin(fmax(-g_diff(Py, Qy, pbar, cnew), 0.0) / denom, 1.0);
                 }
+                cbar = cnew;
+                if (rank == 0) {
+                    pb.ws.a[((size_t)b * (L + 1) + j) * K + k2] = (float)a;
+                    if (pb.mode != SDV_MODE_TOKEN) {
+                        const size_t sc = ((size_t)b * (L + 1) + j + 1) * K + k2;
+                        if (pb.ws.owner[sc] == k2) pb.ws.pbar[sc] = (float)abar;  // child first reached here
+                    }
+                }
+                sm->aT = (float)(p / rT.z);
+                sm->aD = (float)((1.0 + cbar) / rD.z);
             }
-            Csum += D;
-            // S_j = sum_x max(p P(x) - C_j Q(x), 0)
-            const float aT = p * invZT, aD = Csum * invZD;
+            __syncthreads();
+            const float aT = sm->aT, aD = sm->aD;
             float w = 0.f;
             for (int u = cu0; u < cu1; ++u) {
                 float t[EPU], d[EPU];
                 unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, t);
                 unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, d);
 #pragma unroll
-                for (int e = 0; e < EPU; ++e) {
-                    const float eT = ex2(fmaf(t[e], c, negT));
-                    const float eD = ex2(fmaf(d[e], c, negD));
-                    w += fmaxf(fmaf(eT, aT, -(eD * aD)), 0.f);
-                }
+                for (int e = 0; e < EPU; ++e)
+                    w += res_term(ex2(fmaf(t[e], c, negT)), ex2(fmaf(d[e], c, negD)), aT, aD);
             }
             sm->part[tid] = w;
             float dummy = 0.f;
             block_sum2(w, dummy, sm->red);
             par ^= 1;
             cluster_publish(cl, sm, par, rank, C, &w, 1);
-            S = 0.f;
-            for (int r = 0; r < C; ++r) S += sm->xbuf[par][r][0];
-            D = 1.f - p + S;
-            have_part = true;
+            if (tid == 0) {
+                // fp32 sweep sums, with the dominant tokens' terms replaced
+                // by their exact values
+                double Sj = 0.0;
+                for (int r = 0; r < C; ++r) {
+                    Sj += (double)sm->xbuf[par][r][0];
+                    sm->tot[r] = sm->xbuf[par][r][0];
+                }
+                for (int i = 0; i < 2; ++i) {
+                    const int x = sm->spec_x[i];
+                    if (x < 0) continue;
+                    const ProbD Px = row_prob<DT>(rT, gT, x, c);
+                    const ProbD Qx = row_prob<DT>(rD, gD, x, c);
+                    const double exact = fmax(g_diff(Px, Qx, pbar, cbar), 0.0);
+                    const float f32 = res_term(ex2(fmaf(E::load(gT, x), c, negT)),
+                                               ex2(fmaf(E::load(gD, x), c, negD)), aT, aD);
+                    Sj += exact - (double)f32;
+                    sm->spec_w[i] = (float)exact;
+                    const int rx = (x / EPU) / sh.units_per_cta;
+                    sm->tot[rx] += (float)exact - f32;
+                    if (rx == rank) {
+                        const int tx = ((x / EPU) - u_base) / sh.units_per_thr;
+                        sm->part[tx] += (float)exact - f32;
+                    }
+                }
+                S = fmax(Sj, 0.0);
+                D = pbar + S;
+                sm->use_res = S > 0.0;
+            }
+            first = false;
         }
     }
-    const float h = leaf ? p : (D > 0.f ? S / D : 1.f);
-    if (rank == 0 && tid == 0) {
-        pb.ws.h[s] = h;
-        pb.ws.S[s] = S;
-    }
 
-    // ---- candidate correction: inverse CDF over the end distribution ----
-    // residual R_n (weights aT, aD of the last sweep) when S > 0, else P.
-    const bool use_res = have_part && S > 0.f;
-    const float aT = p * invZT, aD = Csum * invZD;
-    float tot[kMaxCluster];
-    for (int r = 0; r < C; ++r) tot[r] = use_res ? sm->xbuf[par][r][0] : sm->totT[r];
-    float Stot = 0.f;
-    for (int r = 0; r < C; ++r) Stot += tot[r];
-    const float u = pb.sample_u[((size_t)b * K + k) * (L + 1) + j];
-    const float thr = u * Stot;
-    int rstar = -1;
-    float base = 0.f;
-    {
-        float run = 0.f;
-        int last = -1;
-        float last_base = 0.f;
+    // ---- node outputs and the candidate correction ----
+    if (tid == 0) {
+        const double h = leaf ? p : (D > 0.0 ? S / D : 1.0);
+        if (rank == 0) {
+            pb.ws.h[s] = (float)h;
+            pb.ws.S[s] = (float)S;
+        }
+        if (!sm->use_res) {
+            // sample P: per-CTA target mass
+            for (int r = 0; r < C; ++r)
+                sm->tot[r] = sm->xbuf[1][r][0] + (float)__float_as_int(sm->xbuf[1][r][2]) * emaxT;
+        }
+        float Stot = 0.f;
+        for (int r = 0; r < C; ++r) Stot += sm->tot[r];
+        const float u = pb.sample_u[((size_t)b * K + k) * (L + 1) + j];
+        const float thr = u * Stot;
+        int rstar = -1, last = -1;
+        float run = 0.f, base = 0.f, last_base = 0.f;
         for (int r = 0; r < C; ++r) {
-            if (tot[r] > 0.f) {
+            if (sm->tot[r] > 0.f) {
                 last = r;
                 last_base = run;
-                if (run + tot[r] > thr) {
+                if (run + sm->tot[r] > thr) {
                     rstar = r;
                     base = run;
                     break;
                 }
             }
-            run += tot[r];
+            run += sm->tot[r];
         }
         if (rstar < 0) {
             rstar = last;
             base = last_base;
         }
+        sm->rstar = sm->bad ? -1 : rstar;
+        sm->base = base;
+        sm->thr = thr;
     }
+    __syncthreads();
+    const bool use_res = sm->use_res != 0;
+    const int rstar = sm->rstar;
     if (rank == rstar) {
         const float* parts = use_res ? sm->part : sm->partT;
-        const float local = thr - base;
+        const float local = sm->thr - sm->base;
         // warp 0 finds the first thread whose running mass exceeds `local`
         if (tid < 32) {
             const int nthr = blockDim.x;
@@ -578,55 +776,36 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                 if (tid >= o) incl += n;
             }
             const float excl = incl - lane_sum;
-            const bool cross = lane_sum > 0.f && incl > local;
-            const unsigned cm = __ballot_sync(0xffffffffu, cross);
+            const unsigned cm = __ballot_sync(0xffffffffu, lane_sum > 0.f && incl > local);
+            const unsigned nz = __ballot_sync(0xffffffffu, lane_sum > 0.f);
+            // the first crossing lane, else (rounding) the last lane of nonzero mass
+            const int l = cm ? __ffs(cm) - 1 : (nz ? 31 - __clz(nz) : -1);
             int tsel = -1;
             float tbase = 0.f;
-            if (cm) {
-                const int l = __ffs(cm) - 1;
-                if (tid == l) {
-                    float run = excl;
-                    for (int t = t0; t < t1; ++t) {
-                        if (parts[t] > 0.f) {
-                            if (run + parts[t] > local) {
-                                tsel = t;
-                                tbase = run;
-                                break;
-                            }
-                            tsel = t;  // rounding fallback inside the lane
-                            tbase = run;
-                        }
-                        run += parts[t];
+            if (tid == l) {
+                float run = excl;
+                for (int t = t0; t < t1; ++t) {
+                    if (parts[t] > 0.f) {
+                        const bool hit = run + parts[t] > local;
+                        tsel = t;
+                        tbase = run;
+                        if (hit && cm) break;
                     }
-                }
-                tsel = __shfl_sync(0xffffffffu, tsel, l);
-                tbase = __shfl_sync(0xffffffffu, tbase, l);
-            } else {
-                // rounding: the last thread of nonzero mass
-                const unsigned nz = __ballot_sync(0xffffffffu, lane_sum > 0.f);
-                if (nz) {
-                    const int l = 31 - __clz(nz);
-                    if (tid == l) {
-                        float run = excl;
-                        for (int t = t0; t < t1; ++t) {
-                            if (parts[t] > 0.f) {
-                                tsel = t;
-                                tbase = run;
-                            }
-                            run += parts[t];
-                        }
-                    }
-                    tsel = __shfl_sync(0xffffffffu, tsel, l);
-                    tbase = __shfl_sync(0xffffffffu, tbase, l);
+                    run += parts[t];
                 }
             }
+            if (l >= 0) {
+                tsel = __shfl_sync(0xffffffffu, tsel, l);
+                tbase = __shfl_sync(0xffffffffu, tbase, l);
+            }
             if (tid == 0) {
-                sm->pick[0] = tsel;
+                sm->pick = tsel;
                 sm->pick_base = tbase;
             }
         }
         __syncthreads();
-        if (tid == sm->pick[0]) {
+        if (tid == sm->pick) {
+            const float aT = sm->aT, aD = sm->aD;
             float run = sm->pick_base;
             int chosen = -1, last = -1;
             for (int uu = cu0; uu < cu1 && chosen < 0; ++uu) {
@@ -634,13 +813,16 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                 unpack_masked<DT>(smT[uu], (u_base + uu) * EPU, V, t);
                 if (use_res) unpack_masked<DT>(smD[uu], (u_base + uu) * EPU, V, d);
                 for (int e = 0; e < EPU; ++e) {
+                    const int x = (u_base + uu) * EPU + e;
                     const float eT = ex2(fmaf(t[e], c, negT));
-                    const float wx = use_res ? fmaxf(fmaf(eT, aT, -(ex2(fmaf(d[e], c, negD)) * aD)), 0.f) : eT;
+                    float wx = use_res ? res_term(eT, ex2(fmaf(d[e], c, negD)), aT, aD) : eT;
+                    if (use_res && x == sm->spec_x[0]) wx = sm->spec_w[0];
+                    if (use_res && x == sm->spec_x[1]) wx = sm->spec_w[1];
                     if (wx > 0.f) {
                         run += wx;
-                        last = (u_base + uu) * EPU + e;
+                        last = x;
                         if (run > local) {
-                            chosen = last;
+                            chosen = x;
                             break;
                         }
                     }
