@@ -182,6 +182,36 @@ const char *sdv_status_string(int status);
  * shared memory per CTA.  Returns SDV_OK or SDV_ERR_INVALID. */
 int sdv_launch_shape(int V, int dtype, int *cluster, int *threads, int *smem_bytes);
 
+/* Fixed scratch of sdv_verify_multidraft_static: 4 MiB of device memory
+ * that every GPU loading the library reserves until the process exits. */
+#define SDV_STATIC_SCRATCH_BYTES (4u << 20)
+
+/* SpecTr-GBV verification (as sdv_verify_multidraft) for callers that cannot
+ * allocate device memory: a plugin whose host framework owns all device
+ * memory and passes it only input and output buffers, code running inside a
+ * device allocator's own hooks, or a serving loop that forbids cudaMalloc
+ * because it can synchronise the device.  The source pages have no
+ * counterpart: this is a library convenience.
+ *   Arguments and outputs are those of sdv_verify_multidraft, without
+ *   workspace and workspace_bytes: the scratch is a fixed device array of
+ *   SDV_STATIC_SCRATCH_BYTES inside the library.  A problem whose
+ *   sdv_workspace_bytes(SDV_MODE_MULTIDRAFT, B, K, L, V) exceeds that is
+ *   rejected with SDV_ERR_WORKSPACE before anything is launched (e.g.
+ *   B = 256, K = 8, L = 8 needs about 0.5 MiB).
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current and keeps it; make that
+ *   first call before any stream capture.  Nothing is allocated, then or
+ *   later.
+ *   Every call on a device shares the one array: two calls whose kernels
+ *   overlap on the GPU (different streams without ordering, or different
+ *   host threads) race and give wrong results.  Nothing in the array needs
+ *   to start at zero; each call writes every record before reading it. */
+int sdv_verify_multidraft_static(int B, int K, int L, int V, long long row_stride, int dtype, float temperature,
+                                 const void *target_logits, const void *draft_logits, const int *draft_tokens,
+                                 const int *lengths, const float *accept_u, const float *sample_u,
+                                 int *accept_len, int *accept_draft, int *out_token, float *accept_prob,
+                                 float *residual_mass, int *device_status, void *cuda_stream);
+
 /* Profiling hook.  With start and stop both cudaEvent_t handles, every
  * later call made from the calling host thread records `start` on its
  * stream just before its first vocabulary-row kernel and `stop` just after
