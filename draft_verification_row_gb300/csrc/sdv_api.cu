@@ -189,7 +189,12 @@ int choose_shape(int V, int dtype, Shape* s)
     for (;; C *= 2) {
         if (C > 16) return SDV_ERR_UNSUPPORTED;
         const int upc = (n_units + C - 1) / C;
-        const int threads = upc >= 1024 ? 512 : (upc >= 256 ? 256 : 128);
+        int threads = upc >= 1024 ? 512 : (upc >= 256 ? 256 : 128);
+        const char* tenv = std::getenv("SDV_THREADS");
+        if (tenv && *tenv) {
+            threads = std::atoi(tenv);
+            if (threads != 128 && threads != 256 && threads != 512) return SDV_ERR_INVALID;
+        }
         int eu = (upc + threads - 1) / threads;
         if (eu % 2 == 0) ++eu;  // odd: 16-byte loads of a warp hit distinct banks
         const size_t smem = node_smem_bytes(upc);

@@ -206,27 +206,8 @@ __device__ __forceinline__ float warp_max_nan(float v)
     return v;
 }
 
-// Block-wide sum / max of two values; every thread gets the result.
+// Block-wide maxima of two values; every thread gets the result.
 // red must hold 64 floats; ends with a barrier so red can be reused.
-__device__ void block_sum2(float& a, float& b, float* red)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    a = warp_sum(a);
-    b = warp_sum(b);
-    if (lane == 0) {
-        red[warp] = a;
-        red[32 + warp] = b;
-    }
-    __syncthreads();
-    a = 0.f;
-    b = 0.f;
-    for (int w = 0; w < nw; ++w) {
-        a += red[w];
-        b += red[32 + w];
-    }
-    __syncthreads();
-}
-
 __device__ void block_max2(float& a, float& b, float* red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -246,44 +227,82 @@ __device__ void block_max2(float& a, float& b, float* red)
     __syncthreads();
 }
 
-// Softmax of one row in fp64, from the fp32 sweep results.  The row
-// maximum is excluded from `zrest`, so that P and 1 - P of a dominant
-// token are both exact to fp64 rounding of fp32-accurate addends.
-struct RowD {
-    double z;      // sum of e(x) = 2^(x c - m c) over the row
-    double zrest;  // the same without the elements equal to the maximum
-    float emax;    // e at the maximum
-    float neg;     // -(m c)
-    int n;         // elements equal to the maximum
-    int ux;        // index of the unique maximum, or -1
-};
+// Block-wide sums of two floats and two ints, valid in thread 0 only.  One
+// barrier; the caller must pass another barrier before `red` is reused.
+__device__ void block_sum_f2i2_t0(float& a, float& b, int& m, int& n, float* red, int (*ired)[32])
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+        m += __shfl_xor_sync(0xffffffffu, m, o);
+        n += __shfl_xor_sync(0xffffffffu, n, o);
+    }
+    if (lane == 0) {
+        red[warp] = a;
+        red[32 + warp] = b;
+        ired[0][warp] = m;
+        ired[1][warp] = n;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        a = b = 0.f;
+        m = n = 0;
+        for (int w = 0; w < nw; ++w) {
+            a += red[w];
+            b += red[32 + w];
+            m += ired[0][w];
+            n += ired[1][w];
+        }
+    }
+}
 
-struct ProbD {
-    double P, Pbar;
-};
+// Block-wide sum valid in thread 0 only (one barrier, same rule).
+__device__ float block_sum_t0(float a, float* red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    a = warp_sum(a);
+    if (lane == 0) red[warp] = a;
+    __syncthreads();
+    float s = 0.f;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < nw; ++w) s += red[w];
+    return s;
+}
+
+// Cluster exchange words published by each CTA after the normaliser sweep.
+enum { X_MT, X_MD, X_ZT, X_ZD, X_NT, X_ND, X_FT, X_FD, X_PT, X_PD, X_WORDS };
 
 // Shared-memory layout of the node kernel (after the two row slices).
 struct NodeSmem {
     float part[kMaxThreads];          // per-thread partial mass of the last residual sweep
-    float partT[kMaxThreads];         // per-thread partial target mass (normaliser sweep)
-    float xbuf[2][kMaxCluster][8];    // cluster exchange, double-buffered
-    float red[64];                    // block reductions
-    int ired[4][32];                  // block reductions of counts / indices
+    float partT[kMaxThreads];         // per-thread partial target mass, in this CTA's units
+    float xbuf[2][kMaxCluster][12];   // cluster exchange, double-buffered
+    float red[64];                    // block sums
+    float redm[64];                   // block maxima
+    int ired[2][32];                  // block sums of counts
+    unsigned long long firstT, firstD;  // (first index of the CTA maximum << 32) | partner logit bits
     uint64_t bar[2];                  // row-slice mbarriers
-    // scalar state, written by thread 0 and read by every thread
-    float aT, aD;                     // sweep weights p / Z_T and C_j / Z_D
-    float tot[kMaxCluster];           // per-CTA mass of the sampled distribution
-    float thr;                        // u * total mass
-    int use_res;                      // sample the residual (else P)
-    int rstar;                        // CTA holding the sample
-    float base;                       // mass before CTA rstar
-    int spec_x[2];                    // indices whose residual weight is exact (or -1)
+    float gT[SDV_MAX_K], gD[SDV_MAX_K];  // target / draft logits at each draft's drawn token
+    // scalar state of thread 0 (fp64 where it matters)
+    double zT, zD;                    // normalisers, in units of the row's global reference
+    double zrestT, zrestD;            // the same without the unique maximum
+    double sclT[kMaxCluster], sclD[kMaxCluster];  // CTA r's unit 2^(x c - m_r c) in global units
+    float negT[kMaxCluster], negD[kMaxCluster];   // CTA references -(m_r c)
+    float gnegT, gnegD;               // global references -(m c)
+    float MT, MD;                     // row maxima
+    float emaxT, emaxD;               // e of the unique maxima (global units)
+    int uT, uD;                       // unique maxima, or -1
+    float duT, tuD;                   // draft logit at uT, target logit at uD
+    double S, D, cbar;                // residual recursion
+    float aT, aD;                     // this CTA's sweep weights
+    float tot[kMaxCluster];           // per-CTA mass of the sampled distribution (global units)
+    float thr, base, unit;            // sampling threshold, mass before CTA rstar, its unit
+    int use_res, rstar, bad, pick;
+    int spec_x[2];                    // indices whose residual weight is exact, or -1
     float spec_w[2];                  // their exact weights
-    int bad;                          // a used row is not finite
-    int pick;                         // sampling: chosen thread
-    float pick_base;                  // sampling: mass before the chosen thread
-    RowD rT, rD;                      // fp64 row state (thread 0)
-    double S, D, cbar;                // residual recursion state (thread 0)
+    float pick_base;
 };
 
 }  // namespace
@@ -293,11 +312,12 @@ size_t node_smem_bytes(int units_per_cta) { return (size_t)units_per_cta * 16 * 
 namespace {
 
 // ------------------------------------------------------------------------
-// prep: one thread per request
+// prep: one warp per request
 
 __global__ void prep_kernel(Problem pb)
 {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (b >= pb.B) return;
     const int K = pb.K, L = pb.L, V = pb.V;
     const int Lb = pb.lengths ? pb.lengths[b] : L;
@@ -305,45 +325,44 @@ __global__ void prep_kernel(Problem pb)
     if (Lb < 0 || Lb > L) {
         st = SDV_REQ_BAD_LENGTH;
     } else {
-        for (int k = 0; k < K; ++k)
-            for (int j = 0; j < Lb; ++j) {
-                const int t = pb.tokens[((size_t)b * K + k) * L + j];
-                if (t < 0 || t >= V) st = SDV_REQ_BAD_TOKEN;
-            }
-    }
-    pb.ws.req[b] = st;
-    if (st) {
-        if (pb.device_status) atomicOr(pb.device_status, st);
-        return;
-    }
-    // owner[j][k]: lowest k2 whose first j tokens equal draft k's.  Drafts
-    // share a prefix of length j iff they share the one of length j-1 and
-    // token j-1.
-    unsigned char* own = pb.ws.owner + (size_t)b * (L + 1) * K;
-    for (int k = 0; k < K; ++k) own[k] = 0;
-    for (int j = 1; j <= Lb; ++j) {
-        for (int k = 0; k < K; ++k) {
-            const int tk = pb.tokens[((size_t)b * K + k) * L + j - 1];
-            int o = k;
-            for (int k2 = 0; k2 < k; ++k2) {
-                if (own[(j - 1) * K + k2] == own[(j - 1) * K + k] &&
-                    pb.tokens[((size_t)b * K + k2) * L + j - 1] == tk) {
-                    o = k2;
-                    break;
-                }
-            }
-            own[j * K + k] = (unsigned char)o;
+        int bad = 0;
+        for (int i = lane; i < K * Lb; i += 32) {
+            const int t = pb.tokens[((size_t)b * K + i / Lb) * L + i % Lb];
+            bad |= (t < 0 || t >= V);
         }
+        if (__any_sync(0xffffffffu, bad)) st = SDV_REQ_BAD_TOKEN;
     }
-    pb.ws.pbar[(size_t)b * (L + 1) * K] = 0.f;  // root weight 1
+    if (lane == 0) {
+        pb.ws.req[b] = st;
+        if (st && pb.device_status) atomicOr(pb.device_status, st);
+    }
+    if (st) return;
+    // owner[j][k] = lowest k2 whose first j tokens equal draft k's: drafts
+    // share a prefix of length j iff they share the one of length j-1 and
+    // token j-1.  Lane k holds draft k.
+    unsigned char* own = pb.ws.owner + (size_t)b * (L + 1) * K;
+    int o = 0;
+    if (lane < K) own[lane] = 0;
+    for (int j = 1; j <= Lb; ++j) {
+        const int tk = lane < K ? pb.tokens[((size_t)b * K + lane) * L + j - 1] : -1;
+        int no = lane;
+        for (int k2 = K - 1; k2 >= 0; --k2) {
+            const int o2 = __shfl_sync(0xffffffffu, o, k2);
+            const int t2 = __shfl_sync(0xffffffffu, tk, k2);
+            if (k2 <= lane && o2 == o && t2 == tk) no = k2;
+        }
+        o = no;
+        if (lane < K) own[j * K + lane] = (unsigned char)o;
+    }
+    if (lane == 0) pb.ws.pbar[(size_t)b * (L + 1) * K] = 0.f;  // root weight 1
 }
 
 // ------------------------------------------------------------------------
 // node kernel
 
-// Cluster-wide exchange: thread 0 of every CTA publishes n (<= 8) words
-// into slot [rank] of buffer `par` of every CTA; after the cluster barrier
-// each CTA reads all slots locally.
+// Cluster-wide exchange: thread 0 of every CTA publishes n words into slot
+// [rank] of buffer `par` of every CTA; after the cluster barrier each CTA
+// reads all slots locally.
 __device__ __forceinline__ void cluster_publish(cg::cluster_group& cl, NodeSmem* sm, int par, int rank, int C,
                                                 const float* v, int n)
 {
@@ -356,55 +375,15 @@ __device__ __forceinline__ void cluster_publish(cg::cluster_group& cl, NodeSmem*
     cl.sync();
 }
 
-// Block-wide sum of two ints and minimum of two ints (thread 0's result).
-__device__ void block_int4(int& s0, int& s1, int& m0, int& m1, int (*ired)[32])
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-        m0 = min(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-        m1 = min(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-    }
-    if (lane == 0) {
-        ired[0][warp] = s0;
-        ired[1][warp] = s1;
-        ired[2][warp] = m0;
-        ired[3][warp] = m1;
-    }
-    __syncthreads();
-    s0 = s1 = 0;
-    m0 = m1 = 0x7fffffff;
-    for (int w = 0; w < nw; ++w) {
-        s0 += ired[0][w];
-        s1 += ired[1][w];
-        m0 = min(m0, ired[2][w]);
-        m1 = min(m1, ired[3][w]);
-    }
-    __syncthreads();
-}
-
 // The residual term of one element as every sweep computes it, in fp32.
 __device__ __forceinline__ float res_term(float eT, float eD, float aT, float aD)
 {
     return fmaxf(__fmaf_rn(eT, aT, -__fmul_rn(eD, aD)), 0.f);
 }
 
-template <int DT>
-__device__ ProbD row_prob(const RowD& r, const char* g, int x, float c)
-{
-    ProbD o;
-    if (x == r.ux) {
-        o.P = (double)r.emax / r.z;
-        o.Pbar = r.zrest / r.z;
-    } else {
-        const float e = ex2(fmaf(Elem<DT>::load(g, x), c, r.neg));
-        o.P = (double)e / r.z;
-        o.Pbar = 1.0 - o.P;
-    }
-    return o;
-}
+struct ProbD {
+    double P, Pbar;
+};
 
 // alpha P(x) - beta Q(x) with alpha = 1 - pbar and beta = 1 + cbar, written
 // with complements so that nothing of order one cancels when P and Q are
@@ -412,6 +391,89 @@ __device__ ProbD row_prob(const RowD& r, const char* g, int x, float c)
 __device__ __forceinline__ double g_diff(const ProbD& P, const ProbD& Q, double pbar, double cbar)
 {
     return Q.Pbar - P.Pbar + pbar * P.Pbar + cbar * Q.Pbar - pbar - cbar;
+}
+
+// P(x) of the target row (is_t) or Q(x) of the draft row, in fp64, from the
+// logit at x.  The unique maximum uses the sum without it, so 1 - P is exact.
+__device__ __forceinline__ ProbD prob_at(const NodeSmem* sm, bool is_t, int x, float logit, float c)
+{
+    ProbD o;
+    const int u = is_t ? sm->uT : sm->uD;
+    const double z = is_t ? sm->zT : sm->zD;
+    if (x == u) {
+        o.P = (double)(is_t ? sm->emaxT : sm->emaxD) / z;
+        o.Pbar = (is_t ? sm->zrestT : sm->zrestD) / z;
+    } else {
+        o.P = (double)ex2(fmaf(logit, c, is_t ? sm->gnegT : sm->gnegD)) / z;
+        o.Pbar = 1.0 - o.P;
+    }
+    return o;
+}
+
+// Sweep weights of CTA r: P(x) = e_r(x) sclT_r / zT, Q likewise.
+__device__ __forceinline__ void sweep_weights(const NodeSmem* sm, int r, double p, double cbar, float& aT, float& aD)
+{
+    aT = (float)(p * sm->sclT[r] / sm->zT);
+    aD = (float)((1.0 + cbar) * sm->sclD[r] / sm->zD);
+}
+
+// Per-row fp64 state from the exchanged per-CTA statistics (thread 0).
+__device__ void row_state(NodeSmem* sm, const float (*xb)[12], int C, bool is_t, float c)
+{
+    const int iM = is_t ? X_MT : X_MD, iZ = is_t ? X_ZT : X_ZD, iN = is_t ? X_NT : X_ND;
+    const int iF = is_t ? X_FT : X_FD, iP = is_t ? X_PT : X_PD;
+    float M = -INFINITY;
+    for (int r = 0; r < C; ++r) M = max_nan(M, xb[r][iM]);
+    const float gneg = -(M * c);
+    double z = 0.0, zrest = 0.0, contrib_star = 0.0;
+    int nmax = 0, rstar = -1;
+    float emax = 0.f;
+    for (int r = 0; r < C; ++r) {
+        const float m = xb[r][iM];
+        const float neg = -(m * c);
+        const int n = __float_as_int(xb[r][iN]);
+        const double scl = exp2((double)(gneg - neg));  // exact shift between the references
+        double contrib = scl * (double)xb[r][iZ];
+        float em = 0.f;
+        if (n > 0) {
+            em = ex2(fmaf(m, c, neg));
+            contrib += scl * (double)n * (double)em;
+        }
+        if (is_t) {
+            sm->sclT[r] = scl;
+            sm->negT[r] = neg;
+        } else {
+            sm->sclD[r] = scl;
+            sm->negD[r] = neg;
+        }
+        z += contrib;
+        if (m == M && n > 0) {
+            nmax += n;
+            rstar = r;
+            emax = em;
+            contrib_star = scl * (double)xb[r][iZ];  // the CTA holding the maximum, without it
+        } else {
+            zrest += contrib;
+        }
+    }
+    const bool uniq = nmax == 1;
+    if (is_t) {
+        sm->MT = M;
+        sm->gnegT = gneg;
+        sm->zT = z;
+        sm->zrestT = zrest + contrib_star;
+        sm->emaxT = emax;
+        sm->uT = uniq ? __float_as_int(xb[rstar][iF]) : -1;
+        sm->duT = uniq ? xb[rstar][iP] : 0.f;
+    } else {
+        sm->MD = M;
+        sm->gnegD = gneg;
+        sm->zD = z;
+        sm->zrestD = zrest + contrib_star;
+        sm->emaxD = emax;
+        sm->uD = uniq ? __float_as_int(xb[rstar][iF]) : -1;
+        sm->tuD = uniq ? xb[rstar][iP] : 0.f;
+    }
 }
 
 template <int DT>
@@ -434,7 +496,8 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
     if (pb.ws.req[b] & (SDV_REQ_BAD_LENGTH | SDV_REQ_BAD_TOKEN)) return;
     const int Lb = pb.lengths ? pb.lengths[b] : L;
     if (j > Lb) return;
-    const size_t s = ((size_t)b * (L + 1) + j) * K + k;
+    const size_t sbase = ((size_t)b * (L + 1) + j) * K;
+    const size_t s = sbase + k;
     if (pb.ws.owner[s] != k) return;
     const bool leaf = j == Lb;
 
@@ -459,6 +522,7 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
         mbar_init(&sm->bar[0], 1);
         mbar_init(&sm->bar[1], 1);
         mbar_fence_init();
+        sm->firstT = sm->firstD = ~0ull;
     }
     __syncthreads();
     if (tid == 0 && nU > 0) {
@@ -476,9 +540,15 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
         }
     }
     if (rank == 0 && tid == 0) pb.ws.tok[s] = -1;
+    // logits at the drawn tokens, fetched while the slices land
+    if (!leaf && tid >= k && tid < K && pb.ws.owner[sbase + tid] == k) {
+        const int y = pb.tokens[((size_t)b * K + tid) * L + j];
+        sm->gT[tid] = E::load(gT, y);
+        sm->gD[tid] = E::load(gD, y);
+    }
 
     bool timed_out = false;
-    // ---- row maxima (NaN-propagating) ----
+    // ---- maxima of this CTA's slices (NaN-propagating) ----
     float mlT = -INFINITY, mlD = -INFINITY;
     if (nU > 0) {
         if (!mbar_wait_bounded(&sm->bar[0], 0)) timed_out = true;
@@ -505,146 +575,137 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
         }
     }
     float mT = mlT, mD = mlD;
-    block_max2(mT, mD, sm->red);
-    {
-        float v[2] = {mT, mD};
-        cluster_publish(cl, sm, 0, rank, C, v, 2);
-    }
-    mT = -INFINITY;
-    mD = -INFINITY;
-    for (int r = 0; r < C; ++r) {
-        mT = max_nan(mT, sm->xbuf[0][r][0]);
-        mD = max_nan(mD, sm->xbuf[0][r][1]);
-    }
+    block_max2(mT, mD, sm->redm);
     const float c = pb.c;
-    // e(x) = 2^(x c - m c): the shift by the rounded m c is common to the
-    // whole row and cancels in e(x) / sum e.
-    const float negT = -(mT * c);
-    const float negD = -(mD * c);
-    const float emaxT = ex2(fmaf(mT, c, negT));
-    const float emaxD = ex2(fmaf(mD, c, negD));
+    // this CTA's reference: e_r(x) = 2^(x c - m_r c)
+    const float nTr = -(mT * c);
+    const float nDr = -(mD * c);
+    const float emT = ex2(fmaf(mT, c, nTr));
 
-    // ---- softmax normalisers, the maxima counted apart ----
+    // ---- normalisers: the CTA maxima are counted apart ----
     float zT = 0.f, zD = 0.f;
-    int cntT = 0, cntD = 0, firstT = 0x7fffffff, firstD = 0x7fffffff;
-    if (mlT == mT) {  // this thread holds the target maximum
+    int cntT = 0, cntD = 0;
+    if (mlT == mT) {  // this thread holds the CTA's target maximum
+        int first = -1;
         for (int u = cu0; u < cu1; ++u) {
             float t[EPU];
             unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, t);
             for (int e = 0; e < EPU; ++e) {
                 if (t[e] == mT) {
-                    ++cntT;
-                    firstT = min(firstT, (u_base + u) * EPU + e);
+                    if (cntT++ == 0) first = u * EPU + e;
                 } else {
-                    zT += ex2(fmaf(t[e], c, negT));
+                    zT += ex2(fmaf(t[e], c, nTr));
                 }
             }
+        }
+        if (first >= 0) {
+            const float partner = leaf ? 0.f : [&] {
+                float d[EPU];
+                Elem<DT>::unpack(smD[first / EPU], d);
+                return d[first % EPU];
+            }();
+            atomicMin(&sm->firstT,
+                      ((unsigned long long)(u_base * EPU + first) << 32) | __float_as_uint(partner));
         }
     } else {
         for (int u = cu0; u < cu1; ++u) {
             float t[EPU];
             unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, t);
 #pragma unroll
-            for (int e = 0; e < EPU; ++e) zT += ex2(fmaf(t[e], c, negT));
+            for (int e = 0; e < EPU; ++e) zT += ex2(fmaf(t[e], c, nTr));
         }
     }
     if (!leaf) {
         if (mlD == mD) {
+            int first = -1;
             for (int u = cu0; u < cu1; ++u) {
                 float d[EPU];
                 unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, d);
                 for (int e = 0; e < EPU; ++e) {
                     if (d[e] == mD) {
-                        ++cntD;
-                        firstD = min(firstD, (u_base + u) * EPU + e);
+                        if (cntD++ == 0) first = u * EPU + e;
                     } else {
-                        zD += ex2(fmaf(d[e], c, negD));
+                        zD += ex2(fmaf(d[e], c, nDr));
                     }
                 }
+            }
+            if (first >= 0) {
+                float t[EPU];
+                Elem<DT>::unpack(smT[first / EPU], t);
+                atomicMin(&sm->firstD,
+                          ((unsigned long long)(u_base * EPU + first) << 32) | __float_as_uint(t[first % EPU]));
             }
         } else {
             for (int u = cu0; u < cu1; ++u) {
                 float d[EPU];
                 unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, d);
 #pragma unroll
-                for (int e = 0; e < EPU; ++e) zD += ex2(fmaf(d[e], c, negD));
+                for (int e = 0; e < EPU; ++e) zD += ex2(fmaf(d[e], c, nDr));
             }
         }
     }
-    sm->partT[tid] = zT + (float)cntT * emaxT;
-    block_sum2(zT, zD, sm->red);
-    block_int4(cntT, cntD, firstT, firstD, sm->ired);
+    sm->partT[tid] = zT + (float)cntT * emT;
+    block_sum_f2i2_t0(zT, zD, cntT, cntD, sm->red, sm->ired);
     {
-        float v[6] = {zT, zD, __int_as_float(cntT), __int_as_float(cntD), __int_as_float(firstT),
-                      __int_as_float(firstD)};
-        cluster_publish(cl, sm, 1, rank, C, v, 6);
+        const unsigned long long fT = sm->firstT, fD = sm->firstD;
+        float v[X_WORDS];
+        v[X_MT] = mT;
+        v[X_MD] = mD;
+        v[X_ZT] = zT;
+        v[X_ZD] = zD;
+        v[X_NT] = __int_as_float(cntT);
+        v[X_ND] = __int_as_float(cntD);
+        v[X_FT] = __int_as_float((int)(fT >> 32));
+        v[X_FD] = __int_as_float((int)(fD >> 32));
+        v[X_PT] = __uint_as_float((unsigned)(fT & 0xffffffffu));
+        v[X_PD] = __uint_as_float((unsigned)(fD & 0xffffffffu));
+        cluster_publish(cl, sm, 1, rank, C, v, X_WORDS);
     }
 
     // ---- scalar state (thread 0, fp64, kept in shared memory) ----
-    RowD& rT = sm->rT;
-    RowD& rD = sm->rD;
-    const double p_in = (j == 0 || pb.mode == SDV_MODE_TOKEN) ? 0.0 : (double)pb.ws.pbar[s];
-    const double pbar = p_in;
+    const double pbar = (j == 0 || pb.mode == SDV_MODE_TOKEN) ? 0.0 : (double)pb.ws.pbar[s];
     const double p = 1.0 - pbar;
     if (tid == 0) {
-        rT.zrest = rD.zrest = 0.0;
-        rT.n = rD.n = 0;
-        int fT = 0x7fffffff, fD = 0x7fffffff;
+        row_state(sm, sm->xbuf[1], C, true, c);
+        if (!leaf) row_state(sm, sm->xbuf[1], C, false, c);
+        float MT = -INFINITY, MD = -INFINITY;
         for (int r = 0; r < C; ++r) {
-            rT.zrest += (double)sm->xbuf[1][r][0];
-            rD.zrest += (double)sm->xbuf[1][r][1];
-            rT.n += __float_as_int(sm->xbuf[1][r][2]);
-            rD.n += __float_as_int(sm->xbuf[1][r][3]);
-            fT = min(fT, __float_as_int(sm->xbuf[1][r][4]));
-            fD = min(fD, __float_as_int(sm->xbuf[1][r][5]));
+            MT = max_nan(MT, sm->xbuf[1][r][X_MT]);
+            MD = max_nan(MD, sm->xbuf[1][r][X_MD]);
         }
-        rT.emax = emaxT;
-        rD.emax = emaxD;
-        rT.neg = negT;
-        rD.neg = negD;
-        rT.z = rT.n * (double)emaxT + rT.zrest;
-        rD.z = rD.n * (double)emaxD + rD.zrest;
-        rT.ux = rT.n == 1 ? fT : -1;
-        rD.ux = rD.n == 1 ? fD : -1;
-        const bool bad = !(isfinite(mT) && isfinite(rT.z) && rT.z > 0.0) ||
-                         (!leaf && !(isfinite(mD) && isfinite(rD.z) && rD.z > 0.0));
+        const bool bad = !(isfinite(MT) && isfinite(sm->zT) && sm->zT > 0.0) ||
+                         (!leaf && !(isfinite(MD) && isfinite(sm->zD) && sm->zD > 0.0));
         sm->bad = bad;
         if (bad && rank == 0) {
             atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
             if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
         }
-        sm->spec_x[0] = leaf ? -1 : rT.ux;
-        sm->spec_x[1] = (leaf || rD.ux == rT.ux) ? -1 : rD.ux;
+        sm->spec_x[0] = leaf ? -1 : sm->uT;
+        sm->spec_x[1] = (leaf || sm->uD == sm->uT) ? -1 : sm->uD;
         sm->spec_w[0] = sm->spec_w[1] = 0.f;
-        for (int r = 0; r < C; ++r)
-            sm->tot[r] = sm->xbuf[1][r][0] + (float)__float_as_int(sm->xbuf[1][r][2]) * emaxT;
         sm->use_res = 0;
+        sm->S = p;
+        sm->D = 1.0;
+        sm->cbar = 0.0;
     }
 
     // ---- residual recursion over the draws of the drafts through the node ----
     // R_j = max(p P - C_j Q, 0), S_j = sum R_j, D_j = 1 - p + S_j,
-    // C_1 = 1, C_{j+1} = C_j + D_j.  Thread 0 keeps the scalars in fp64 as
-    // pbar = 1 - p and cbar = C_j - 1.
-    double& S = sm->S;
-    double& D = sm->D;
-    double& cbar = sm->cbar;
-    if (tid == 0) {
-        S = p;
-        D = 1.0;
-        cbar = 0.0;
-    }
+    // C_1 = 1, C_{j+1} = C_j + D_j; thread 0 keeps pbar = 1 - p and
+    // cbar = C_j - 1 in fp64.
     int par = 1;
-    bool first = true;
+    bool first_draw = true;
     if (!leaf) {
         for (int k2 = k; k2 < K; ++k2) {
-            if (pb.ws.owner[((size_t)b * (L + 1) + j) * K + k2] != k) continue;
+            if (pb.ws.owner[sbase + k2] != k) continue;
             if (tid == 0) {
                 const int y = pb.tokens[((size_t)b * K + k2) * L + j];
-                const ProbD Py = row_prob<DT>(rT, gT, y, c);
-                const ProbD Qy = row_prob<DT>(rD, gD, y, c);
-                // R_{j-1}(y): C_0 = 0 for the first draw
-                const double R = first ? p * Py.P : fmax(g_diff(Py, Qy, pbar, cbar), 0.0);
-                const double cnew = first ? 0.0 : cbar + D;
+                const ProbD Py = prob_at(sm, true, y, sm->gT[k2], c);
+                const ProbD Qy = prob_at(sm, false, y, sm->gD[k2], c);
+                const double D = sm->D;
+                // R_{j-1}(y); C_0 = 0 for the first draw
+                const double R = first_draw ? p * Py.P : fmax(g_diff(Py, Qy, pbar, sm->cbar), 0.0);
+                const double cnew = first_draw ? 0.0 : sm->cbar + D;
                 const double denom = D * Qy.P;
                 double a, abar;
                 if (!(denom > 0.0) || R >= denom) {
@@ -658,16 +719,18 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                     // 1 - a = (C_j Q(y) - p P(y)) / (D Q(y))
                     abar = fmin(fmax(-g_diff(Py, Qy, pbar, cnew), 0.0) / denom, 1.0);
                 }
-                cbar = cnew;
+                sm->cbar = cnew;
                 if (rank == 0) {
-                    pb.ws.a[((size_t)b * (L + 1) + j) * K + k2] = (float)a;
+                    pb.ws.a[sbase + k2] = (float)a;
                     if (pb.mode != SDV_MODE_TOKEN) {
-                        const size_t sc = ((size_t)b * (L + 1) + j + 1) * K + k2;
+                        const size_t sc = sbase + K + k2;
                         if (pb.ws.owner[sc] == k2) pb.ws.pbar[sc] = (float)abar;  // child first reached here
                     }
                 }
-                sm->aT = (float)(p / rT.z);
-                sm->aD = (float)((1.0 + cbar) / rD.z);
+                float wT, wD;
+                sweep_weights(sm, rank, p, cnew, wT, wD);
+                sm->aT = wT;
+                sm->aD = wD;
             }
             __syncthreads();
             const float aT = sm->aT, aD = sm->aD;
@@ -677,17 +740,16 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                 unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, t);
                 unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, d);
 #pragma unroll
-                for (int e = 0; e < EPU; ++e)
-                    w += res_term(ex2(fmaf(t[e], c, negT)), ex2(fmaf(d[e], c, negD)), aT, aD);
+                for (int e = 0; e < EPU; ++e) w += res_term(ex2(fmaf(t[e], c, nTr)), ex2(fmaf(d[e], c, nDr)), aT, aD);
             }
             sm->part[tid] = w;
-            float dummy = 0.f;
-            block_sum2(w, dummy, sm->red);
+            w = block_sum_t0(w, sm->red);
             par ^= 1;
             cluster_publish(cl, sm, par, rank, C, &w, 1);
             if (tid == 0) {
-                // fp32 sweep sums, with the dominant tokens' terms replaced
-                // by their exact values
+                // fp32 sweep sums with the dominant tokens' terms replaced by
+                // their exact values
+                const double cbar = sm->cbar;
                 double Sj = 0.0;
                 for (int r = 0; r < C; ++r) {
                     Sj += (double)sm->xbuf[par][r][0];
@@ -696,39 +758,43 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                 for (int i = 0; i < 2; ++i) {
                     const int x = sm->spec_x[i];
                     if (x < 0) continue;
-                    const ProbD Px = row_prob<DT>(rT, gT, x, c);
-                    const ProbD Qx = row_prob<DT>(rD, gD, x, c);
-                    const double exact = fmax(g_diff(Px, Qx, pbar, cbar), 0.0);
-                    const float f32 = res_term(ex2(fmaf(E::load(gT, x), c, negT)),
-                                               ex2(fmaf(E::load(gD, x), c, negD)), aT, aD);
+                    const float t_x = x == sm->uT ? sm->MT : sm->tuD;
+                    const float d_x = x == sm->uD ? sm->MD : sm->duT;
+                    const double exact = fmax(g_diff(prob_at(sm, true, x, t_x, c), prob_at(sm, false, x, d_x, c),
+                                                     pbar, cbar), 0.0);
+                    const int rx = (x / EPU) / sh.units_per_cta;
+                    float wT, wD;
+                    sweep_weights(sm, rx, p, cbar, wT, wD);
+                    const float f32 = res_term(ex2(fmaf(t_x, c, sm->negT[rx])), ex2(fmaf(d_x, c, sm->negD[rx])), wT, wD);
                     Sj += exact - (double)f32;
                     sm->spec_w[i] = (float)exact;
-                    const int rx = (x / EPU) / sh.units_per_cta;
                     sm->tot[rx] += (float)exact - f32;
-                    if (rx == rank) {
-                        const int tx = ((x / EPU) - u_base) / sh.units_per_thr;
-                        sm->part[tx] += (float)exact - f32;
-                    }
+                    if (rx == rank) sm->part[((x / EPU) - u_base) / sh.units_per_thr] += (float)exact - f32;
                 }
-                S = fmax(Sj, 0.0);
-                D = pbar + S;
-                sm->use_res = S > 0.0;
+                sm->S = fmax(Sj, 0.0);
+                sm->D = pbar + sm->S;
+                sm->use_res = sm->S > 0.0;
             }
-            first = false;
+            first_draw = false;
         }
     }
 
     // ---- node outputs and the candidate correction ----
     if (tid == 0) {
+        const double S = sm->S, D = sm->D;
         const double h = leaf ? p : (D > 0.0 ? S / D : 1.0);
         if (rank == 0) {
             pb.ws.h[s] = (float)h;
             pb.ws.S[s] = (float)S;
         }
         if (!sm->use_res) {
-            // sample P: per-CTA target mass
-            for (int r = 0; r < C; ++r)
-                sm->tot[r] = sm->xbuf[1][r][0] + (float)__float_as_int(sm->xbuf[1][r][2]) * emaxT;
+            // sample P: per-CTA target mass in global units
+            for (int r = 0; r < C; ++r) {
+                const int n = __float_as_int(sm->xbuf[1][r][X_NT]);
+                const float m = sm->xbuf[1][r][X_MT];
+                const float em = n > 0 ? ex2(fmaf(m, c, sm->negT[r])) : 0.f;
+                sm->tot[r] = (float)(sm->sclT[r] * ((double)sm->xbuf[1][r][X_ZT] + (double)n * (double)em));
+            }
         }
         float Stot = 0.f;
         for (int r = 0; r < C; ++r) Stot += sm->tot[r];
@@ -753,15 +819,18 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
             base = last_base;
         }
         sm->rstar = sm->bad ? -1 : rstar;
-        sm->base = base;
         sm->thr = thr;
+        sm->base = base;
+        // the residual partials are in probability units; the target
+        // partials in units of CTA rstar's reference
+        sm->unit = (sm->use_res || rstar < 0) ? 1.f : (float)sm->sclT[rstar];
     }
     __syncthreads();
     const bool use_res = sm->use_res != 0;
     const int rstar = sm->rstar;
     if (rank == rstar) {
         const float* parts = use_res ? sm->part : sm->partT;
-        const float local = sm->thr - sm->base;
+        const float local = (sm->thr - sm->base) / sm->unit;
         // warp 0 finds the first thread whose running mass exceeds `local`
         if (tid < 32) {
             const int nthr = blockDim.x;
@@ -783,15 +852,15 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
             int tsel = -1;
             float tbase = 0.f;
             if (tid == l) {
-                float run = excl;
+                float acc = excl;
                 for (int t = t0; t < t1; ++t) {
                     if (parts[t] > 0.f) {
-                        const bool hit = run + parts[t] > local;
+                        const bool hit = acc + parts[t] > local;
                         tsel = t;
-                        tbase = run;
+                        tbase = acc;
                         if (hit && cm) break;
                     }
-                    run += parts[t];
+                    acc += parts[t];
                 }
             }
             if (l >= 0) {
@@ -806,7 +875,7 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
         __syncthreads();
         if (tid == sm->pick) {
             const float aT = sm->aT, aD = sm->aD;
-            float run = sm->pick_base;
+            float acc = sm->pick_base;
             int chosen = -1, last = -1;
             for (int uu = cu0; uu < cu1 && chosen < 0; ++uu) {
                 float t[EPU], d[EPU];
@@ -814,14 +883,14 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                 if (use_res) unpack_masked<DT>(smD[uu], (u_base + uu) * EPU, V, d);
                 for (int e = 0; e < EPU; ++e) {
                     const int x = (u_base + uu) * EPU + e;
-                    const float eT = ex2(fmaf(t[e], c, negT));
-                    float wx = use_res ? res_term(eT, ex2(fmaf(d[e], c, negD)), aT, aD) : eT;
+                    const float eT = ex2(fmaf(t[e], c, nTr));
+                    float wx = use_res ? res_term(eT, ex2(fmaf(d[e], c, nDr)), aT, aD) : eT;
                     if (use_res && x == sm->spec_x[0]) wx = sm->spec_w[0];
                     if (use_res && x == sm->spec_x[1]) wx = sm->spec_w[1];
                     if (wx > 0.f) {
-                        run += wx;
+                        acc += wx;
                         last = x;
-                        if (run > local) {
+                        if (acc > local) {
                             chosen = x;
                             break;
                         }
@@ -920,60 +989,94 @@ __global__ void __launch_bounds__(256) argmax_kernel(Problem pb)
 }
 
 // ------------------------------------------------------------------------
-// decision: one thread per request
+// decision: one warp per request; the request's node records are copied to
+// shared memory first, then lane 0 walks them
 
-__global__ void decide_kernel(Problem pb, int greedy)
+constexpr int kDecideWarps = 4;
+constexpr int kSlotsMax = (SDV_MAX_L + 1) * SDV_MAX_K;
+
+__global__ void __launch_bounds__(32 * kDecideWarps) decide_kernel(Problem pb, int greedy)
 {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    __shared__ unsigned char s_own[kDecideWarps][kSlotsMax];
+    __shared__ float s_val[kDecideWarps][kSlotsMax];  // a (token), h (block) or argmax bits (greedy)
+    __shared__ float s_u[kDecideWarps][SDV_MAX_K * SDV_MAX_L];
+    __shared__ int s_tok[kDecideWarps][SDV_MAX_K * SDV_MAX_L];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int b = blockIdx.x * kDecideWarps + w;
     if (b >= pb.B) return;
     const int K = pb.K, L = pb.L;
     const int st = pb.ws.req[b];
     float* ap = pb.accept_prob ? pb.accept_prob + (size_t)b * K * L : nullptr;
-    if (ap)
-        for (int i = 0; i < K * L; ++i) ap[i] = 0.f;
     if (st) {
-        pb.accept_len[b] = 0;
-        pb.accept_draft[b] = 0;
-        pb.out_token[b] = -1;
-        if (pb.residual_mass) pb.residual_mass[b] = 0.f;
-        if (pb.device_status) atomicOr(pb.device_status, st);
+        if (ap)
+            for (int i = lane; i < K * L; i += 32) ap[i] = 0.f;
+        if (lane == 0) {
+            pb.accept_len[b] = 0;
+            pb.accept_draft[b] = 0;
+            pb.out_token[b] = -1;
+            if (pb.residual_mass) pb.residual_mass[b] = 0.f;
+            if (pb.device_status) atomicOr(pb.device_status, st);
+        }
         return;
     }
     const int Lb = pb.lengths ? pb.lengths[b] : L;
-    const unsigned char* own = pb.ws.owner + (size_t)b * (L + 1) * K;
-    auto S = [&](int j, int k) { return ((size_t)b * (L + 1) + j) * K + k; };
+    const size_t s0 = (size_t)b * (L + 1) * K;
+    const bool token = pb.mode == SDV_MODE_TOKEN;
+    unsigned char* own = s_own[w];
+    float* val = s_val[w];
+    float* uu = s_u[w];
+    int* tk = s_tok[w];
+    for (int i = lane; i < (Lb + 1) * K; i += 32) {
+        own[i] = pb.ws.owner[s0 + i];
+        val[i] = greedy ? __int_as_float(pb.ws.am[s0 + i]) : (token ? pb.ws.a[s0 + i] : pb.ws.h[s0 + i]);
+    }
+    for (int i = lane; i < K * L; i += 32) {
+        tk[i] = pb.tokens[(size_t)b * K * L + i];
+        uu[i] = greedy ? 0.f : pb.accept_u[(size_t)b * K * L + i];
+    }
+    __syncwarp();
+    // accept_prob[k][d]: the threshold draft k's position d is tested against
+    if (ap) {
+        for (int i = lane; i < K * L; i += 32) {
+            const int kk = i / L, d = i % L;
+            float v = 0.f;
+            if (d < Lb) {
+                if (greedy)
+                    v = tk[i] == __float_as_int(val[d * K + own[d * K + kk]]) ? 1.f : 0.f;
+                else if (token)
+                    v = val[d * K + kk];
+                else
+                    v = val[(d + 1) * K + own[(d + 1) * K + kk]];
+            }
+            ap[i] = v;
+        }
+    }
+    if (lane != 0) return;
     int ej = 0, eo = 0;
     if (greedy) {
         int best = -1, bestk = 0;
-        for (int k = 0; k < K; ++k) {
+        for (int kk = 0; kk < K; ++kk) {
             int m = 0;
-            while (m < Lb && pb.tokens[((size_t)b * K + k) * L + m] == pb.ws.am[S(m, own[m * K + k])]) ++m;
+            while (m < Lb && tk[kk * L + m] == __float_as_int(val[m * K + own[m * K + kk]])) ++m;
             if (m > best) {
                 best = m;
-                bestk = k;
+                bestk = kk;
             }
-            if (ap)
-                for (int d = 0; d < Lb; ++d)
-                    ap[k * L + d] =
-                        pb.tokens[((size_t)b * K + k) * L + d] == pb.ws.am[S(d, own[d * K + k])] ? 1.f : 0.f;
         }
         ej = best;
         eo = own[best * K + bestk];
         pb.accept_len[b] = best;
         pb.accept_draft[b] = bestk;
-        pb.out_token[b] = pb.ws.am[S(ej, eo)];
+        pb.out_token[b] = __float_as_int(val[ej * K + eo]);
         if (pb.residual_mass) pb.residual_mass[b] = 1.f;
         return;
     }
-    if (pb.mode == SDV_MODE_TOKEN) {
-        if (ap)
-            for (int k = 0; k < K; ++k)
-                for (int d = 0; d < Lb; ++d) ap[k * L + d] = pb.ws.a[S(d, k)];
+    if (token) {
         int j = 0, o = 0;
         while (j < Lb) {
             int acc = -1;
-            for (int k = 0; k < K && acc < 0; ++k)
-                if (own[j * K + k] == o && pb.accept_u[((size_t)b * K + k) * L + j] <= pb.ws.a[S(j, k)]) acc = k;
+            for (int kk = 0; kk < K && acc < 0; ++kk)
+                if (own[j * K + kk] == o && uu[kk * L + j] <= val[j * K + kk]) acc = kk;
             if (acc < 0) break;
             o = own[(j + 1) * K + acc];
             ++j;
@@ -981,17 +1084,13 @@ __global__ void decide_kernel(Problem pb, int greedy)
         ej = j;
         eo = o;
     } else {
-        if (ap)
-            for (int k = 0; k < K; ++k)
-                for (int d = 0; d < Lb; ++d) ap[k * L + d] = pb.ws.h[S(d + 1, own[(d + 1) * K + k])];
-        // depth-first: children in order of first appearance, then the
+        // depth first: children in order of first appearance, then the
         // node's own test; the first accepted node ends the search
         int stk_o[SDV_MAX_L + 1], stk_next[SDV_MAX_L + 1];
         int top = 0;
         stk_o[0] = 0;
         stk_next[0] = 0;
-        bool done = false;
-        while (!done) {
+        for (;;) {
             const int jj = top, o = stk_o[top];
             int child = -1;
             if (jj < Lb) {
@@ -1012,20 +1111,20 @@ __global__ void decide_kernel(Problem pb, int greedy)
             if (jj == 0) {
                 ej = 0;
                 eo = 0;
-                done = true;
-            } else if (pb.accept_u[((size_t)b * K + o) * L + jj - 1] <= pb.ws.h[S(jj, o)]) {
+                break;
+            }
+            if (uu[o * L + jj - 1] <= val[jj * K + o]) {
                 ej = jj;
                 eo = o;
-                done = true;
-            } else {
-                --top;
+                break;
             }
+            --top;
         }
     }
     pb.accept_len[b] = ej;
     pb.accept_draft[b] = eo;
-    pb.out_token[b] = pb.ws.tok[S(ej, eo)];
-    if (pb.residual_mass) pb.residual_mass[b] = pb.ws.S[S(ej, eo)];
+    pb.out_token[b] = pb.ws.tok[s0 + (size_t)ej * K + eo];
+    if (pb.residual_mass) pb.residual_mass[b] = pb.ws.S[s0 + (size_t)ej * K + eo];
 }
 
 }  // namespace
@@ -1035,8 +1134,8 @@ __global__ void decide_kernel(Problem pb, int greedy)
 
 cudaError_t launch_prep(const Problem& pb, cudaStream_t st)
 {
-    const int threads = 128;
-    prep_kernel<<<(pb.B + threads - 1) / threads, threads, 0, st>>>(pb);
+    const int warps = 4;  // one warp per request
+    prep_kernel<<<(pb.B + warps - 1) / warps, 32 * warps, 0, st>>>(pb);
     return cudaGetLastError();
 }
 
@@ -1089,8 +1188,7 @@ cudaError_t launch_argmax(const Problem& pb, cudaStream_t st)
 
 cudaError_t launch_decide(const Problem& pb, bool greedy, cudaStream_t st)
 {
-    const int threads = 128;
-    decide_kernel<<<(pb.B + threads - 1) / threads, threads, 0, st>>>(pb, greedy ? 1 : 0);
+    decide_kernel<<<(pb.B + kDecideWarps - 1) / kDecideWarps, 32 * kDecideWarps, 0, st>>>(pb, greedy ? 1 : 0);
     return cudaGetLastError();
 }
 
