@@ -285,17 +285,17 @@ struct NodeSmem {
     unsigned long long firstT, firstD;  // (first index of the CTA maximum << 32) | partner logit bits
     uint64_t bar[2];                  // row-slice mbarriers
     float gT[SDV_MAX_K], gD[SDV_MAX_K];  // target / draft logits at each draft's drawn token
-    // scalar state of thread 0 (fp64 where it matters)
-    double zT, zD;                    // normalisers, in units of the row's global reference
-    double zrestT, zrestD;            // the same without the unique maximum
-    double sclT[kMaxCluster], sclD[kMaxCluster];  // CTA r's unit 2^(x c - m_r c) in global units
+    // scalar state of thread 0
+    float zT, zD;                     // normalisers, in units of the row's global reference
+    float zrestT, zrestD;             // the same without the unique maximum
+    float sclT[kMaxCluster], sclD[kMaxCluster];  // CTA r's unit 2^(x c - m_r c) in global units
     float negT[kMaxCluster], negD[kMaxCluster];   // CTA references -(m_r c)
     float gnegT, gnegD;               // global references -(m c)
     float MT, MD;                     // row maxima
     float emaxT, emaxD;               // e of the unique maxima (global units)
     int uT, uD;                       // unique maxima, or -1
     float duT, tuD;                   // draft logit at uT, target logit at uD
-    double S, D, cbar;                // residual recursion
+    float S, D, cbar;                 // residual recursion
     float aT, aD;                     // this CTA's sweep weights
     float tot[kMaxCluster];           // per-CTA mass of the sampled distribution (global units)
     float thr, base, unit;            // sampling threshold, mass before CTA rstar, its unit
@@ -382,15 +382,18 @@ __device__ __forceinline__ float res_term(float eT, float eD, float aT, float aD
 }
 
 struct ProbD {
-    double P, Pbar;
+    float P, Pbar;
 };
 
-// alpha P(x) - beta Q(x) with alpha = 1 - pbar and beta = 1 + cbar, written
-// with complements so that nothing of order one cancels when P and Q are
-// both close to 1.
-__device__ __forceinline__ double g_diff(const ProbD& P, const ProbD& Q, double pbar, double cbar)
+// alpha P(x) - beta Q(x) with alpha = 1 - pbar and beta = 1 + cbar.  For a
+// row's dominant token it is written with complements, so that nothing of
+// order one cancels when P and Q are both close to 1; the complements are
+// small and fp32 keeps their relative precision.  Elsewhere P and Q are at
+// most 1/2 and the direct form is the accurate one.
+__device__ __forceinline__ float g_diff(const ProbD& P, const ProbD& Q, float pbar, float cbar, bool dominant)
 {
-    return Q.Pbar - P.Pbar + pbar * P.Pbar + cbar * Q.Pbar - pbar - cbar;
+    if (dominant) return (((Q.Pbar - P.Pbar) + pbar * P.Pbar) + cbar * Q.Pbar) - (pbar + cbar);
+    return (1.f - pbar) * P.P - (1.f + cbar) * Q.P;
 }
 
 // P(x) of the target row (is_t) or Q(x) of the draft row, in fp64, from the
@@ -399,25 +402,26 @@ __device__ __forceinline__ ProbD prob_at(const NodeSmem* sm, bool is_t, int x, f
 {
     ProbD o;
     const int u = is_t ? sm->uT : sm->uD;
-    const double z = is_t ? sm->zT : sm->zD;
+    const float z = is_t ? sm->zT : sm->zD;
     if (x == u) {
-        o.P = (double)(is_t ? sm->emaxT : sm->emaxD) / z;
+        o.P = (is_t ? sm->emaxT : sm->emaxD) / z;
         o.Pbar = (is_t ? sm->zrestT : sm->zrestD) / z;
     } else {
-        o.P = (double)ex2(fmaf(logit, c, is_t ? sm->gnegT : sm->gnegD)) / z;
-        o.Pbar = 1.0 - o.P;
+        o.P = ex2(fmaf(logit, c, is_t ? sm->gnegT : sm->gnegD)) / z;
+        o.Pbar = 1.f - o.P;
     }
     return o;
 }
 
 // Sweep weights of CTA r: P(x) = e_r(x) sclT_r / zT, Q likewise.
-__device__ __forceinline__ void sweep_weights(const NodeSmem* sm, int r, double p, double cbar, float& aT, float& aD)
+__device__ __forceinline__ void sweep_weights(const NodeSmem* sm, int r, float p, float cbar, float& aT, float& aD)
 {
-    aT = (float)(p * sm->sclT[r] / sm->zT);
-    aD = (float)((1.0 + cbar) * sm->sclD[r] / sm->zD);
+    aT = p * sm->sclT[r] / sm->zT;
+    aD = (1.f + cbar) * sm->sclD[r] / sm->zD;
 }
 
-// Per-row fp64 state from the exchanged per-CTA statistics (thread 0).
+// Per-row state from the exchanged per-CTA statistics (thread 0).  Every
+// sum is of nonnegative terms, so fp32 keeps its relative precision.
 __device__ void row_state(NodeSmem* sm, const float (*xb)[12], int C, bool is_t, float c)
 {
     const int iM = is_t ? X_MT : X_MD, iZ = is_t ? X_ZT : X_ZD, iN = is_t ? X_NT : X_ND;
@@ -425,19 +429,21 @@ __device__ void row_state(NodeSmem* sm, const float (*xb)[12], int C, bool is_t,
     float M = -INFINITY;
     for (int r = 0; r < C; ++r) M = max_nan(M, xb[r][iM]);
     const float gneg = -(M * c);
-    double z = 0.0, zrest = 0.0, contrib_star = 0.0;
+    float z = 0.f, zrest = 0.f, contrib_star = 0.f;
     int nmax = 0, rstar = -1;
     float emax = 0.f;
     for (int r = 0; r < C; ++r) {
         const float m = xb[r][iM];
         const float neg = -(m * c);
         const int n = __float_as_int(xb[r][iN]);
-        const double scl = exp2((double)(gneg - neg));  // exact shift between the references
-        double contrib = scl * (double)xb[r][iZ];
+        // shift between the references (gneg - neg is exact when the two
+        // maxima are close, which is when the CTA's mass matters)
+        const float scl = n > 0 || xb[r][iZ] > 0.f ? ex2(gneg - neg) : 0.f;
+        float contrib = scl * xb[r][iZ];
         float em = 0.f;
         if (n > 0) {
             em = ex2(fmaf(m, c, neg));
-            contrib += scl * (double)n * (double)em;
+            contrib += scl * (float)n * em;
         }
         if (is_t) {
             sm->sclT[r] = scl;
@@ -451,7 +457,7 @@ __device__ void row_state(NodeSmem* sm, const float (*xb)[12], int C, bool is_t,
             nmax += n;
             rstar = r;
             emax = em;
-            contrib_star = scl * (double)xb[r][iZ];  // the CTA holding the maximum, without it
+            contrib_star = scl * xb[r][iZ];  // the CTA holding the maximum, without it
         } else {
             zrest += contrib;
         }
@@ -662,9 +668,9 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
         cluster_publish(cl, sm, 1, rank, C, v, X_WORDS);
     }
 
-    // ---- scalar state (thread 0, fp64, kept in shared memory) ----
-    const double pbar = (j == 0 || pb.mode == SDV_MODE_TOKEN) ? 0.0 : (double)pb.ws.pbar[s];
-    const double p = 1.0 - pbar;
+    // ---- scalar state (thread 0, kept in shared memory) ----
+    const float pbar = (j == 0 || pb.mode == SDV_MODE_TOKEN) ? 0.f : pb.ws.pbar[s];
+    const float p = 1.f - pbar;
     if (tid == 0) {
         row_state(sm, sm->xbuf[1], C, true, c);
         if (!leaf) row_state(sm, sm->xbuf[1], C, false, c);
@@ -673,8 +679,8 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
             MT = max_nan(MT, sm->xbuf[1][r][X_MT]);
             MD = max_nan(MD, sm->xbuf[1][r][X_MD]);
         }
-        const bool bad = !(isfinite(MT) && isfinite(sm->zT) && sm->zT > 0.0) ||
-                         (!leaf && !(isfinite(MD) && isfinite(sm->zD) && sm->zD > 0.0));
+        const bool bad = !(isfinite(MT) && isfinite(sm->zT) && sm->zT > 0.f) ||
+                         (!leaf && !(isfinite(MD) && isfinite(sm->zD) && sm->zD > 0.f));
         sm->bad = bad;
         if (bad && rank == 0) {
             atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
@@ -685,14 +691,14 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
         sm->spec_w[0] = sm->spec_w[1] = 0.f;
         sm->use_res = 0;
         sm->S = p;
-        sm->D = 1.0;
-        sm->cbar = 0.0;
+        sm->D = 1.f;
+        sm->cbar = 0.f;
     }
 
     // ---- residual recursion over the draws of the drafts through the node ----
     // R_j = max(p P - C_j Q, 0), S_j = sum R_j, D_j = 1 - p + S_j,
     // C_1 = 1, C_{j+1} = C_j + D_j; thread 0 keeps pbar = 1 - p and
-    // cbar = C_j - 1 in fp64.
+    // cbar = C_j - 1, which stay accurate where p -> 1 and C -> 1.
     int par = 1;
     bool first_draw = true;
     if (!leaf) {
@@ -702,29 +708,30 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                 const int y = pb.tokens[((size_t)b * K + k2) * L + j];
                 const ProbD Py = prob_at(sm, true, y, sm->gT[k2], c);
                 const ProbD Qy = prob_at(sm, false, y, sm->gD[k2], c);
-                const double D = sm->D;
+                const bool dom = y == sm->uT || y == sm->uD;
+                const float D = sm->D;
                 // R_{j-1}(y); C_0 = 0 for the first draw
-                const double R = first_draw ? p * Py.P : fmax(g_diff(Py, Qy, pbar, sm->cbar), 0.0);
-                const double cnew = first_draw ? 0.0 : sm->cbar + D;
-                const double denom = D * Qy.P;
-                double a, abar;
-                if (!(denom > 0.0) || R >= denom) {
-                    a = 1.0;
-                    abar = 0.0;
-                } else if (!(R > 0.0)) {
-                    a = 0.0;
-                    abar = 1.0;
+                const float R = first_draw ? p * Py.P : fmaxf(g_diff(Py, Qy, pbar, sm->cbar, dom), 0.f);
+                const float cnew = first_draw ? 0.f : sm->cbar + D;
+                const float denom = D * Qy.P;
+                float a, abar;
+                if (!(denom > 0.f) || R >= denom) {
+                    a = 1.f;
+                    abar = 0.f;
+                } else if (!(R > 0.f)) {
+                    a = 0.f;
+                    abar = 1.f;
                 } else {
                     a = R / denom;
                     // 1 - a = (C_j Q(y) - p P(y)) / (D Q(y))
-                    abar = fmin(fmax(-g_diff(Py, Qy, pbar, cnew), 0.0) / denom, 1.0);
+                    abar = fminf(fmaxf(-g_diff(Py, Qy, pbar, cnew, dom), 0.f) / denom, 1.f);
                 }
                 sm->cbar = cnew;
                 if (rank == 0) {
-                    pb.ws.a[sbase + k2] = (float)a;
+                    pb.ws.a[sbase + k2] = a;
                     if (pb.mode != SDV_MODE_TOKEN) {
                         const size_t sc = sbase + K + k2;
-                        if (pb.ws.owner[sc] == k2) pb.ws.pbar[sc] = (float)abar;  // child first reached here
+                        if (pb.ws.owner[sc] == k2) pb.ws.pbar[sc] = abar;  // child first reached here
                     }
                 }
                 float wT, wD;
@@ -749,10 +756,10 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
             if (tid == 0) {
                 // fp32 sweep sums with the dominant tokens' terms replaced by
                 // their exact values
-                const double cbar = sm->cbar;
-                double Sj = 0.0;
+                const float cbar = sm->cbar;
+                float Sj = 0.f;
                 for (int r = 0; r < C; ++r) {
-                    Sj += (double)sm->xbuf[par][r][0];
+                    Sj += sm->xbuf[par][r][0];
                     sm->tot[r] = sm->xbuf[par][r][0];
                 }
                 for (int i = 0; i < 2; ++i) {
@@ -760,20 +767,20 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                     if (x < 0) continue;
                     const float t_x = x == sm->uT ? sm->MT : sm->tuD;
                     const float d_x = x == sm->uD ? sm->MD : sm->duT;
-                    const double exact = fmax(g_diff(prob_at(sm, true, x, t_x, c), prob_at(sm, false, x, d_x, c),
-                                                     pbar, cbar), 0.0);
+                    const float exact = fmaxf(g_diff(prob_at(sm, true, x, t_x, c), prob_at(sm, false, x, d_x, c),
+                                                     pbar, cbar, true), 0.f);
                     const int rx = (x / EPU) / sh.units_per_cta;
                     float wT, wD;
                     sweep_weights(sm, rx, p, cbar, wT, wD);
                     const float f32 = res_term(ex2(fmaf(t_x, c, sm->negT[rx])), ex2(fmaf(d_x, c, sm->negD[rx])), wT, wD);
-                    Sj += exact - (double)f32;
-                    sm->spec_w[i] = (float)exact;
-                    sm->tot[rx] += (float)exact - f32;
-                    if (rx == rank) sm->part[((x / EPU) - u_base) / sh.units_per_thr] += (float)exact - f32;
+                    Sj += exact - f32;
+                    sm->spec_w[i] = exact;
+                    sm->tot[rx] += exact - f32;
+                    if (rx == rank) sm->part[((x / EPU) - u_base) / sh.units_per_thr] += exact - f32;
                 }
-                sm->S = fmax(Sj, 0.0);
+                sm->S = fmaxf(Sj, 0.f);
                 sm->D = pbar + sm->S;
-                sm->use_res = sm->S > 0.0;
+                sm->use_res = sm->S > 0.f;
             }
             first_draw = false;
         }
@@ -781,11 +788,11 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
 
     // ---- node outputs and the candidate correction ----
     if (tid == 0) {
-        const double S = sm->S, D = sm->D;
-        const double h = leaf ? p : (D > 0.0 ? S / D : 1.0);
+        const float S = sm->S, D = sm->D;
+        const float h = leaf ? p : (D > 0.f ? S / D : 1.f);
         if (rank == 0) {
-            pb.ws.h[s] = (float)h;
-            pb.ws.S[s] = (float)S;
+            pb.ws.h[s] = h;
+            pb.ws.S[s] = S;
         }
         if (!sm->use_res) {
             // sample P: per-CTA target mass in global units
@@ -793,7 +800,7 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                 const int n = __float_as_int(sm->xbuf[1][r][X_NT]);
                 const float m = sm->xbuf[1][r][X_MT];
                 const float em = n > 0 ? ex2(fmaf(m, c, sm->negT[r])) : 0.f;
-                sm->tot[r] = (float)(sm->sclT[r] * ((double)sm->xbuf[1][r][X_ZT] + (double)n * (double)em));
+                sm->tot[r] = sm->sclT[r] * (sm->xbuf[1][r][X_ZT] + (float)n * em);
             }
         }
         float Stot = 0.f;
@@ -823,7 +830,7 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
         sm->base = base;
         // the residual partials are in probability units; the target
         // partials in units of CTA rstar's reference
-        sm->unit = (sm->use_res || rstar < 0) ? 1.f : (float)sm->sclT[rstar];
+        sm->unit = (sm->use_res || rstar < 0) ? 1.f : sm->sclT[rstar];
     }
     __syncthreads();
     const bool use_res = sm->use_res != 0;
