@@ -713,18 +713,21 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                 // R_{j-1}(y); C_0 = 0 for the first draw
                 const float R = first_draw ? p * Py.P : fmaxf(g_diff(Py, Qy, pbar, sm->cbar, dom), 0.f);
                 const float cnew = first_draw ? 0.f : sm->cbar + D;
-                const float denom = D * Qy.P;
+                // a = min(R / (D Q(y)), 1).  D and Q(y) can both be ~1e-30 at
+                // low temperature: divide twice instead of forming D Q(y),
+                // which would underflow fp32.
                 float a, abar;
-                if (!(denom > 0.f) || R >= denom) {
+                const float ratio = (D > 0.f && Qy.P > 0.f) ? (R / D) / Qy.P : INFINITY;
+                if (ratio >= 1.f) {
                     a = 1.f;
                     abar = 0.f;
                 } else if (!(R > 0.f)) {
                     a = 0.f;
                     abar = 1.f;
                 } else {
-                    a = R / denom;
+                    a = ratio;
                     // 1 - a = (C_j Q(y) - p P(y)) / (D Q(y))
-                    abar = fminf(fmaxf(-g_diff(Py, Qy, pbar, cnew, dom), 0.f) / denom, 1.f);
+                    abar = fminf((fmaxf(-g_diff(Py, Qy, pbar, cnew, dom), 0.f) / D) / Qy.P, 1.f);
                 }
                 sm->cbar = cnew;
                 if (rank == 0) {
