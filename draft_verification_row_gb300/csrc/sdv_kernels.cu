@@ -296,6 +296,8 @@ struct NodeSmem {
     int uT, uD;                       // unique maxima, or -1
     float duT, tuD;                   // draft logit at uT, target logit at uD
     float S, D, cbar;                 // residual recursion
+    float Pbs, Qbs;                   // 1 - P and 1 - Q at the shared dominant token x*
+    float Rs, Ts, Rj;                 // R_j(x*), residual mass elsewhere, R_j(x*) before clamping
     float aT, aD;                     // this CTA's sweep weights
     float tot[kMaxCluster];           // per-CTA mass of the sampled distribution (global units)
     float thr, base, unit;            // sampling threshold, mass before CTA rstar, its unit
@@ -360,16 +362,18 @@ __global__ void prep_kernel(Problem pb)
 // ------------------------------------------------------------------------
 // node kernel
 
-// Cluster-wide exchange: thread 0 of every CTA publishes n words into slot
-// [rank] of buffer `par` of every CTA; after the cluster barrier each CTA
-// reads all slots locally.
+// Cluster-wide exchange: thread 0's n words are written, by the lanes of
+// warp 0 in parallel, into slot [rank] of buffer `par` of every CTA; after
+// the cluster barrier each CTA reads all slots locally.
 __device__ __forceinline__ void cluster_publish(cg::cluster_group& cl, NodeSmem* sm, int par, int rank, int C,
                                                 const float* v, int n)
 {
-    if (threadIdx.x == 0) {
-        for (int r = 0; r < C; ++r) {
-            float* dst = cl.map_shared_rank(&sm->xbuf[par][rank][0], r);
-            for (int i = 0; i < n; ++i) dst[i] = v[i];
+    if (threadIdx.x < 32) {  // lane r writes to CTA r; the values are thread 0's
+        const int lane = threadIdx.x;
+        float* dst = lane < C ? cl.map_shared_rank(&sm->xbuf[par][rank][0], lane) : nullptr;
+        for (int i = 0; i < n; ++i) {
+            const float x = __shfl_sync(0xffffffffu, v[i], 0);
+            if (lane < C) dst[i] = x;
         }
     }
     cl.sync();
@@ -420,65 +424,65 @@ __device__ __forceinline__ void sweep_weights(const NodeSmem* sm, int r, float p
     aD = (1.f + cbar) * sm->sclD[r] / sm->zD;
 }
 
-// Per-row state from the exchanged per-CTA statistics (thread 0).  Every
-// sum is of nonnegative terms, so fp32 keeps its relative precision.
-__device__ void row_state(NodeSmem* sm, const float (*xb)[12], int C, bool is_t, float c)
+// Per-row state from the exchanged per-CTA statistics, computed by warp 0
+// with lane r holding CTA r.  Every sum is of nonnegative terms, so fp32
+// keeps its relative precision.
+__device__ void row_state_warp(NodeSmem* sm, const float (*xb)[12], int C, bool is_t, float c)
 {
+    const int lane = threadIdx.x & 31;
+    const bool act = lane < C;
     const int iM = is_t ? X_MT : X_MD, iZ = is_t ? X_ZT : X_ZD, iN = is_t ? X_NT : X_ND;
     const int iF = is_t ? X_FT : X_FD, iP = is_t ? X_PT : X_PD;
-    float M = -INFINITY;
-    for (int r = 0; r < C; ++r) M = max_nan(M, xb[r][iM]);
+    const float m = act ? xb[lane][iM] : -INFINITY;
+    const int n = act ? __float_as_int(xb[lane][iN]) : 0;
+    const float zr = act ? xb[lane][iZ] : 0.f;
+    const float M = warp_max_nan(m);
     const float gneg = -(M * c);
-    float z = 0.f, zrest = 0.f, contrib_star = 0.f;
-    int nmax = 0, rstar = -1;
-    float emax = 0.f;
-    for (int r = 0; r < C; ++r) {
-        const float m = xb[r][iM];
-        const float neg = -(m * c);
-        const int n = __float_as_int(xb[r][iN]);
-        // shift between the references (gneg - neg is exact when the two
-        // maxima are close, which is when the CTA's mass matters)
-        const float scl = n > 0 || xb[r][iZ] > 0.f ? ex2(gneg - neg) : 0.f;
-        float contrib = scl * xb[r][iZ];
-        float em = 0.f;
-        if (n > 0) {
-            em = ex2(fmaf(m, c, neg));
-            contrib += scl * (float)n * em;
-        }
+    const float neg = -(m * c);
+    // shift between the CTA's reference and the row's (gneg - neg is exact
+    // when the two maxima are close, which is when the CTA's mass matters)
+    const float scl = (n > 0 || zr > 0.f) ? ex2(gneg - neg) : 0.f;
+    const float em = n > 0 ? ex2(fmaf(m, c, neg)) : 0.f;
+    const float contrib = n > 0 ? scl * zr + scl * (float)n * em : scl * zr;
+    const bool ismax = act && m == M && n > 0;
+    const float z = warp_sum(contrib);
+    const float zrest = warp_sum(ismax ? scl * zr : contrib);  // without the maximum's own mass
+    int nmax = ismax ? n : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nmax += __shfl_xor_sync(0xffffffffu, nmax, o);
+    const unsigned bm = __ballot_sync(0xffffffffu, ismax);
+    const int rs = bm ? __ffs(bm) - 1 : 0;
+    const float em_s = __shfl_sync(0xffffffffu, em, rs);
+    const int f_s = __shfl_sync(0xffffffffu, act ? __float_as_int(xb[lane][iF]) : -1, rs);
+    const float p_s = __shfl_sync(0xffffffffu, act ? xb[lane][iP] : 0.f, rs);
+    if (act) {
         if (is_t) {
-            sm->sclT[r] = scl;
-            sm->negT[r] = neg;
+            sm->sclT[lane] = scl;
+            sm->negT[lane] = neg;
         } else {
-            sm->sclD[r] = scl;
-            sm->negD[r] = neg;
-        }
-        z += contrib;
-        if (m == M && n > 0) {
-            nmax += n;
-            rstar = r;
-            emax = em;
-            contrib_star = scl * xb[r][iZ];  // the CTA holding the maximum, without it
-        } else {
-            zrest += contrib;
+            sm->sclD[lane] = scl;
+            sm->negD[lane] = neg;
         }
     }
-    const bool uniq = nmax == 1;
-    if (is_t) {
-        sm->MT = M;
-        sm->gnegT = gneg;
-        sm->zT = z;
-        sm->zrestT = zrest + contrib_star;
-        sm->emaxT = emax;
-        sm->uT = uniq ? __float_as_int(xb[rstar][iF]) : -1;
-        sm->duT = uniq ? xb[rstar][iP] : 0.f;
-    } else {
-        sm->MD = M;
-        sm->gnegD = gneg;
-        sm->zD = z;
-        sm->zrestD = zrest + contrib_star;
-        sm->emaxD = emax;
-        sm->uD = uniq ? __float_as_int(xb[rstar][iF]) : -1;
-        sm->tuD = uniq ? xb[rstar][iP] : 0.f;
+    if (lane == 0) {
+        const bool uniq = nmax == 1;
+        if (is_t) {
+            sm->MT = M;
+            sm->gnegT = gneg;
+            sm->zT = z;
+            sm->zrestT = zrest;
+            sm->emaxT = em_s;
+            sm->uT = uniq ? f_s : -1;
+            sm->duT = uniq ? p_s : 0.f;
+        } else {
+            sm->MD = M;
+            sm->gnegD = gneg;
+            sm->zD = z;
+            sm->zrestD = zrest;
+            sm->emaxD = em_s;
+            sm->uD = uniq ? f_s : -1;
+            sm->tuD = uniq ? p_s : 0.f;
+        }
     }
 }
 
@@ -668,27 +672,33 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
         cluster_publish(cl, sm, 1, rank, C, v, X_WORDS);
     }
 
-    // ---- scalar state (thread 0, kept in shared memory) ----
+    // ---- scalar state (warp 0 / thread 0, kept in shared memory) ----
     const float pbar = (j == 0 || pb.mode == SDV_MODE_TOKEN) ? 0.f : pb.ws.pbar[s];
     const float p = 1.f - pbar;
+    if (tid < 32) {
+        row_state_warp(sm, sm->xbuf[1], C, true, c);
+        if (!leaf) row_state_warp(sm, sm->xbuf[1], C, false, c);
+        __syncwarp();
+    }
     if (tid == 0) {
-        row_state(sm, sm->xbuf[1], C, true, c);
-        if (!leaf) row_state(sm, sm->xbuf[1], C, false, c);
-        float MT = -INFINITY, MD = -INFINITY;
-        for (int r = 0; r < C; ++r) {
-            MT = max_nan(MT, sm->xbuf[1][r][X_MT]);
-            MD = max_nan(MD, sm->xbuf[1][r][X_MD]);
-        }
-        const bool bad = !(isfinite(MT) && isfinite(sm->zT) && sm->zT > 0.f) ||
-                         (!leaf && !(isfinite(MD) && isfinite(sm->zD) && sm->zD > 0.f));
+        const bool bad = !(isfinite(sm->MT) && isfinite(sm->zT) && sm->zT > 0.f) ||
+                         (!leaf && !(isfinite(sm->MD) && isfinite(sm->zD) && sm->zD > 0.f));
         sm->bad = bad;
         if (bad && rank == 0) {
             atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
             if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
         }
-        sm->spec_x[0] = leaf ? -1 : sm->uT;
-        sm->spec_x[1] = (leaf || sm->uD == sm->uT) ? -1 : sm->uD;
+        // The token that is the unique maximum of both rows: its residual
+        // term shrinks geometrically through the recursion (p P and C_j Q
+        // both near 1), so it is carried apart, in a form with small terms.
+        const int xs = (!leaf && sm->uT >= 0 && sm->uT == sm->uD) ? sm->uT : -1;
+        sm->spec_x[0] = xs;
+        sm->spec_x[1] = -1;
         sm->spec_w[0] = sm->spec_w[1] = 0.f;
+        sm->Pbs = xs >= 0 ? sm->zrestT / sm->zT : 0.f;  // 1 - P(x*)
+        sm->Qbs = xs >= 0 ? sm->zrestD / sm->zD : 0.f;  // 1 - Q(x*)
+        sm->Rs = 0.f;
+        sm->Ts = 0.f;
         sm->use_res = 0;
         sm->S = p;
         sm->D = 1.f;
@@ -699,6 +709,9 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
     // R_j = max(p P - C_j Q, 0), S_j = sum R_j, D_j = 1 - p + S_j,
     // C_1 = 1, C_{j+1} = C_j + D_j; thread 0 keeps pbar = 1 - p and
     // cbar = C_j - 1, which stay accurate where p -> 1 and C -> 1.
+    // At the shared dominant token x*, with T_j the residual mass elsewhere:
+    //   R_1(x*) = p P(x*) - Q(x*) = Qbar - Pbar - pbar + pbar Pbar,
+    //   R_j(x*) = R_{j-1}(x*) Qbar - (pbar + T_{j-1}) (1 - Qbar).
     int par = 1;
     bool first_draw = true;
     if (!leaf) {
@@ -706,18 +719,32 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
             if (pb.ws.owner[sbase + k2] != k) continue;
             if (tid == 0) {
                 const int y = pb.tokens[((size_t)b * K + k2) * L + j];
-                const ProbD Py = prob_at(sm, true, y, sm->gT[k2], c);
-                const ProbD Qy = prob_at(sm, false, y, sm->gD[k2], c);
-                const bool dom = y == sm->uT || y == sm->uD;
+                const int xs = sm->spec_x[0];
                 const float D = sm->D;
-                // R_{j-1}(y); C_0 = 0 for the first draw
-                const float R = first_draw ? p * Py.P : fmaxf(g_diff(Py, Qy, pbar, sm->cbar, dom), 0.f);
                 const float cnew = first_draw ? 0.f : sm->cbar + D;
+                const float Pbs = sm->Pbs, Qbs = sm->Qbs;
+                // R_j(x*) before clamping, for this draw's sweep
+                const float Rj = first_draw ? ((Qbs - Pbs) - pbar) + pbar * Pbs
+                                            : sm->Rs * Qbs - (pbar + sm->Ts) * (1.f - Qbs);
+                sm->Rj = Rj;
+                float R, Qy, abar_num;
+                if (y == xs) {
+                    Qy = 1.f - Qbs;
+                    R = first_draw ? (1.f - pbar) * (1.f - Pbs) : sm->Rs;  // R_{j-1}(x*)
+                    abar_num = fmaxf(-Rj, 0.f);                              // D Q - R
+                } else {
+                    const ProbD Py = prob_at(sm, true, y, sm->gT[k2], c);
+                    const ProbD Qp = prob_at(sm, false, y, sm->gD[k2], c);
+                    Qy = Qp.P;
+                    // R_{j-1}(y); C_0 = 0 for the first draw
+                    R = first_draw ? p * Py.P : fmaxf(g_diff(Py, Qp, pbar, sm->cbar, false), 0.f);
+                    abar_num = fmaxf(-g_diff(Py, Qp, pbar, cnew, false), 0.f);  // C_j Q - p P
+                }
                 // a = min(R / (D Q(y)), 1).  D and Q(y) can both be ~1e-30 at
                 // low temperature: divide twice instead of forming D Q(y),
                 // which would underflow fp32.
                 float a, abar;
-                const float ratio = (D > 0.f && Qy.P > 0.f) ? (R / D) / Qy.P : INFINITY;
+                const float ratio = (D > 0.f && Qy > 0.f) ? (R / D) / Qy : INFINITY;
                 if (ratio >= 1.f) {
                     a = 1.f;
                     abar = 0.f;
@@ -726,8 +753,7 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
                     abar = 1.f;
                 } else {
                     a = ratio;
-                    // 1 - a = (C_j Q(y) - p P(y)) / (D Q(y))
-                    abar = fminf((fmaxf(-g_diff(Py, Qy, pbar, cnew, dom), 0.f) / D) / Qy.P, 1.f);
+                    abar = fminf((abar_num / D) / Qy, 1.f);
                 }
                 sm->cbar = cnew;
                 if (rank == 0) {
@@ -744,42 +770,48 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
             }
             __syncthreads();
             const float aT = sm->aT, aD = sm->aD;
+            const int xs = sm->spec_x[0];
             float w = 0.f;
-            for (int u = cu0; u < cu1; ++u) {
-                float t[EPU], d[EPU];
-                unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, t);
-                unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, d);
+            if (xs >= (u_base + cu0) * EPU && xs < (u_base + cu1) * EPU) {
+                // this thread holds x*: leave it out, its term is carried apart
+                for (int u = cu0; u < cu1; ++u) {
+                    float t[EPU], d[EPU];
+                    unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, t);
+                    unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, d);
+                    for (int e = 0; e < EPU; ++e)
+                        if ((u_base + u) * EPU + e != xs)
+                            w += res_term(ex2(fmaf(t[e], c, nTr)), ex2(fmaf(d[e], c, nDr)), aT, aD);
+                }
+            } else {
+                for (int u = cu0; u < cu1; ++u) {
+                    float t[EPU], d[EPU];
+                    unpack_masked<DT>(smT[u], (u_base + u) * EPU, V, t);
+                    unpack_masked<DT>(smD[u], (u_base + u) * EPU, V, d);
 #pragma unroll
-                for (int e = 0; e < EPU; ++e) w += res_term(ex2(fmaf(t[e], c, nTr)), ex2(fmaf(d[e], c, nDr)), aT, aD);
+                    for (int e = 0; e < EPU; ++e) w += res_term(ex2(fmaf(t[e], c, nTr)), ex2(fmaf(d[e], c, nDr)), aT, aD);
+                }
             }
             sm->part[tid] = w;
             w = block_sum_t0(w, sm->red);
             par ^= 1;
             cluster_publish(cl, sm, par, rank, C, &w, 1);
             if (tid == 0) {
-                // fp32 sweep sums with the dominant tokens' terms replaced by
-                // their exact values
-                const float cbar = sm->cbar;
                 float Sj = 0.f;
                 for (int r = 0; r < C; ++r) {
                     Sj += sm->xbuf[par][r][0];
                     sm->tot[r] = sm->xbuf[par][r][0];
                 }
-                for (int i = 0; i < 2; ++i) {
-                    const int x = sm->spec_x[i];
-                    if (x < 0) continue;
-                    const float t_x = x == sm->uT ? sm->MT : sm->tuD;
-                    const float d_x = x == sm->uD ? sm->MD : sm->duT;
-                    const float exact = fmaxf(g_diff(prob_at(sm, true, x, t_x, c), prob_at(sm, false, x, d_x, c),
-                                                     pbar, cbar, true), 0.f);
-                    const int rx = (x / EPU) / sh.units_per_cta;
-                    float wT, wD;
-                    sweep_weights(sm, rx, p, cbar, wT, wD);
-                    const float f32 = res_term(ex2(fmaf(t_x, c, sm->negT[rx])), ex2(fmaf(d_x, c, sm->negD[rx])), wT, wD);
-                    Sj += exact - f32;
-                    sm->spec_w[i] = exact;
-                    sm->tot[rx] += exact - f32;
-                    if (rx == rank) sm->part[((x / EPU) - u_base) / sh.units_per_thr] += exact - f32;
+                const int xs = sm->spec_x[0];
+                if (xs >= 0) {
+                    // the sweeps left x* out: their sum is the mass elsewhere
+                    const int rx = (xs / EPU) / sh.units_per_cta;
+                    const float Rs = fmaxf(sm->Rj, 0.f);
+                    sm->Ts = Sj;
+                    sm->Rs = Rs;
+                    Sj += Rs;
+                    sm->spec_w[0] = Rs;
+                    sm->tot[rx] += Rs;
+                    if (rx == rank) sm->part[((xs / EPU) - u_base) / sh.units_per_thr] += Rs;
                 }
                 sm->S = fmaxf(Sj, 0.f);
                 sm->D = pbar + sm->S;
@@ -797,43 +829,47 @@ __global__ void __launch_bounds__(kMaxThreads) node_kernel(Problem pb, Shape sh,
             pb.ws.h[s] = h;
             pb.ws.S[s] = S;
         }
-        if (!sm->use_res) {
-            // sample P: per-CTA target mass in global units
-            for (int r = 0; r < C; ++r) {
-                const int n = __float_as_int(sm->xbuf[1][r][X_NT]);
-                const float m = sm->xbuf[1][r][X_MT];
-                const float em = n > 0 ? ex2(fmaf(m, c, sm->negT[r])) : 0.f;
-                sm->tot[r] = sm->sclT[r] * (sm->xbuf[1][r][X_ZT] + (float)n * em);
+    }
+    if (tid < 32) {
+        // lane r holds CTA r's mass of the sampled distribution
+        __syncwarp();
+        const int lane = tid;
+        const bool act = lane < C;
+        const bool ures = sm->use_res != 0;
+        float tr = 0.f;
+        if (act) {
+            if (ures) {
+                tr = sm->tot[lane];
+            } else {  // sample P: per-CTA target mass in global units
+                const int n = __float_as_int(sm->xbuf[1][lane][X_NT]);
+                const float m = sm->xbuf[1][lane][X_MT];
+                const float em = n > 0 ? ex2(fmaf(m, c, sm->negT[lane])) : 0.f;
+                tr = sm->sclT[lane] * (sm->xbuf[1][lane][X_ZT] + (float)n * em);
             }
         }
-        float Stot = 0.f;
-        for (int r = 0; r < C; ++r) Stot += sm->tot[r];
+        float incl = tr;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const float Stot = __shfl_sync(0xffffffffu, incl, 31);
         const float u = pb.sample_u[((size_t)b * K + k) * (L + 1) + j];
         const float thr = u * Stot;
-        int rstar = -1, last = -1;
-        float run = 0.f, base = 0.f, last_base = 0.f;
-        for (int r = 0; r < C; ++r) {
-            if (sm->tot[r] > 0.f) {
-                last = r;
-                last_base = run;
-                if (run + sm->tot[r] > thr) {
-                    rstar = r;
-                    base = run;
-                    break;
-                }
-            }
-            run += sm->tot[r];
+        const unsigned cross = __ballot_sync(0xffffffffu, act && tr > 0.f && incl > thr);
+        const unsigned nz = __ballot_sync(0xffffffffu, act && tr > 0.f);
+        // the first CTA whose running mass exceeds u * S, else (rounding) the
+        // last CTA of nonzero mass
+        const int rs = cross ? __ffs(cross) - 1 : (nz ? 31 - __clz(nz) : -1);
+        const float base = __shfl_sync(0xffffffffu, incl - tr, rs < 0 ? 0 : rs);
+        if (lane == 0) {
+            sm->rstar = (sm->bad || rs < 0) ? -1 : rs;
+            sm->thr = thr;
+            sm->base = base;
+            // the residual partials are in probability units; the target
+            // partials in units of CTA rstar's reference
+            sm->unit = (ures || rs < 0) ? 1.f : sm->sclT[rs];
         }
-        if (rstar < 0) {
-            rstar = last;
-            base = last_base;
-        }
-        sm->rstar = sm->bad ? -1 : rstar;
-        sm->thr = thr;
-        sm->base = base;
-        // the residual partials are in probability units; the target
-        // partials in units of CTA rstar's reference
-        sm->unit = (sm->use_res || rstar < 0) ? 1.f : sm->sclT[rstar];
     }
     __syncthreads();
     const bool use_res = sm->use_res != 0;
