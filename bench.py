@@ -40,7 +40,9 @@ import torch  # noqa: E402
 
 METRIC = "verified draft positions/sec at V=151936, B=256; achieved HBM GB/s vs GB300 peak"
 UNIT = "positions/s"
-KERNEL_SRC = os.path.join(ROOT, "draft_verification_row_gb300", "csrc", "sdv_kernels.cu")
+CSRC = os.path.join(ROOT, "draft_verification_row_gb300", "csrc")
+# the node kernel's sources: a recorded ncu traffic figure holds only while these are unchanged
+KERNEL_SRCS = [os.path.join(CSRC, f) for f in ("sdv_stream.cu", "sdv_device.cuh", "sdv_internal.h")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "node_kernel_traffic.json")
 
 
@@ -123,14 +125,21 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def kernel_sha():
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def recorded_traffic():
     """DRAM bytes per call of the node kernels from a committed ncu capture,
     valid only while the kernel source is unchanged."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
-        with open(KERNEL_SRC, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        sha = kernel_sha()
         if d.get("kernel_source_sha256") != sha:
             return None
         return float(d["dram_bytes_per_call"])
@@ -309,8 +318,7 @@ def run_ours(args, world, rank, local):
     all_positions = sum_over_ranks(positions, world)
     ms_step = total_ms / args.steps
     value = all_positions / (ms_step / 1000.0)
-    row_launches = 1 if args.mode == "token" else batch.L + 1
-    launches = (2 + row_launches) * args.steps
+    launches = 3 * args.steps  # per call: prep, the node kernel, decide
 
     peak, peak_kind = measured_peaks()
     row_step_s = row_ms / args.steps / 1000.0
@@ -323,7 +331,7 @@ def run_ours(args, world, rank, local):
             "positions_per_step": all_positions,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
-                         "traffic": traffic, "kernel": "node_kernel",
+                         "traffic": traffic, "kernel": "stream_kernel",
                          "algorithmic_bytes_per_step": alg_bytes,
                          "kernel_ms_per_step": row_ms / args.steps,
                          "rows_read_per_step": {"target": nt, "draft": nd}},

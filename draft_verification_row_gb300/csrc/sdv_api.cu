@@ -27,7 +27,8 @@ bool sizes_ok(int B, int K, int L, int V)
 size_t workspace_size(int B, int K, int L)
 {
     const size_t n = slot_count(B, K, L);
-    return 6 * align_up(n * 4) + align_up(n) + align_up((size_t)B * 4);
+    return 7 * align_up(n * 4) + align_up(n) + align_up((size_t)B * 4) + align_up((size_t)(L + 1) * B * K * 4) +
+           align_up((size_t)(L + 2) * 4);
 }
 
 Workspace carve(void* base, int B, int K, int L)
@@ -50,6 +51,12 @@ Workspace carve(void* base, int B, int K, int L)
     w.owner = reinterpret_cast<unsigned char*>(p);
     p += align_up(n);
     w.req = reinterpret_cast<int*>(p);
+    p += align_up((size_t)B * 4);
+    w.ready = reinterpret_cast<int*>(p);
+    p += align_up(n * 4);
+    w.nodes = reinterpret_cast<int*>(p);
+    p += align_up((size_t)(L + 1) * B * K * 4);
+    w.ncount = reinterpret_cast<int*>(p);
     return w;
 }
 
@@ -154,10 +161,16 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
         }
     }
     if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (cudaMemsetAsync(pb.ws.ncount, 0, sizeof(int) * (L + 2), st) != cudaSuccess) return SDV_ERR_CUDA;
     if (launch_prep(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
     if (!prof_record(g_prof_start, st)) return SDV_ERR_CUDA;
+    const char* kenv = std::getenv("SDV_NODE_KERNEL");
+    const bool cluster_kernel = kenv && std::strcmp(kenv, "cluster") == 0;
     if (greedy) {
         if (launch_argmax(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
+    } else if (!cluster_kernel) {
+        // every node of every depth in one persistent launch
+        if (launch_stream(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
     } else if (mode == SDV_MODE_TOKEN) {
         // node weights are all 1: every node of every depth at once
         if (launch_nodes(pb, sh, 0, L, st) != cudaSuccess) return SDV_ERR_CUDA;

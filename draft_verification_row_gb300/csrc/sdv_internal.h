@@ -24,6 +24,9 @@ struct Workspace {
     int* am;               // node argmax (greedy)
     unsigned char* owner;  // lowest draft sharing draft k's first j tokens
     int* req;              // [B] request status bits
+    int* ready;            // node weight published by the parent (slot flags)
+    int* nodes;            // [L+1][B*K] node slots by depth, listed by the prep kernel
+    int* ncount;           // [L+1] nodes per depth, then the streaming kernel's work counter
 };
 
 struct Problem {
@@ -56,7 +59,6 @@ struct Shape {
     int smem;          // dynamic shared memory bytes per CTA
 };
 
-constexpr int kSlotRecordBytes = 6 * 4 + 1;
 
 inline size_t slot_count(int B, int K, int L) { return (size_t)B * (size_t)(L + 1) * (size_t)K; }
 
@@ -68,5 +70,6 @@ cudaError_t launch_nodes(const Problem& pb, const Shape& sh, int j_lo, int j_hi,
 cudaError_t launch_argmax(const Problem& pb, cudaStream_t st);
 cudaError_t launch_decide(const Problem& pb, bool greedy, cudaStream_t st);
 cudaError_t prepare_node_kernel(const Shape& sh, int dtype);
+cudaError_t launch_stream(const Problem& pb, cudaStream_t st);
 
 }  // namespace sdv

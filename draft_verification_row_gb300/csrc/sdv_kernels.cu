@@ -22,254 +22,12 @@
 #include <cooperative_groups.h>
 
 #include "sdv_internal.h"
+#include "sdv_device.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace sdv {
 namespace {
-
-constexpr int kMaxThreads = 512;
-constexpr int kMaxCluster = 16;
-constexpr uint64_t kWaitNs = 2000000000ull;  // bounded waits: 2 s
-
-// ------------------------------------------------------------------------
-// PTX helpers
-
-__device__ __forceinline__ float ex2(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ float max_nan(float a, float b)
-{
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b)
-{
-    uint32_t r;
-    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ uint64_t globaltimer()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_fence_init()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(phase)
-        : "memory");
-    return ok != 0;
-}
-
-// Waits for phase `phase` of the barrier for at most kWaitNs.
-__device__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase)
-{
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, phase)) {
-        if (globaltimer() - t0 > kWaitNs) return false;
-    }
-    return true;
-}
-
-// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// ------------------------------------------------------------------------
-// element access: rows are held as 16-byte units (4 fp32 or 8 bf16)
-
-template <int DT>
-struct Elem;
-
-template <>
-struct Elem<SDV_F32> {
-    static constexpr int kPerUnit = 4;
-    static constexpr int kBytes = 4;
-    __device__ static __forceinline__ void unpack(const uint4& u, float (&v)[4])
-    {
-        v[0] = __uint_as_float(u.x);
-        v[1] = __uint_as_float(u.y);
-        v[2] = __uint_as_float(u.z);
-        v[3] = __uint_as_float(u.w);
-    }
-    __device__ static __forceinline__ float unit_max(const uint4& u, float m)
-    {
-        m = max_nan(m, __uint_as_float(u.x));
-        m = max_nan(m, __uint_as_float(u.y));
-        m = max_nan(m, __uint_as_float(u.z));
-        return max_nan(m, __uint_as_float(u.w));
-    }
-    __device__ static __forceinline__ float load(const void* row, int x)
-    {
-        return __ldg(reinterpret_cast<const float*>(row) + x);
-    }
-};
-
-template <>
-struct Elem<SDV_BF16> {
-    static constexpr int kPerUnit = 8;
-    static constexpr int kBytes = 2;
-    __device__ static __forceinline__ void unpack(const uint4& u, float (&v)[8])
-    {
-        v[0] = bf_lo(u.x);
-        v[1] = bf_hi(u.x);
-        v[2] = bf_lo(u.y);
-        v[3] = bf_hi(u.y);
-        v[4] = bf_lo(u.z);
-        v[5] = bf_hi(u.z);
-        v[6] = bf_lo(u.w);
-        v[7] = bf_hi(u.w);
-    }
-    __device__ static __forceinline__ float unit_max(const uint4& u, float m)
-    {
-        uint32_t a = max_nan_bf16x2(max_nan_bf16x2(u.x, u.y), max_nan_bf16x2(u.z, u.w));
-        return max_nan(m, max_nan(bf_lo(a), bf_hi(a)));
-    }
-    __device__ static __forceinline__ float load(const void* row, int x)
-    {
-        const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + x);
-        return __uint_as_float(static_cast<uint32_t>(h) << 16);
-    }
-};
-
-// Elements of a unit at or past V read as -inf (no mass, never chosen).
-template <int DT>
-__device__ __forceinline__ void unpack_masked(const uint4& u, int x0, int V, float (&v)[Elem<DT>::kPerUnit])
-{
-    Elem<DT>::unpack(u, v);
-    if (x0 + Elem<DT>::kPerUnit > V) {
-#pragma unroll
-        for (int e = 0; e < Elem<DT>::kPerUnit; ++e)
-            if (x0 + e >= V) v[e] = -INFINITY;
-    }
-}
-
-// ------------------------------------------------------------------------
-// reductions
-
-__device__ __forceinline__ float warp_sum(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-__device__ __forceinline__ float warp_max_nan(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-// Block-wide maxima of two values; every thread gets the result.
-// red must hold 64 floats; ends with a barrier so red can be reused.
-__device__ void block_max2(float& a, float& b, float* red)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    a = warp_max_nan(a);
-    b = warp_max_nan(b);
-    if (lane == 0) {
-        red[warp] = a;
-        red[32 + warp] = b;
-    }
-    __syncthreads();
-    a = -INFINITY;
-    b = -INFINITY;
-    for (int w = 0; w < nw; ++w) {
-        a = max_nan(a, red[w]);
-        b = max_nan(b, red[32 + w]);
-    }
-    __syncthreads();
-}
-
-// Block-wide sums of two floats and two ints, valid in thread 0 only.  One
-// barrier; the caller must pass another barrier before `red` is reused.
-__device__ void block_sum_f2i2_t0(float& a, float& b, int& m, int& n, float* red, int (*ired)[32])
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        a += __shfl_xor_sync(0xffffffffu, a, o);
-        b += __shfl_xor_sync(0xffffffffu, b, o);
-        m += __shfl_xor_sync(0xffffffffu, m, o);
-        n += __shfl_xor_sync(0xffffffffu, n, o);
-    }
-    if (lane == 0) {
-        red[warp] = a;
-        red[32 + warp] = b;
-        ired[0][warp] = m;
-        ired[1][warp] = n;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        a = b = 0.f;
-        m = n = 0;
-        for (int w = 0; w < nw; ++w) {
-            a += red[w];
-            b += red[32 + w];
-            m += ired[0][w];
-            n += ired[1][w];
-        }
-    }
-}
-
-// Block-wide sum valid in thread 0 only (one barrier, same rule).
-__device__ float block_sum_t0(float a, float* red)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    a = warp_sum(a);
-    if (lane == 0) red[warp] = a;
-    __syncthreads();
-    float s = 0.f;
-    if (threadIdx.x == 0)
-        for (int w = 0; w < nw; ++w) s += red[w];
-    return s;
-}
 
 // Cluster exchange words published by each CTA after the normaliser sweep.
 enum { X_MT, X_MD, X_ZT, X_ZD, X_NT, X_ND, X_FT, X_FD, X_PT, X_PD, X_WORDS };
@@ -357,6 +115,19 @@ __global__ void prep_kernel(Problem pb)
         if (lane < K) own[j * K + lane] = (unsigned char)o;
     }
     if (lane == 0) pb.ws.pbar[(size_t)b * (L + 1) * K] = 0.f;  // root weight 1
+    // list the request's nodes by depth (for the streaming kernel) and clear
+    // the flags through which parents publish their children's weights
+    const size_t BK = (size_t)pb.B * K;
+    for (int j = 0; j <= Lb; ++j) {
+        const bool node = lane < K && own[j * K + lane] == lane;
+        const unsigned m = __ballot_sync(0xffffffffu, node);
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&pb.ws.ncount[j], __popc(m));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const size_t slot = ((size_t)b * (L + 1) + j) * K + lane;
+        if (node) pb.ws.nodes[j * BK + base + __popc(m & ((1u << lane) - 1))] = (int)slot;
+        if (lane < K) pb.ws.ready[slot] = 0;
+    }
 }
 
 // ------------------------------------------------------------------------

@@ -1,0 +1,899 @@
+// sdv_stream.cu -- the streaming node kernel.
+//
+// One persistent CTA per SM verifies one draft-trie node at a time; the
+// node's target and draft rows stream through shared memory:
+//   pass 1 (from HBM): per-thread online maxima and softmax normalisers of
+//           both rows, the row maxima counted apart so that 1 - P of a
+//           dominant token stays exact;
+//   pass 2 (from L2, once per draw): the residual sweep
+//           S_j = sum_x max(p P(x) - C_j Q(x), 0), and, on the last sweep,
+//           per-chunk per-warp masses for the inverse-CDF sample;
+//   leaf:   one target-only pass for the bonus sample.
+// Warp 0 produces: it takes nodes from the list the prep kernel built
+// (depth-major) and streams their rows in 16 KB-per-row chunks through a
+// 4-stage ring with 1-D TMA bulk copies (mbarrier full/empty handshake),
+// pass-1 reads marked evict_last and pass-2 reads evict_first in L2.
+// Warps 1..16 consume.  A node's weight p comes from its parent through a
+// flag (release/acquire); waiting happens only before pass 2.  Every wait is
+// bounded and a timeout is reported, never a hang or a trap.
+//
+// The rules computed are stated in include/sdv.h (SpecTr-GBV:
+// Multi-Draft Block Verification Accelerating Speculative Decoding,
+// sections 1 and 2).
+#include <algorithm>
+
+#include "sdv_device.cuh"
+#include "sdv_internal.h"
+
+namespace sdv {
+namespace {
+
+constexpr int kSW = 16;                  // consumer warps
+constexpr int kCT = 32 * kSW;            // consumer threads
+constexpr int kSThreads = kCT + 64;      // plus the metadata warp and the copy warp
+constexpr int kUPT = 2;                  // 16-byte units per consumer thread per row per chunk
+constexpr int kWU = 32 * kUPT;           // units per warp per chunk, contiguous
+constexpr int kChunk = kCT * kUPT;       // units per row per chunk (16 KB)
+constexpr int kStages = 4;
+constexpr int kMaxChunks = (SDV_MAX_V / 4 + kChunk - 1) / kChunk;
+constexpr int kQ = 4;                    // node descriptor queue depth
+
+__device__ __forceinline__ void cbar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(int* p, int v)
+{
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// What the metadata warp prepares for each node, ahead of its rows.
+struct NodeDesc {
+    int slot, b, j, k, leaf, nd;
+    int dk[SDV_MAX_K];            // drafts of the draws, in index order
+    int y[SDV_MAX_K];             // their tokens
+    float gT[SDV_MAX_K], gD[SDV_MAX_K];  // target / draft logits at those tokens
+    float usample;
+};
+
+struct StreamSmem {
+    uint4 ring[kStages][2][kChunk];  // [stage][target, draft][units]
+    uint64_t full[kStages], empty[kStages];
+    uint64_t qfull[kQ], qempty[kQ];
+    NodeDesc qd[kQ];
+    NodeDesc cur;                    // the consumers' copy of the current node
+    float table[kMaxChunks][kSW];    // mass of the sampled distribution per (chunk, warp): index order
+    float redf[4][kSW];
+    int redi[4][kSW];
+    unsigned long long firstT, firstD;  // (first index of the row maximum << 32) | partner logit bits
+    int abort;
+    // scalar state (consumer thread 0)
+    float MT, MD, gnegT, gnegD, zT, zD, zrestT, zrestD, emaxT, emaxD;
+    int uT, uD;
+    float S, D, cbar, pbar, Pbs, Qbs, Rs, Ts, Rj, aT, aD;
+    int xs, use_res, bad;
+    float thr, base;
+    int pick_c, pick_w;
+};
+
+// Online statistics of one row, per thread, in a reference shared by the
+// warp: e(x) = 2^(x c - m c) with m the largest logit the warp has seen.
+// z sums the thread's elements below m; cnt counts its elements equal to m
+// (first: the lowest such index, partner: the other row's logit there).
+// The reference moves once per chunk, uniformly across the warp, so only
+// the lane holding a new maximum ever leaves the branch-free path.
+struct Online {
+    float m = -INFINITY;
+    float neg = INFINITY;
+    float z = 0.f;
+    int cnt = 0;
+    int first = 0x7fffffff;
+    float partner = 0.f;
+};
+
+// Unit maximum; the last unit of a row may extend past V.
+template <int DT>
+__device__ __forceinline__ float unit_max_masked(const uint4& u, int x0, int V)
+{
+    using E = Elem<DT>;
+    if (x0 + E::kPerUnit <= V) return E::unit_max(u, -INFINITY);
+    float v[E::kPerUnit];
+    unpack_masked<DT>(u, x0, V, v);
+    float um = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < E::kPerUnit; ++e) um = max_nan(um, v[e]);
+    return um;
+}
+
+// Move the warp's reference to the chunk's maximum cm (warp-uniform).
+__device__ __forceinline__ void online_rebase(Online& s, float cm, float c)
+{
+    const float wm = warp_max_redux(cm);
+    if (wm > s.m || wm != wm) {
+        const float nneg = -(wm * c);
+        s.z = s.z * ex2(nneg - s.neg) + (s.cnt > 0 ? (float)s.cnt * ex2(fmaf(s.m, c, nneg)) : 0.f);
+        s.cnt = 0;
+        s.first = 0x7fffffff;
+        s.m = wm;
+        s.neg = nneg;
+    }
+}
+
+// Sum of one unit's elements below the reference, counting those equal to
+// it apart (cnt, first, partner).  Only a unit whose maximum equals the
+// reference (it holds it, or ties it) comes here.
+template <int DT, bool OTHER>
+__device__ __forceinline__ float careful_unit(Online& s, const uint4 u, const uint4 o, int x0, int V, float c)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+    float v[EPU], w[EPU];
+    unpack_masked<DT>(u, x0, V, v);
+    if (OTHER) unpack_masked<DT>(o, x0, V, w);
+    float z = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPU; ++e) {
+        if (v[e] == s.m) {
+            ++s.cnt;
+            if (x0 + e < s.first) {
+                s.first = x0 + e;
+                s.partner = OTHER ? w[e] : 0.f;
+            }
+        } else {
+            z += ex2(fmaf(v[e], c, s.neg));
+        }
+    }
+    return z;
+}
+
+template <int DT>
+__device__ __forceinline__ float unit_sum(const uint4& u, int x0, int V, float c, float neg)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+    float v[EPU];
+    unpack_masked<DT>(u, x0, V, v);
+    float z = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPU; ++e) z += ex2(fmaf(v[e], c, neg));
+    return z;
+}
+
+// Unit index of (chunk, warp, sub-unit, lane): a warp's units of a chunk
+// are contiguous, consecutive lanes on consecutive units.
+__device__ __forceinline__ int unit_local(int cw, int i, int lane) { return cw * kWU + i * 32 + lane; }
+
+// Maximum of a thread's units of one row in one chunk.  Only the last
+// chunk of a row holds units past V (masked) or no unit at all.
+template <int DT>
+__device__ __forceinline__ float chunk_max(const uint4 (&u)[kUPT], int ug0, int n_units, int V, bool tail)
+{
+    static_assert(kUPT == 2, "pair_max covers two units");
+    if (!tail) return Elem<DT>::pair_max(u[0], u[1]);
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kUPT; ++i) {
+        const int ug = ug0 + i * 32;
+        if (ug < n_units) m = max_nan(m, unit_max_masked<DT>(u[i], ug * Elem<DT>::kPerUnit, V));
+    }
+    return m;
+}
+
+// Pass 1 over one node's rows: OTHER is false for a leaf (target row only).
+// Every unit is summed on the branch-free path; in the few chunks where a
+// lane holds a unit at the reference, those units are summed again with
+// the maxima counted apart (the check is warp-uniform).
+template <int DT, bool OTHER>
+__device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, uint32_t& g, bool& timed_out,
+                                      int nc, int n_units, int V, float c, int cw, int lane)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+#pragma unroll 1
+    for (int ch = 0; ch < nc; ++ch, ++g) {
+        const int s = g % kStages;
+        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
+        const bool tail = ch == nc - 1;
+        const int ug0 = ch * kChunk + unit_local(cw, 0, lane);
+        uint4 t[kUPT], d[kUPT];
+#pragma unroll
+        for (int i = 0; i < kUPT; ++i) {
+            const int ul = unit_local(cw, i, lane);
+            t[i] = d[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (!tail || ug0 + i * 32 < n_units) {
+                t[i] = sm->ring[s][0][ul];
+                if (OTHER) d[i] = sm->ring[s][1][ul];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->empty[s]);  // the units are in registers now
+        const float cmT = chunk_max<DT>(t, ug0, n_units, V, tail);
+        const float cmD = OTHER ? chunk_max<DT>(d, ug0, n_units, V, tail) : -INFINITY;
+        online_rebase(sT, cmT, c);
+        if (OTHER) online_rebase(sD, cmD, c);
+        // a reference of -inf means nothing finite yet (nothing to add);
+        // NaN means the row is unusable
+        const bool liveT = sT.m > -INFINITY, liveD = OTHER && sD.m > -INFINITY;
+        float zt[kUPT], zd[kUPT];
+#pragma unroll
+        for (int i = 0; i < kUPT; ++i) {
+            const int ug = ug0 + i * 32;
+            zt[i] = zd[i] = 0.f;
+            if (!tail || ug < n_units) {
+                if (liveT) zt[i] = unit_sum<DT>(t[i], ug * EPU, V, c, sT.neg);
+                if (liveD) zd[i] = unit_sum<DT>(d[i], ug * EPU, V, c, sD.neg);
+            }
+        }
+        const bool spT = liveT && cmT == sT.m, spD = liveD && cmD == sD.m;
+        if (__any_sync(0xffffffffu, spT || spD)) {
+#pragma unroll
+            for (int i = 0; i < kUPT; ++i) {
+                const int ug = ug0 + i * 32;
+                if (ug < n_units) {
+                    if (spT && unit_max_masked<DT>(t[i], ug * EPU, V) == sT.m)
+                        zt[i] = careful_unit<DT, OTHER>(sT, t[i], d[i], ug * EPU, V, c);
+                    if (spD && unit_max_masked<DT>(d[i], ug * EPU, V) == sD.m)
+                        zd[i] = careful_unit<DT, true>(sD, d[i], t[i], ug * EPU, V, c);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kUPT; ++i) {
+            sT.z += zt[i];
+            if (OTHER) sD.z += zd[i];
+        }
+    }
+}
+
+__device__ __forceinline__ float res_term_s(float eT, float eD, float aT, float aD)
+{
+    return fmaxf(__fmaf_rn(eT, aT, -__fmul_rn(eD, aD)), 0.f);
+}
+
+// Combine the consumers' online statistics of one row (all consumer
+// threads call it; results in shared memory from consumer thread 0).
+__device__ __forceinline__ void combine_row(StreamSmem* sm, const Online s, bool is_t, float c, int ct)
+{
+    const int lane = ct & 31, w = ct >> 5;
+    float M = warp_max_redux(s.m);
+    if (lane == 0) sm->redf[0][w] = M;
+    if (ct == 0) (is_t ? sm->firstT : sm->firstD) = ~0ull;  // read by thread 0 after the next barrier
+    cbar_sync();
+    M = -INFINITY;
+    for (int i = 0; i < kSW; ++i) M = max_nan(M, sm->redf[0][i]);
+    const float gneg = -(M * c);
+    float contrib;
+    int nmax;
+    if (s.m == M) {  // same reference as the row's
+        contrib = s.z;
+        nmax = s.cnt;
+        if (s.cnt > 0) {
+            const unsigned long long key =
+                ((unsigned long long)(unsigned)s.first << 32) | __float_as_uint(s.partner);
+            atomicMin(is_t ? &sm->firstT : &sm->firstD, key);
+        }
+    } else {
+        const float scl = (s.cnt > 0 || s.z > 0.f) ? ex2(gneg - s.neg) : 0.f;
+        contrib = s.cnt > 0 ? scl * (s.z + (float)s.cnt * ex2(fmaf(s.m, c, s.neg))) : scl * s.z;
+        nmax = 0;
+    }
+    contrib = warp_sum(contrib);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nmax += __shfl_xor_sync(0xffffffffu, nmax, o);
+    if (lane == 0) {
+        sm->redf[1][w] = contrib;
+        sm->redi[1][w] = nmax;
+    }
+    cbar_sync();
+    if (ct == 0) {
+        float zr = 0.f;
+        int n = 0;
+        for (int i = 0; i < kSW; ++i) {
+            zr += sm->redf[1][i];
+            n += sm->redi[1][i];
+        }
+        const float em = ex2(fmaf(M, c, gneg));
+        const unsigned long long key = is_t ? sm->firstT : sm->firstD;
+        const int first = (int)(key >> 32);
+        const float partner = __uint_as_float((unsigned)(key & 0xffffffffu));
+        if (is_t) {
+            sm->MT = M;
+            sm->gnegT = gneg;
+            sm->zrestT = zr;
+            sm->zT = (float)n * em + zr;
+            sm->emaxT = em;
+            sm->uT = n == 1 ? first : -1;
+            (void)partner;
+        } else {
+            sm->MD = M;
+            sm->gnegD = gneg;
+            sm->zrestD = zr;
+            sm->zD = (float)n * em + zr;
+            sm->emaxD = em;
+            sm->uD = n == 1 ? first : -1;
+        }
+    }
+}
+
+struct ProbS {
+    float P, Pbar;
+};
+
+__device__ __forceinline__ ProbS prob_s(const StreamSmem* sm, bool is_t, int x, float logit, float c)
+{
+    ProbS o;
+    if (x == (is_t ? sm->uT : sm->uD)) {
+        const float z = is_t ? sm->zT : sm->zD;
+        o.P = (is_t ? sm->emaxT : sm->emaxD) / z;
+        o.Pbar = (is_t ? sm->zrestT : sm->zrestD) / z;
+    } else {
+        o.P = ex2(fmaf(logit, c, is_t ? sm->gnegT : sm->gnegD)) / (is_t ? sm->zT : sm->zD);
+        o.Pbar = 1.f - o.P;
+    }
+    return o;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
+{
+    using E = Elem<DT>;
+    constexpr int EPU = E::kPerUnit;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    StreamSmem* sm = reinterpret_cast<StreamSmem*>(smem_raw);
+    const int tid = threadIdx.x;
+    const int K = pb.K, L = pb.L, V = pb.V;
+    const int BK = pb.B * K;
+    const int n_units = (V + EPU - 1) / EPU;
+    const int nc = (n_units + kChunk - 1) / kChunk;
+    const float c = pb.c;
+    int* const counter = pb.ws.ncount + (L + 1);
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm->full[i], 1);
+            mbar_init(&sm->empty[i], kSW);
+        }
+        for (int i = 0; i < kQ; ++i) {
+            mbar_init(&sm->qfull[i], 1);
+            mbar_init(&sm->qempty[i], 2);  // read by the copy warp and by the consumers
+        }
+        mbar_fence_init();
+        sm->abort = 0;
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- metadata warp
+    // Takes nodes from the prep kernel's depth-major list (every parent
+    // before its children) and fills the descriptor queue up to kQ nodes
+    // ahead: draws, their tokens and logits, the sample uniform.
+    if (tid < 32) {
+        const int lane = tid;
+        // lane j holds the node count of depth j
+        const int cnt = lane <= L ? pb.ws.ncount[lane] : 0;
+        int n_items = cnt;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) n_items += __shfl_xor_sync(0xffffffffu, n_items, o);
+        for (uint32_t it = 0;; ++it) {
+            const int q = it % kQ;
+            int w = 0;
+            if (lane == 0) w = atomicAdd(counter, 1);
+            w = __shfl_sync(0xffffffffu, w, 0);
+            int slot = -1;
+            if (w < n_items) {
+                // depth j: the first whose inclusive prefix of counts passes w
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += n;
+                }
+                const int j = __ffs(__ballot_sync(0xffffffffu, incl > w)) - 1;
+                const int before = __shfl_sync(0xffffffffu, incl - cnt, j);
+                slot = pb.ws.nodes[(size_t)j * BK + (w - before)];
+            }
+            bool ok = true;
+            if (lane == 0 && it >= kQ) ok = mbar_wait_bounded(&sm->qempty[q], (it / kQ - 1) & 1);
+            if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
+                sm->abort = 1;
+                break;
+            }
+            NodeDesc& d = sm->qd[q];
+            if (slot >= 0) {
+                const int k = slot % K, j = (slot / K) % (L + 1), b = slot / (K * (L + 1));
+                const int Lb = pb.lengths ? pb.lengths[b] : L;
+                const bool leaf = j == Lb;
+                const size_t sbase = (size_t)slot - k;
+                const bool draw = !leaf && lane < K && lane >= k && pb.ws.owner[sbase + lane] == k;
+                const unsigned m = __ballot_sync(0xffffffffu, draw);
+                if (draw) {
+                    const int pos = __popc(m & ((1u << lane) - 1));
+                    const int y = pb.tokens[((size_t)b * K + lane) * L + j];
+                    const char* gT = static_cast<const char*>(pb.target) +
+                                     (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
+                    const char* gD = static_cast<const char*>(pb.draft) +
+                                     (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
+                    d.dk[pos] = lane;
+                    d.y[pos] = y;
+                    d.gT[pos] = E::load(gT, y);
+                    d.gD[pos] = E::load(gD, y);
+                }
+                if (lane == 0) {
+                    d.slot = slot;
+                    d.b = b;
+                    d.j = j;
+                    d.k = k;
+                    d.leaf = leaf;
+                    d.nd = __popc(m);
+                    d.usample = pb.sample_u[((size_t)b * K + k) * (L + 1) + j];
+                }
+            } else if (lane == 0) {
+                d.slot = -1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm->qfull[q]);
+            if (slot < 0) break;
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- copy warp
+    // Streams each node's rows: pass 1 (evict_last), then one pass per draw
+    // (or the leaf's target-only pass), evict_first.
+    if (tid < 64) {
+        if (tid != 32) return;
+        const uint64_t pol_last = policy_evict_last();
+        const uint64_t pol_first = policy_evict_first();
+        uint32_t g = 0;
+        for (uint32_t it = 0;; ++it) {
+            const int q = it % kQ;
+            if (!mbar_wait_bounded(&sm->qfull[q], (it / kQ) & 1)) {
+                sm->abort = 1;
+                break;
+            }
+            const NodeDesc& d = sm->qd[q];
+            const int slot = d.slot, b = d.b, j = d.j, k = d.k, nd = d.nd;
+            const bool leaf = d.leaf != 0;
+            mbar_arrive(&sm->qempty[q]);
+            if (slot < 0) break;
+            const char* gT = static_cast<const char*>(pb.target) +
+                             (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
+            const char* gD = leaf ? nullptr
+                                  : static_cast<const char*>(pb.draft) +
+                                        (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
+            const int passes = 1 + (leaf ? 1 : nd);
+            bool ok = true;
+            for (int ps = 0; ps < passes && ok; ++ps) {
+                const bool with_d = !leaf;
+                const uint64_t pol = ps == 0 ? pol_last : pol_first;
+                for (int ch = 0; ch < nc; ++ch, ++g) {
+                    const int s = g % kStages;
+                    const uint32_t use = g / kStages;
+                    if (use > 0 && !mbar_wait_bounded(&sm->empty[s], (use - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const int u0 = ch * kChunk;
+                    const uint32_t bytes = (uint32_t)min(kChunk, n_units - u0) * 16u;
+                    mbar_expect_tx(&sm->full[s], with_d ? 2 * bytes : bytes);
+                    bulk_g2s_hint(&sm->ring[s][0][0], gT + (size_t)u0 * 16, bytes, &sm->full[s], pol);
+                    if (with_d) bulk_g2s_hint(&sm->ring[s][1][0], gD + (size_t)u0 * 16, bytes, &sm->full[s], pol);
+                }
+            }
+            if (!ok) {
+                sm->abort = 1;
+                break;
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int ct = tid - 64, lane = ct & 31, cw = ct >> 5;
+    uint32_t g = 0;
+    bool timed_out = false;
+    for (uint32_t it = 0;; ++it) {
+        const int q = it % kQ;
+        // copy the descriptor, then hand the queue slot back
+        const bool got = mbar_wait_bounded(&sm->qfull[q], (it / kQ) & 1);
+        if (!got) atomicExch(&sm->abort, 1);
+        cbar_sync();  // the previous node's readers of sm->cur are done
+        if (ct < (int)(sizeof(NodeDesc) / 4))
+            reinterpret_cast<int*>(&sm->cur)[ct] = reinterpret_cast<const int*>(&sm->qd[q])[ct];
+        cbar_sync();
+        if (ct == 0) mbar_arrive(&sm->qempty[q]);
+        const int slot = *static_cast<volatile int*>(&sm->abort) ? -1 : sm->cur.slot;
+        if (slot < 0) break;
+
+        const int k = sm->cur.k, j = sm->cur.j, b = sm->cur.b;
+        const size_t sbase = (size_t)slot - k;
+        const bool leaf = sm->cur.leaf != 0;
+        const int nd = sm->cur.nd;
+        const char* gT = static_cast<const char*>(pb.target) +
+                         (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
+        const char* gD = leaf ? nullptr
+                              : static_cast<const char*>(pb.draft) +
+                                    (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
+
+        // ---- pass 1: online statistics ----
+        Online sT, sD;
+        if (leaf)
+            pass1<DT, false>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
+        else
+            pass1<DT, true>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
+        combine_row(sm, sT, true, c, ct);
+        if (!leaf) combine_row(sm, sD, false, c, ct);
+
+        // ---- scalar state ----
+        if (ct == 0) {
+            const bool bad = !(isfinite(sm->MT) && isfinite(sm->zT) && sm->zT > 0.f) ||
+                             (!leaf && !(isfinite(sm->MD) && isfinite(sm->zD) && sm->zD > 0.f));
+            sm->bad = bad;
+            if (bad) {
+                atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
+                if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
+            }
+            // the node weight: from the parent, through its flag
+            float pbar = 0.f;
+            if (j > 0 && pb.mode != SDV_MODE_TOKEN) {
+                const uint64_t t0 = globaltimer();
+                while (ld_acquire(&pb.ws.ready[slot]) == 0) {
+                    if (globaltimer() - t0 > 2000000000ull) {
+                        sm->abort = 1;
+                        break;
+                    }
+                }
+                pbar = pb.ws.pbar[slot];
+            }
+            sm->pbar = pbar;
+            const int xs = (!leaf && sm->uT >= 0 && sm->uT == sm->uD) ? sm->uT : -1;
+            sm->xs = xs;
+            sm->Pbs = xs >= 0 ? sm->zrestT / sm->zT : 0.f;
+            sm->Qbs = xs >= 0 ? sm->zrestD / sm->zD : 0.f;
+            sm->Rs = sm->Ts = 0.f;
+            sm->S = 1.f - pbar;
+            sm->D = 1.f;
+            sm->cbar = 0.f;
+            sm->use_res = 0;
+        }
+        cbar_sync();
+        const float pbar = sm->pbar, p = 1.f - pbar;
+        const float gnegT = sm->gnegT, gnegD = sm->gnegD;
+        const int xs = sm->xs;
+
+        // ---- pass 2: the residual recursion, one sweep per draw ----
+        // (the same recursion and complement forms as the cluster kernel:
+        // R_j(x*) of the shared dominant token x* is carried apart)
+        for (int di = 0; di < nd && !leaf; ++di) {
+            const int k2 = sm->cur.dk[di];
+            const bool first_draw = di == 0;
+            const bool last = di == nd - 1;
+            if (ct == 0) {
+                const int y = sm->cur.y[di];
+                const float D = sm->D;
+                const float cnew = first_draw ? 0.f : sm->cbar + D;
+                const float Pbs = sm->Pbs, Qbs = sm->Qbs;
+                const float Rj = first_draw ? ((Qbs - Pbs) - pbar) + pbar * Pbs
+                                            : sm->Rs * Qbs - (pbar + sm->Ts) * (1.f - Qbs);
+                sm->Rj = Rj;
+                float R, Qy, abar_num;
+                if (y == xs) {
+                    Qy = 1.f - Qbs;
+                    R = first_draw ? (1.f - pbar) * (1.f - Pbs) : sm->Rs;
+                    abar_num = fmaxf(-Rj, 0.f);
+                } else {
+                    const ProbS Py = prob_s(sm, true, y, sm->cur.gT[di], c);
+                    const ProbS Qp = prob_s(sm, false, y, sm->cur.gD[di], c);
+                    Qy = Qp.P;
+                    R = first_draw ? p * Py.P : fmaxf((1.f - pbar) * Py.P - (1.f + sm->cbar) * Qp.P, 0.f);
+                    abar_num = fmaxf((1.f + cnew) * Qp.P - (1.f - pbar) * Py.P, 0.f);
+                }
+                float a, abar;
+                const float ratio = (D > 0.f && Qy > 0.f) ? (R / D) / Qy : INFINITY;
+                if (ratio >= 1.f) {
+                    a = 1.f;
+                    abar = 0.f;
+                } else if (!(R > 0.f)) {
+                    a = 0.f;
+                    abar = 1.f;
+                } else {
+                    a = ratio;
+                    abar = fminf((abar_num / D) / Qy, 1.f);
+                }
+                sm->cbar = cnew;
+                pb.ws.a[sbase + k2] = a;
+                bool first_of_token = true;  // this draw's child is new: it owns it
+                for (int e = 0; e < di; ++e) first_of_token &= sm->cur.y[e] != y;
+                if (pb.mode != SDV_MODE_TOKEN) {
+                    const size_t sc = sbase + K + k2;
+                    if (first_of_token) {  // child first reached by this draw
+                        pb.ws.pbar[sc] = abar;
+                        st_release(&pb.ws.ready[sc], 1);
+                    }
+                }
+                sm->aT = p / sm->zT;
+                sm->aD = (1.f + cnew) / sm->zD;
+            }
+            cbar_sync();
+            const float aT = sm->aT, aD = sm->aD;
+            const int xs_ch = xs >= 0 ? xs / EPU / kChunk : -1;  // x* is carried apart: its chunk skips it
+            float tot = 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < nc; ++ch, ++g) {
+                const int s = g % kStages;
+                if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
+                float w = 0.f;
+#pragma unroll
+                for (int i = 0; i < kUPT; ++i) {
+                    const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
+                    if (ug < n_units) {
+                        float t[EPU], d[EPU];
+                        unpack_masked<DT>(sm->ring[s][0][ul], ug * EPU, V, t);
+                        unpack_masked<DT>(sm->ring[s][1][ul], ug * EPU, V, d);
+                        if (ch != xs_ch) {
+#pragma unroll
+                            for (int e = 0; e < EPU; ++e)
+                                w += res_term_s(ex2(fmaf(t[e], c, gnegT)), ex2(fmaf(d[e], c, gnegD)), aT, aD);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < EPU; ++e) {
+                                const float r = res_term_s(ex2(fmaf(t[e], c, gnegT)), ex2(fmaf(d[e], c, gnegD)), aT, aD);
+                                w += (ug * EPU + e == xs) ? 0.f : r;
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm->empty[s]);
+                tot += w;
+                if (last) {
+                    const float ws = warp_sum(w);
+                    if (lane == 0) sm->table[ch][cw] = ws;
+                }
+            }
+            tot = warp_sum(tot);
+            if (lane == 0) sm->redf[2][cw] = tot;
+            cbar_sync();
+            if (ct == 0) {
+                float Sj = 0.f;
+                for (int i = 0; i < kSW; ++i) Sj += sm->redf[2][i];
+                if (xs >= 0) {  // the sweeps left x* out: their sum is the mass elsewhere
+                    const float Rs = fmaxf(sm->Rj, 0.f);
+                    sm->Ts = Sj;
+                    sm->Rs = Rs;
+                    Sj += Rs;
+                    if (last) {
+                        const int ux = xs / EPU;
+                        sm->table[ux / kChunk][(ux % kChunk) / kWU] += Rs;
+                    }
+                }
+                sm->S = fmaxf(Sj, 0.f);
+                sm->D = pbar + sm->S;
+                sm->use_res = sm->S > 0.f;
+            }
+        }
+        if (leaf) {
+            // bonus: a target-only pass builds the table of P's mass
+#pragma unroll 1
+            for (int ch = 0; ch < nc; ++ch, ++g) {
+                const int s = g % kStages;
+                if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
+                float w = 0.f;
+#pragma unroll
+                for (int i = 0; i < kUPT; ++i) {
+                    const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
+                    if (ug < n_units) w += unit_sum<DT>(sm->ring[s][0][ul], ug * EPU, V, c, gnegT);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm->empty[s]);
+                const float ws = warp_sum(w);
+                if (lane == 0) sm->table[ch][cw] = ws;
+            }
+        }
+        cbar_sync();
+        const bool use_res = sm->use_res != 0;
+        if (!leaf && !use_res) {
+            // S = 0 (rare): the correction comes from P; build its table
+            // from L2 directly
+            for (int ch = 0; ch < nc; ++ch) {
+                float w = 0.f;
+#pragma unroll
+                for (int i = 0; i < kUPT; ++i) {
+                    const int ug = ch * kChunk + unit_local(cw, i, lane);
+                    if (ug < n_units)
+                        w += unit_sum<DT>(__ldg(reinterpret_cast<const uint4*>(gT) + ug), ug * EPU, V, c, gnegT);
+                }
+                const float ws = warp_sum(w);
+                if (lane == 0) sm->table[ch][cw] = ws;
+            }
+            cbar_sync();
+        }
+
+        // ---- the candidate correction: inverse CDF over the table ----
+        if (cw == 0) {
+            // lanes scan the table in index order, 32 entries at a time
+            const int n_ent = nc * kSW;
+            const float* tab = &sm->table[0][0];
+            float run = 0.f, Stot = 0.f;
+            for (int i = lane; i < ((n_ent + 31) & ~31); i += 32) Stot += i < n_ent ? tab[i] : 0.f;
+            Stot = warp_sum(Stot);
+            const float thr = sm->cur.usample * Stot;
+            int found = -1, last_nz = -1;
+            float fbase = 0.f, lbase = 0.f;
+            for (int i0 = 0; i0 < n_ent && found < 0; i0 += 32) {
+                const int i = i0 + lane;
+                const float v = i < n_ent ? tab[i] : 0.f;
+                float incl = v;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float n = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += n;
+                }
+                const unsigned cross = __ballot_sync(0xffffffffu, v > 0.f && run + incl > thr);
+                const unsigned nz = __ballot_sync(0xffffffffu, v > 0.f);
+                if (cross) {
+                    const int l = __ffs(cross) - 1;
+                    found = i0 + l;
+                    fbase = run + __shfl_sync(0xffffffffu, incl - v, l);
+                } else if (nz) {
+                    const int l = 31 - __clz(nz);
+                    last_nz = i0 + l;
+                    lbase = run + __shfl_sync(0xffffffffu, incl - v, l);
+                }
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (found < 0) {
+                found = last_nz;
+                fbase = lbase;
+            }
+            if (lane == 0) {
+                sm->thr = thr;
+                sm->base = fbase;
+                sm->pick_c = (found < 0 || sm->bad) ? -1 : found / kSW;
+                sm->pick_w = found < 0 ? 0 : found % kSW;
+            }
+        }
+        cbar_sync();
+        if (sm->pick_c >= 0 && cw == sm->pick_w) {
+            // the chosen warp re-reads its units of the chunk (from L2), in
+            // index order: sub-unit i, then lane
+            const float local = sm->thr - sm->base;
+            const float aT = sm->aT, aD = sm->aD;
+            float run = 0.f;
+            int chosen = -1, lastx = -1;
+#pragma unroll 1
+            for (int i = 0; i < kUPT && chosen < 0; ++i) {
+                const int ug = sm->pick_c * kChunk + unit_local(cw, i, lane);
+                float vals[EPU];
+                float lsum = 0.f;
+                int lnz = -1;
+                {
+                    float t[EPU], d[EPU];
+                    if (ug < n_units) {
+                        unpack_masked<DT>(__ldg(reinterpret_cast<const uint4*>(gT) + ug), ug * EPU, V, t);
+                        if (use_res)
+                            unpack_masked<DT>(__ldg(reinterpret_cast<const uint4*>(gD) + ug), ug * EPU, V, d);
+                    }
+#pragma unroll
+                    for (int e = 0; e < EPU; ++e) {
+                        float wx = 0.f;
+                        if (ug < n_units) {
+                            const float eT = ex2(fmaf(t[e], c, gnegT));
+                            wx = use_res ? res_term_s(eT, ex2(fmaf(d[e], c, gnegD)), aT, aD) : eT;
+                            if (use_res && ug * EPU + e == xs) wx = sm->Rs;
+                        }
+                        vals[e] = wx;
+                        lsum += wx;
+                        if (wx > 0.f) lnz = ug * EPU + e;
+                    }
+                }
+                float incl = lsum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float n = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += n;
+                }
+                const unsigned cross = __ballot_sync(0xffffffffu, lsum > 0.f && run + incl > local);
+                const unsigned nz = __ballot_sync(0xffffffffu, lnz >= 0);
+                if (cross) {
+                    const int l = __ffs(cross) - 1;
+                    int pick = -1;
+                    if (lane == l) {
+                        float acc = run + incl - lsum;
+                        for (int e = 0; e < EPU; ++e) {
+                            if (vals[e] > 0.f) {
+                                acc += vals[e];
+                                if (acc > local) {
+                                    pick = ug * EPU + e;
+                                    break;
+                                }
+                            }
+                        }
+                        if (pick < 0) pick = lnz;  // rounding: the lane's last nonzero
+                    }
+                    chosen = __shfl_sync(0xffffffffu, pick, l);
+                } else if (nz) {
+                    lastx = __shfl_sync(0xffffffffu, lnz, 31 - __clz(nz));
+                }
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) pb.ws.tok[slot] = chosen >= 0 ? chosen : lastx;
+        } else if (sm->pick_c < 0 && ct == 0) {
+            pb.ws.tok[slot] = -1;
+        }
+        if (ct == 0) {
+            const float S = sm->S, D = sm->D;
+            pb.ws.h[slot] = leaf ? p : (D > 0.f ? S / D : 1.f);
+            pb.ws.S[slot] = S;
+        }
+        // a timed-out wait anywhere stops every consumer together (the
+        // decision is read after the node's last barrier, so it is uniform)
+        if (timed_out) atomicExch(&sm->abort, 1);
+        cbar_sync();
+        if (*static_cast<volatile int*>(&sm->abort)) {
+            if (ct == 0) {
+                atomicOr(&pb.ws.req[b], SDV_DEV_TIMEOUT);
+                if (pb.device_status) atomicOr(pb.device_status, SDV_DEV_TIMEOUT);
+            }
+            break;
+        }
+    }
+}
+
+}  // namespace
+
+size_t stream_smem_bytes() { return sizeof(StreamSmem); }
+
+cudaError_t launch_stream(const Problem& pb, cudaStream_t st)
+{
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 1;
+    }
+    const void* fn = pb.dtype == SDV_BF16 ? reinterpret_cast<const void*>(stream_kernel<SDV_BF16>)
+                                          : reinterpret_cast<const void*>(stream_kernel<SDV_F32>);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StreamSmem));
+    if (e != cudaSuccess) return e;
+    // at most one node per request and depth per draft
+    const long long upper = (long long)pb.B * (1 + (long long)pb.K * pb.L);
+    const int grid = (int)std::max(1LL, std::min((long long)sms, upper));
+    if (pb.dtype == SDV_BF16)
+        stream_kernel<SDV_BF16><<<grid, kSThreads, sizeof(StreamSmem), st>>>(pb);
+    else
+        stream_kernel<SDV_F32><<<grid, kSThreads, sizeof(StreamSmem), st>>>(pb);
+    return cudaGetLastError();
+}
+
+}  // namespace sdv
