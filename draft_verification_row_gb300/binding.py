@@ -72,7 +72,7 @@ def launch_shape(V, dtype="bf16"):
                                 ctypes.byref(c), ctypes.byref(t), ctypes.byref(s))
     if rc:
         raise SDVError(rc, "sdv_launch_shape")
-    return {"cluster": c.value, "threads": t.value, "smem_bytes": s.value}
+    return {"ctas_per_sm": c.value, "threads": t.value, "smem_bytes": s.value}
 
 
 def set_profile_events(start=None, stop=None):

@@ -8,14 +8,9 @@
 #include "sdv_internal.h"
 
 namespace sdv {
-
-size_t node_smem_bytes(int units_per_cta);
-
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kSmemTarget = 110 * 1024;    // two CTAs per SM
-constexpr int kSmemMax = 227 * 1024;
 
 size_t align_up(size_t n) { return (n + kAlign - 1) / kAlign * kAlign; }
 
@@ -151,33 +146,21 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
     pb.device_status = device_status;
     pb.ws = carve(workspace, B, K, L);
 
-    Shape sh;
-    if (!greedy) {
-        const int rc = choose_shape(V, dtype, &sh);
-        if (rc != SDV_OK) return rc;
-        if (prepare_node_kernel(sh, dtype) != cudaSuccess) {
-            cudaGetLastError();
-            return SDV_ERR_UNSUPPORTED;
-        }
-    }
     if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
     if (cudaMemsetAsync(pb.ws.ncount, 0, sizeof(int) * (L + 2), st) != cudaSuccess) return SDV_ERR_CUDA;
     if (launch_prep(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
     if (!prof_record(g_prof_start, st)) return SDV_ERR_CUDA;
-    const char* kenv = std::getenv("SDV_NODE_KERNEL");
-    const bool cluster_kernel = kenv && std::strcmp(kenv, "cluster") == 0;
     if (greedy) {
         if (launch_argmax(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
-    } else if (!cluster_kernel) {
-        // every node of every depth in one persistent launch
-        if (launch_stream(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
-    } else if (mode == SDV_MODE_TOKEN) {
-        // node weights are all 1: every node of every depth at once
-        if (launch_nodes(pb, sh, 0, L, st) != cudaSuccess) return SDV_ERR_CUDA;
     } else {
-        // a node's weight comes from its parent: one depth at a time
-        for (int j = 0; j <= L; ++j)
-            if (launch_nodes(pb, sh, j, j, st) != cudaSuccess) return SDV_ERR_CUDA;
+        // every node of every depth in one persistent launch; a node's
+        // weight comes from its parent through a flag
+        const cudaError_t e = launch_stream(pb, st);
+        if (e == cudaErrorInvalidValue || e == cudaErrorNoKernelImageForDevice) {
+            cudaGetLastError();
+            return SDV_ERR_UNSUPPORTED;  // e.g. not enough shared memory on this device
+        }
+        if (e != cudaSuccess) return SDV_ERR_CUDA;
     }
     if (!prof_record(g_prof_stop, st)) return SDV_ERR_CUDA;
     if (launch_decide(pb, greedy, st) != cudaSuccess) return SDV_ERR_CUDA;
@@ -185,41 +168,6 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
 }
 
 }  // namespace
-
-int choose_shape(int V, int dtype, Shape* s)
-{
-    if (V < 1 || V > SDV_MAX_V || (dtype != SDV_F32 && dtype != SDV_BF16)) return SDV_ERR_INVALID;
-    const int epu = dtype == SDV_BF16 ? 8 : 4;
-    const int n_units = (V + epu - 1) / epu;
-    int C = 1;
-    const char* env = std::getenv("SDV_CLUSTER");
-    if (env && *env) {
-        C = std::atoi(env);
-        if (C != 1 && C != 2 && C != 4 && C != 8 && C != 16) return SDV_ERR_INVALID;
-    } else {
-        while (C < 16 && (size_t)(n_units + C - 1) / C * 32 > (size_t)kSmemTarget) C *= 2;
-    }
-    for (;; C *= 2) {
-        if (C > 16) return SDV_ERR_UNSUPPORTED;
-        const int upc = (n_units + C - 1) / C;
-        int threads = upc >= 1024 ? 512 : (upc >= 256 ? 256 : 128);
-        const char* tenv = std::getenv("SDV_THREADS");
-        if (tenv && *tenv) {
-            threads = std::atoi(tenv);
-            if (threads != 128 && threads != 256 && threads != 512) return SDV_ERR_INVALID;
-        }
-        int eu = (upc + threads - 1) / threads;
-        if (eu % 2 == 0) ++eu;  // odd: 16-byte loads of a warp hit distinct banks
-        const size_t smem = node_smem_bytes(upc);
-        if (smem > (size_t)kSmemMax) continue;
-        s->cluster = C;
-        s->threads = threads;
-        s->units_per_cta = upc;
-        s->units_per_thr = eu;
-        s->smem = (int)smem;
-        return SDV_OK;
-    }
-}
 
 }  // namespace sdv
 
@@ -263,14 +211,12 @@ int sdv_set_profile_events(void* start, void* stop)
     return SDV_OK;
 }
 
-int sdv_launch_shape(int V, int dtype, int* cluster, int* threads, int* smem_bytes)
+int sdv_launch_shape(int V, int dtype, int* ctas_per_sm, int* threads, int* smem_bytes)
 {
-    sdv::Shape s;
-    const int rc = sdv::choose_shape(V, dtype, &s);
-    if (rc != SDV_OK) return rc;
-    if (cluster) *cluster = s.cluster;
-    if (threads) *threads = s.threads;
-    if (smem_bytes) *smem_bytes = s.smem;
+    if (V < 1 || V > SDV_MAX_V || (dtype != SDV_F32 && dtype != SDV_BF16)) return SDV_ERR_INVALID;
+    if (ctas_per_sm) *ctas_per_sm = 1;
+    if (threads) *threads = sdv::stream_threads();
+    if (smem_bytes) *smem_bytes = (int)sdv::stream_smem_bytes();
     return SDV_OK;
 }
 

@@ -1,6 +1,6 @@
 // sdv_device.cuh -- device helpers shared by the verification kernels:
-// inline PTX (ex2, NaN-propagating max, mbarrier, 1-D TMA bulk copies),
-// element unpacking of 16-byte units, warp and block reductions.
+// inline PTX (ex2, NaN-propagating max, mbarrier waits), element unpacking
+// of 16-byte units, warp reductions.
 #pragma once
 
 #include <cstdint>
@@ -10,8 +10,6 @@
 namespace sdv {
 namespace {
 
-constexpr int kMaxThreads = 512;
-constexpr int kMaxCluster = 16;
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded waits: 2 s
 
 // ------------------------------------------------------------------------
@@ -91,16 +89,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase)
         if (globaltimer() - t0 > kWaitNs) return false;
     }
     return true;
-}
-
-// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
 }
 
 // ------------------------------------------------------------------------
@@ -205,78 +193,6 @@ __device__ __forceinline__ float warp_max_redux(float v)
     float r;
     asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
     return r;
-}
-
-__device__ __forceinline__ float warp_max_nan(float v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-// Block-wide maxima of two values; every thread gets the result.
-// red must hold 64 floats; ends with a barrier so red can be reused.
-__device__ void block_max2(float& a, float& b, float* red)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    a = warp_max_nan(a);
-    b = warp_max_nan(b);
-    if (lane == 0) {
-        red[warp] = a;
-        red[32 + warp] = b;
-    }
-    __syncthreads();
-    a = -INFINITY;
-    b = -INFINITY;
-    for (int w = 0; w < nw; ++w) {
-        a = max_nan(a, red[w]);
-        b = max_nan(b, red[32 + w]);
-    }
-    __syncthreads();
-}
-
-// Block-wide sums of two floats and two ints, valid in thread 0 only.  One
-// barrier; the caller must pass another barrier before `red` is reused.
-__device__ void block_sum_f2i2_t0(float& a, float& b, int& m, int& n, float* red, int (*ired)[32])
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        a += __shfl_xor_sync(0xffffffffu, a, o);
-        b += __shfl_xor_sync(0xffffffffu, b, o);
-        m += __shfl_xor_sync(0xffffffffu, m, o);
-        n += __shfl_xor_sync(0xffffffffu, n, o);
-    }
-    if (lane == 0) {
-        red[warp] = a;
-        red[32 + warp] = b;
-        ired[0][warp] = m;
-        ired[1][warp] = n;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        a = b = 0.f;
-        m = n = 0;
-        for (int w = 0; w < nw; ++w) {
-            a += red[w];
-            b += red[32 + w];
-            m += ired[0][w];
-            n += ired[1][w];
-        }
-    }
-}
-
-// Block-wide sum valid in thread 0 only (one barrier, same rule).
-__device__ float block_sum_t0(float a, float* red)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    a = warp_sum(a);
-    if (lane == 0) red[warp] = a;
-    __syncthreads();
-    float s = 0.f;
-    if (threadIdx.x == 0)
-        for (int w = 0; w < nw; ++w) s += red[w];
-    return s;
 }
 
 }  // namespace

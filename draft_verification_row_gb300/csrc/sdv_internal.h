@@ -1,5 +1,6 @@
 // sdv_internal.h -- declarations shared by the host API (sdv_api.cu) and
-// the kernels (sdv_kernels.cu).  Not part of the public interface.
+// the kernels (sdv_kernels.cu, sdv_stream.cu).  Not part of the public
+// interface.
 #pragma once
 
 #include <cstddef>
@@ -50,26 +51,17 @@ struct Problem {
     Workspace ws;
 };
 
-// Launch shape of the node kernel for rows of V elements.
-struct Shape {
-    int cluster;       // CTAs sharing one node's rows (vocabulary split)
-    int threads;       // threads per CTA
-    int units_per_cta; // 16-byte units of one row held by each CTA
-    int units_per_thr; // contiguous units per thread (odd: conflict-free)
-    int smem;          // dynamic shared memory bytes per CTA
-};
-
-
 inline size_t slot_count(int B, int K, int L) { return (size_t)B * (size_t)(L + 1) * (size_t)K; }
 
-int choose_shape(int V, int dtype, Shape* s);
-
-// Kernel launchers (sdv_kernels.cu); each returns a cudaError_t.
+// Kernel launchers (sdv_kernels.cu, sdv_stream.cu); each returns a cudaError_t.
 cudaError_t launch_prep(const Problem& pb, cudaStream_t st);
-cudaError_t launch_nodes(const Problem& pb, const Shape& sh, int j_lo, int j_hi, cudaStream_t st);
 cudaError_t launch_argmax(const Problem& pb, cudaStream_t st);
 cudaError_t launch_decide(const Problem& pb, bool greedy, cudaStream_t st);
-cudaError_t prepare_node_kernel(const Shape& sh, int dtype);
 cudaError_t launch_stream(const Problem& pb, cudaStream_t st);
+
+// The node kernel's launch shape: threads per CTA and dynamic shared memory
+// (one persistent CTA per SM).
+int stream_threads();
+size_t stream_smem_bytes();
 
 }  // namespace sdv

@@ -1,20 +1,23 @@
-// sdv_stream.cu -- the streaming node kernel.
+// sdv_stream.cu -- the node kernel: every vocabulary-row computation of a
+// verification call, in one persistent launch.
 //
-// One persistent CTA per SM verifies one draft-trie node at a time; the
-// node's target and draft rows stream through shared memory:
-//   pass 1 (from HBM): per-thread online maxima and softmax normalisers of
-//           both rows, the row maxima counted apart so that 1 - P of a
-//           dominant token stays exact;
+// One CTA per SM verifies one draft-trie node at a time; the node's target
+// and draft rows stream through shared memory:
+//   pass 1 (from HBM): online maxima and softmax normalisers of both rows,
+//           in a warp-uniform reference, the row maxima counted apart so
+//           that 1 - P of a dominant token stays exact;
 //   pass 2 (from L2, once per draw): the residual sweep
 //           S_j = sum_x max(p P(x) - C_j Q(x), 0), and, on the last sweep,
-//           per-chunk per-warp masses for the inverse-CDF sample;
+//           the mass per (chunk, warp) for the inverse-CDF sample;
 //   leaf:   one target-only pass for the bonus sample.
-// Warp 0 produces: it takes nodes from the list the prep kernel built
-// (depth-major) and streams their rows in 16 KB-per-row chunks through a
+// Warp 0 (metadata) takes nodes from the depth-major list the prep kernel
+// built and fills a descriptor queue: draws, their tokens and logits.
+// Warp 1 (copy) streams each node's rows in 16 KB-per-row chunks through a
 // 4-stage ring with 1-D TMA bulk copies (mbarrier full/empty handshake),
 // pass-1 reads marked evict_last and pass-2 reads evict_first in L2.
-// Warps 1..16 consume.  A node's weight p comes from its parent through a
-// flag (release/acquire); waiting happens only before pass 2.  Every wait is
+// Warps 2..17 consume: a warp owns 64 contiguous 16-byte units of each
+// chunk.  A node's weight p comes from its parent through a flag
+// (release/acquire); waiting happens only before pass 2.  Every wait is
 // bounded and a timeout is reported, never a hang or a trap.
 //
 // The rules computed are stated in include/sdv.h (SpecTr-GBV:
@@ -591,8 +594,15 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
         const int xs = sm->xs;
 
         // ---- pass 2: the residual recursion, one sweep per draw ----
-        // (the same recursion and complement forms as the cluster kernel:
-        // R_j(x*) of the shared dominant token x* is carried apart)
+        // R_0 = p P, R_j = max(R_{j-1} - D_{j-1} Q, 0), S_j = sum R_j,
+        // D_j = (1 - p) + S_j.  Scalars are kept as complements (pbar =
+        // 1 - p, cbar = C - 1, Pbs = 1 - P(x*), Qbs = 1 - Q(x*)) so that
+        // nothing cancels when p, P or Q is close to 1.  The shared
+        // dominant token x* (the unique maximum of both rows) is left out
+        // of the sweeps and carried in closed form:
+        //   R_1(x*) = Qbs - Pbs - pbar + pbar Pbs,
+        //   R_j(x*) = R_{j-1}(x*) Qbs - (pbar + T_{j-1}) (1 - Qbs),
+        // with T_{j-1} the sweep's sum over the other tokens.
         for (int di = 0; di < nd && !leaf; ++di) {
             const int k2 = sm->cur.dk[di];
             const bool first_draw = di == 0;
@@ -872,19 +882,18 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
 }  // namespace
 
 size_t stream_smem_bytes() { return sizeof(StreamSmem); }
+int stream_threads() { return kSThreads; }
 
 cudaError_t launch_stream(const Problem& pb, cudaStream_t st)
 {
-    static int sms = 0;
-    if (!sms) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 1;
-    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (sms <= 0) sms = 1;
     const void* fn = pb.dtype == SDV_BF16 ? reinterpret_cast<const void*>(stream_kernel<SDV_BF16>)
                                           : reinterpret_cast<const void*>(stream_kernel<SDV_F32>);
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StreamSmem));
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StreamSmem));
     if (e != cudaSuccess) return e;
     // at most one node per request and depth per draft
     const long long upper = (long long)pb.B * (1 + (long long)pb.K * pb.L);

@@ -177,10 +177,13 @@ size_t sdv_workspace_bytes(int mode, int B, int K, int L, int V);
 /* Static description of a return code (not of device status bits). */
 const char *sdv_status_string(int status);
 
-/* Launch shape the library picks for rows of V elements of dtype: cluster
- * size (CTAs sharing one vocabulary row), threads per CTA and dynamic
- * shared memory per CTA.  Returns SDV_OK or SDV_ERR_INVALID. */
-int sdv_launch_shape(int V, int dtype, int *cluster, int *threads, int *smem_bytes);
+/* Launch shape of the node kernel (the one that reads vocabulary rows) for
+ * rows of V elements of dtype: CTAs per SM (it is persistent, one CTA per
+ * SM, as many CTAs as the device has SMs), threads per CTA and dynamic
+ * shared memory per CTA.  For callers that share the GPU with other work.
+ * Needs no GPU.  Returns SDV_OK or SDV_ERR_INVALID (V or dtype out of
+ * range). */
+int sdv_launch_shape(int V, int dtype, int *ctas_per_sm, int *threads, int *smem_bytes);
 
 /* Fixed scratch of sdv_verify_multidraft_static: 4 MiB of device memory
  * that every GPU loading the library reserves until the process exits. */

@@ -140,12 +140,17 @@ def test_deterministic():
                 np.testing.assert_array_equal(a[key], b[key])
 
 
-@pytest.mark.parametrize("C", ["1", "2", "4", "8", "16"])
-def test_every_cluster_size(C, monkeypatch):
-    monkeypatch.setenv("SDV_CLUSTER", C)
-    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=4, K=4, L=4, V=20011)
+# The node kernel streams rows in chunks of 1024 16-byte units (8192 bf16 or
+# 4096 fp32 logits), 64 contiguous units per warp: vocabularies at and
+# around those boundaries, a tail chunk that only some warps reach, and a
+# tail unit that only part of a warp's lanes reach.
+@pytest.mark.parametrize("V,dtype", [(8191, "bf16"), (8192, "bf16"), (8193, "bf16"), (8192 + 64 * 8, "bf16"),
+                                     (8192 + 40 * 8 + 3, "bf16"), (16384, "bf16"), (4095, "f32"),
+                                     (4096, "f32"), (4096 + 64 * 4 + 1, "f32")])
+def test_chunk_boundaries(V, dtype):
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=4, K=4, L=3, V=V, dtype=dtype)
     for mode in ("token", "multidraft"):
-        P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"C={C}/{mode}")
+        P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"V={V}/{dtype}/{mode}")
 
 
 @pytest.mark.parametrize("mode,K", [("token", 1), ("token", 2), ("block", 1), ("multidraft", 2)])
