@@ -99,6 +99,7 @@ struct StreamSmem {
     NodeDesc qd[kQ];
     NodeDesc cur;                    // the consumers' copy of the current node
     float table[kMaxChunks][kSW];    // mass of the sampled distribution per (chunk, warp): index order
+    float tableP[kMaxChunks][kSW];   // the same for the target P (last sweep), for S = 0
     float redf[4][kSW];
     int redi[4][kSW];
     unsigned long long firstT, firstD;  // (first index of the row maximum << 32) | partner logit bits
@@ -113,11 +114,19 @@ struct StreamSmem {
 };
 
 // Online statistics of one row, per thread, in a reference shared by the
-// warp: e(x) = 2^(x c - m c) with m the largest logit the warp has seen.
-// z sums the thread's elements below m; cnt counts its elements equal to m
-// (first: the lowest such index, partner: the other row's logit there).
-// The reference moves once per chunk, uniformly across the warp, so only
-// the lane holding a new maximum ever leaves the branch-free path.
+// warp: e(x) = 2^(x c - m c) with m the largest logit the warp has seen in
+// earlier chunks.  z sums the thread's elements below the row maximum; cnt
+// counts its elements equal to it (first: the lowest such index, partner:
+// the other row's logit there).
+//
+// A chunk is summed against the reference of the chunks before it, and
+// the reference moves after the chunk (one redux.sync, its latency hidden
+// behind the chunk's exponentials).  A lane whose chunk reaches the
+// reference (a new maximum, or a tie) does not add that chunk: it only
+// remembers the chunk (d0, d1), and after the pass re-reads those units
+// (from L2) and sums them against the final maximum, counting the elements
+// equal to it apart.  Such chunks are rare (a handful per row per warp);
+// a lane with more than two takes a synchronous, exact path instead.
 struct Online {
     float m = -INFINITY;
     float neg = INFINITY;
@@ -125,6 +134,8 @@ struct Online {
     int cnt = 0;
     int first = 0x7fffffff;
     float partner = 0.f;
+    int nd = 0;
+    int d0 = 0, d1 = 0;
 };
 
 // Unit maximum; the last unit of a row may extend past V.
@@ -141,10 +152,9 @@ __device__ __forceinline__ float unit_max_masked(const uint4& u, int x0, int V)
     return um;
 }
 
-// Move the warp's reference to the chunk's maximum cm (warp-uniform).
-__device__ __forceinline__ void online_rebase(Online& s, float cm, float c)
+// Move the warp's reference to wm (warp-uniform) if it is larger (or NaN).
+__device__ __forceinline__ void online_rebase(Online& s, float wm, float c)
 {
-    const float wm = warp_max_redux(cm);
     if (wm > s.m || wm != wm) {
         const float nneg = -(wm * c);
         s.z = s.z * ex2(nneg - s.neg) + (s.cnt > 0 ? (float)s.cnt * ex2(fmaf(s.m, c, nneg)) : 0.f);
@@ -156,8 +166,7 @@ __device__ __forceinline__ void online_rebase(Online& s, float cm, float c)
 }
 
 // Sum of one unit's elements below the reference, counting those equal to
-// it apart (cnt, first, partner).  Only a unit whose maximum equals the
-// reference (it holds it, or ties it) comes here.
+// it apart (cnt, first, partner).  o is the same unit of the other row.
 template <int DT, bool OTHER>
 __device__ __forceinline__ float careful_unit(Online& s, const uint4 u, const uint4 o, int x0, int V, float c)
 {
@@ -213,10 +222,56 @@ __device__ __forceinline__ float chunk_max(const uint4 (&u)[kUPT], int ug0, int 
     return m;
 }
 
+// A lane whose chunk reaches the reference sets the chunk aside (d0, d1),
+// or, with no room left, flags it for the exact path.
+__device__ __forceinline__ bool set_aside(Online& s, bool sp, int ch)
+{
+    if (!sp) return false;
+    if (s.nd < 2) {
+        s.d1 = s.d0;
+        s.d0 = ch;
+        ++s.nd;
+        return false;
+    }
+    return true;
+}
+
+// After the pass: the set-aside chunks of this lane, re-read and summed
+// against the final maximum.
+template <int DT, bool OTHER>
+__device__ __forceinline__ void online_finish(Online& s, const char* row, const char* other, int cw, int lane,
+                                              int n_units, int V, float c)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+    if (!(s.m > -INFINITY)) return;
+    const int n = s.nd;
+    s.nd = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        if (k < n) {
+            const int ug0 = (k == 0 ? s.d0 : s.d1) * kChunk + unit_local(cw, 0, lane);
+            uint4 u[kUPT], o[kUPT];
+#pragma unroll
+            for (int i = 0; i < kUPT; ++i) {
+                const int ug = ug0 + i * 32;
+                u[i] = o[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (ug < n_units) {
+                    u[i] = __ldg(reinterpret_cast<const uint4*>(row) + ug);
+                    if (OTHER) o[i] = __ldg(reinterpret_cast<const uint4*>(other) + ug);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kUPT; ++i) {
+                const int ug = ug0 + i * 32;
+                if (ug < n_units) s.z += careful_unit<DT, OTHER>(s, u[i], o[i], ug * EPU, V, c);
+            }
+        }
+    }
+}
+
 // Pass 1 over one node's rows: OTHER is false for a leaf (target row only).
-// Every unit is summed on the branch-free path; in the few chunks where a
-// lane holds a unit at the reference, those units are summed again with
-// the maxima counted apart (the check is warp-uniform).
+// Both rows' exponentials sit in one branch-free block; the reference
+// checks and moves are warp-uniform around it.
 template <int DT, bool OTHER>
 __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, uint32_t& g, bool& timed_out,
                                       int nc, int n_units, int V, float c, int cw, int lane)
@@ -242,38 +297,42 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
         if (lane == 0) mbar_arrive(&sm->empty[s]);  // the units are in registers now
         const float cmT = chunk_max<DT>(t, ug0, n_units, V, tail);
         const float cmD = OTHER ? chunk_max<DT>(d, ug0, n_units, V, tail) : -INFINITY;
-        online_rebase(sT, cmT, c);
-        if (OTHER) online_rebase(sD, cmD, c);
-        // a reference of -inf means nothing finite yet (nothing to add);
-        // NaN means the row is unusable
+        const float wmT = warp_max_redux(cmT);
+        const float wmD = OTHER ? warp_max_redux(cmD) : -INFINITY;
+        // nothing finite seen yet: move first (the first chunk, in practice)
+        if (!(sT.m > -INFINITY) || (OTHER && !(sD.m > -INFINITY))) {
+            if (!(sT.m > -INFINITY)) online_rebase(sT, wmT, c);
+            if (OTHER && !(sD.m > -INFINITY)) online_rebase(sD, wmD, c);
+        }
         const bool liveT = sT.m > -INFINITY, liveD = OTHER && sD.m > -INFINITY;
-        float zt[kUPT], zd[kUPT];
+        float zt = 0.f, zd = 0.f;
 #pragma unroll
         for (int i = 0; i < kUPT; ++i) {
             const int ug = ug0 + i * 32;
-            zt[i] = zd[i] = 0.f;
             if (!tail || ug < n_units) {
-                if (liveT) zt[i] = unit_sum<DT>(t[i], ug * EPU, V, c, sT.neg);
-                if (liveD) zd[i] = unit_sum<DT>(d[i], ug * EPU, V, c, sD.neg);
+                zt += unit_sum<DT>(t[i], ug * EPU, V, c, sT.neg);
+                if (OTHER) zd += unit_sum<DT>(d[i], ug * EPU, V, c, sD.neg);
             }
         }
-        const bool spT = liveT && cmT == sT.m, spD = liveD && cmD == sD.m;
-        if (__any_sync(0xffffffffu, spT || spD)) {
+        // a chunk that reaches the reference is not added here
+        const bool spT = liveT && cmT >= sT.m, spD = liveD && cmD >= sD.m;
+        if (liveT) sT.z += spT ? 0.f : zt;
+        if (liveD) sD.z += spD ? 0.f : zd;
+        const bool ovT = set_aside(sT, spT, ch), ovD = set_aside(sD, spD, ch);
+        // the chunk's sums are in the old reference: move it now
+        online_rebase(sT, wmT, c);
+        if (OTHER) online_rebase(sD, wmD, c);
+        if (__any_sync(0xffffffffu, ovT || ovD)) {
+            // lanes with no room left: their units, exactly, against the
+            // moved reference (which is at least their maximum)
 #pragma unroll
             for (int i = 0; i < kUPT; ++i) {
                 const int ug = ug0 + i * 32;
-                if (ug < n_units) {
-                    if (spT && unit_max_masked<DT>(t[i], ug * EPU, V) == sT.m)
-                        zt[i] = careful_unit<DT, OTHER>(sT, t[i], d[i], ug * EPU, V, c);
-                    if (spD && unit_max_masked<DT>(d[i], ug * EPU, V) == sD.m)
-                        zd[i] = careful_unit<DT, true>(sD, d[i], t[i], ug * EPU, V, c);
+                if (!tail || ug < n_units) {
+                    if (ovT) sT.z += careful_unit<DT, OTHER>(sT, t[i], d[i], ug * EPU, V, c);
+                    if (ovD) sD.z += careful_unit<DT, true>(sD, d[i], t[i], ug * EPU, V, c);
                 }
             }
-        }
-#pragma unroll
-        for (int i = 0; i < kUPT; ++i) {
-            sT.z += zt[i];
-            if (OTHER) sD.z += zd[i];
         }
     }
 }
@@ -281,6 +340,62 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
 __device__ __forceinline__ float res_term_s(float eT, float eD, float aT, float aD)
 {
     return fmaxf(__fmaf_rn(eT, aT, -__fmul_rn(eD, aD)), 0.f);
+}
+
+// One residual sweep over a node's rows (from the ring): returns this
+// thread's share of S_j = sum over x != x* of max(aT e_T(x) - aD e_D(x), 0).
+// The last sweep (LAST) also fills the sampling tables: the residual's mass
+// and the target's mass per (chunk, warp).
+template <int DT, bool LAST>
+__device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_out, int nc, int n_units, int V,
+                                       float c, float gnegT, float gnegD, float aT, float aD, int xs, int cw,
+                                       int lane)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+    const int xs_ch = xs >= 0 ? xs / EPU / kChunk : -1;  // x* is carried apart: its chunk skips it
+    float tot = 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < nc; ++ch, ++g) {
+        const int s = g % kStages;
+        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
+        float w = 0.f, wp = 0.f;
+#pragma unroll
+        for (int i = 0; i < kUPT; ++i) {
+            const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
+            if (ug < n_units) {
+                float t[EPU], d[EPU];
+                unpack_masked<DT>(sm->ring[s][0][ul], ug * EPU, V, t);
+                unpack_masked<DT>(sm->ring[s][1][ul], ug * EPU, V, d);
+                if (ch != xs_ch) {
+#pragma unroll
+                    for (int e = 0; e < EPU; ++e) {
+                        const float eT = ex2(fmaf(t[e], c, gnegT));
+                        w += res_term_s(eT, ex2(fmaf(d[e], c, gnegD)), aT, aD);
+                        if (LAST) wp += eT;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPU; ++e) {
+                        const float eT = ex2(fmaf(t[e], c, gnegT));
+                        const float r = res_term_s(eT, ex2(fmaf(d[e], c, gnegD)), aT, aD);
+                        w += (ug * EPU + e == xs) ? 0.f : r;
+                        if (LAST) wp += eT;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->empty[s]);
+        tot += w;
+        if (LAST) {
+            const float ws = warp_sum(w), wps = warp_sum(wp);
+            if (lane == 0) {
+                sm->table[ch][cw] = ws;
+                sm->tableP[ch][cw] = wps;
+            }
+        }
+    }
+    return tot;
 }
 
 // Combine the consumers' online statistics of one row (all consumer
@@ -549,10 +664,14 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
 
         // ---- pass 1: online statistics ----
         Online sT, sD;
-        if (leaf)
+        if (leaf) {
             pass1<DT, false>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
-        else
+            online_finish<DT, false>(sT, gT, nullptr, cw, lane, n_units, V, c);
+        } else {
             pass1<DT, true>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
+            online_finish<DT, true>(sT, gT, gD, cw, lane, n_units, V, c);
+            online_finish<DT, true>(sD, gD, gT, cw, lane, n_units, V, c);
+        }
         combine_row(sm, sT, true, c, ct);
         if (!leaf) combine_row(sm, sD, false, c, ct);
 
@@ -655,41 +774,8 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
             }
             cbar_sync();
             const float aT = sm->aT, aD = sm->aD;
-            const int xs_ch = xs >= 0 ? xs / EPU / kChunk : -1;  // x* is carried apart: its chunk skips it
-            float tot = 0.f;
-#pragma unroll 1
-            for (int ch = 0; ch < nc; ++ch, ++g) {
-                const int s = g % kStages;
-                if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
-                float w = 0.f;
-#pragma unroll
-                for (int i = 0; i < kUPT; ++i) {
-                    const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
-                    if (ug < n_units) {
-                        float t[EPU], d[EPU];
-                        unpack_masked<DT>(sm->ring[s][0][ul], ug * EPU, V, t);
-                        unpack_masked<DT>(sm->ring[s][1][ul], ug * EPU, V, d);
-                        if (ch != xs_ch) {
-#pragma unroll
-                            for (int e = 0; e < EPU; ++e)
-                                w += res_term_s(ex2(fmaf(t[e], c, gnegT)), ex2(fmaf(d[e], c, gnegD)), aT, aD);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < EPU; ++e) {
-                                const float r = res_term_s(ex2(fmaf(t[e], c, gnegT)), ex2(fmaf(d[e], c, gnegD)), aT, aD);
-                                w += (ug * EPU + e == xs) ? 0.f : r;
-                            }
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm->empty[s]);
-                tot += w;
-                if (last) {
-                    const float ws = warp_sum(w);
-                    if (lane == 0) sm->table[ch][cw] = ws;
-                }
-            }
+            float tot = last ? sweep<DT, true>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, aT, aD, xs, cw, lane)
+                             : sweep<DT, false>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, aT, aD, xs, cw, lane);
             tot = warp_sum(tot);
             if (lane == 0) sm->redf[2][cw] = tot;
             cbar_sync();
@@ -732,19 +818,9 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
         cbar_sync();
         const bool use_res = sm->use_res != 0;
         if (!leaf && !use_res) {
-            // S = 0 (rare): the correction comes from P; build its table
-            // from L2 directly
-            for (int ch = 0; ch < nc; ++ch) {
-                float w = 0.f;
-#pragma unroll
-                for (int i = 0; i < kUPT; ++i) {
-                    const int ug = ch * kChunk + unit_local(cw, i, lane);
-                    if (ug < n_units)
-                        w += unit_sum<DT>(__ldg(reinterpret_cast<const uint4*>(gT) + ug), ug * EPU, V, c, gnegT);
-                }
-                const float ws = warp_sum(w);
-                if (lane == 0) sm->table[ch][cw] = ws;
-            }
+            // S = 0: the correction comes from P, whose table the last sweep
+            // built beside the residual's
+            for (int i = ct; i < nc * kSW; i += kCT) (&sm->table[0][0])[i] = (&sm->tableP[0][0])[i];
             cbar_sync();
         }
 
