@@ -107,7 +107,7 @@ struct StreamSmem {
     // scalar state (consumer thread 0)
     float MT, MD, gnegT, gnegD, zT, zD, zrestT, zrestD, emaxT, emaxD;
     int uT, uD;
-    float S, D, cbar, pbar, Pbs, Qbs, Rs, Ts, Rj, aT, aD;
+    float S, D, cbar, pbar, Pbs, Qbs, Rs, Ts, Rj, aT, aD, rD;
     int xs, use_res, bad;
     float thr, base;
     int pick_c, pick_w;
@@ -337,10 +337,11 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
     }
 }
 
-__device__ __forceinline__ float res_term_s(float eT, float eD, float aT, float aD)
-{
-    return fmaxf(__fmaf_rn(eT, aT, -__fmul_rn(eD, aD)), 0.f);
-}
+// The residual term of one token divided by aT = p / Z_T:
+// max(aT e_T - aD e_D, 0) / aT = max(e_T - r e_D, 0), r = aD / aT.  One FMA
+// per token; the sums are scaled by aT once.  (With p = 0, aT = 0 and r is
+// the largest float: every term is finite and scaled to 0.)
+__device__ __forceinline__ float res_unscaled(float eT, float eD, float r) { return fmaxf(fmaf(-r, eD, eT), 0.f); }
 
 // One residual sweep over a node's rows (from the ring): returns this
 // thread's share of S_j = sum over x != x* of max(aT e_T(x) - aD e_D(x), 0).
@@ -348,7 +349,7 @@ __device__ __forceinline__ float res_term_s(float eT, float eD, float aT, float 
 // and the target's mass per (chunk, warp).
 template <int DT, bool LAST>
 __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_out, int nc, int n_units, int V,
-                                       float c, float gnegT, float gnegD, float aT, float aD, int xs, int cw,
+                                       float c, float gnegT, float gnegD, float aT, float r, int xs, int cw,
                                        int lane)
 {
     constexpr int EPU = Elem<DT>::kPerUnit;
@@ -370,15 +371,15 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
 #pragma unroll
                     for (int e = 0; e < EPU; ++e) {
                         const float eT = ex2(fmaf(t[e], c, gnegT));
-                        w += res_term_s(eT, ex2(fmaf(d[e], c, gnegD)), aT, aD);
+                        w += res_unscaled(eT, ex2(fmaf(d[e], c, gnegD)), r);
                         if (LAST) wp += eT;
                     }
                 } else {
 #pragma unroll
                     for (int e = 0; e < EPU; ++e) {
                         const float eT = ex2(fmaf(t[e], c, gnegT));
-                        const float r = res_term_s(eT, ex2(fmaf(d[e], c, gnegD)), aT, aD);
-                        w += (ug * EPU + e == xs) ? 0.f : r;
+                        const float rt = res_unscaled(eT, ex2(fmaf(d[e], c, gnegD)), r);
+                        w += (ug * EPU + e == xs) ? 0.f : rt;
                         if (LAST) wp += eT;
                     }
                 }
@@ -390,12 +391,12 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
         if (LAST) {
             const float ws = warp_sum(w), wps = warp_sum(wp);
             if (lane == 0) {
-                sm->table[ch][cw] = ws;
+                sm->table[ch][cw] = aT * ws;
                 sm->tableP[ch][cw] = wps;
             }
         }
     }
-    return tot;
+    return aT * tot;
 }
 
 // Combine the consumers' online statistics of one row (all consumer
@@ -612,7 +613,8 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
             bool ok = true;
             for (int ps = 0; ps < passes && ok; ++ps) {
                 const bool with_d = !leaf;
-                const uint64_t pol = ps == 0 ? pol_last : pol_first;
+                // keep the rows in L2 until the node's last pass over them
+                const uint64_t pol = ps == passes - 1 ? pol_first : pol_last;
                 for (int ch = 0; ch < nc; ++ch, ++g) {
                     const int s = g % kStages;
                     const uint32_t use = g / kStages;
@@ -771,11 +773,12 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
                 }
                 sm->aT = p / sm->zT;
                 sm->aD = (1.f + cnew) / sm->zD;
+                sm->rD = sm->aT > 0.f ? sm->aD / sm->aT : 3.402823466e38f;
             }
             cbar_sync();
-            const float aT = sm->aT, aD = sm->aD;
-            float tot = last ? sweep<DT, true>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, aT, aD, xs, cw, lane)
-                             : sweep<DT, false>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, aT, aD, xs, cw, lane);
+            const float aT = sm->aT, rD = sm->rD;
+            float tot = last ? sweep<DT, true>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, aT, rD, xs, cw, lane)
+                             : sweep<DT, false>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, aT, rD, xs, cw, lane);
             tot = warp_sum(tot);
             if (lane == 0) sm->redf[2][cw] = tot;
             cbar_sync();
@@ -873,7 +876,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
             // the chosen warp re-reads its units of the chunk (from L2), in
             // index order: sub-unit i, then lane
             const float local = sm->thr - sm->base;
-            const float aT = sm->aT, aD = sm->aD;
+            const float aT = sm->aT, rD = sm->rD;
             float run = 0.f;
             int chosen = -1, lastx = -1;
 #pragma unroll 1
@@ -894,7 +897,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
                         float wx = 0.f;
                         if (ug < n_units) {
                             const float eT = ex2(fmaf(t[e], c, gnegT));
-                            wx = use_res ? res_term_s(eT, ex2(fmaf(d[e], c, gnegD)), aT, aD) : eT;
+                            wx = use_res ? aT * res_unscaled(eT, ex2(fmaf(d[e], c, gnegD)), rD) : eT;
                             if (use_res && ug * EPU + e == xs) wx = sm->Rs;
                         }
                         vals[e] = wx;
