@@ -214,7 +214,7 @@ int sdv_set_profile_events(void* start, void* stop)
 int sdv_launch_shape(int V, int dtype, int* ctas_per_sm, int* threads, int* smem_bytes)
 {
     if (V < 1 || V > SDV_MAX_V || (dtype != SDV_F32 && dtype != SDV_BF16)) return SDV_ERR_INVALID;
-    if (ctas_per_sm) *ctas_per_sm = 1;
+    if (ctas_per_sm) *ctas_per_sm = sdv::stream_ctas_per_sm();
     if (threads) *threads = sdv::stream_threads();
     if (smem_bytes) *smem_bytes = (int)sdv::stream_smem_bytes();
     return SDV_OK;

@@ -59,8 +59,9 @@ cudaError_t launch_argmax(const Problem& pb, cudaStream_t st);
 cudaError_t launch_decide(const Problem& pb, bool greedy, cudaStream_t st);
 cudaError_t launch_stream(const Problem& pb, cudaStream_t st);
 
-// The node kernel's launch shape: threads per CTA and dynamic shared memory
-// (one persistent CTA per SM).
+// The node kernel's launch shape: persistent CTAs per SM, threads per CTA
+// and dynamic shared memory.
+int stream_ctas_per_sm();
 int stream_threads();
 size_t stream_smem_bytes();
 

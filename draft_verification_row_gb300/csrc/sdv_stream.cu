@@ -31,7 +31,8 @@
 namespace sdv {
 namespace {
 
-constexpr int kSW = 16;                  // consumer warps
+constexpr int kCtasPerSm = 2;            // two nodes in flight per SM
+constexpr int kSW = 8;                   // consumer warps
 constexpr int kCT = 32 * kSW;            // consumer threads
 constexpr int kSThreads = kCT + 64;      // plus the metadata warp and the copy warp
 constexpr int kUPT = 2;                  // 16-byte units per consumer thread per row per chunk
@@ -165,6 +166,18 @@ __device__ __forceinline__ void online_rebase(Online& s, float wm, float c)
     }
 }
 
+// Pairwise sum of a unit's terms: a dependency chain of depth log2(N)
+// instead of N (the exponentials of a unit are independent).
+template <int N>
+__device__ __forceinline__ float tree_sum(float (&a)[N])
+{
+#pragma unroll
+    for (int w = 1; w < N; w *= 2)
+#pragma unroll
+        for (int i = 0; i + w < N; i += 2 * w) a[i] += a[i + w];
+    return a[0];
+}
+
 // Sum of one unit's elements below the reference, counting those equal to
 // it apart (cnt, first, partner).  o is the same unit of the other row.
 template <int DT, bool OTHER>
@@ -196,10 +209,9 @@ __device__ __forceinline__ float unit_sum(const uint4& u, int x0, int V, float c
     constexpr int EPU = Elem<DT>::kPerUnit;
     float v[EPU];
     unpack_masked<DT>(u, x0, V, v);
-    float z = 0.f;
 #pragma unroll
-    for (int e = 0; e < EPU; ++e) z += ex2(fmaf(v[e], c, neg));
-    return z;
+    for (int e = 0; e < EPU; ++e) v[e] = ex2(fmaf(v[e], c, neg));
+    return tree_sum(v);
 }
 
 // Unit index of (chunk, warp, sub-unit, lane): a warp's units of a chunk
@@ -270,8 +282,11 @@ __device__ __forceinline__ void online_finish(Online& s, const char* row, const 
 }
 
 // Pass 1 over one node's rows: OTHER is false for a leaf (target row only).
-// Both rows' exponentials sit in one branch-free block; the reference
-// checks and moves are warp-uniform around it.
+// Both rows' exponentials sit in one branch-free block.  A chunk can reach
+// the reference only where one of its terms e = 2^(x c - m c) is at least
+// 1, so a lane whose chunk sum is below 1/2 holds no maximum: the chunk
+// maxima, the warp reduction and the reference moves run only when some
+// lane's sum is not (in practice a few chunks per row and warp).
 template <int DT, bool OTHER>
 __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, uint32_t& g, bool& timed_out,
                                       int nc, int n_units, int V, float c, int cw, int lane)
@@ -295,44 +310,55 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->empty[s]);  // the units are in registers now
-        const float cmT = chunk_max<DT>(t, ug0, n_units, V, tail);
-        const float cmD = OTHER ? chunk_max<DT>(d, ug0, n_units, V, tail) : -INFINITY;
-        const float wmT = warp_max_redux(cmT);
-        const float wmD = OTHER ? warp_max_redux(cmD) : -INFINITY;
-        // nothing finite seen yet: move first (the first chunk, in practice)
+        // nothing finite seen yet: set the reference first (the first chunk,
+        // in practice)
         if (!(sT.m > -INFINITY) || (OTHER && !(sD.m > -INFINITY))) {
-            if (!(sT.m > -INFINITY)) online_rebase(sT, wmT, c);
-            if (OTHER && !(sD.m > -INFINITY)) online_rebase(sD, wmD, c);
+            if (!(sT.m > -INFINITY)) online_rebase(sT, warp_max_redux(chunk_max<DT>(t, ug0, n_units, V, tail)), c);
+            if (OTHER && !(sD.m > -INFINITY))
+                online_rebase(sD, warp_max_redux(chunk_max<DT>(d, ug0, n_units, V, tail)), c);
         }
         const bool liveT = sT.m > -INFINITY, liveD = OTHER && sD.m > -INFINITY;
+        // (a row with nothing finite yet sums against 0: never added)
+        const float negT = liveT ? sT.neg : 0.f, negD = liveD ? sD.neg : 0.f;
         float zt = 0.f, zd = 0.f;
 #pragma unroll
         for (int i = 0; i < kUPT; ++i) {
             const int ug = ug0 + i * 32;
             if (!tail || ug < n_units) {
-                zt += unit_sum<DT>(t[i], ug * EPU, V, c, sT.neg);
-                if (OTHER) zd += unit_sum<DT>(d[i], ug * EPU, V, c, sD.neg);
+                zt += unit_sum<DT>(t[i], ug * EPU, V, c, negT);
+                if (OTHER) zd += unit_sum<DT>(d[i], ug * EPU, V, c, negD);
             }
         }
-        // a chunk that reaches the reference is not added here
-        const bool spT = liveT && cmT >= sT.m, spD = liveD && cmD >= sD.m;
-        if (liveT) sT.z += spT ? 0.f : zt;
-        if (liveD) sD.z += spD ? 0.f : zd;
-        const bool ovT = set_aside(sT, spT, ch), ovD = set_aside(sD, spD, ch);
-        // the chunk's sums are in the old reference: move it now
-        online_rebase(sT, wmT, c);
-        if (OTHER) online_rebase(sD, wmD, c);
-        if (__any_sync(0xffffffffu, ovT || ovD)) {
-            // lanes with no room left: their units, exactly, against the
-            // moved reference (which is at least their maximum)
+        // a sum of 1/2 or more (or NaN) may hold the maximum
+        const bool hotT = liveT && !(zt < 0.5f), hotD = liveD && !(zd < 0.5f);
+        if (__any_sync(0xffffffffu, hotT || hotD)) {
+            const float cmT = hotT ? chunk_max<DT>(t, ug0, n_units, V, tail) : -INFINITY;
+            const float cmD = hotD ? chunk_max<DT>(d, ug0, n_units, V, tail) : -INFINITY;
+            const float wmT = warp_max_redux(cmT);
+            const float wmD = OTHER ? warp_max_redux(cmD) : -INFINITY;
+            // a chunk that reaches the reference is not added here
+            const bool spT = hotT && cmT >= sT.m, spD = hotD && cmD >= sD.m;
+            if (liveT) sT.z += spT ? 0.f : zt;
+            if (liveD) sD.z += spD ? 0.f : zd;
+            const bool ovT = set_aside(sT, spT, ch), ovD = set_aside(sD, spD, ch);
+            // the chunk's sums are in the old reference: move it now
+            online_rebase(sT, wmT, c);
+            if (OTHER) online_rebase(sD, wmD, c);
+            if (__any_sync(0xffffffffu, ovT || ovD)) {
+                // lanes with no room left: their units, exactly, against
+                // the moved reference (which is at least their maximum)
 #pragma unroll
-            for (int i = 0; i < kUPT; ++i) {
-                const int ug = ug0 + i * 32;
-                if (!tail || ug < n_units) {
-                    if (ovT) sT.z += careful_unit<DT, OTHER>(sT, t[i], d[i], ug * EPU, V, c);
-                    if (ovD) sD.z += careful_unit<DT, true>(sD, d[i], t[i], ug * EPU, V, c);
+                for (int i = 0; i < kUPT; ++i) {
+                    const int ug = ug0 + i * 32;
+                    if (!tail || ug < n_units) {
+                        if (ovT) sT.z += careful_unit<DT, OTHER>(sT, t[i], d[i], ug * EPU, V, c);
+                        if (ovD) sD.z += careful_unit<DT, true>(sD, d[i], t[i], ug * EPU, V, c);
+                    }
                 }
             }
+        } else {
+            if (liveT) sT.z += zt;
+            if (liveD) sD.z += zd;
         }
     }
 }
@@ -359,30 +385,33 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
     for (int ch = 0; ch < nc; ++ch, ++g) {
         const int s = g % kStages;
         if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
+        const bool tail = ch == nc - 1;
         float w = 0.f, wp = 0.f;
 #pragma unroll
         for (int i = 0; i < kUPT; ++i) {
             const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
-            if (ug < n_units) {
+            if (!tail || ug < n_units) {
                 float t[EPU], d[EPU];
-                unpack_masked<DT>(sm->ring[s][0][ul], ug * EPU, V, t);
-                unpack_masked<DT>(sm->ring[s][1][ul], ug * EPU, V, d);
-                if (ch != xs_ch) {
-#pragma unroll
-                    for (int e = 0; e < EPU; ++e) {
-                        const float eT = ex2(fmaf(t[e], c, gnegT));
-                        w += res_unscaled(eT, ex2(fmaf(d[e], c, gnegD)), r);
-                        if (LAST) wp += eT;
-                    }
+                if (tail) {
+                    unpack_masked<DT>(sm->ring[s][0][ul], ug * EPU, V, t);
+                    unpack_masked<DT>(sm->ring[s][1][ul], ug * EPU, V, d);
                 } else {
-#pragma unroll
-                    for (int e = 0; e < EPU; ++e) {
-                        const float eT = ex2(fmaf(t[e], c, gnegT));
-                        const float rt = res_unscaled(eT, ex2(fmaf(d[e], c, gnegD)), r);
-                        w += (ug * EPU + e == xs) ? 0.f : rt;
-                        if (LAST) wp += eT;
-                    }
+                    Elem<DT>::unpack(sm->ring[s][0][ul], t);
+                    Elem<DT>::unpack(sm->ring[s][1][ul], d);
                 }
+#pragma unroll
+                for (int e = 0; e < EPU; ++e) {
+                    const float eT = ex2(fmaf(t[e], c, gnegT));
+                    d[e] = res_unscaled(eT, ex2(fmaf(d[e], c, gnegD)), r);
+                    t[e] = eT;
+                }
+                if (ch == xs_ch) {
+#pragma unroll
+                    for (int e = 0; e < EPU; ++e)
+                        if (ug * EPU + e == xs) d[e] = 0.f;
+                }
+                w += tree_sum(d);
+                if (LAST) wp += tree_sum(t);
             }
         }
         __syncwarp();
@@ -483,7 +512,7 @@ __device__ __forceinline__ ProbS prob_s(const StreamSmem* sm, bool is_t, int x, 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
+__global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem pb)
 {
     using E = Elem<DT>;
     constexpr int EPU = E::kPerUnit;
@@ -962,6 +991,7 @@ __global__ void __launch_bounds__(kSThreads, 1) stream_kernel(Problem pb)
 
 size_t stream_smem_bytes() { return sizeof(StreamSmem); }
 int stream_threads() { return kSThreads; }
+int stream_ctas_per_sm() { return kCtasPerSm; }
 
 cudaError_t launch_stream(const Problem& pb, cudaStream_t st)
 {
@@ -976,7 +1006,7 @@ cudaError_t launch_stream(const Problem& pb, cudaStream_t st)
     if (e != cudaSuccess) return e;
     // at most one node per request and depth per draft
     const long long upper = (long long)pb.B * (1 + (long long)pb.K * pb.L);
-    const int grid = (int)std::max(1LL, std::min((long long)sms, upper));
+    const int grid = (int)std::max(1LL, std::min((long long)sms * kCtasPerSm, upper));
     if (pb.dtype == SDV_BF16)
         stream_kernel<SDV_BF16><<<grid, kSThreads, sizeof(StreamSmem), st>>>(pb);
     else

@@ -178,9 +178,9 @@ size_t sdv_workspace_bytes(int mode, int B, int K, int L, int V);
 const char *sdv_status_string(int status);
 
 /* Launch shape of the node kernel (the one that reads vocabulary rows) for
- * rows of V elements of dtype: CTAs per SM (it is persistent, one CTA per
- * SM, as many CTAs as the device has SMs), threads per CTA and dynamic
- * shared memory per CTA.  For callers that share the GPU with other work.
+ * rows of V elements of dtype: CTAs per SM (it is persistent: that many
+ * CTAs per SM of the device), threads per CTA and dynamic shared memory per
+ * CTA.  For callers that share the GPU with other work.
  * Needs no GPU.  Returns SDV_OK or SDV_ERR_INVALID (V or dtype out of
  * range). */
 int sdv_launch_shape(int V, int dtype, int *ctas_per_sm, int *threads, int *smem_bytes);

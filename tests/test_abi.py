@@ -45,9 +45,9 @@ def test_workspace_bytes(lib):
 def test_launch_shape(lib, V, dtype):
     import draft_verification_row_gb300 as sdv
     s = sdv.launch_shape(V, dtype)
-    assert s["ctas_per_sm"] == 1
-    assert 128 * 1024 <= s["smem_bytes"] <= 227 * 1024
-    assert s["threads"] == 576
+    assert s["ctas_per_sm"] >= 1
+    assert s["ctas_per_sm"] * (s["smem_bytes"] + 1024) <= 228 * 1024  # fits an SM's shared memory
+    assert s["threads"] % 32 == 0 and s["ctas_per_sm"] * s["threads"] <= 2048
     with pytest.raises(sdv.SDVError):
         sdv.launch_shape(262145, dtype)
 

@@ -164,22 +164,29 @@ def _pattern_row(kind, V):
     elif kind == 3:    # flat with one spike at the last index
         r = np.zeros(V)
         r[-1] = 6.0
-    else:              # two equal maxima far apart, a wavy floor
+    elif kind == 4:    # two equal maxima far apart, a wavy floor
         r = np.sin(x * 0.37)
         r[3] = r[-5] = 5.0
+    elif kind == 5:    # the first half masked to -inf, as a filtered vocabulary
+        r = np.sin(x * 0.11) * 2.0
+        r[: V // 2] = -np.inf
+    else:              # top-3 filtering: three finite logits, the rest -inf
+        r = np.full(V, -np.inf)
+        r[[V // 7, V // 2, V - 2]] = [1.0, 2.5, 0.5]
     return torch.as_tensor(r, dtype=torch.float32)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_degenerate_rows(dtype):
     """Rows whose maximum ties across lanes and chunks, moves every chunk,
-    or sits at either end: the online normaliser's set-aside and exact
+    or sits at either end, and rows filtered to -inf (half the vocabulary,
+    or all but three tokens): the online normaliser's set-aside and exact
     paths, against the oracle."""
     V = 40007
-    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=10, K=3, L=3, V=V, dtype=dtype)
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=14, K=3, L=3, V=V, dtype=dtype)
     for b in range(batch.B):
-        t = _pattern_row(b % 5, V).to(batch.target.dtype).to(DEV)
-        d = _pattern_row((b // 5 + b + 2) % 5, V).to(batch.draft.dtype).to(DEV)
+        t = _pattern_row(b % 7, V).to(batch.target.dtype).to(DEV)
+        d = _pattern_row((b // 7 + b + 2) % 7, V).to(batch.draft.dtype).to(DEV)
         batch.target[b, :, :, :V] = t
         batch.draft[b, :, :, :V] = d
     for mode in ("token", "multidraft"):
