@@ -103,7 +103,8 @@ struct StreamSmem {
     float tableP[kMaxChunks][kSW];   // the same for the target P (last sweep), for S = 0
     float redf[4][kSW];
     int redi[4][kSW];
-    unsigned long long firstT, firstD;  // (first index of the row maximum << 32) | partner logit bits
+    int firstT, firstD;              // lowest index of each row's maximum
+    uint4 stash[2][kCT][2][kUPT];    // set-aside units: [row][consumer thread][slot][unit]
     int abort;
     // scalar state (consumer thread 0)
     float MT, MD, gnegT, gnegD, zT, zD, zrestT, zrestD, emaxT, emaxD;
@@ -117,24 +118,22 @@ struct StreamSmem {
 // Online statistics of one row, per thread, in a reference shared by the
 // warp: e(x) = 2^(x c - m c) with m the largest logit the warp has seen in
 // earlier chunks.  z sums the thread's elements below the row maximum; cnt
-// counts its elements equal to it (first: the lowest such index, partner:
-// the other row's logit there).
+// counts its elements equal to it (first: the lowest such index).
 //
 // A chunk is summed against the reference of the chunks before it, and
 // the reference moves after the chunk (one redux.sync, its latency hidden
 // behind the chunk's exponentials).  A lane whose chunk reaches the
-// reference (a new maximum, or a tie) does not add that chunk: it only
-// remembers the chunk (d0, d1), and after the pass re-reads those units
-// (from L2) and sums them against the final maximum, counting the elements
-// equal to it apart.  Such chunks are rare (a handful per row per warp);
-// a lane with more than two takes a synchronous, exact path instead.
+// reference (a new maximum, or a tie) does not add that chunk: it copies
+// the chunk's units to its stash in shared memory (chunk indices d0, d1)
+// and, after the pass, sums them against the final maximum, counting the
+// elements equal to it apart.  Such chunks are rare (a handful per row
+// per warp); a lane with more than two takes a synchronous, exact path.
 struct Online {
     float m = -INFINITY;
     float neg = INFINITY;
     float z = 0.f;
     int cnt = 0;
     int first = 0x7fffffff;
-    float partner = 0.f;
     int nd = 0;
     int d0 = 0, d1 = 0;
 };
@@ -179,23 +178,19 @@ __device__ __forceinline__ float tree_sum(float (&a)[N])
 }
 
 // Sum of one unit's elements below the reference, counting those equal to
-// it apart (cnt, first, partner).  o is the same unit of the other row.
-template <int DT, bool OTHER>
-__device__ __forceinline__ float careful_unit(Online& s, const uint4 u, const uint4 o, int x0, int V, float c)
+// it apart (cnt, first).
+template <int DT>
+__device__ __forceinline__ float careful_unit(Online& s, const uint4 u, int x0, int V, float c)
 {
     constexpr int EPU = Elem<DT>::kPerUnit;
-    float v[EPU], w[EPU];
+    float v[EPU];
     unpack_masked<DT>(u, x0, V, v);
-    if (OTHER) unpack_masked<DT>(o, x0, V, w);
     float z = 0.f;
 #pragma unroll
     for (int e = 0; e < EPU; ++e) {
         if (v[e] == s.m) {
             ++s.cnt;
-            if (x0 + e < s.first) {
-                s.first = x0 + e;
-                s.partner = OTHER ? w[e] : 0.f;
-            }
+            s.first = min(s.first, x0 + e);
         } else {
             z += ex2(fmaf(v[e], c, s.neg));
         }
@@ -234,25 +229,30 @@ __device__ __forceinline__ float chunk_max(const uint4 (&u)[kUPT], int ug0, int 
     return m;
 }
 
-// A lane whose chunk reaches the reference sets the chunk aside (d0, d1),
-// or, with no room left, flags it for the exact path.
-__device__ __forceinline__ bool set_aside(Online& s, bool sp, int ch)
+// A lane whose chunk reaches the reference sets the chunk aside: its units
+// go to the lane's stash (slot nd) and the chunk index to d0 or d1.  With no
+// room left it flags the chunk for the exact path.
+__device__ __forceinline__ bool set_aside(Online& s, bool sp, int ch, uint4 (*stash)[kUPT], const uint4 (&u)[kUPT])
 {
     if (!sp) return false;
     if (s.nd < 2) {
-        s.d1 = s.d0;
-        s.d0 = ch;
+#pragma unroll
+        for (int i = 0; i < kUPT; ++i) stash[s.nd][i] = u[i];
+        if (s.nd == 0)
+            s.d0 = ch;
+        else
+            s.d1 = ch;
         ++s.nd;
         return false;
     }
     return true;
 }
 
-// After the pass: the set-aside chunks of this lane, re-read and summed
-// against the final maximum.
-template <int DT, bool OTHER>
-__device__ __forceinline__ void online_finish(Online& s, const char* row, const char* other, int cw, int lane,
-                                              int n_units, int V, float c)
+// After the pass: the set-aside chunks of this lane, from its stash,
+// summed against the final maximum.
+template <int DT>
+__device__ __forceinline__ void online_finish(Online& s, const uint4 (*stash)[kUPT], int cw, int lane, int n_units,
+                                              int V, float c)
 {
     constexpr int EPU = Elem<DT>::kPerUnit;
     if (!(s.m > -INFINITY)) return;
@@ -262,20 +262,10 @@ __device__ __forceinline__ void online_finish(Online& s, const char* row, const 
     for (int k = 0; k < 2; ++k) {
         if (k < n) {
             const int ug0 = (k == 0 ? s.d0 : s.d1) * kChunk + unit_local(cw, 0, lane);
-            uint4 u[kUPT], o[kUPT];
 #pragma unroll
             for (int i = 0; i < kUPT; ++i) {
                 const int ug = ug0 + i * 32;
-                u[i] = o[i] = make_uint4(0u, 0u, 0u, 0u);
-                if (ug < n_units) {
-                    u[i] = __ldg(reinterpret_cast<const uint4*>(row) + ug);
-                    if (OTHER) o[i] = __ldg(reinterpret_cast<const uint4*>(other) + ug);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kUPT; ++i) {
-                const int ug = ug0 + i * 32;
-                if (ug < n_units) s.z += careful_unit<DT, OTHER>(s, u[i], o[i], ug * EPU, V, c);
+                if (ug < n_units) s.z += careful_unit<DT>(s, stash[k][i], ug * EPU, V, c);
             }
         }
     }
@@ -291,6 +281,8 @@ template <int DT, bool OTHER>
 __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, uint32_t& g, bool& timed_out,
                                       int nc, int n_units, int V, float c, int cw, int lane)
 {
+    uint4(*const stashT)[kUPT] = sm->stash[0][cw * 32 + lane];
+    uint4(*const stashD)[kUPT] = sm->stash[1][cw * 32 + lane];
     constexpr int EPU = Elem<DT>::kPerUnit;
 #pragma unroll 1
     for (int ch = 0; ch < nc; ++ch, ++g) {
@@ -340,7 +332,7 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
             const bool spT = hotT && cmT >= sT.m, spD = hotD && cmD >= sD.m;
             if (liveT) sT.z += spT ? 0.f : zt;
             if (liveD) sD.z += spD ? 0.f : zd;
-            const bool ovT = set_aside(sT, spT, ch), ovD = set_aside(sD, spD, ch);
+            const bool ovT = set_aside(sT, spT, ch, stashT, t), ovD = OTHER && set_aside(sD, spD, ch, stashD, d);
             // the chunk's sums are in the old reference: move it now
             online_rebase(sT, wmT, c);
             if (OTHER) online_rebase(sD, wmD, c);
@@ -351,8 +343,8 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
                 for (int i = 0; i < kUPT; ++i) {
                     const int ug = ug0 + i * 32;
                     if (!tail || ug < n_units) {
-                        if (ovT) sT.z += careful_unit<DT, OTHER>(sT, t[i], d[i], ug * EPU, V, c);
-                        if (ovD) sD.z += careful_unit<DT, true>(sD, d[i], t[i], ug * EPU, V, c);
+                        if (ovT) sT.z += careful_unit<DT>(sT, t[i], ug * EPU, V, c);
+                        if (ovD) sD.z += careful_unit<DT>(sD, d[i], ug * EPU, V, c);
                     }
                 }
             }
@@ -428,67 +420,87 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
     return aT * tot;
 }
 
-// Combine the consumers' online statistics of one row (all consumer
-// threads call it; results in shared memory from consumer thread 0).
-__device__ __forceinline__ void combine_row(StreamSmem* sm, const Online s, bool is_t, float c, int ct)
+// Combine the consumers' online statistics of both rows (all consumer
+// threads call it; results in shared memory from consumer thread 0): row
+// maximum M, reference -(M c), Z_rest (the sum below M), the count n of
+// maxima, Z = n e(M) + Z_rest, and the index of a unique maximum.
+__device__ __forceinline__ void combine_rows(StreamSmem* sm, const Online& sT, const Online& sD, bool two, float c,
+                                             int ct)
 {
     const int lane = ct & 31, w = ct >> 5;
-    float M = warp_max_redux(s.m);
-    if (lane == 0) sm->redf[0][w] = M;
-    if (ct == 0) (is_t ? sm->firstT : sm->firstD) = ~0ull;  // read by thread 0 after the next barrier
-    cbar_sync();
-    M = -INFINITY;
-    for (int i = 0; i < kSW; ++i) M = max_nan(M, sm->redf[0][i]);
-    const float gneg = -(M * c);
-    float contrib;
-    int nmax;
-    if (s.m == M) {  // same reference as the row's
-        contrib = s.z;
-        nmax = s.cnt;
-        if (s.cnt > 0) {
-            const unsigned long long key =
-                ((unsigned long long)(unsigned)s.first << 32) | __float_as_uint(s.partner);
-            atomicMin(is_t ? &sm->firstT : &sm->firstD, key);
-        }
-    } else {
-        const float scl = (s.cnt > 0 || s.z > 0.f) ? ex2(gneg - s.neg) : 0.f;
-        contrib = s.cnt > 0 ? scl * (s.z + (float)s.cnt * ex2(fmaf(s.m, c, s.neg))) : scl * s.z;
-        nmax = 0;
-    }
-    contrib = warp_sum(contrib);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nmax += __shfl_xor_sync(0xffffffffu, nmax, o);
+    float MT = warp_max_redux(sT.m), MD = two ? warp_max_redux(sD.m) : -INFINITY;
     if (lane == 0) {
-        sm->redf[1][w] = contrib;
-        sm->redi[1][w] = nmax;
+        sm->redf[0][w] = MT;
+        sm->redf[1][w] = MD;
+    }
+    if (ct == 0) sm->firstT = sm->firstD = 0x7fffffff;  // read by thread 0 after the next barrier
+    cbar_sync();
+    MT = MD = -INFINITY;
+    for (int i = 0; i < kSW; ++i) {
+        MT = max_nan(MT, sm->redf[0][i]);
+        MD = max_nan(MD, sm->redf[1][i]);
+    }
+    const float gnegT = -(MT * c), gnegD = -(MD * c);
+    // a thread whose reference is the row's adds its sums as they are;
+    // another rescales them (its maxima are then ordinary elements)
+    float cT, cD = 0.f;
+    int nT = 0, nD = 0;
+    if (sT.m == MT) {
+        cT = sT.z;
+        nT = sT.cnt;
+        if (nT > 0) atomicMin(&sm->firstT, sT.first);
+    } else {
+        const float scl = (sT.cnt > 0 || sT.z > 0.f) ? ex2(gnegT - sT.neg) : 0.f;
+        cT = sT.cnt > 0 ? scl * (sT.z + (float)sT.cnt * ex2(fmaf(sT.m, c, sT.neg))) : scl * sT.z;
+    }
+    if (two) {
+        if (sD.m == MD) {
+            cD = sD.z;
+            nD = sD.cnt;
+            if (nD > 0) atomicMin(&sm->firstD, sD.first);
+        } else {
+            const float scl = (sD.cnt > 0 || sD.z > 0.f) ? ex2(gnegD - sD.neg) : 0.f;
+            cD = sD.cnt > 0 ? scl * (sD.z + (float)sD.cnt * ex2(fmaf(sD.m, c, sD.neg))) : scl * sD.z;
+        }
+    }
+    cT = warp_sum(cT);
+    cD = warp_sum(cD);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        nT += __shfl_xor_sync(0xffffffffu, nT, o);
+        nD += __shfl_xor_sync(0xffffffffu, nD, o);
+    }
+    if (lane == 0) {
+        sm->redf[2][w] = cT;
+        sm->redf[3][w] = cD;
+        sm->redi[0][w] = nT;
+        sm->redi[1][w] = nD;
     }
     cbar_sync();
     if (ct == 0) {
-        float zr = 0.f;
-        int n = 0;
+        float zT = 0.f, zD = 0.f;
+        int n1 = 0, n2 = 0;
         for (int i = 0; i < kSW; ++i) {
-            zr += sm->redf[1][i];
-            n += sm->redi[1][i];
+            zT += sm->redf[2][i];
+            zD += sm->redf[3][i];
+            n1 += sm->redi[0][i];
+            n2 += sm->redi[1][i];
         }
-        const float em = ex2(fmaf(M, c, gneg));
-        const unsigned long long key = is_t ? sm->firstT : sm->firstD;
-        const int first = (int)(key >> 32);
-        const float partner = __uint_as_float((unsigned)(key & 0xffffffffu));
-        if (is_t) {
-            sm->MT = M;
-            sm->gnegT = gneg;
-            sm->zrestT = zr;
-            sm->zT = (float)n * em + zr;
-            sm->emaxT = em;
-            sm->uT = n == 1 ? first : -1;
-            (void)partner;
-        } else {
-            sm->MD = M;
-            sm->gnegD = gneg;
-            sm->zrestD = zr;
-            sm->zD = (float)n * em + zr;
-            sm->emaxD = em;
-            sm->uD = n == 1 ? first : -1;
+        const float emT = ex2(fmaf(MT, c, gnegT));
+        sm->MT = MT;
+        sm->gnegT = gnegT;
+        sm->zrestT = zT;
+        sm->zT = (float)n1 * emT + zT;
+        sm->emaxT = emT;
+        sm->uT = n1 == 1 ? sm->firstT : -1;
+        if (two) {
+            const float emD = ex2(fmaf(MD, c, gnegD));
+            sm->MD = MD;
+            sm->gnegD = gnegD;
+            sm->zrestD = zD;
+            sm->zD = (float)n2 * emD + zD;
+            sm->emaxD = emD;
+            sm->uD = n2 == 1 ? sm->firstD : -1;
         }
     }
 }
@@ -695,16 +707,13 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
 
         // ---- pass 1: online statistics ----
         Online sT, sD;
-        if (leaf) {
+        if (leaf)
             pass1<DT, false>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
-            online_finish<DT, false>(sT, gT, nullptr, cw, lane, n_units, V, c);
-        } else {
+        else
             pass1<DT, true>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
-            online_finish<DT, true>(sT, gT, gD, cw, lane, n_units, V, c);
-            online_finish<DT, true>(sD, gD, gT, cw, lane, n_units, V, c);
-        }
-        combine_row(sm, sT, true, c, ct);
-        if (!leaf) combine_row(sm, sD, false, c, ct);
+        online_finish<DT>(sT, sm->stash[0][ct], cw, lane, n_units, V, c);
+        if (!leaf) online_finish<DT>(sD, sm->stash[1][ct], cw, lane, n_units, V, c);
+        combine_rows(sm, sT, sD, !leaf, c, ct);
 
         // ---- scalar state ----
         if (ct == 0) {
