@@ -12,10 +12,10 @@
 //   leaf:   one target-only pass for the bonus sample.
 // Warp 0 (metadata) takes nodes from the depth-major list the prep kernel
 // built and fills a descriptor queue: draws, their tokens and logits.
-// Warp 1 (copy) streams each node's rows in 16 KB-per-row chunks through a
-// 4-stage ring with 1-D TMA bulk copies (mbarrier full/empty handshake),
-// pass-1 reads marked evict_last and pass-2 reads evict_first in L2.
-// Warps 2..17 consume: a warp owns 64 contiguous 16-byte units of each
+// Warp 1 (copy) streams each node's rows in 12 KB-per-row chunks through a
+// 3-stage ring with 1-D TMA bulk copies (mbarrier full/empty handshake),
+// marked evict_last in L2 until the node's last pass, which is evict_first.
+// Warps 2..13 consume: a warp owns 64 contiguous 16-byte units of each
 // chunk.  A node's weight p comes from its parent through a flag
 // (release/acquire); waiting happens only before pass 2.  Every wait is
 // bounded and a timeout is reported, never a hang or a trap.
@@ -32,13 +32,15 @@ namespace sdv {
 namespace {
 
 constexpr int kCtasPerSm = 2;            // two nodes in flight per SM
-constexpr int kSW = 8;                   // consumer warps
+constexpr int kSW = 12;                  // consumer warps
 constexpr int kCT = 32 * kSW;            // consumer threads
 constexpr int kSThreads = kCT + 64;      // plus the metadata warp and the copy warp
 constexpr int kUPT = 2;                  // 16-byte units per consumer thread per row per chunk
 constexpr int kWU = 32 * kUPT;           // units per warp per chunk, contiguous
-constexpr int kChunk = kCT * kUPT;       // units per row per chunk (16 KB)
-constexpr int kStages = 4;
+constexpr int kChunk = kCT * kUPT;       // units per row per chunk (12 KB)
+constexpr int kStages = 3;               // 3 x 24 KB in flight per CTA
+constexpr int kStash = 1;                // set-aside chunks a lane can hold (at most 2: d0, d1)
+static_assert(kStash >= 1 && kStash <= 2, "a lane keeps at most two set-aside chunk indices");
 constexpr int kMaxChunks = (SDV_MAX_V / 4 + kChunk - 1) / kChunk;
 constexpr int kQ = 4;                    // node descriptor queue depth
 
@@ -104,7 +106,7 @@ struct StreamSmem {
     float redf[4][kSW];
     int redi[4][kSW];
     int firstT, firstD;              // lowest index of each row's maximum
-    uint4 stash[2][kCT][2][kUPT];    // set-aside units: [row][consumer thread][slot][unit]
+    uint4 stash[2][kCT][kStash][kUPT];  // set-aside units: [row][consumer thread][slot][unit]
     int abort;
     // scalar state (consumer thread 0)
     float MT, MD, gnegT, gnegD, zT, zD, zrestT, zrestD, emaxT, emaxD;
@@ -127,7 +129,7 @@ struct StreamSmem {
 // the chunk's units to its stash in shared memory (chunk indices d0, d1)
 // and, after the pass, sums them against the final maximum, counting the
 // elements equal to it apart.  Such chunks are rare (a handful per row
-// per warp); a lane with more than two takes a synchronous, exact path.
+// per warp); a lane with more than kStash takes a synchronous, exact path.
 struct Online {
     float m = -INFINITY;
     float neg = INFINITY;
@@ -235,7 +237,7 @@ __device__ __forceinline__ float chunk_max(const uint4 (&u)[kUPT], int ug0, int 
 __device__ __forceinline__ bool set_aside(Online& s, bool sp, int ch, uint4 (*stash)[kUPT], const uint4 (&u)[kUPT])
 {
     if (!sp) return false;
-    if (s.nd < 2) {
+    if (s.nd < kStash) {
 #pragma unroll
         for (int i = 0; i < kUPT; ++i) stash[s.nd][i] = u[i];
         if (s.nd == 0)
@@ -259,7 +261,7 @@ __device__ __forceinline__ void online_finish(Online& s, const uint4 (*stash)[kU
     const int n = s.nd;
     s.nd = 0;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kStash; ++k) {
         if (k < n) {
             const int ug0 = (k == 0 ? s.d0 : s.d1) * kChunk + unit_local(cw, 0, lane);
 #pragma unroll
