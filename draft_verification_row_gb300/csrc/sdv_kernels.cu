@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(32 * kDecideWarps) decide_kernel(Problem pb, i
     __shared__ float s_val[kDecideWarps][kSlotsMax];  // a (token), h (block) or argmax bits (greedy)
     __shared__ float s_u[kDecideWarps][SDV_MAX_K * SDV_MAX_L];
     __shared__ int s_tok[kDecideWarps][SDV_MAX_K * SDV_MAX_L];
+    __shared__ signed char s_sib[kDecideWarps][kSlotsMax];  // next sibling's draft, or -1
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int b = blockIdx.x * kDecideWarps + w;
     if (b >= pb.B) return;
@@ -212,9 +213,9 @@ __global__ void __launch_bounds__(32 * kDecideWarps) decide_kernel(Problem pb, i
             ap[i] = v;
         }
     }
-    if (lane != 0) return;
     int ej = 0, eo = 0;
     if (greedy) {
+        if (lane != 0) return;
         int best = -1, bestk = 0;
         for (int kk = 0; kk < K; ++kk) {
             int m = 0;
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(32 * kDecideWarps) decide_kernel(Problem pb, i
         return;
     }
     if (token) {
+        if (lane != 0) return;
         int j = 0, o = 0;
         while (j < Lb) {
             int acc = -1;
@@ -245,30 +247,30 @@ __global__ void __launch_bounds__(32 * kDecideWarps) decide_kernel(Problem pb, i
         ej = j;
         eo = o;
     } else {
-        // depth first: children in order of first appearance, then the
-        // node's own test; the first accepted node ends the search
-        int stk_o[SDV_MAX_L + 1], stk_next[SDV_MAX_L + 1];
-        int top = 0;
-        stk_o[0] = 0;
-        stk_next[0] = 0;
-        for (;;) {
-            const int jj = top, o = stk_o[top];
-            int child = -1;
-            if (jj < Lb) {
-                for (int k2 = stk_next[top]; k2 < K; ++k2) {
-                    if (own[jj * K + k2] == o && own[(jj + 1) * K + k2] == k2) {
-                        child = k2;
+        // Depth first, children in order of first appearance, each node
+        // tested after its subtree: the end node is the first accepted
+        // node in that post-order (the root always accepts).  A node
+        // (j, o) is owned by draft o; its first child is (j + 1, o), its
+        // parent (j - 1, own[j - 1][o]), and its next sibling the lowest
+        // later draft through the parent that owns a node at depth j.
+        signed char* sib = s_sib[w];
+        for (int i = lane + K; i < (Lb + 1) * K; i += 32) {  // depths 1..Lb (owned nodes only)
+            const int j = i / K, k = i % K;
+            int nx = -1;
+            if (own[i] == k) {
+                const int par = own[(j - 1) * K + k];
+                for (int k3 = k + 1; k3 < K; ++k3)
+                    if (own[(j - 1) * K + k3] == par && own[j * K + k3] == k3) {
+                        nx = k3;
                         break;
                     }
-                }
             }
-            if (child >= 0) {
-                stk_next[top] = child + 1;
-                ++top;
-                stk_o[top] = child;
-                stk_next[top] = 0;
-                continue;
-            }
+            sib[i] = (signed char)nx;
+        }
+        __syncwarp();
+        if (lane != 0) return;
+        int jj = Lb, o = 0;  // the leftmost deepest node
+        for (;;) {
             if (jj == 0) {
                 ej = 0;
                 eo = 0;
@@ -279,7 +281,14 @@ __global__ void __launch_bounds__(32 * kDecideWarps) decide_kernel(Problem pb, i
                 eo = o;
                 break;
             }
-            --top;
+            const int nx = sib[jj * K + o];
+            if (nx >= 0) {
+                o = nx;   // the next sibling's subtree, from its leftmost deepest node
+                jj = Lb;  // (a draft's own nodes run down to depth Lb)
+            } else {
+                o = own[(jj - 1) * K + o];  // the parent
+                --jj;
+            }
         }
     }
     pb.accept_len[b] = ej;
