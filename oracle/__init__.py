@@ -51,6 +51,7 @@ def lib():
         _lib.sdvo_exact_outcomes.restype = ctypes.c_int
         _lib.sdvo_exact_streams.restype = ctypes.c_int
         _lib.sdvo_prefix_index.restype = ctypes.c_longlong
+        _lib.sdvo_sample_rows.restype = ctypes.c_int
     return _lib
 
 
@@ -154,6 +155,28 @@ def verify(mode, prob: Problem, residual_out=False, trace_cap=0):
     if tr is not None:
         out["trace"] = [(entries[i].kind, entries[i].index, entries[i].lo, entries[i].hi)
                         for i in range(min(tr.n, trace_cap))]
+    return out
+
+
+def sample_rows(logits, n_samples, u, temperature, V=None):
+    """Draft-token sampling: n_samples inverse-CDF draws per row of
+    softmax(logits / T).  logits [n_rows][stride] (f32, or bf16 as a CPU
+    torch tensor or uint16 bits), u [n_rows][n_samples].  Returns a dict with
+    tokens [n_rows][n_samples], margin [n_rows][n_samples], row_status
+    [n_rows] and rc."""
+    lg = _np(logits)
+    n_rows, stride = lg.shape[0], lg.shape[1]
+    V = stride if V is None else int(V)
+    dtype = BF16 if lg.dtype in (np.uint16, np.int16) else F32
+    uu = None if u is None else np.ascontiguousarray(_np(u), dtype=np.float64)
+    out = {"tokens": np.zeros((n_rows, n_samples), np.int32),
+           "margin": np.zeros((n_rows, n_samples), np.float64),
+           "row_status": np.zeros(n_rows, np.int32)}
+    rc = lib().sdvo_sample_rows(
+        ctypes.c_int(n_rows), ctypes.c_int(V), ctypes.c_longlong(stride), ctypes.c_int(dtype),
+        ctypes.c_double(float(temperature)), _ptr(lg), ctypes.c_int(n_samples), _ptr(uu),
+        _ptr(out["tokens"]), _ptr(out["margin"]), _ptr(out["row_status"]))
+    out["rc"] = rc
     return out
 
 

@@ -534,3 +534,80 @@ long long sdvo_prefix_index(const int* tokens, int j, int V)
     for (int i = 0; i < j; ++i) num = num * V + tokens[i];
     return off + num;
 }
+
+/* ------------------------------------------------------------------------ */
+/* draft-token sampling                                                      */
+
+int sdvo_sample_rows(int n_rows, int V, long long row_stride, int dtype, double temperature,
+                     const void* logits, int n_samples, const double* u, int* tokens, double* margin,
+                     int* row_status)
+{
+    if (n_rows < 0 || V < 1 || row_stride < V || n_samples < 0 || (dtype != SDVO_F32 && dtype != SDVO_BF16) ||
+        !(temperature >= 0.0) || isinf(temperature))
+        return SDVO_ERR_INVALID;
+    if (n_rows == 0 || n_samples == 0) return SDVO_OK;
+    if (!logits || !tokens || (temperature > 0.0 && !u)) return SDVO_ERR_INVALID;
+    /* the row helpers read V and dtype from a problem */
+    sdvo_problem pb;
+    memset(&pb, 0, sizeof pb);
+    pb.V = V;
+    pb.dtype = dtype;
+    pb.row_stride = row_stride;
+    double* P = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!P) return SDVO_ERR_NOMEM;
+    for (int r = 0; r < n_rows; ++r) {
+        const unsigned char* row = (const unsigned char*)logits + (size_t)r * (size_t)row_stride * elem_size(dtype);
+        int* out = tokens + (size_t)r * n_samples;
+        double* mg = margin ? margin + (size_t)r * n_samples : NULL;
+        const int ok = row_usable(&pb, row);
+        if (row_status) row_status[r] = ok ? 0 : SDVO_REQ_NONFINITE;
+        if (!ok) {
+            for (int s = 0; s < n_samples; ++s) {
+                out[s] = -1;
+                if (mg) mg[s] = INFINITY;
+            }
+            continue;
+        }
+        if (temperature == 0.0) {
+            const int am = argmax_row(&pb, row);
+            for (int s = 0; s < n_samples; ++s) {
+                out[s] = am;
+                if (mg) mg[s] = INFINITY;
+            }
+            continue;
+        }
+        softmax(&pb, row, temperature, P);
+        double S = 0.0;
+        for (int x = 0; x < V; ++x) S += P[x];
+        for (int s = 0; s < n_samples; ++s) {
+            /* the same inverse CDF as the correction draws of sdvo_verify */
+            const double us = u[(size_t)r * n_samples + s];
+            double cum = 0.0, lo = 0.0, hi = INFINITY, last_prev = 0.0;
+            int chosen = -1, last = -1;
+            for (int x = 0; x < V; ++x) {
+                if (P[x] > 0.0) {
+                    double prev = cum;
+                    cum += P[x];
+                    last = x;
+                    last_prev = prev;
+                    if (cum > us * S) {
+                        chosen = x;
+                        lo = prev / S;
+                        hi = cum / S;
+                        break;
+                    }
+                }
+            }
+            if (chosen < 0) {
+                chosen = last;
+                lo = last_prev / S;
+                hi = INFINITY;
+            }
+            out[s] = chosen;
+            if (mg) mg[s] = fmin(us - lo, hi - us);
+        }
+    }
+    free(P);
+    return SDVO_OK;
+}
+

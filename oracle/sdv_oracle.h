@@ -108,6 +108,26 @@ int sdvo_exact_streams(int mode, int V, int K, int L, double temperature,
                        const float* tgt_tab, const float* dft_tab, const double* q_tab,
                        double* stream_prob, double* tau_prob);
 
+/* Draft-token sampling: n_samples independent draws from each row's
+ * distribution softmax(logits / T), the step before verification in which a
+ * draft model proposes its tokens ("SpecTr-GBV: Multi-Draft Block
+ * Verification Accelerating Speculative Decoding", section 1: every draft
+ * token is drawn from the draft model's distribution).
+ *   logits   [n_rows][row_stride]  f32 or bf16 bits; columns >= V unread
+ *   u        [n_rows][n_samples]   uniforms in [0,1) (double)
+ *   tokens   [n_rows][n_samples]   out: the inverse-CDF draw of each uniform:
+ *            the first token in index order whose running sum exceeds u*S
+ *            (S the row's total), else the last token of nonzero mass;
+ *            T = 0: the row's argmax (lowest index on ties) for every sample
+ *   margin   [n_rows][n_samples]   out, may be NULL: distance of u to the
+ *            ends of the chosen token's CDF interval (infinite at T = 0)
+ *   row_status [n_rows]            out, may be NULL: SDVO_REQ_NONFINITE for a
+ *            row with NaN, +Inf or no finite logit (its tokens are -1)
+ * Returns SDVO_OK, SDVO_ERR_INVALID or SDVO_ERR_NOMEM. */
+int sdvo_sample_rows(int n_rows, int V, long long row_stride, int dtype, double temperature,
+                     const void* logits, int n_samples, const double* u, int* tokens, double* margin,
+                     int* row_status);
+
 /* Index of a prefix of length j: all prefixes of length < j come first,
  * then the base-V number of the tokens (first token most significant). */
 long long sdvo_prefix_index(const int* tokens, int j, int V);
