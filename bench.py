@@ -13,7 +13,9 @@ The JSON line also carries the roofline of the dominant kernel (the node
 kernel: vocabulary-row work), timed live with CUDA events recorded by the
 library around those launches, the end-to-end figure through the C-ABI with
 host buffers, the oracle timed on host cores, the launch count and the SM
-clocks sampled during the timed region.
+clocks sampled during the timed region.  "next_draft_sampling" measures the
+draft-token sampling step (sdv_sample_rows) on the batch's depth-0 draft
+rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -376,6 +378,33 @@ def run_ours(args, world, rank, local):
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": te / args.e2e_steps}
         del host
+        # the next row of the path: draft-token sampling, one draw per draft
+        # from each request's depth-0 draft rows (B*K rows of V logits)
+        rows = batch.draft[:, :, 0, :].reshape(batch.B * batch.K, batch.stride).contiguous()
+        n_rows = rows.shape[0]
+        su = torch.rand((n_rows, 1), device=dev, generator=torch.Generator(device=dev).manual_seed(17))
+        toks = torch.empty((n_rows, 1), dtype=torch.int32, device=dev)
+        dst = torch.empty(1, dtype=torch.int32, device=dev)
+
+        def sample_call():
+            sdv.sample_rows(rows, 1, su, batch.temperature, V=batch.V, tokens=toks, device_status=dst,
+                            stream=stream)
+
+        for _ in range(args.warmup):
+            sample_call()
+        ts, _ = time_calls(sample_call, args.steps, stream)
+        ts = max_over_ranks(ts, world)
+        ms_s = ts / args.steps
+        s_bytes = n_rows * batch.V * esz
+        s_gbs = s_bytes / (ms_s / 1000.0) / 1e9
+        line["next_draft_sampling"] = {
+            "metric": "sampled draft tokens/s", "value": sum_over_ranks(n_rows, world) / (ms_s / 1000.0),
+            "unit": "tokens/s", "ms_per_call": ms_s, "rows": n_rows, "draws_per_row": 1, "V": batch.V,
+            "gpu_launches_per_call": 1,
+            "roofline": {"bound": "hbm", "achieved": s_gbs, "peak": peak, "unit": "GB/s", "frac": s_gbs / peak,
+                         "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_call": s_bytes,
+                         "kernel": "sample_rows_kernel"}}
+        del rows
         if rank == 0:
             rng = np.random.default_rng(1)
             req = sorted(rng.choice(batch.B, size=min(args.cpu_requests, batch.B), replace=False).tolist())

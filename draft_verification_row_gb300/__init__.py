@@ -1,4 +1,5 @@
-"""Batched speculative-decoding verification on GB300 (sm_103a).
+"""Batched speculative-decoding verification on GB300 (sm_103a), and the
+draft-token sampling step before it.
 
 A thin ctypes binding of the C-ABI in include/sdv.h (libsdv.so, built
 in-tree by ``draft_verification_row_gb300.build``).  Every step of the
@@ -12,6 +13,7 @@ from .binding import (  # noqa: F401
     SDVError,
     launch_shape,
     lib,
+    sample_rows,
     set_profile_events,
     verify,
     verify_block,

@@ -25,7 +25,7 @@ _VERIFY_ARGTYPES = [
 ]
 
 EXPORTS = list(_ENTRY.values()) + ["sdv_workspace_bytes", "sdv_status_string", "sdv_launch_shape",
-                                   "sdv_set_profile_events"]
+                                   "sdv_set_profile_events", "sdv_sample_rows"]
 
 
 class SDVError(RuntimeError):
@@ -58,6 +58,10 @@ def lib(path: str = LIB_PATH):
     h.sdv_launch_shape.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.POINTER(ctypes.c_int)] * 3
     h.sdv_set_profile_events.restype = ctypes.c_int
     h.sdv_set_profile_events.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    h.sdv_sample_rows.restype = ctypes.c_int
+    h.sdv_sample_rows.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_longlong, ctypes.c_int, ctypes.c_float,
+                                  ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_void_p, ctypes.c_void_p]
     _lib = h
     return h
 
@@ -171,3 +175,35 @@ def verify_block(*args, **kw):
 
 def verify_multidraft(*args, **kw):
     return verify("multidraft", *args, **kw)
+
+
+def sample_rows(logits, n_samples, u, temperature, *, V=None, tokens=None, device_status=None, stream=None):
+    """Draft-token sampling: n_samples inverse-CDF draws per row of
+    softmax(logits / T).
+
+    logits [n_rows][stride] (float32 or bfloat16, CUDA, contiguous),
+    u [n_rows][n_samples] float32 (may be None when T == 0).  Returns
+    (tokens [n_rows][n_samples] int32, device_status [1] int32); the call is
+    asynchronous.
+    """
+    h = lib()
+    if logits.dim() != 2 or not logits.is_cuda or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous CUDA [n_rows][stride] tensor")
+    n_rows, stride = logits.shape
+    V = stride if V is None else int(V)
+    if u is not None and (u.dtype != torch.float32 or not u.is_cuda or not u.is_contiguous()
+                          or tuple(u.shape) != (n_rows, n_samples)):
+        raise ValueError("u must be a contiguous CUDA float32 [n_rows][n_samples] tensor")
+    if tokens is None:
+        tokens = torch.empty((n_rows, n_samples), dtype=torch.int32, device=logits.device)
+    if device_status is None:
+        device_status = torch.empty(1, dtype=torch.int32, device=logits.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device)
+    rc = h.sdv_sample_rows(n_rows, V, stride, _dtype_code(logits), float(temperature), _ptr(logits),
+                           int(n_samples), _ptr(u), _ptr(tokens), _ptr(device_status),
+                           ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SDVError(rc, "sdv_sample_rows")
+    return tokens, device_status
+

@@ -211,6 +211,39 @@ int sdv_set_profile_events(void* start, void* stop)
     return SDV_OK;
 }
 
+int sdv_sample_rows(int n_rows, int V, long long row_stride, int dtype, float temperature, const void* logits,
+                    int n_samples, const float* u, int* tokens, int* device_status, void* cuda_stream)
+{
+    if (n_rows < 0 || V < 1 || V > SDV_MAX_V || (dtype != SDV_F32 && dtype != SDV_BF16)) return SDV_ERR_INVALID;
+    if (row_stride < V || row_stride % 8 != 0) return SDV_ERR_INVALID;
+    if (n_samples < 1 || n_samples > SDV_MAX_SAMPLES) return SDV_ERR_INVALID;
+    if (!(temperature >= 0.f) || std::isinf(temperature)) return SDV_ERR_INVALID;
+    const bool greedy = temperature == 0.f;
+    const float c = greedy ? 0.f : (float)(1.4426950408889634 / (double)temperature);
+    if (!greedy && !std::isfinite(c)) return SDV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    if (device_status && !sdv::device_accessible(device_status)) return SDV_ERR_INVALID;
+    if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (n_rows == 0) return SDV_OK;
+    if (!logits || !tokens || (!greedy && !u)) return SDV_ERR_INVALID;
+    if (!sdv::aligned(logits, 16)) return SDV_ERR_INVALID;
+    const void* ptrs[] = {logits, greedy ? nullptr : u, tokens};
+    for (const void* q : ptrs)
+        if (q && !sdv::device_accessible(q)) return SDV_ERR_INVALID;
+    sdv::SampleArgs a;
+    a.n_rows = n_rows;
+    a.V = V;
+    a.n_samples = n_samples;
+    a.dtype = dtype;
+    a.stride = row_stride;
+    a.c = c;
+    a.logits = logits;
+    a.u = u;
+    a.tokens = tokens;
+    a.device_status = device_status;
+    return sdv::launch_sample_rows(a, st) == cudaSuccess ? SDV_OK : SDV_ERR_CUDA;
+}
+
 int sdv_launch_shape(int V, int dtype, int* ctas_per_sm, int* threads, int* smem_bytes)
 {
     if (V < 1 || V > SDV_MAX_V || (dtype != SDV_F32 && dtype != SDV_BF16)) return SDV_ERR_INVALID;

@@ -1,6 +1,6 @@
 // sdv_internal.h -- declarations shared by the host API (sdv_api.cu) and
-// the kernels (sdv_kernels.cu, sdv_stream.cu).  Not part of the public
-// interface.
+// the kernels (sdv_kernels.cu, sdv_stream.cu, sdv_sample.cu).  Not part of
+// the public interface.
 #pragma once
 
 #include <cstddef>
@@ -58,6 +58,19 @@ cudaError_t launch_prep(const Problem& pb, cudaStream_t st);
 cudaError_t launch_argmax(const Problem& pb, cudaStream_t st);
 cudaError_t launch_decide(const Problem& pb, bool greedy, cudaStream_t st);
 cudaError_t launch_stream(const Problem& pb, cudaStream_t st);
+
+// Draft-token sampling (sdv_sample.cu): n_samples draws per row.
+struct SampleArgs {
+    int n_rows, V, n_samples, dtype;
+    long long stride;
+    float c;  // log2(e) / T; 0 means T = 0 (argmax)
+    const void* logits;
+    const float* u;  // [n_rows][n_samples], unread when c == 0
+    int* tokens;     // [n_rows][n_samples]
+    int* device_status;
+};
+cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st);
+int sample_threads();
 
 // The node kernel's launch shape: persistent CTAs per SM, threads per CTA
 // and dynamic shared memory.

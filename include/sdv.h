@@ -87,6 +87,7 @@ extern "C" {
 #define SDV_MAX_K 16      /* drafts per request */
 #define SDV_MAX_L 16      /* draft tokens per draft */
 #define SDV_MAX_V 262144  /* vocabulary size */
+#define SDV_MAX_SAMPLES 64 /* draws per row in sdv_sample_rows */
 
 /* logit element types */
 enum { SDV_F32 = 0, SDV_BF16 = 1 };
@@ -176,6 +177,34 @@ size_t sdv_workspace_bytes(int mode, int B, int K, int L, int V);
 
 /* Static description of a return code (not of device status bits). */
 const char *sdv_status_string(int status);
+
+/* Draft-token sampling: the step before verification, in which a draft
+ * model proposes its tokens, each drawn from the model's distribution
+ * softmax(logits / T) ("SpecTr-GBV: Multi-Draft Block Verification
+ * Accelerating Speculative Decoding", section 1).  n_samples independent
+ * draws per row (K drafts sharing a prefix draw K tokens from one row).
+ *   n_rows       rows (>= 0); V vocabulary size (1..SDV_MAX_V); row_stride
+ *                elements between rows (>= V, a multiple of 8); dtype
+ *                SDV_F32 or SDV_BF16; temperature T >= 0, finite.
+ *   logits       [n_rows][row_stride] device, 16-byte aligned; columns >= V
+ *                are never read.
+ *   n_samples    draws per row, 1..SDV_MAX_SAMPLES.
+ *   u            [n_rows][n_samples] device fp32 uniforms in [0, 1); may be
+ *                NULL when T == 0.
+ *   tokens       [n_rows][n_samples] device int32 out.  Each draw is the
+ *                inverse CDF of its uniform: the first token in index order
+ *                whose running sum of probabilities exceeds u * S (S the
+ *                row's total), else the last token of nonzero probability.
+ *                T == 0: the row's argmax, lowest index on ties.  A row
+ *                holding NaN or +Inf, or no finite logit, gives -1.
+ *   device_status [1] device int32 or NULL: zeroed, then SDV_REQ_NONFINITE
+ *                if some row was unusable (other rows are unaffected).
+ *   cuda_stream  the stream to run on (NULL: the default stream).
+ * Asynchronous; allocates nothing.  Returns SDV_OK, SDV_ERR_INVALID or
+ * SDV_ERR_CUDA.  Arithmetic is fp32; a draw whose uniform lies within
+ * about 1e-6 of a CDF boundary may fall on the neighbouring token. */
+int sdv_sample_rows(int n_rows, int V, long long row_stride, int dtype, float temperature, const void *logits,
+                    int n_samples, const float *u, int *tokens, int *device_status, void *cuda_stream);
 
 /* Launch shape of the node kernel (the one that reads vocabulary rows) for
  * rows of V elements of dtype: CTAs per SM (it is persistent: that many

@@ -82,3 +82,28 @@ def compare(gpu, ref, what=""):
     if len(idx) == len(gpu["out_token"]):
         assert int(gpu["device_status"][0]) == status_or, f"{what}: device status {gpu['device_status'][0]}"
     return mism
+
+
+def pattern_row(kind, V):
+    """Degenerate logit rows (kinds 0..6) for the online-maximum and masking
+    paths; a float32 tensor of V logits."""
+    x = np.arange(V, dtype=np.float64)
+    if kind == 0:      # every logit equal: the maximum ties everywhere
+        r = np.full(V, 1.5)
+    elif kind == 1:    # ascending: every chunk holds a new maximum
+        r = 8.0 * x / V
+    elif kind == 2:    # descending: the maximum at index 0
+        r = 8.0 - 8.0 * x / V
+    elif kind == 3:    # flat with one spike at the last index
+        r = np.zeros(V)
+        r[-1] = 6.0
+    elif kind == 4:    # two equal maxima far apart, a wavy floor
+        r = np.sin(x * 0.37)
+        r[3] = r[-5] = 5.0
+    elif kind == 5:    # the first half masked to -inf, as a filtered vocabulary
+        r = np.sin(x * 0.11) * 2.0
+        r[: V // 2] = -np.inf
+    else:              # top-3 filtering: three finite logits, the rest -inf
+        r = np.full(V, -np.inf)
+        r[[V // 7, V // 2, V - 2]] = [1.0, 2.5, 0.5]
+    return torch.as_tensor(r, dtype=torch.float32)

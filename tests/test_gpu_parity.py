@@ -153,29 +153,6 @@ def test_chunk_boundaries(V, dtype):
         P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"V={V}/{dtype}/{mode}")
 
 
-def _pattern_row(kind, V):
-    x = np.arange(V, dtype=np.float64)
-    if kind == 0:      # every logit equal: the maximum ties everywhere
-        r = np.full(V, 1.5)
-    elif kind == 1:    # ascending: every chunk holds a new maximum
-        r = 8.0 * x / V
-    elif kind == 2:    # descending: the maximum at index 0
-        r = 8.0 - 8.0 * x / V
-    elif kind == 3:    # flat with one spike at the last index
-        r = np.zeros(V)
-        r[-1] = 6.0
-    elif kind == 4:    # two equal maxima far apart, a wavy floor
-        r = np.sin(x * 0.37)
-        r[3] = r[-5] = 5.0
-    elif kind == 5:    # the first half masked to -inf, as a filtered vocabulary
-        r = np.sin(x * 0.11) * 2.0
-        r[: V // 2] = -np.inf
-    else:              # top-3 filtering: three finite logits, the rest -inf
-        r = np.full(V, -np.inf)
-        r[[V // 7, V // 2, V - 2]] = [1.0, 2.5, 0.5]
-    return torch.as_tensor(r, dtype=torch.float32)
-
-
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_degenerate_rows(dtype):
     """Rows whose maximum ties across lanes and chunks, moves every chunk,
@@ -185,8 +162,8 @@ def test_degenerate_rows(dtype):
     V = 40007
     batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=14, K=3, L=3, V=V, dtype=dtype)
     for b in range(batch.B):
-        t = _pattern_row(b % 7, V).to(batch.target.dtype).to(DEV)
-        d = _pattern_row((b // 7 + b + 2) % 7, V).to(batch.draft.dtype).to(DEV)
+        t = P.pattern_row(b % 7, V).to(batch.target.dtype).to(DEV)
+        d = P.pattern_row((b // 7 + b + 2) % 7, V).to(batch.draft.dtype).to(DEV)
         batch.target[b, :, :, :V] = t
         batch.draft[b, :, :, :V] = d
     for mode in ("token", "multidraft"):
