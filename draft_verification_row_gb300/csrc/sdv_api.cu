@@ -16,14 +16,16 @@ size_t align_up(size_t n) { return (n + kAlign - 1) / kAlign * kAlign; }
 
 bool sizes_ok(int B, int K, int L, int V)
 {
-    return B >= 0 && K >= 1 && K <= SDV_MAX_K && L >= 0 && L <= SDV_MAX_L && V >= 1 && V <= SDV_MAX_V;
+    // node slots are kept in 30 bits (the decision's end-node record)
+    return B >= 0 && K >= 1 && K <= SDV_MAX_K && L >= 0 && L <= SDV_MAX_L && V >= 1 && V <= SDV_MAX_V &&
+           slot_count(B, K, L) < ((size_t)1 << 30);
 }
 
 size_t workspace_size(int B, int K, int L)
 {
     const size_t n = slot_count(B, K, L);
-    return 7 * align_up(n * 4) + align_up(n) + align_up((size_t)B * 4) + align_up((size_t)(L + 1) * B * K * 4) +
-           align_up((size_t)(L + 2) * 4);
+    return 7 * align_up(n * 4) + align_up(n * 5 * 4) + align_up(n) + 2 * align_up((size_t)B * 4) +
+           align_up((size_t)(L + 1) * B * K * 4) + align_up((size_t)(L + 2) * 4);
 }
 
 Workspace carve(void* base, int B, int K, int L)
@@ -39,8 +41,12 @@ Workspace carve(void* base, int B, int K, int L)
     p += align_up(n * 4);
     w.pbar = reinterpret_cast<float*>(p);
     p += align_up(n * 4);
-    w.tok = reinterpret_cast<int*>(p);
+    w.prm = reinterpret_cast<float*>(p);
+    p += align_up(n * 5 * 4);
+    w.xs = reinterpret_cast<int*>(p);
     p += align_up(n * 4);
+    w.endn = reinterpret_cast<int*>(p);
+    p += align_up((size_t)B * 4);
     w.am = reinterpret_cast<int*>(p);
     p += align_up(n * 4);
     w.owner = reinterpret_cast<unsigned char*>(p);
@@ -164,6 +170,8 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
     }
     if (!prof_record(g_prof_stop, st)) return SDV_ERR_CUDA;
     if (launch_decide(pb, greedy, st) != cudaSuccess) return SDV_ERR_CUDA;
+    // the correction (or bonus) token, drawn at each request's end node only
+    if (!greedy && launch_correction(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
     return SDV_OK;
 }
 

@@ -21,7 +21,10 @@ struct Workspace {
     float* h;              // node block acceptance probability h_v
     float* S;              // node residual mass S_n
     float* pbar;           // node weight complement 1 - p_v
-    int* tok;              // node candidate correction token
+    float* prm;            // node residual for the correction draw: [slot][5] =
+                           //   -(M_T c), -(M_D c), aT = p / Z_T, aD / aT, R_n(x*)
+    int* xs;               // node shared dominant token x* (or -1)
+    int* endn;             // [B] end node of the decision: slot | leaf << 30, or -1
     int* am;               // node argmax (greedy)
     unsigned char* owner;  // lowest draft sharing draft k's first j tokens
     int* req;              // [B] request status bits
@@ -70,6 +73,8 @@ struct SampleArgs {
     int* device_status;
 };
 cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st);
+// The correction (or bonus) draw at each request's end node, after decide.
+cudaError_t launch_correction(const Problem& pb, cudaStream_t st);
 int sample_threads();
 
 // The node kernel's launch shape: persistent CTAs per SM, threads per CTA

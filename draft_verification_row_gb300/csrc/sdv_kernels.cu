@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(32 * kDecideWarps) decide_kernel(Problem pb, i
             pb.accept_len[b] = 0;
             pb.accept_draft[b] = 0;
             pb.out_token[b] = -1;
+            pb.ws.endn[b] = -1;  // no correction draw
             if (pb.residual_mass) pb.residual_mass[b] = 0.f;
             if (pb.device_status) atomicOr(pb.device_status, st);
         }
@@ -190,7 +191,14 @@ __global__ void __launch_bounds__(32 * kDecideWarps) decide_kernel(Problem pb, i
     int* tk = s_tok[w];
     for (int i = lane; i < (Lb + 1) * K; i += 32) {
         own[i] = pb.ws.owner[s0 + i];
-        val[i] = greedy ? __int_as_float(pb.ws.am[s0 + i]) : (token ? pb.ws.a[s0 + i] : pb.ws.h[s0 + i]);
+        float v;
+        if (greedy)
+            v = __int_as_float(pb.ws.am[s0 + i]);
+        else if (token)
+            v = pb.ws.a[s0 + i];
+        else  // a leaf's block acceptance is its weight p (the node kernel only checks leaves)
+            v = i >= Lb * K ? (Lb == 0 ? 1.f : 1.f - pb.ws.pbar[s0 + i]) : pb.ws.h[s0 + i];
+        val[i] = v;
     }
     for (int i = lane; i < K * L; i += 32) {
         tk[i] = pb.tokens[(size_t)b * K * L + i];
@@ -291,10 +299,15 @@ __global__ void __launch_bounds__(32 * kDecideWarps) decide_kernel(Problem pb, i
             }
         }
     }
+    // the correction (or bonus) token is drawn at the end node afterwards;
+    // a leaf's residual is p P (mass p; p = 1 in the token rule)
+    const size_t se = s0 + (size_t)ej * K + eo;
+    const bool leaf = ej == Lb;
     pb.accept_len[b] = ej;
     pb.accept_draft[b] = eo;
-    pb.out_token[b] = pb.ws.tok[s0 + (size_t)ej * K + eo];
-    if (pb.residual_mass) pb.residual_mass[b] = pb.ws.S[s0 + (size_t)ej * K + eo];
+    pb.ws.endn[b] = (int)(se | (leaf ? (1u << 30) : 0u));
+    if (pb.residual_mass)
+        pb.residual_mass[b] = leaf ? (token || Lb == 0 ? 1.f : 1.f - pb.ws.pbar[se]) : pb.ws.S[se];
 }
 
 }  // namespace

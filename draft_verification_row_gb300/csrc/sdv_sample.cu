@@ -13,6 +13,13 @@
 // segment (from L2) and finds the element the same way.  When rounding
 // leaves no crossing, the last element of nonzero mass is taken, as the
 // rule states.  T = 0 gives the argmax, lowest index on ties.
+//
+// The same machinery draws verification's correction (or bonus) token, once
+// per request, at the end node the decision chose: from the node's final
+// residual R_n = aT max(e_T - (aD / aT) e_D, 0) with R_n(x*) apart (kept by
+// the node kernel), or from P at a leaf or where S_n = 0 ("SpecTr-GBV"
+// page, section 2, step 4: the correction comes from the adjusted
+// residual at the end of the accepted sub-block).
 #include "sdv_device.cuh"
 #include "sdv_internal.h"
 
@@ -27,26 +34,59 @@ constexpr int kRStep = kRW * kRSeg;                       // units per step
 constexpr int kRMaxSeg = (SDV_MAX_V / 4 + kRSeg - 1) / kRSeg;  // segments of the longest row
 
 struct RowSmem {
-    float mass[kRMaxSeg];  // per segment: sum of 2^(x c - ref c)
-    float ref[kRMaxSeg];   // per segment: its maximum (the reference)
-    float redm[kRW];
+    float mass[kRMaxSeg];  // per segment: sum of its masses (softmax: against ref)
+    float ref[kRMaxSeg];   // softmax: the segment's maximum; residual: unused
     int bad;
 };
 
+// The distribution a draw is taken from.
+struct Dist {
+    const char* rowT;  // softmax: the row; residual: the target row
+    const char* rowD;  // residual: the draft row
+    float c;           // log2(e) / T (0: argmax)
+    int residual;      // 0: softmax(row / T); 1: aT max(e_T - rD e_D, 0), x* apart
+    float negT, negD, aT, rD, Rs;  // residual: references -(M c), scale, ratio, mass at x*
+    int xs;                        // residual: x*, or -1
+    float M, negM;                 // softmax, after the pass: row maximum, -(M c)
+};
+
+// Masses of one unit's elements (ug: its index in the row).
 template <int DT>
-__device__ __forceinline__ uint4 load_unit(const char* row, int ug, int n_units)
+__device__ __forceinline__ void unit_masses(const Dist& d, int ug, int n_units, int V, bool greedy,
+                                            float (&w)[Elem<DT>::kPerUnit])
 {
-    if (ug >= n_units) return make_uint4(0u, 0u, 0u, 0u);  // never summed: the caller masks it
-    return __ldg(reinterpret_cast<const uint4*>(row) + ug);
+    constexpr int EPU = Elem<DT>::kPerUnit;
+    float t[EPU];
+    if (ug < n_units) {
+        unpack_masked<DT>(__ldg(reinterpret_cast<const uint4*>(d.rowT) + ug), ug * EPU, V, t);
+    } else {
+#pragma unroll
+        for (int e = 0; e < EPU; ++e) t[e] = -INFINITY;
+    }
+    if (!d.residual) {
+#pragma unroll
+        for (int e = 0; e < EPU; ++e) w[e] = greedy ? (t[e] == d.M ? 1.f : 0.f) : ex2(fmaf(t[e], d.c, d.negM));
+        return;
+    }
+    float q[EPU];
+    if (ug < n_units) {
+        unpack_masked<DT>(__ldg(reinterpret_cast<const uint4*>(d.rowD) + ug), ug * EPU, V, q);
+    } else {
+#pragma unroll
+        for (int e = 0; e < EPU; ++e) q[e] = -INFINITY;
+    }
+#pragma unroll
+    for (int e = 0; e < EPU; ++e) {
+        const float r = fmaxf(fmaf(-d.rD, ex2(fmaf(q[e], d.c, d.negD)), ex2(fmaf(t[e], d.c, d.negT))), 0.f);
+        w[e] = ug * EPU + e == d.xs ? d.Rs : d.aT * r;
+    }
 }
 
-// Inverse CDF inside segment seg of a row: the masses of its elements are
-// recomputed (2^(x c - M c), or 1 at the maximum for T = 0) and the first
-// element whose running sum exceeds `local` is returned (the last element
-// of nonzero mass if rounding leaves none).  Warp-wide; every lane gets it.
+// Inverse CDF inside segment seg: the first element whose running sum
+// exceeds `local` (the last element of nonzero mass if rounding leaves
+// none).  Warp-wide; every lane gets the result.
 template <int DT>
-__device__ int pick_in_segment(const char* row, int seg, int n_units, int V, float c, float negM, float local,
-                               bool greedy, float M, int lane)
+__device__ int pick_in_segment(const Dist& d, int seg, int n_units, int V, float local, bool greedy, int lane)
 {
     constexpr int EPU = Elem<DT>::kPerUnit;
     float run = 0.f;
@@ -55,20 +95,13 @@ __device__ int pick_in_segment(const char* row, int seg, int n_units, int V, flo
     for (int i = 0; i < kRU; ++i) {
         const int ug = seg * kRSeg + i * 32 + lane;
         float v[EPU];
-        if (ug < n_units) {
-            unpack_masked<DT>(__ldg(reinterpret_cast<const uint4*>(row) + ug), ug * EPU, V, v);
-        } else {
-#pragma unroll
-            for (int e = 0; e < EPU; ++e) v[e] = -INFINITY;
-        }
+        unit_masses<DT>(d, ug, n_units, V, greedy, v);
         float lsum = 0.f;
         int lnz = -1;
 #pragma unroll
         for (int e = 0; e < EPU; ++e) {
-            const float w = greedy ? (v[e] == M ? 1.f : 0.f) : ex2(fmaf(v[e], c, negM));
-            v[e] = w;
-            lsum += w;
-            if (w > 0.f) lnz = ug * EPU + e;
+            lsum += v[e];
+            if (v[e] > 0.f) lnz = ug * EPU + e;
         }
         float incl = lsum;
 #pragma unroll
@@ -102,24 +135,16 @@ __device__ int pick_in_segment(const char* row, int seg, int n_units, int V, flo
     return lastx;
 }
 
+// Softmax pass over a row (all warps): per segment its maximum and its mass
+// against that maximum; NaN or +Inf sets sm.bad.
 template <int DT>
-__global__ void __launch_bounds__(kRT, 2) sample_rows_kernel(SampleArgs a)
+__device__ void softmax_pass(const char* row, int V, float c, bool greedy, RowSmem& sm, int lane, int w)
 {
     using E = Elem<DT>;
     constexpr int EPU = E::kPerUnit;
-    __shared__ RowSmem sm;
-    const int r = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int V = a.V;
     const int n_units = (V + EPU - 1) / EPU;
     const int n_seg = (n_units + kRSeg - 1) / kRSeg;
     const int n_steps = (n_units + kRStep - 1) / kRStep;
-    const char* row = static_cast<const char*>(a.logits) + (size_t)r * (size_t)a.stride * E::kBytes;
-    const bool greedy = a.c == 0.f;
-    const float c = a.c;
-    if (tid == 0) sm.bad = 0;
-
-    // ---- one pass: per-segment maximum and mass ----
     bool bad = false;
 #pragma unroll 1
     for (int st = 0; st < n_steps; ++st) {
@@ -127,8 +152,9 @@ __global__ void __launch_bounds__(kRT, 2) sample_rows_kernel(SampleArgs a)
         const int ug0 = seg * kRSeg + lane;
         uint4 u[kRU];
 #pragma unroll
-        for (int i = 0; i < kRU; ++i) u[i] = load_unit<DT>(row, ug0 + i * 32, n_units);
-        // the segment's maximum: whole units packed, the row's last unit masked
+        for (int i = 0; i < kRU; ++i)
+            u[i] = ug0 + i * 32 < n_units ? __ldg(reinterpret_cast<const uint4*>(row) + ug0 + i * 32)
+                                          : make_uint4(0u, 0u, 0u, 0u);
         float cm = -INFINITY;
 #pragma unroll
         for (int i = 0; i < kRU; ++i) {
@@ -144,7 +170,7 @@ __global__ void __launch_bounds__(kRT, 2) sample_rows_kernel(SampleArgs a)
                 }
             }
         }
-        bad |= (cm != cm) || cm == INFINITY;  // NaN or +Inf makes the row unusable
+        bad |= (cm != cm) || cm == INFINITY;
         const float m = warp_max_redux(cm);
         float z = 0.f;
         if (!greedy && m > -INFINITY && m < INFINITY) {
@@ -172,81 +198,215 @@ __global__ void __launch_bounds__(kRT, 2) sample_rows_kernel(SampleArgs a)
         }
     }
     if (bad) atomicOr(&sm.bad, 1);
-    __syncthreads();
+}
 
-    // ---- the row maximum, and whether the row can be used ----
-    float M = -INFINITY;
+// Residual pass over a node's two rows (all warps): per segment the mass of
+// aT max(e_T - rD e_D, 0), x* apart with mass Rs.
+template <int DT>
+__device__ void residual_pass(const Dist& d, int V, RowSmem& sm, int lane, int w)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+    const int n_units = (V + EPU - 1) / EPU;
+    const int n_seg = (n_units + kRSeg - 1) / kRSeg;
+    const int n_steps = (n_units + kRStep - 1) / kRStep;
+#pragma unroll 1
+    for (int st = 0; st < n_steps; ++st) {
+        const int seg = st * kRW + w;
+        float z = 0.f;
+#pragma unroll 2
+        for (int i = 0; i < kRU; ++i) {
+            float v[EPU];
+            unit_masses<DT>(d, seg * kRSeg + i * 32 + lane, n_units, V, false, v);
+#pragma unroll
+            for (int s2 = 1; s2 < EPU; s2 *= 2)
+#pragma unroll
+                for (int e = 0; e + s2 < EPU; e += 2 * s2) v[e] += v[e + s2];
+            z += v[0];
+        }
+        z = warp_sum(z);
+        if (lane == 0 && seg < n_seg) {
+            sm.mass[seg] = z;
+            sm.ref[seg] = 0.f;
+        }
+    }
+}
+
+// One draw with uniform u (warp-wide).  Softmax distributions rescale each
+// segment from its own maximum to the row's.
+template <int DT>
+__device__ int draw(const Dist& d, const RowSmem& sm, int V, float u, bool greedy, int lane)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+    const int n_units = (V + EPU - 1) / EPU;
+    const int n_seg = (n_units + kRSeg - 1) / kRSeg;
+    auto seg_mass = [&](int i) -> float {
+        if (d.residual) return sm.mass[i];
+        const float ref = sm.ref[i];
+        return ref > -INFINITY ? sm.mass[i] * ex2((ref - d.M) * d.c) : 0.f;
+    };
+    int seg = -1;
+    float base = 0.f, thr = 0.5f;
+    if (greedy) {  // the first segment holding the maximum; its first element equal to it
+        for (int i0 = 0; i0 < n_seg && seg < 0; i0 += 32) {
+            const int i = i0 + lane;
+            const unsigned hit = __ballot_sync(0xffffffffu, i < n_seg && sm.ref[i] == d.M);
+            if (hit) seg = i0 + __ffs(hit) - 1;
+        }
+    } else {
+        float tot = 0.f;
+        for (int i = lane; i < n_seg; i += 32) tot += seg_mass(i);
+        tot = warp_sum(tot);
+        thr = u * tot;
+        float run = 0.f, lbase = 0.f;
+        int last_nz = -1;
+        for (int i0 = 0; i0 < n_seg && seg < 0; i0 += 32) {
+            const int i = i0 + lane;
+            const float v = i < n_seg ? seg_mass(i) : 0.f;
+            float incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            const unsigned cross = __ballot_sync(0xffffffffu, v > 0.f && run + incl > thr);
+            const unsigned nz = __ballot_sync(0xffffffffu, v > 0.f);
+            if (cross) {
+                const int l = __ffs(cross) - 1;
+                seg = i0 + l;
+                base = run + __shfl_sync(0xffffffffu, incl - v, l);
+            } else if (nz) {
+                const int l = 31 - __clz(nz);
+                last_nz = i0 + l;
+                lbase = run + __shfl_sync(0xffffffffu, incl - v, l);
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (seg < 0) {  // rounding: the last segment of nonzero mass
+            seg = last_nz;
+            base = lbase;
+        }
+    }
+    return seg >= 0 ? pick_in_segment<DT>(d, seg, n_units, V, thr - base, greedy, lane) : -1;
+}
+
+// The row maximum after a softmax pass (every thread); false if the row
+// holds NaN or +Inf or no finite logit.
+__device__ __forceinline__ bool row_max(const RowSmem& sm, int n_seg, int lane, float& M)
+{
+    M = -INFINITY;
     for (int i = lane; i < n_seg; i += 32) M = max_nan(M, sm.ref[i]);
     M = warp_max_redux(M);
-    const bool unusable = sm.bad != 0 || !(M > -INFINITY) || M != M;
+    return sm.bad == 0 && M > -INFINITY && M == M;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kRT, 2) sample_rows_kernel(SampleArgs a)
+{
+    using E = Elem<DT>;
+    constexpr int EPU = E::kPerUnit;
+    __shared__ RowSmem sm;
+    const int r = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int V = a.V;
+    const int n_seg = ((V + EPU - 1) / EPU + kRSeg - 1) / kRSeg;
+    const bool greedy = a.c == 0.f;
+    if (tid == 0) sm.bad = 0;
+    __syncthreads();
+    Dist d;
+    d.rowT = static_cast<const char*>(a.logits) + (size_t)r * (size_t)a.stride * E::kBytes;
+    d.rowD = nullptr;
+    d.c = a.c;
+    d.residual = 0;
+    d.xs = -1;
+    softmax_pass<DT>(d.rowT, V, a.c, greedy, sm, lane, w);
+    __syncthreads();
+    float M;
+    const bool ok = row_max(sm, n_seg, lane, M);
     int* const out = a.tokens + (size_t)r * a.n_samples;
-    if (unusable) {
+    if (!ok) {
         for (int s = tid; s < a.n_samples; s += kRT) out[s] = -1;
         if (tid == 0 && a.device_status) atomicOr(a.device_status, SDV_REQ_NONFINITE);
         return;
     }
-    const float negM = -(M * c);
-
-    // ---- draws: warp w takes draws w, w + 16, ... ----
+    d.M = M;
+    d.negM = -(M * a.c);
+    // warp w takes draws w, w + 16, ...
 #pragma unroll 1
     for (int s = w; s < a.n_samples; s += kRW) {
-        int seg = -1;
-        float base = 0.f, thr = 0.f;
-        if (greedy) {
-            // the first segment holding the maximum
-            for (int i0 = 0; i0 < n_seg && seg < 0; i0 += 32) {
-                const int i = i0 + lane;
-                const unsigned hit = __ballot_sync(0xffffffffu, i < n_seg && sm.ref[i] == M);
-                if (hit) seg = i0 + __ffs(hit) - 1;
-            }
-            thr = 0.5f;  // the first element equal to M (mass 1) crosses 0.5
-        } else {
-            // segment masses in the row's reference; their total S
-            float tot = 0.f;
-            for (int i = lane; i < n_seg; i += 32) {
-                const float ref = sm.ref[i];
-                tot += ref > -INFINITY ? sm.mass[i] * ex2((ref - M) * c) : 0.f;
-            }
-            tot = warp_sum(tot);
-            thr = a.u[(size_t)r * a.n_samples + s] * tot;
-            float run = 0.f, lbase = 0.f;
-            int last_nz = -1;
-            for (int i0 = 0; i0 < n_seg && seg < 0; i0 += 32) {
-                const int i = i0 + lane;
-                const float ref = i < n_seg ? sm.ref[i] : -INFINITY;
-                const float v = ref > -INFINITY ? sm.mass[i] * ex2((ref - M) * c) : 0.f;
-                float incl = v;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float n = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += n;
-                }
-                const unsigned cross = __ballot_sync(0xffffffffu, v > 0.f && run + incl > thr);
-                const unsigned nz = __ballot_sync(0xffffffffu, v > 0.f);
-                if (cross) {
-                    const int l = __ffs(cross) - 1;
-                    seg = i0 + l;
-                    base = run + __shfl_sync(0xffffffffu, incl - v, l);
-                } else if (nz) {
-                    const int l = 31 - __clz(nz);
-                    last_nz = i0 + l;
-                    lbase = run + __shfl_sync(0xffffffffu, incl - v, l);
-                }
-                run += __shfl_sync(0xffffffffu, incl, 31);
-            }
-            if (seg < 0) {  // rounding: the last segment of nonzero mass
-                seg = last_nz;
-                base = lbase;
-            }
-        }
-        const int x = seg >= 0 ? pick_in_segment<DT>(row, seg, n_units, V, c, negM, thr - base, greedy, M, lane) : -1;
+        const float u = greedy ? 0.f : a.u[(size_t)r * a.n_samples + s];
+        const int x = draw<DT>(d, sm, V, u, greedy, lane);
         if (lane == 0) out[s] = x;
+    }
+}
+
+// The correction (or bonus) token of request blockIdx.x, at the end node
+// the decision chose: from the node's final residual R_n (kept by the node
+// kernel), or from P at a leaf or where S_n = 0.
+template <int DT>
+__global__ void __launch_bounds__(kRT, 2) correction_kernel(Problem pb)
+{
+    using E = Elem<DT>;
+    constexpr int EPU = E::kPerUnit;
+    __shared__ RowSmem sm;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int e = pb.ws.endn[b];
+    if (e < 0) return;  // invalid request: decide wrote its outputs
+    const int K = pb.K, L = pb.L, V = pb.V;
+    const size_t slot = (size_t)(e & ((1 << 30) - 1));
+    const bool leaf = (e >> 30) != 0;
+    const int k = (int)(slot % K), j = (int)((slot / K) % (L + 1));
+    const float u = pb.sample_u[((size_t)b * K + k) * (L + 1) + j];
+    const int n_seg = ((V + EPU - 1) / EPU + kRSeg - 1) / kRSeg;
+    if (tid == 0) sm.bad = 0;
+    __syncthreads();
+    Dist d;
+    d.rowT = static_cast<const char*>(pb.target) + (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
+    d.rowD = leaf ? nullptr
+                  : static_cast<const char*>(pb.draft) + (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
+    d.c = pb.c;
+    d.residual = !leaf && pb.ws.S[slot] > 0.f;
+    d.xs = -1;
+    if (d.residual) {
+        const float* prm = pb.ws.prm + slot * 5;
+        d.negT = prm[0];
+        d.negD = prm[1];
+        d.aT = prm[2];
+        d.rD = prm[3];
+        d.Rs = prm[4];
+        d.xs = pb.ws.xs[slot];
+        residual_pass<DT>(d, V, sm, lane, w);
+        __syncthreads();
+    } else {
+        softmax_pass<DT>(d.rowT, V, d.c, false, sm, lane, w);
+        __syncthreads();
+        float M;
+        if (!row_max(sm, n_seg, lane, M)) {  // checked before; kept for safety
+            if (tid == 0) pb.out_token[b] = -1;
+            return;
+        }
+        d.M = M;
+        d.negM = -(M * d.c);
+    }
+    if (w == 0) {
+        const int x = draw<DT>(d, sm, V, u, false, lane);
+        if (lane == 0) pb.out_token[b] = x;
     }
 }
 
 }  // namespace
 
 int sample_threads() { return kRT; }
+
+cudaError_t launch_correction(const Problem& pb, cudaStream_t st)
+{
+    if (pb.B == 0) return cudaSuccess;
+    if (pb.dtype == SDV_BF16)
+        correction_kernel<SDV_BF16><<<pb.B, kRT, 0, st>>>(pb);
+    else
+        correction_kernel<SDV_F32><<<pb.B, kRT, 0, st>>>(pb);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st)
 {

@@ -41,7 +41,6 @@ constexpr int kChunk = kCT * kUPT;       // units per row per chunk (12 KB)
 constexpr int kStages = 3;               // 3 x 24 KB in flight per CTA
 constexpr int kStash = 1;                // set-aside chunks a lane can hold (at most 2: d0, d1)
 static_assert(kStash >= 1 && kStash <= 2, "a lane keeps at most two set-aside chunk indices");
-constexpr int kMaxChunks = (SDV_MAX_V / 4 + kChunk - 1) / kChunk;
 constexpr int kQ = 4;                    // node descriptor queue depth
 
 __device__ __forceinline__ void cbar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory"); }
@@ -92,7 +91,6 @@ struct NodeDesc {
     int dk[SDV_MAX_K];            // drafts of the draws, in index order
     int y[SDV_MAX_K];             // their tokens
     float gT[SDV_MAX_K], gD[SDV_MAX_K];  // target / draft logits at those tokens
-    float usample;
 };
 
 struct StreamSmem {
@@ -101,8 +99,6 @@ struct StreamSmem {
     uint64_t qfull[kQ], qempty[kQ];
     NodeDesc qd[kQ];
     NodeDesc cur;                    // the consumers' copy of the current node
-    float table[kMaxChunks][kSW];    // mass of the sampled distribution per (chunk, warp): index order
-    float tableP[kMaxChunks][kSW];   // the same for the target P (last sweep), for S = 0
     float redf[4][kSW];
     int redi[4][kSW];
     int firstT, firstD;              // lowest index of each row's maximum
@@ -112,9 +108,8 @@ struct StreamSmem {
     float MT, MD, gnegT, gnegD, zT, zD, zrestT, zrestD, emaxT, emaxD;
     int uT, uD;
     float S, D, cbar, pbar, Pbs, Qbs, Rs, Ts, Rj, aT, aD, rD;
-    int xs, use_res, bad;
-    float thr, base;
-    int pick_c, pick_w;
+    int xs, bad;
+    int lbad, lfin;                  // leaf check: NaN or +Inf seen, a finite logit seen
 };
 
 // Online statistics of one row, per thread, in a reference shared by the
@@ -357,6 +352,34 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
     }
 }
 
+// A leaf's target row is only checked (no NaN or +Inf, some finite logit):
+// its bonus token, if the decision ends there, is drawn after the decision.
+template <int DT>
+__device__ __forceinline__ void leaf_check(StreamSmem* sm, uint32_t& g, bool& timed_out, int nc, int n_units, int V,
+                                           int cw, int lane)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+    bool bad = false, fin = false;
+#pragma unroll 1
+    for (int ch = 0; ch < nc; ++ch, ++g) {
+        const int s = g % kStages;
+        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
+#pragma unroll
+        for (int i = 0; i < kUPT; ++i) {
+            const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
+            if (ug < n_units) {
+                const float um = unit_max_masked<DT>(sm->ring[s][0][ul], ug * EPU, V);
+                bad |= (um != um) || um == INFINITY;
+                fin |= um > -INFINITY;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->empty[s]);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&sm->lbad, 1);
+    if (__any_sync(0xffffffffu, fin) && lane == 0) atomicOr(&sm->lfin, 1);
+}
+
 // The residual term of one token divided by aT = p / Z_T:
 // max(aT e_T - aD e_D, 0) / aT = max(e_T - r e_D, 0), r = aD / aT.  One FMA
 // per token; the sums are scaled by aT once.  (With p = 0, aT = 0 and r is
@@ -365,9 +388,7 @@ __device__ __forceinline__ float res_unscaled(float eT, float eD, float r) { ret
 
 // One residual sweep over a node's rows (from the ring): returns this
 // thread's share of S_j = sum over x != x* of max(aT e_T(x) - aD e_D(x), 0).
-// The last sweep (LAST) also fills the sampling tables: the residual's mass
-// and the target's mass per (chunk, warp).
-template <int DT, bool LAST>
+template <int DT>
 __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_out, int nc, int n_units, int V,
                                        float c, float gnegT, float gnegD, float aT, float r, int xs, int cw,
                                        int lane)
@@ -380,7 +401,7 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
         const int s = g % kStages;
         if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
         const bool tail = ch == nc - 1;
-        float w = 0.f, wp = 0.f;
+        float w = 0.f;
 #pragma unroll
         for (int i = 0; i < kUPT; ++i) {
             const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
@@ -394,30 +415,18 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
                     Elem<DT>::unpack(sm->ring[s][1][ul], d);
                 }
 #pragma unroll
-                for (int e = 0; e < EPU; ++e) {
-                    const float eT = ex2(fmaf(t[e], c, gnegT));
-                    d[e] = res_unscaled(eT, ex2(fmaf(d[e], c, gnegD)), r);
-                    t[e] = eT;
-                }
+                for (int e = 0; e < EPU; ++e) d[e] = res_unscaled(ex2(fmaf(t[e], c, gnegT)), ex2(fmaf(d[e], c, gnegD)), r);
                 if (ch == xs_ch) {
 #pragma unroll
                     for (int e = 0; e < EPU; ++e)
                         if (ug * EPU + e == xs) d[e] = 0.f;
                 }
                 w += tree_sum(d);
-                if (LAST) wp += tree_sum(t);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->empty[s]);
         tot += w;
-        if (LAST) {
-            const float ws = warp_sum(w), wps = warp_sum(wp);
-            if (lane == 0) {
-                sm->table[ch][cw] = aT * ws;
-                sm->tableP[ch][cw] = wps;
-            }
-        }
     }
     return aT * tot;
 }
@@ -616,7 +625,6 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                     d.k = k;
                     d.leaf = leaf;
                     d.nd = __popc(m);
-                    d.usample = pb.sample_u[((size_t)b * K + k) * (L + 1) + j];
                 }
             } else if (lane == 0) {
                 d.slot = -1;
@@ -652,7 +660,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
             const char* gD = leaf ? nullptr
                                   : static_cast<const char*>(pb.draft) +
                                         (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
-            const int passes = 1 + (leaf ? 1 : nd);
+            const int passes = leaf ? 1 : 1 + nd;  // a leaf is only checked
             bool ok = true;
             for (int ps = 0; ps < passes && ok; ++ps) {
                 const bool with_d = !leaf;
@@ -692,6 +700,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
         cbar_sync();  // the previous node's readers of sm->cur are done
         if (ct < (int)(sizeof(NodeDesc) / 4))
             reinterpret_cast<int*>(&sm->cur)[ct] = reinterpret_cast<const int*>(&sm->qd[q])[ct];
+        if (ct == 0) sm->lbad = sm->lfin = 0;
         cbar_sync();
         if (ct == 0) mbar_arrive(&sm->qempty[q]);
         const int slot = *static_cast<volatile int*>(&sm->abort) ? -1 : sm->cur.slot;
@@ -707,282 +716,151 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                               : static_cast<const char*>(pb.draft) +
                                     (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
 
-        // ---- pass 1: online statistics ----
-        Online sT, sD;
-        if (leaf)
-            pass1<DT, false>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
-        else
-            pass1<DT, true>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
-        online_finish<DT>(sT, sm->stash[0][ct], cw, lane, n_units, V, c);
-        if (!leaf) online_finish<DT>(sD, sm->stash[1][ct], cw, lane, n_units, V, c);
-        combine_rows(sm, sT, sD, !leaf, c, ct);
-
-        // ---- scalar state ----
-        if (ct == 0) {
-            const bool bad = !(isfinite(sm->MT) && isfinite(sm->zT) && sm->zT > 0.f) ||
-                             (!leaf && !(isfinite(sm->MD) && isfinite(sm->zD) && sm->zD > 0.f));
-            sm->bad = bad;
-            if (bad) {
+        if (leaf) {
+            // ---- a leaf: its target row is only checked ----
+            leaf_check<DT>(sm, g, timed_out, nc, n_units, V, cw, lane);
+            cbar_sync();
+            if (ct == 0 && (sm->lbad || !sm->lfin)) {
                 atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
                 if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
             }
-            // the node weight: from the parent, through its flag
-            float pbar = 0.f;
-            if (j > 0 && pb.mode != SDV_MODE_TOKEN) {
-                const uint64_t t0 = globaltimer();
-                while (ld_acquire(&pb.ws.ready[slot]) == 0) {
-                    if (globaltimer() - t0 > 2000000000ull) {
-                        sm->abort = 1;
-                        break;
-                    }
-                }
-                pbar = pb.ws.pbar[slot];
-            }
-            sm->pbar = pbar;
-            const int xs = (!leaf && sm->uT >= 0 && sm->uT == sm->uD) ? sm->uT : -1;
-            sm->xs = xs;
-            sm->Pbs = xs >= 0 ? sm->zrestT / sm->zT : 0.f;
-            sm->Qbs = xs >= 0 ? sm->zrestD / sm->zD : 0.f;
-            sm->Rs = sm->Ts = 0.f;
-            sm->S = 1.f - pbar;
-            sm->D = 1.f;
-            sm->cbar = 0.f;
-            sm->use_res = 0;
-        }
-        cbar_sync();
-        const float pbar = sm->pbar, p = 1.f - pbar;
-        const float gnegT = sm->gnegT, gnegD = sm->gnegD;
-        const int xs = sm->xs;
+        } else {
+            // ---- pass 1: online statistics ----
+            Online sT, sD;
+            pass1<DT, true>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
+            online_finish<DT>(sT, sm->stash[0][ct], cw, lane, n_units, V, c);
+            online_finish<DT>(sD, sm->stash[1][ct], cw, lane, n_units, V, c);
+            combine_rows(sm, sT, sD, true, c, ct);
 
-        // ---- pass 2: the residual recursion, one sweep per draw ----
-        // R_0 = p P, R_j = max(R_{j-1} - D_{j-1} Q, 0), S_j = sum R_j,
-        // D_j = (1 - p) + S_j.  Scalars are kept as complements (pbar =
-        // 1 - p, cbar = C - 1, Pbs = 1 - P(x*), Qbs = 1 - Q(x*)) so that
-        // nothing cancels when p, P or Q is close to 1.  The shared
-        // dominant token x* (the unique maximum of both rows) is left out
-        // of the sweeps and carried in closed form:
-        //   R_1(x*) = Qbs - Pbs - pbar + pbar Pbs,
-        //   R_j(x*) = R_{j-1}(x*) Qbs - (pbar + T_{j-1}) (1 - Qbs),
-        // with T_{j-1} the sweep's sum over the other tokens.
-        for (int di = 0; di < nd && !leaf; ++di) {
-            const int k2 = sm->cur.dk[di];
-            const bool first_draw = di == 0;
-            const bool last = di == nd - 1;
+            // ---- scalar state ----
             if (ct == 0) {
-                const int y = sm->cur.y[di];
-                const float D = sm->D;
-                const float cnew = first_draw ? 0.f : sm->cbar + D;
-                const float Pbs = sm->Pbs, Qbs = sm->Qbs;
-                const float Rj = first_draw ? ((Qbs - Pbs) - pbar) + pbar * Pbs
-                                            : sm->Rs * Qbs - (pbar + sm->Ts) * (1.f - Qbs);
-                sm->Rj = Rj;
-                float R, Qy, abar_num;
-                if (y == xs) {
-                    Qy = 1.f - Qbs;
-                    R = first_draw ? (1.f - pbar) * (1.f - Pbs) : sm->Rs;
-                    abar_num = fmaxf(-Rj, 0.f);
-                } else {
-                    const ProbS Py = prob_s(sm, true, y, sm->cur.gT[di], c);
-                    const ProbS Qp = prob_s(sm, false, y, sm->cur.gD[di], c);
-                    Qy = Qp.P;
-                    R = first_draw ? p * Py.P : fmaxf((1.f - pbar) * Py.P - (1.f + sm->cbar) * Qp.P, 0.f);
-                    abar_num = fmaxf((1.f + cnew) * Qp.P - (1.f - pbar) * Py.P, 0.f);
+                const bool bad = !(isfinite(sm->MT) && isfinite(sm->zT) && sm->zT > 0.f) ||
+                                 !(isfinite(sm->MD) && isfinite(sm->zD) && sm->zD > 0.f);
+                sm->bad = bad;
+                if (bad) {
+                    atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
+                    if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
                 }
-                float a, abar;
-                const float ratio = (D > 0.f && Qy > 0.f) ? (R / D) / Qy : INFINITY;
-                if (ratio >= 1.f) {
-                    a = 1.f;
-                    abar = 0.f;
-                } else if (!(R > 0.f)) {
-                    a = 0.f;
-                    abar = 1.f;
-                } else {
-                    a = ratio;
-                    abar = fminf((abar_num / D) / Qy, 1.f);
-                }
-                sm->cbar = cnew;
-                pb.ws.a[sbase + k2] = a;
-                bool first_of_token = true;  // this draw's child is new: it owns it
-                for (int e = 0; e < di; ++e) first_of_token &= sm->cur.y[e] != y;
-                if (pb.mode != SDV_MODE_TOKEN) {
-                    const size_t sc = sbase + K + k2;
-                    if (first_of_token) {  // child first reached by this draw
-                        pb.ws.pbar[sc] = abar;
-                        st_release(&pb.ws.ready[sc], 1);
+                // the node weight: from the parent, through its flag
+                float pbar = 0.f;
+                if (j > 0 && pb.mode != SDV_MODE_TOKEN) {
+                    const uint64_t t0 = globaltimer();
+                    while (ld_acquire(&pb.ws.ready[slot]) == 0) {
+                        if (globaltimer() - t0 > 2000000000ull) {
+                            sm->abort = 1;
+                            break;
+                        }
                     }
+                    pbar = pb.ws.pbar[slot];
                 }
-                sm->aT = p / sm->zT;
-                sm->aD = (1.f + cnew) / sm->zD;
-                sm->rD = sm->aT > 0.f ? sm->aD / sm->aT : 3.402823466e38f;
+                sm->pbar = pbar;
+                const int xs = (sm->uT >= 0 && sm->uT == sm->uD) ? sm->uT : -1;
+                sm->xs = xs;
+                sm->Pbs = xs >= 0 ? sm->zrestT / sm->zT : 0.f;
+                sm->Qbs = xs >= 0 ? sm->zrestD / sm->zD : 0.f;
+                sm->Rs = sm->Ts = 0.f;
+                sm->S = 1.f - pbar;
+                sm->D = 1.f;
+                sm->cbar = 0.f;
             }
             cbar_sync();
-            const float aT = sm->aT, rD = sm->rD;
-            float tot = last ? sweep<DT, true>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, aT, rD, xs, cw, lane)
-                             : sweep<DT, false>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, aT, rD, xs, cw, lane);
-            tot = warp_sum(tot);
-            if (lane == 0) sm->redf[2][cw] = tot;
-            cbar_sync();
-            if (ct == 0) {
-                float Sj = 0.f;
-                for (int i = 0; i < kSW; ++i) Sj += sm->redf[2][i];
-                if (xs >= 0) {  // the sweeps left x* out: their sum is the mass elsewhere
-                    const float Rs = fmaxf(sm->Rj, 0.f);
-                    sm->Ts = Sj;
-                    sm->Rs = Rs;
-                    Sj += Rs;
-                    if (last) {
-                        const int ux = xs / EPU;
-                        sm->table[ux / kChunk][(ux % kChunk) / kWU] += Rs;
-                    }
-                }
-                sm->S = fmaxf(Sj, 0.f);
-                sm->D = pbar + sm->S;
-                sm->use_res = sm->S > 0.f;
-            }
-        }
-        if (leaf) {
-            // bonus: a target-only pass builds the table of P's mass
-#pragma unroll 1
-            for (int ch = 0; ch < nc; ++ch, ++g) {
-                const int s = g % kStages;
-                if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
-                float w = 0.f;
-#pragma unroll
-                for (int i = 0; i < kUPT; ++i) {
-                    const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
-                    if (ug < n_units) w += unit_sum<DT>(sm->ring[s][0][ul], ug * EPU, V, c, gnegT);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm->empty[s]);
-                const float ws = warp_sum(w);
-                if (lane == 0) sm->table[ch][cw] = ws;
-            }
-        }
-        cbar_sync();
-        const bool use_res = sm->use_res != 0;
-        if (!leaf && !use_res) {
-            // S = 0: the correction comes from P, whose table the last sweep
-            // built beside the residual's
-            for (int i = ct; i < nc * kSW; i += kCT) (&sm->table[0][0])[i] = (&sm->tableP[0][0])[i];
-            cbar_sync();
-        }
+            const float pbar = sm->pbar, p = 1.f - pbar;
+            const float gnegT = sm->gnegT, gnegD = sm->gnegD;
+            const int xs = sm->xs;
 
-        // ---- the candidate correction: inverse CDF over the table ----
-        if (cw == 0) {
-            // lanes scan the table in index order, 32 entries at a time
-            const int n_ent = nc * kSW;
-            const float* tab = &sm->table[0][0];
-            float run = 0.f, Stot = 0.f;
-            for (int i = lane; i < ((n_ent + 31) & ~31); i += 32) Stot += i < n_ent ? tab[i] : 0.f;
-            Stot = warp_sum(Stot);
-            const float thr = sm->cur.usample * Stot;
-            int found = -1, last_nz = -1;
-            float fbase = 0.f, lbase = 0.f;
-            for (int i0 = 0; i0 < n_ent && found < 0; i0 += 32) {
-                const int i = i0 + lane;
-                const float v = i < n_ent ? tab[i] : 0.f;
-                float incl = v;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float n = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += n;
-                }
-                const unsigned cross = __ballot_sync(0xffffffffu, v > 0.f && run + incl > thr);
-                const unsigned nz = __ballot_sync(0xffffffffu, v > 0.f);
-                if (cross) {
-                    const int l = __ffs(cross) - 1;
-                    found = i0 + l;
-                    fbase = run + __shfl_sync(0xffffffffu, incl - v, l);
-                } else if (nz) {
-                    const int l = 31 - __clz(nz);
-                    last_nz = i0 + l;
-                    lbase = run + __shfl_sync(0xffffffffu, incl - v, l);
-                }
-                run += __shfl_sync(0xffffffffu, incl, 31);
-            }
-            if (found < 0) {
-                found = last_nz;
-                fbase = lbase;
-            }
-            if (lane == 0) {
-                sm->thr = thr;
-                sm->base = fbase;
-                sm->pick_c = (found < 0 || sm->bad) ? -1 : found / kSW;
-                sm->pick_w = found < 0 ? 0 : found % kSW;
-            }
-        }
-        cbar_sync();
-        if (sm->pick_c >= 0 && cw == sm->pick_w) {
-            // the chosen warp re-reads its units of the chunk (from L2), in
-            // index order: sub-unit i, then lane
-            const float local = sm->thr - sm->base;
-            const float aT = sm->aT, rD = sm->rD;
-            float run = 0.f;
-            int chosen = -1, lastx = -1;
-#pragma unroll 1
-            for (int i = 0; i < kUPT && chosen < 0; ++i) {
-                const int ug = sm->pick_c * kChunk + unit_local(cw, i, lane);
-                float vals[EPU];
-                float lsum = 0.f;
-                int lnz = -1;
-                {
-                    float t[EPU], d[EPU];
-                    if (ug < n_units) {
-                        unpack_masked<DT>(__ldg(reinterpret_cast<const uint4*>(gT) + ug), ug * EPU, V, t);
-                        if (use_res)
-                            unpack_masked<DT>(__ldg(reinterpret_cast<const uint4*>(gD) + ug), ug * EPU, V, d);
+            // ---- pass 2: the residual recursion, one sweep per draw ----
+            // R_0 = p P, R_j = max(R_{j-1} - D_{j-1} Q, 0), S_j = sum R_j,
+            // D_j = (1 - p) + S_j.  Scalars are kept as complements (pbar =
+            // 1 - p, cbar = C - 1, Pbs = 1 - P(x*), Qbs = 1 - Q(x*)) so that
+            // nothing cancels when p, P or Q is close to 1.  The shared
+            // dominant token x* (the unique maximum of both rows) is left out
+            // of the sweeps and carried in closed form:
+            //   R_1(x*) = Qbs - Pbs - pbar + pbar Pbs,
+            //   R_j(x*) = R_{j-1}(x*) Qbs - (pbar + T_{j-1}) (1 - Qbs),
+            // with T_{j-1} the sweep's sum over the other tokens.
+            for (int di = 0; di < nd; ++di) {
+                const int k2 = sm->cur.dk[di];
+                const bool first_draw = di == 0;
+                if (ct == 0) {
+                    const int y = sm->cur.y[di];
+                    const float D = sm->D;
+                    const float cnew = first_draw ? 0.f : sm->cbar + D;
+                    const float Pbs = sm->Pbs, Qbs = sm->Qbs;
+                    const float Rj = first_draw ? ((Qbs - Pbs) - pbar) + pbar * Pbs
+                                                : sm->Rs * Qbs - (pbar + sm->Ts) * (1.f - Qbs);
+                    sm->Rj = Rj;
+                    float R, Qy, abar_num;
+                    if (y == xs) {
+                        Qy = 1.f - Qbs;
+                        R = first_draw ? (1.f - pbar) * (1.f - Pbs) : sm->Rs;
+                        abar_num = fmaxf(-Rj, 0.f);
+                    } else {
+                        const ProbS Py = prob_s(sm, true, y, sm->cur.gT[di], c);
+                        const ProbS Qp = prob_s(sm, false, y, sm->cur.gD[di], c);
+                        Qy = Qp.P;
+                        R = first_draw ? p * Py.P : fmaxf((1.f - pbar) * Py.P - (1.f + sm->cbar) * Qp.P, 0.f);
+                        abar_num = fmaxf((1.f + cnew) * Qp.P - (1.f - pbar) * Py.P, 0.f);
                     }
-#pragma unroll
-                    for (int e = 0; e < EPU; ++e) {
-                        float wx = 0.f;
-                        if (ug < n_units) {
-                            const float eT = ex2(fmaf(t[e], c, gnegT));
-                            wx = use_res ? aT * res_unscaled(eT, ex2(fmaf(d[e], c, gnegD)), rD) : eT;
-                            if (use_res && ug * EPU + e == xs) wx = sm->Rs;
+                    float a, abar;
+                    const float ratio = (D > 0.f && Qy > 0.f) ? (R / D) / Qy : INFINITY;
+                    if (ratio >= 1.f) {
+                        a = 1.f;
+                        abar = 0.f;
+                    } else if (!(R > 0.f)) {
+                        a = 0.f;
+                        abar = 1.f;
+                    } else {
+                        a = ratio;
+                        abar = fminf((abar_num / D) / Qy, 1.f);
+                    }
+                    sm->cbar = cnew;
+                    pb.ws.a[sbase + k2] = a;
+                    bool first_of_token = true;  // this draw's child is new: it owns it
+                    for (int e = 0; e < di; ++e) first_of_token &= sm->cur.y[e] != y;
+                    if (pb.mode != SDV_MODE_TOKEN) {
+                        const size_t sc = sbase + K + k2;
+                        if (first_of_token) {  // child first reached by this draw
+                            pb.ws.pbar[sc] = abar;
+                            st_release(&pb.ws.ready[sc], 1);
                         }
-                        vals[e] = wx;
-                        lsum += wx;
-                        if (wx > 0.f) lnz = ug * EPU + e;
                     }
+                    sm->aT = p / sm->zT;
+                    sm->aD = (1.f + cnew) / sm->zD;
+                    sm->rD = sm->aT > 0.f ? sm->aD / sm->aT : 3.402823466e38f;
                 }
-                float incl = lsum;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float n = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += n;
-                }
-                const unsigned cross = __ballot_sync(0xffffffffu, lsum > 0.f && run + incl > local);
-                const unsigned nz = __ballot_sync(0xffffffffu, lnz >= 0);
-                if (cross) {
-                    const int l = __ffs(cross) - 1;
-                    int pick = -1;
-                    if (lane == l) {
-                        float acc = run + incl - lsum;
-                        for (int e = 0; e < EPU; ++e) {
-                            if (vals[e] > 0.f) {
-                                acc += vals[e];
-                                if (acc > local) {
-                                    pick = ug * EPU + e;
-                                    break;
-                                }
-                            }
-                        }
-                        if (pick < 0) pick = lnz;  // rounding: the lane's last nonzero
+                cbar_sync();
+                float tot = sweep<DT>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, sm->aT, sm->rD, xs, cw, lane);
+                tot = warp_sum(tot);
+                if (lane == 0) sm->redf[2][cw] = tot;
+                cbar_sync();
+                if (ct == 0) {
+                    float Sj = 0.f;
+                    for (int i = 0; i < kSW; ++i) Sj += sm->redf[2][i];
+                    if (xs >= 0) {  // the sweeps left x* out: their sum is the mass elsewhere
+                        const float Rs = fmaxf(sm->Rj, 0.f);
+                        sm->Ts = Sj;
+                        sm->Rs = Rs;
+                        Sj += Rs;
                     }
-                    chosen = __shfl_sync(0xffffffffu, pick, l);
-                } else if (nz) {
-                    lastx = __shfl_sync(0xffffffffu, lnz, 31 - __clz(nz));
+                    sm->S = fmaxf(Sj, 0.f);
+                    sm->D = pbar + sm->S;
                 }
-                run += __shfl_sync(0xffffffffu, incl, 31);
             }
-            if (lane == 0) pb.ws.tok[slot] = chosen >= 0 ? chosen : lastx;
-        } else if (sm->pick_c < 0 && ct == 0) {
-            pb.ws.tok[slot] = -1;
-        }
-        if (ct == 0) {
-            const float S = sm->S, D = sm->D;
-            pb.ws.h[slot] = leaf ? p : (D > 0.f ? S / D : 1.f);
-            pb.ws.S[slot] = S;
+            if (ct == 0) {
+                // the node's block acceptance and, for the correction draw
+                // should the decision end here, its final residual
+                // R_n = aT max(e_T - (aD / aT) e_D, 0) with R_n(x*) apart
+                const float S = sm->S, D = sm->D;
+                pb.ws.h[slot] = D > 0.f ? S / D : 1.f;
+                pb.ws.S[slot] = S;
+                float* prm = pb.ws.prm + (size_t)slot * 5;
+                prm[0] = gnegT;
+                prm[1] = gnegD;
+                prm[2] = sm->aT;
+                prm[3] = sm->rD;
+                prm[4] = sm->Rs;
+                pb.ws.xs[slot] = xs;
+            }
         }
         // a timed-out wait anywhere stops every consumer together (the
         // decision is read after the node's last barrier, so it is uniform)
