@@ -50,15 +50,16 @@ struct Dist {
     float M, negM;                 // softmax, after the pass: row maximum, -(M c)
 };
 
-// Masses of one unit's elements (ug: its index in the row).
+// Masses of one unit's elements (ug: its index in the row; tu, du: the
+// unit of the row and, for a residual, of the draft row).
 template <int DT>
-__device__ __forceinline__ void unit_masses(const Dist& d, int ug, int n_units, int V, bool greedy,
-                                            float (&w)[Elem<DT>::kPerUnit])
+__device__ __forceinline__ void masses_of(const Dist& d, const uint4& tu, const uint4& du, int ug, int n_units, int V,
+                                          bool greedy, float (&w)[Elem<DT>::kPerUnit])
 {
     constexpr int EPU = Elem<DT>::kPerUnit;
     float t[EPU];
     if (ug < n_units) {
-        unpack_masked<DT>(__ldg(reinterpret_cast<const uint4*>(d.rowT) + ug), ug * EPU, V, t);
+        unpack_masked<DT>(tu, ug * EPU, V, t);
     } else {
 #pragma unroll
         for (int e = 0; e < EPU; ++e) t[e] = -INFINITY;
@@ -70,7 +71,7 @@ __device__ __forceinline__ void unit_masses(const Dist& d, int ug, int n_units, 
     }
     float q[EPU];
     if (ug < n_units) {
-        unpack_masked<DT>(__ldg(reinterpret_cast<const uint4*>(d.rowD) + ug), ug * EPU, V, q);
+        unpack_masked<DT>(du, ug * EPU, V, q);
     } else {
 #pragma unroll
         for (int e = 0; e < EPU; ++e) q[e] = -INFINITY;
@@ -80,6 +81,21 @@ __device__ __forceinline__ void unit_masses(const Dist& d, int ug, int n_units, 
         const float r = fmaxf(fmaf(-d.rD, ex2(fmaf(q[e], d.c, d.negD)), ex2(fmaf(t[e], d.c, d.negT))), 0.f);
         w[e] = ug * EPU + e == d.xs ? d.Rs : d.aT * r;
     }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 unit_at(const char* row, int ug, int n_units)
+{
+    return ug < n_units && row ? __ldg(reinterpret_cast<const uint4*>(row) + ug) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+template <int DT>
+__device__ __forceinline__ void unit_masses(const Dist& d, int ug, int n_units, int V, bool greedy,
+                                            float (&w)[Elem<DT>::kPerUnit])
+{
+    const uint4 tu = unit_at<DT>(d.rowT, ug, n_units);
+    const uint4 du = d.residual ? unit_at<DT>(d.rowD, ug, n_units) : tu;
+    masses_of<DT>(d, tu, du, ug, n_units, V, greedy, w);
 }
 
 // Inverse CDF inside segment seg: the first element whose running sum
@@ -209,19 +225,30 @@ __device__ void residual_pass(const Dist& d, int V, RowSmem& sm, int lane, int w
     const int n_units = (V + EPU - 1) / EPU;
     const int n_seg = (n_units + kRSeg - 1) / kRSeg;
     const int n_steps = (n_units + kRStep - 1) / kRStep;
+    constexpr int kHalf = kRU / 2;  // units of both rows loaded before they are used
 #pragma unroll 1
     for (int st = 0; st < n_steps; ++st) {
         const int seg = st * kRW + w;
         float z = 0.f;
-#pragma unroll 2
-        for (int i = 0; i < kRU; ++i) {
-            float v[EPU];
-            unit_masses<DT>(d, seg * kRSeg + i * 32 + lane, n_units, V, false, v);
 #pragma unroll
-            for (int s2 = 1; s2 < EPU; s2 *= 2)
+        for (int h = 0; h < kRU; h += kHalf) {
+            uint4 tu[kHalf], du[kHalf];
 #pragma unroll
-                for (int e = 0; e + s2 < EPU; e += 2 * s2) v[e] += v[e + s2];
-            z += v[0];
+            for (int i = 0; i < kHalf; ++i) {
+                const int ug = seg * kRSeg + (h + i) * 32 + lane;
+                tu[i] = unit_at<DT>(d.rowT, ug, n_units);
+                du[i] = unit_at<DT>(d.rowD, ug, n_units);
+            }
+#pragma unroll
+            for (int i = 0; i < kHalf; ++i) {
+                float v[EPU];
+                masses_of<DT>(d, tu[i], du[i], seg * kRSeg + (h + i) * 32 + lane, n_units, V, false, v);
+#pragma unroll
+                for (int s2 = 1; s2 < EPU; s2 *= 2)
+#pragma unroll
+                    for (int e = 0; e + s2 < EPU; e += 2 * s2) v[e] += v[e + s2];
+                z += v[0];
+            }
         }
         z = warp_sum(z);
         if (lane == 0 && seg < n_seg) {
