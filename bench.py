@@ -320,7 +320,7 @@ def run_ours(args, world, rank, local):
     all_positions = sum_over_ranks(positions, world)
     ms_step = total_ms / args.steps
     value = all_positions / (ms_step / 1000.0)
-    launches = 4 * args.steps  # per call: prep, the node kernel, decide, the correction draw
+    launches = 3 * args.steps  # per call: prep, the node kernel, the decision and correction draw
 
     peak, peak_kind = measured_peaks()
     row_step_s = row_ms / args.steps / 1000.0

@@ -24,7 +24,7 @@ bool sizes_ok(int B, int K, int L, int V)
 size_t workspace_size(int B, int K, int L)
 {
     const size_t n = slot_count(B, K, L);
-    return 7 * align_up(n * 4) + align_up(n * 5 * 4) + align_up(n) + 2 * align_up((size_t)B * 4) +
+    return 7 * align_up(n * 4) + align_up(n * 5 * 4) + align_up(n) + align_up((size_t)B * 4) +
            align_up((size_t)(L + 1) * B * K * 4) + align_up((size_t)(L + 2) * 4);
 }
 
@@ -45,8 +45,6 @@ Workspace carve(void* base, int B, int K, int L)
     p += align_up(n * 5 * 4);
     w.xs = reinterpret_cast<int*>(p);
     p += align_up(n * 4);
-    w.endn = reinterpret_cast<int*>(p);
-    p += align_up((size_t)B * 4);
     w.am = reinterpret_cast<int*>(p);
     p += align_up(n * 4);
     w.owner = reinterpret_cast<unsigned char*>(p);
@@ -169,9 +167,9 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
         if (e != cudaSuccess) return SDV_ERR_CUDA;
     }
     if (!prof_record(g_prof_stop, st)) return SDV_ERR_CUDA;
-    if (launch_decide(pb, greedy, st) != cudaSuccess) return SDV_ERR_CUDA;
-    // the correction (or bonus) token, drawn at each request's end node only
-    if (!greedy && launch_correction(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
+    // per request: the decision, then the correction (or bonus) token drawn
+    // at its end node only
+    if (launch_finish(pb, greedy, st) != cudaSuccess) return SDV_ERR_CUDA;
     return SDV_OK;
 }
 

@@ -24,7 +24,6 @@ struct Workspace {
     float* prm;            // node residual for the correction draw: [slot][5] =
                            //   -(M_T c), -(M_D c), aT = p / Z_T, aD / aT, R_n(x*)
     int* xs;               // node shared dominant token x* (or -1)
-    int* endn;             // [B] end node of the decision: slot | leaf << 30, or -1
     int* am;               // node argmax (greedy)
     unsigned char* owner;  // lowest draft sharing draft k's first j tokens
     int* req;              // [B] request status bits
@@ -59,7 +58,6 @@ inline size_t slot_count(int B, int K, int L) { return (size_t)B * (size_t)(L + 
 // Kernel launchers (sdv_kernels.cu, sdv_stream.cu); each returns a cudaError_t.
 cudaError_t launch_prep(const Problem& pb, cudaStream_t st);
 cudaError_t launch_argmax(const Problem& pb, cudaStream_t st);
-cudaError_t launch_decide(const Problem& pb, bool greedy, cudaStream_t st);
 cudaError_t launch_stream(const Problem& pb, cudaStream_t st);
 
 // Draft-token sampling (sdv_sample.cu): n_samples draws per row.
@@ -73,8 +71,9 @@ struct SampleArgs {
     int* device_status;
 };
 cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st);
-// The correction (or bonus) draw at each request's end node, after decide.
-cudaError_t launch_correction(const Problem& pb, cudaStream_t st);
+// Per request: the decision, then the correction (or bonus) draw at its end
+// node (sdv_sample.cu).
+cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st);
 int sample_threads();
 
 // The node kernel's launch shape: persistent CTAs per SM, threads per CTA

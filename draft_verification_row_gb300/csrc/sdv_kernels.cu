@@ -5,9 +5,7 @@
 //                 draft-trie owners, the depth-major list of trie nodes the
 //                 node kernel works through.
 // argmax_kernel   greedy: one CTA per node, streaming argmax of the target.
-// decide_kernel   one warp per request: the token-level walk, the
-//                 depth-first block search or greedy matching over the
-//                 node records; writes the outputs.
+// (The decision and the correction draw are in sdv_sample.cu.)
 //
 // The rules (SpecTr-GBV: Multi-Draft Block Verification Accelerating
 // Speculative Decoding, sections 1 and 2) are stated in include/sdv.h.
@@ -149,167 +147,6 @@ __global__ void __launch_bounds__(256) argmax_kernel(Problem pb)
     }
 }
 
-// ------------------------------------------------------------------------
-// decision: one warp per request; the request's node records are copied to
-// shared memory first, then lane 0 walks them
-
-constexpr int kDecideWarps = 4;
-constexpr int kSlotsMax = (SDV_MAX_L + 1) * SDV_MAX_K;
-
-__global__ void __launch_bounds__(32 * kDecideWarps) decide_kernel(Problem pb, int greedy)
-{
-    __shared__ unsigned char s_own[kDecideWarps][kSlotsMax];
-    __shared__ float s_val[kDecideWarps][kSlotsMax];  // a (token), h (block) or argmax bits (greedy)
-    __shared__ float s_u[kDecideWarps][SDV_MAX_K * SDV_MAX_L];
-    __shared__ int s_tok[kDecideWarps][SDV_MAX_K * SDV_MAX_L];
-    __shared__ signed char s_sib[kDecideWarps][kSlotsMax];  // next sibling's draft, or -1
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int b = blockIdx.x * kDecideWarps + w;
-    if (b >= pb.B) return;
-    const int K = pb.K, L = pb.L;
-    const int st = pb.ws.req[b];
-    float* ap = pb.accept_prob ? pb.accept_prob + (size_t)b * K * L : nullptr;
-    if (st) {
-        if (ap)
-            for (int i = lane; i < K * L; i += 32) ap[i] = 0.f;
-        if (lane == 0) {
-            pb.accept_len[b] = 0;
-            pb.accept_draft[b] = 0;
-            pb.out_token[b] = -1;
-            pb.ws.endn[b] = -1;  // no correction draw
-            if (pb.residual_mass) pb.residual_mass[b] = 0.f;
-            if (pb.device_status) atomicOr(pb.device_status, st);
-        }
-        return;
-    }
-    const int Lb = pb.lengths ? pb.lengths[b] : L;
-    const size_t s0 = (size_t)b * (L + 1) * K;
-    const bool token = pb.mode == SDV_MODE_TOKEN;
-    unsigned char* own = s_own[w];
-    float* val = s_val[w];
-    float* uu = s_u[w];
-    int* tk = s_tok[w];
-    for (int i = lane; i < (Lb + 1) * K; i += 32) {
-        own[i] = pb.ws.owner[s0 + i];
-        float v;
-        if (greedy)
-            v = __int_as_float(pb.ws.am[s0 + i]);
-        else if (token)
-            v = pb.ws.a[s0 + i];
-        else  // a leaf's block acceptance is its weight p (the node kernel only checks leaves)
-            v = i >= Lb * K ? (Lb == 0 ? 1.f : 1.f - pb.ws.pbar[s0 + i]) : pb.ws.h[s0 + i];
-        val[i] = v;
-    }
-    for (int i = lane; i < K * L; i += 32) {
-        tk[i] = pb.tokens[(size_t)b * K * L + i];
-        uu[i] = greedy ? 0.f : pb.accept_u[(size_t)b * K * L + i];
-    }
-    __syncwarp();
-    // accept_prob[k][d]: the threshold draft k's position d is tested against
-    if (ap) {
-        for (int i = lane; i < K * L; i += 32) {
-            const int kk = i / L, d = i % L;
-            float v = 0.f;
-            if (d < Lb) {
-                if (greedy)
-                    v = tk[i] == __float_as_int(val[d * K + own[d * K + kk]]) ? 1.f : 0.f;
-                else if (token)
-                    v = val[d * K + kk];
-                else
-                    v = val[(d + 1) * K + own[(d + 1) * K + kk]];
-            }
-            ap[i] = v;
-        }
-    }
-    int ej = 0, eo = 0;
-    if (greedy) {
-        if (lane != 0) return;
-        int best = -1, bestk = 0;
-        for (int kk = 0; kk < K; ++kk) {
-            int m = 0;
-            while (m < Lb && tk[kk * L + m] == __float_as_int(val[m * K + own[m * K + kk]])) ++m;
-            if (m > best) {
-                best = m;
-                bestk = kk;
-            }
-        }
-        ej = best;
-        eo = own[best * K + bestk];
-        pb.accept_len[b] = best;
-        pb.accept_draft[b] = bestk;
-        pb.out_token[b] = __float_as_int(val[ej * K + eo]);
-        if (pb.residual_mass) pb.residual_mass[b] = 1.f;
-        return;
-    }
-    if (token) {
-        if (lane != 0) return;
-        int j = 0, o = 0;
-        while (j < Lb) {
-            int acc = -1;
-            for (int kk = 0; kk < K && acc < 0; ++kk)
-                if (own[j * K + kk] == o && uu[kk * L + j] <= val[j * K + kk]) acc = kk;
-            if (acc < 0) break;
-            o = own[(j + 1) * K + acc];
-            ++j;
-        }
-        ej = j;
-        eo = o;
-    } else {
-        // Depth first, children in order of first appearance, each node
-        // tested after its subtree: the end node is the first accepted
-        // node in that post-order (the root always accepts).  A node
-        // (j, o) is owned by draft o; its first child is (j + 1, o), its
-        // parent (j - 1, own[j - 1][o]), and its next sibling the lowest
-        // later draft through the parent that owns a node at depth j.
-        signed char* sib = s_sib[w];
-        for (int i = lane + K; i < (Lb + 1) * K; i += 32) {  // depths 1..Lb (owned nodes only)
-            const int j = i / K, k = i % K;
-            int nx = -1;
-            if (own[i] == k) {
-                const int par = own[(j - 1) * K + k];
-                for (int k3 = k + 1; k3 < K; ++k3)
-                    if (own[(j - 1) * K + k3] == par && own[j * K + k3] == k3) {
-                        nx = k3;
-                        break;
-                    }
-            }
-            sib[i] = (signed char)nx;
-        }
-        __syncwarp();
-        if (lane != 0) return;
-        int jj = Lb, o = 0;  // the leftmost deepest node
-        for (;;) {
-            if (jj == 0) {
-                ej = 0;
-                eo = 0;
-                break;
-            }
-            if (uu[o * L + jj - 1] <= val[jj * K + o]) {
-                ej = jj;
-                eo = o;
-                break;
-            }
-            const int nx = sib[jj * K + o];
-            if (nx >= 0) {
-                o = nx;   // the next sibling's subtree, from its leftmost deepest node
-                jj = Lb;  // (a draft's own nodes run down to depth Lb)
-            } else {
-                o = own[(jj - 1) * K + o];  // the parent
-                --jj;
-            }
-        }
-    }
-    // the correction (or bonus) token is drawn at the end node afterwards;
-    // a leaf's residual is p P (mass p; p = 1 in the token rule)
-    const size_t se = s0 + (size_t)ej * K + eo;
-    const bool leaf = ej == Lb;
-    pb.accept_len[b] = ej;
-    pb.accept_draft[b] = eo;
-    pb.ws.endn[b] = (int)(se | (leaf ? (1u << 30) : 0u));
-    if (pb.residual_mass)
-        pb.residual_mass[b] = leaf ? (token || Lb == 0 ? 1.f : 1.f - pb.ws.pbar[se]) : pb.ws.S[se];
-}
-
 }  // namespace
 
 // ------------------------------------------------------------------------
@@ -330,12 +167,6 @@ cudaError_t launch_argmax(const Problem& pb, cudaStream_t st)
         argmax_kernel<SDV_BF16><<<(unsigned)n, 256, 0, st>>>(pb);
     else
         argmax_kernel<SDV_F32><<<(unsigned)n, 256, 0, st>>>(pb);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_decide(const Problem& pb, bool greedy, cudaStream_t st)
-{
-    decide_kernel<<<(pb.B + kDecideWarps - 1) / kDecideWarps, 32 * kDecideWarps, 0, st>>>(pb, greedy ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -15,7 +15,8 @@
 // rule states.  T = 0 gives the argmax, lowest index on ties.
 //
 // The same machinery draws verification's correction (or bonus) token, once
-// per request, at the end node the decision chose: from the node's final
+// per request (finish_kernel, after the request's decision), at the end
+// node the decision chose: from the node's final
 // residual R_n = aT max(e_T - (aD / aT) e_D, 0) with R_n(x*) apart (kept by
 // the node kernel), or from P at a leaf or where S_n = 0 ("SpecTr-GBV"
 // page, section 2, step 4: the correction comes from the adjusted
@@ -366,27 +367,192 @@ __global__ void __launch_bounds__(kRT, 2) sample_rows_kernel(SampleArgs a)
     }
 }
 
-// The correction (or bonus) token of request blockIdx.x, at the end node
-// the decision chose: from the node's final residual R_n (kept by the node
-// kernel), or from P at a leaf or where S_n = 0.
+// ------------------------------------------------------------------------
+// decision: one warp per request; the request's node records are copied to
+// shared memory first, then lane 0 walks them
+
+constexpr int kSlotsMax = (SDV_MAX_L + 1) * SDV_MAX_K;
+
+struct DecideSmem {
+    unsigned char own[kSlotsMax];
+    float val[kSlotsMax];  // a (token), h (block) or argmax bits (greedy)
+    float u[SDV_MAX_K * SDV_MAX_L];
+    int tok[SDV_MAX_K * SDV_MAX_L];
+    signed char sib[kSlotsMax];  // next sibling's draft, or -1
+    int endn;                    // the end node: slot | leaf << 30, or -1 (no draw)
+};
+
+// Decide request b (one warp): accept_len, accept_draft, accept_prob,
+// residual_mass, the status; the greedy token; s.endn for the draw.
+__device__ void decide_request(const Problem& pb, int b, bool greedy, DecideSmem& s, int lane)
+{
+    const int K = pb.K, L = pb.L;
+    if (lane == 0) s.endn = -1;
+    const int st = pb.ws.req[b];
+    float* ap = pb.accept_prob ? pb.accept_prob + (size_t)b * K * L : nullptr;
+    if (st) {
+        if (ap)
+            for (int i = lane; i < K * L; i += 32) ap[i] = 0.f;
+        if (lane == 0) {
+            pb.accept_len[b] = 0;
+            pb.accept_draft[b] = 0;
+            pb.out_token[b] = -1;
+            if (pb.residual_mass) pb.residual_mass[b] = 0.f;
+            if (pb.device_status) atomicOr(pb.device_status, st);
+        }
+        return;
+    }
+    const int Lb = pb.lengths ? pb.lengths[b] : L;
+    const size_t s0 = (size_t)b * (L + 1) * K;
+    const bool token = pb.mode == SDV_MODE_TOKEN;
+    unsigned char* own = s.own;
+    float* val = s.val;
+    float* uu = s.u;
+    int* tk = s.tok;
+    for (int i = lane; i < (Lb + 1) * K; i += 32) {
+        own[i] = pb.ws.owner[s0 + i];
+        float v;
+        if (greedy)
+            v = __int_as_float(pb.ws.am[s0 + i]);
+        else if (token)
+            v = pb.ws.a[s0 + i];
+        else  // a leaf's block acceptance is its weight p (the node kernel only checks leaves)
+            v = i >= Lb * K ? (Lb == 0 ? 1.f : 1.f - pb.ws.pbar[s0 + i]) : pb.ws.h[s0 + i];
+        val[i] = v;
+    }
+    for (int i = lane; i < K * L; i += 32) {
+        tk[i] = pb.tokens[(size_t)b * K * L + i];
+        uu[i] = greedy ? 0.f : pb.accept_u[(size_t)b * K * L + i];
+    }
+    __syncwarp();
+    // accept_prob[k][d]: the threshold draft k's position d is tested against
+    if (ap) {
+        for (int i = lane; i < K * L; i += 32) {
+            const int kk = i / L, d = i % L;
+            float v = 0.f;
+            if (d < Lb) {
+                if (greedy)
+                    v = tk[i] == __float_as_int(val[d * K + own[d * K + kk]]) ? 1.f : 0.f;
+                else if (token)
+                    v = val[d * K + kk];
+                else
+                    v = val[(d + 1) * K + own[(d + 1) * K + kk]];
+            }
+            ap[i] = v;
+        }
+    }
+    int ej = 0, eo = 0;
+    if (greedy) {
+        if (lane != 0) return;
+        int best = -1, bestk = 0;
+        for (int kk = 0; kk < K; ++kk) {
+            int m = 0;
+            while (m < Lb && tk[kk * L + m] == __float_as_int(val[m * K + own[m * K + kk]])) ++m;
+            if (m > best) {
+                best = m;
+                bestk = kk;
+            }
+        }
+        ej = best;
+        eo = own[best * K + bestk];
+        pb.accept_len[b] = best;
+        pb.accept_draft[b] = bestk;
+        pb.out_token[b] = __float_as_int(val[ej * K + eo]);
+        if (pb.residual_mass) pb.residual_mass[b] = 1.f;
+        return;
+    }
+    if (token) {
+        if (lane != 0) return;
+        int j = 0, o = 0;
+        while (j < Lb) {
+            int acc = -1;
+            for (int kk = 0; kk < K && acc < 0; ++kk)
+                if (own[j * K + kk] == o && uu[kk * L + j] <= val[j * K + kk]) acc = kk;
+            if (acc < 0) break;
+            o = own[(j + 1) * K + acc];
+            ++j;
+        }
+        ej = j;
+        eo = o;
+    } else {
+        // Depth first, children in order of first appearance, each node
+        // tested after its subtree: the end node is the first accepted
+        // node in that post-order (the root always accepts).  A node
+        // (j, o) is owned by draft o; its first child is (j + 1, o), its
+        // parent (j - 1, own[j - 1][o]), and its next sibling the lowest
+        // later draft through the parent that owns a node at depth j.
+        signed char* sib = s.sib;
+        for (int i = lane + K; i < (Lb + 1) * K; i += 32) {  // depths 1..Lb (owned nodes only)
+            const int j = i / K, k = i % K;
+            int nx = -1;
+            if (own[i] == k) {
+                const int par = own[(j - 1) * K + k];
+                for (int k3 = k + 1; k3 < K; ++k3)
+                    if (own[(j - 1) * K + k3] == par && own[j * K + k3] == k3) {
+                        nx = k3;
+                        break;
+                    }
+            }
+            sib[i] = (signed char)nx;
+        }
+        __syncwarp();
+        if (lane != 0) return;
+        int jj = Lb, o = 0;  // the leftmost deepest node
+        for (;;) {
+            if (jj == 0) {
+                ej = 0;
+                eo = 0;
+                break;
+            }
+            if (uu[o * L + jj - 1] <= val[jj * K + o]) {
+                ej = jj;
+                eo = o;
+                break;
+            }
+            const int nx = sib[jj * K + o];
+            if (nx >= 0) {
+                o = nx;   // the next sibling's subtree, from its leftmost deepest node
+                jj = Lb;  // (a draft's own nodes run down to depth Lb)
+            } else {
+                o = own[(jj - 1) * K + o];  // the parent
+                --jj;
+            }
+        }
+    }
+    // the correction (or bonus) token is drawn at the end node afterwards;
+    // a leaf's residual is p P (mass p; p = 1 in the token rule)
+    const size_t se = s0 + (size_t)ej * K + eo;
+    const bool leaf = ej == Lb;
+    pb.accept_len[b] = ej;
+    pb.accept_draft[b] = eo;
+    s.endn = (int)(se | (leaf ? (1u << 30) : 0u));
+    if (pb.residual_mass)
+        pb.residual_mass[b] = leaf ? (token || Lb == 0 ? 1.f : 1.f - pb.ws.pbar[se]) : pb.ws.S[se];
+}
+
+// One CTA per request: the decision (warp 0), then the correction (or
+// bonus) token at the end node it chose: from the node's final residual R_n
+// (kept by the node kernel), or from P at a leaf or where S_n = 0.
 template <int DT>
-__global__ void __launch_bounds__(kRT, 2) correction_kernel(Problem pb)
+__global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy)
 {
     using E = Elem<DT>;
     constexpr int EPU = E::kPerUnit;
     __shared__ RowSmem sm;
+    __shared__ DecideSmem ds;
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int e = pb.ws.endn[b];
-    if (e < 0) return;  // invalid request: decide wrote its outputs
+    if (w == 0) decide_request(pb, b, greedy != 0, ds, lane);
+    if (tid == 0) sm.bad = 0;
+    __syncthreads();
+    const int e = ds.endn;
+    if (e < 0) return;  // greedy, or an invalid request: the decision wrote the outputs
     const int K = pb.K, L = pb.L, V = pb.V;
     const size_t slot = (size_t)(e & ((1 << 30) - 1));
     const bool leaf = (e >> 30) != 0;
     const int k = (int)(slot % K), j = (int)((slot / K) % (L + 1));
     const float u = pb.sample_u[((size_t)b * K + k) * (L + 1) + j];
     const int n_seg = ((V + EPU - 1) / EPU + kRSeg - 1) / kRSeg;
-    if (tid == 0) sm.bad = 0;
-    __syncthreads();
     Dist d;
     d.rowT = static_cast<const char*>(pb.target) + (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
     d.rowD = leaf ? nullptr
@@ -425,13 +591,13 @@ __global__ void __launch_bounds__(kRT, 2) correction_kernel(Problem pb)
 
 int sample_threads() { return kRT; }
 
-cudaError_t launch_correction(const Problem& pb, cudaStream_t st)
+cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st)
 {
     if (pb.B == 0) return cudaSuccess;
     if (pb.dtype == SDV_BF16)
-        correction_kernel<SDV_BF16><<<pb.B, kRT, 0, st>>>(pb);
+        finish_kernel<SDV_BF16><<<pb.B, kRT, 0, st>>>(pb, greedy ? 1 : 0);
     else
-        correction_kernel<SDV_F32><<<pb.B, kRT, 0, st>>>(pb);
+        finish_kernel<SDV_F32><<<pb.B, kRT, 0, st>>>(pb, greedy ? 1 : 0);
     return cudaGetLastError();
 }
 
