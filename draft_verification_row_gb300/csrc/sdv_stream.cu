@@ -388,16 +388,18 @@ __device__ __forceinline__ float res_unscaled(float eT, float eD, float r) { ret
 
 // One residual sweep over a node's rows (from the ring): returns this
 // thread's share of S_j = sum over x != x* of max(aT e_T(x) - aD e_D(x), 0).
+// `back`: the chunks come last to first (the copy warp's order).
 template <int DT>
 __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_out, int nc, int n_units, int V,
                                        float c, float gnegT, float gnegD, float aT, float r, int xs, int cw,
-                                       int lane)
+                                       int lane, bool back)
 {
     constexpr int EPU = Elem<DT>::kPerUnit;
     const int xs_ch = xs >= 0 ? xs / EPU / kChunk : -1;  // x* is carried apart: its chunk skips it
     float tot = 0.f;
 #pragma unroll 1
-    for (int ch = 0; ch < nc; ++ch, ++g) {
+    for (int it = 0; it < nc; ++it, ++g) {
+        const int ch = back ? nc - 1 - it : it;
         const int s = g % kStages;
         if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
         const bool tail = ch == nc - 1;
@@ -666,7 +668,12 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 const bool with_d = !leaf;
                 // keep the rows in L2 until the node's last pass over them
                 const uint64_t pol = ps == passes - 1 ? pol_first : pol_last;
-                for (int ch = 0; ch < nc; ++ch, ++g) {
+                // passes alternate direction (pass 1 forward, the first
+                // sweep backward, ...): each pass starts on the chunks the
+                // one before just brought into L2
+                const bool back = (ps & 1) != 0;
+                for (int i = 0; i < nc; ++i, ++g) {
+                    const int ch = back ? nc - 1 - i : i;
                     const int s = g % kStages;
                     const uint32_t use = g / kStages;
                     if (use > 0 && !mbar_wait_bounded(&sm->empty[s], (use - 1) & 1)) {
@@ -829,7 +836,9 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                     sm->rD = sm->aT > 0.f ? sm->aD / sm->aT : 3.402823466e38f;
                 }
                 cbar_sync();
-                float tot = sweep<DT>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, sm->aT, sm->rD, xs, cw, lane);
+                // sweep di is pass di + 1 of the node: backward for even di
+                float tot = sweep<DT>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, sm->aT, sm->rD, xs, cw, lane,
+                                      (di & 1) == 0);
                 tot = warp_sum(tot);
                 if (lane == 0) sm->redf[2][cw] = tot;
                 cbar_sync();
