@@ -102,6 +102,12 @@ def sum_over_ranks(x, world):
     return float(t.item())
 
 
+def rank_seed(name, rank):
+    """Seed of rank `rank`'s batch: every rank verifies its own requests."""
+    from draft_verification_row_gb300 import workloads as W
+    return W.WORKLOADS[name]["seed"] + 7919 * rank
+
+
 def trie_rows(tokens, lengths, K):
     """(target rows, draft rows) the method reads: one per distinct draft
     prefix (node) of each request; leaves (depth L_b) read no draft row."""
@@ -287,7 +293,7 @@ def run_ours(args, world, rank, local):
 
     dev = torch.device(f"cuda:{local}")
     name = args.workload or W.HEADLINE
-    seed = W.WORKLOADS[name]["seed"] + 7919 * rank
+    seed = rank_seed(name, rank)
     batch = W.make(name, dev, seed=seed, B=args.B)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
