@@ -230,7 +230,12 @@ static void build_trie(req_t* r)
 }
 
 /* Request status: bad length, else bad token, else an unusable row among
- * the rows the method reads (trie nodes only). */
+ * the rows every decision reads: each trie node's target and draft rows,
+ * except a leaf's target row in the sampling rules.  A leaf's P enters
+ * nothing but its bonus draw (its residual is p P, of mass p), so its row
+ * is read, and checked, only when the decision ends at that leaf
+ * (draw_correction), just as rows past L_b are never read.  Greedy
+ * matching takes every node's argmax, leaves included. */
 static int request_status(req_t* r)
 {
     const sdvo_problem* pb = r->pb;
@@ -244,7 +249,8 @@ static int request_status(req_t* r)
     for (int j = 0; j <= r->Lb; ++j)
         for (int o = 0; o < pb->K; ++o) {
             if (r->owner[j][o] != o) continue;
-            if (!row_usable(pb, row_of(pb, 1, r->b, o, j))) st = SDVO_REQ_NONFINITE;
+            if ((r->greedy || j < r->Lb) && !row_usable(pb, row_of(pb, 1, r->b, o, j)))
+                st = SDVO_REQ_NONFINITE;
             if (!r->greedy && j < r->Lb && !row_usable(pb, row_of(pb, 0, r->b, o, j)))
                 st = SDVO_REQ_NONFINITE;
         }
@@ -254,12 +260,18 @@ static int request_status(req_t* r)
 /* ------------------------------------------------------------------------ */
 /* node evaluation: residual recursion of SpecTr-GBV at node (j, o) with
  * weight p (p = 1 gives recursive rejection sampling).  Leaves R_n in r->R,
- * P_v in r->P; stores a, h and S.  Returns S_n. */
+ * P_v in r->P; stores a, h and S.  Returns S_n.  A leaf has no draws:
+ * S = h = p, and its row is not read here. */
 static double eval_node(req_t* r, int j, int o, double p)
 {
     const sdvo_problem* pb = r->pb;
     int V = pb->V;
     double S = 0.0, D = 1.0;
+    if (j == r->Lb) {
+        r->S[j][o] = p;
+        r->h[j][o] = p;
+        return p;
+    }
     softmax(pb, row_of(pb, 1, r->b, o, j), pb->temperature, r->P);
     for (int x = 0; x < V; ++x) r->R[x] = p * r->P[x];
     for (int x = 0; x < V; ++x) S += r->R[x];
@@ -318,13 +330,26 @@ typedef struct {
 } outcome_t;
 
 /* Draw the correction from the end node's residual (R_n / S_n), or from
- * P_v when S_n = 0. */
-static void draw_correction(req_t* r, int ej, int eo, double p, outcome_t* out, double* residual_out)
+ * P_v when S_n = 0 or at a leaf (the bonus token; R = p P there).  Returns
+ * SDVO_REQ_NONFINITE, drawing nothing, when the end node is a leaf whose
+ * target row is unusable; else 0. */
+static int draw_correction(req_t* r, int ej, int eo, double p, outcome_t* out, double* residual_out)
 {
-    int V = r->pb->V;
-    double S = eval_node(r, ej, eo, p);
-    const double* w = S > 0.0 ? r->R : r->P;
+    const sdvo_problem* pb = r->pb;
+    int V = pb->V;
+    double S;
+    const double* w;
     double tot = 0.0;
+    if (ej == r->Lb) {
+        const unsigned char* row = row_of(pb, 1, r->b, eo, ej);
+        if (!row_usable(pb, row)) return SDVO_REQ_NONFINITE;
+        softmax(pb, row, pb->temperature, r->P);
+        S = p;
+        w = r->P;
+    } else {
+        S = eval_node(r, ej, eo, p);
+        w = S > 0.0 ? r->R : r->P;
+    }
     out->tau = ej;
     out->kstar = eo;
     out->mass = S;
@@ -333,11 +358,12 @@ static void draw_correction(req_t* r, int ej, int eo, double p, outcome_t* out, 
         for (int x = 0; x < V; ++x) tot += w[x];
         for (int x = 0; x < V; ++x) residual_out[x] = w[x] / tot;
     }
+    return 0;
 }
 
 /* Token-level speculative sampling (K = 1) and its per-position
  * multi-draft form (K > 1): every node at p = 1, then the walk. */
-static void run_token(req_t* r, float* accept_prob, outcome_t* out, double* residual_out)
+static int run_token(req_t* r, float* accept_prob, outcome_t* out, double* residual_out)
 {
     const sdvo_problem* pb = r->pb;
     int j = 0, o = 0;
@@ -355,12 +381,12 @@ static void run_token(req_t* r, float* accept_prob, outcome_t* out, double* resi
         o = r->owner[j + 1][acc];
         ++j;
     }
-    draw_correction(r, j, o, 1.0, out, residual_out);
+    return draw_correction(r, j, o, 1.0, out, residual_out);
 }
 
 /* SpecTr-GBV: nodes in breadth-first order (a node's weight comes from its
  * parent), then the depth-first decision. */
-static void run_multidraft(req_t* r, float* accept_prob, outcome_t* out, double* residual_out)
+static int run_multidraft(req_t* r, float* accept_prob, outcome_t* out, double* residual_out)
 {
     const sdvo_problem* pb = r->pb;
     int ej = 0, eo = 0;
@@ -374,11 +400,11 @@ static void run_multidraft(req_t* r, float* accept_prob, outcome_t* out, double*
                 accept_prob[k * pb->L + d] = (float)r->h[d + 1][v];
             }
     dfs_accept(r, 0, 0, &ej, &eo);
-    draw_correction(r, ej, eo, node_weight(r, ej, eo), out, residual_out);
+    return draw_correction(r, ej, eo, node_weight(r, ej, eo), out, residual_out);
 }
 
 /* Greedy block verification, single draft, written from its own steps. */
-static void run_block(req_t* r, float* accept_prob, outcome_t* out, double* residual_out)
+static int run_block(req_t* r, float* accept_prob, outcome_t* out, double* residual_out)
 {
     const sdvo_problem* pb = r->pb;
     int V = pb->V, Lb = r->Lb, tau = 0;
@@ -407,7 +433,9 @@ static void run_block(req_t* r, float* accept_prob, outcome_t* out, double* resi
             tau = i;
             break;
         }
-    /* correction: P_L when tau = L, else norm(max(p_tau P_tau - Q_tau, 0)) */
+    /* correction: P_L when tau = L, else norm(max(p_tau P_tau - Q_tau, 0));
+     * target row L_b is read only here */
+    if (tau == Lb && !row_usable(pb, row_of(pb, 1, r->b, 0, tau))) return SDVO_REQ_NONFINITE;
     softmax(pb, row_of(pb, 1, r->b, 0, tau), pb->temperature, r->P);
     if (tau < Lb) {
         softmax(pb, row_of(pb, 0, r->b, 0, tau), pb->temperature, r->Q);
@@ -426,6 +454,7 @@ static void run_block(req_t* r, float* accept_prob, outcome_t* out, double* resi
         for (int x = 0; x < V; ++x) tot += w[x];
         for (int x = 0; x < V; ++x) residual_out[x] = w[x] / tot;
     }
+    return 0;
 }
 
 /* Greedy T = 0: a draft position matches when its token is the row's
@@ -505,12 +534,17 @@ int sdvo_verify(int mode, const sdvo_problem* pb, int* accept_len, int* accept_d
         st = request_status(&r);
         if (st == 0) {
             if (greedy) run_greedy(&r, ap, &out, ro);
-            else if (mode == SDVO_MODE_TOKEN) run_token(&r, ap, &out, ro);
-            else if (mode == SDVO_MODE_BLOCK) run_block(&r, ap, &out, ro);
-            else run_multidraft(&r, ap, &out, ro);
-        } else if (ap) {
-            memset(ap, 0, sizeof(float) * (size_t)pb->K * pb->L);
+            else if (mode == SDVO_MODE_TOKEN) st = run_token(&r, ap, &out, ro);
+            else if (mode == SDVO_MODE_BLOCK) st = run_block(&r, ap, &out, ro);
+            else st = run_multidraft(&r, ap, &out, ro);
+            if (st) { /* the decision ended at a leaf with an unusable row */
+                out.tau = out.kstar = 0;
+                out.token = -1;
+                out.mass = 0.0;
+                if (ro) memset(ro, 0, sizeof(double) * (size_t)pb->V);
+            }
         }
+        if (st && ap) memset(ap, 0, sizeof(float) * (size_t)pb->K * pb->L);
         accept_len[b] = out.tau;
         accept_draft[b] = out.kstar;
         out_token[b] = out.token;

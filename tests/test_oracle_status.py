@@ -140,3 +140,70 @@ def test_bf16_is_decoded_exactly():
                                                    d["lengths"], d["accept_u"], d["sample_u"], 1.0))
     for key in ("accept_len", "accept_draft", "out_token", "accept_prob", "residual_mass"):
         np.testing.assert_array_equal(f[key], b[key])
+
+
+def _leaves(d, b):
+    """Drafts owning a leaf of request b (no lower draft has its first L_b tokens)."""
+    Lb = int(d["lengths"][b])
+    tok = d["tokens"][b, :, :Lb]
+    return [k for k in range(tok.shape[0]) if not any((tok[k2] == tok[k]).all() for k2 in range(k))]
+
+
+@pytest.mark.parametrize("mode,K", [("token", 2), ("multidraft", 2), ("block", 1)])
+def test_leaf_row_is_read_only_by_its_bonus_draw(mode, K):
+    """A leaf's target row enters only the bonus draw when the decision ends
+    there (its residual is p P, of mass p, whatever P is).  With accept_u = 0
+    every test passes: the decision ends at draft 0's leaf.  Poisoning the
+    other leaves changes nothing; poisoning that one invalidates the request
+    alone."""
+    d = _problem(K=K)
+    d["accept_u"][:] = 0.0
+    base = _run(mode, d)
+    assert (base["req_status"] == 0).all()
+    np.testing.assert_array_equal(base["accept_len"], d["lengths"])
+    np.testing.assert_array_equal(base["accept_draft"], 0)
+    for b in range(3):
+        for k in _leaves(d, b)[1:]:
+            d["target"][b, k, d["lengths"][b], 1] = np.nan
+    o = _run(mode, d)
+    assert (o["req_status"] == 0).all()
+    for key in ("accept_len", "accept_draft", "out_token", "accept_prob", "residual_mass"):
+        np.testing.assert_array_equal(o[key], base[key])
+    d["target"][2, 0, d["lengths"][2], 4] = np.inf
+    o = _run(mode, d)
+    assert o["req_status"].tolist() == [0, 0, oracle.REQ_NONFINITE]
+    assert o["accept_len"][2] == 0 and o["accept_draft"][2] == 0 and o["out_token"][2] == -1
+    assert o["residual_mass"][2] == 0.0 and (o["accept_prob"][2] == 0).all()
+    for key in ("accept_len", "out_token", "accept_prob"):
+        np.testing.assert_array_equal(o[key][:2], base[key][:2])
+
+
+@pytest.mark.parametrize("mode,K", [("token", 2), ("multidraft", 2), ("block", 1)])
+def test_leaf_rows_are_unread_when_a_draft_position_is_rejected(mode, K):
+    """With accept_u near 1 almost every test fails; a request that stops
+    short of its length never reads a leaf row."""
+    d = _problem(K=K, seed=4)
+    d["accept_u"][:] = 0.999
+    base = _run(mode, d)
+    short = [b for b in range(3) if base["accept_len"][b] < d["lengths"][b]]
+    assert short, "the fixture should stop short somewhere"
+    for b in short:
+        for k in range(K):
+            d["target"][b, k, d["lengths"][b]] = np.nan
+    o = _run(mode, d)
+    assert (o["req_status"] == 0).all()
+    for key in ("accept_len", "accept_draft", "out_token", "accept_prob", "residual_mass"):
+        np.testing.assert_array_equal(o[key], base[key])
+
+
+def test_greedy_reads_every_leaf_row():
+    """Greedy matching takes each node's argmax, a leaf's included."""
+    d = _problem()
+    for b in range(3):
+        e = _problem()
+        leaves = _leaves(e, b)
+        e["target"][b, leaves[-1], e["lengths"][b], 0] = np.nan
+        o = _run("greedy", e)
+        assert o["req_status"][b] == oracle.REQ_NONFINITE
+        assert o["out_token"][b] == -1
+    assert (_run("greedy", d)["req_status"] == 0).all()
