@@ -108,20 +108,23 @@ def rank_seed(name, rank):
     return W.WORKLOADS[name]["seed"] + 7919 * rank
 
 
-def trie_rows(tokens, lengths, K):
-    """(target rows, draft rows) the method reads: one per distinct draft
-    prefix (node) of each request; leaves (depth L_b) read no draft row."""
+def trie_nodes(tokens, lengths, K):
+    """(inner nodes, leaves) of the requests' draft tries: one node per
+    distinct draft prefix, leaves at depth L_b.  The node kernel reads an
+    inner node's target and draft rows; a leaf's target row is read only by
+    its bonus draw, when the decision ends there."""
     tok = tokens.cpu().numpy()
     lens = lengths.cpu().numpy()
-    nt = nd = 0
+    inner = leaves = 0
     for b in range(tok.shape[0]):
         Lb = int(lens[b])
         for j in range(Lb + 1):
             n = len({tuple(tok[b, k, :j]) for k in range(K)})
-            nt += n
             if j < Lb:
-                nd += n
-    return nt, nd
+                inner += n
+            else:
+                leaves += n
+    return inner, leaves
 
 
 def measured_peaks():
@@ -298,8 +301,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
     esz = 2 if batch.dtype == "bf16" else 4
-    nt, nd = trie_rows(batch.tokens, batch.lengths, batch.K)
-    alg_bytes = (nt + nd) * batch.V * esz
+    inner, leaves = trie_nodes(batch.tokens, batch.lengths, batch.K)
+    alg_bytes = 2 * inner * batch.V * esz  # the node kernel: both rows of every inner node
     positions = batch.positions
 
     def make_call(mode, out):
@@ -342,7 +345,9 @@ def run_ours(args, world, rank, local):
                          "traffic": traffic, "kernel": "stream_kernel",
                          "algorithmic_bytes_per_step": alg_bytes,
                          "kernel_ms_per_step": row_ms / args.steps,
-                         "rows_read_per_step": {"target": nt, "draft": nd}},
+                         "rows_read_per_step": {"target": inner, "draft": inner},
+                         "leaves": leaves,
+                         "bonus_leaf_rows_per_step": int((out.accept_len == batch.lengths).sum().item())},
             "gpu_launches": launches,
             "clocks": clk}
 

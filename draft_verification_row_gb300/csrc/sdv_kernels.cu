@@ -2,8 +2,8 @@
 // sdv_stream.cu).
 //
 // prep_kernel     one warp per request: length and token checks, the
-//                 draft-trie owners, the depth-major list of trie nodes the
-//                 node kernel works through.
+//                 draft-trie owners, the depth-major list of inner trie
+//                 nodes the node kernel works through.
 // argmax_kernel   greedy: one CTA per node, streaming argmax of the target.
 // (The decision and the correction draw are in sdv_sample.cu.)
 //
@@ -59,14 +59,16 @@ __global__ void prep_kernel(Problem pb)
         if (lane < K) own[j * K + lane] = (unsigned char)o;
     }
     if (lane == 0) pb.ws.pbar[(size_t)b * (L + 1) * K] = 0.f;  // root weight 1
-    // list the request's nodes by depth (for the streaming kernel) and clear
-    // the flags through which parents publish their children's weights
+    // list the request's inner nodes by depth (for the node kernel) and
+    // clear the flags through which parents publish their children's
+    // weights.  Leaves are not listed: a leaf has no draws, and its target
+    // row is read by the bonus draw alone, once the decision ends there.
     const size_t BK = (size_t)pb.B * K;
     for (int j = 0; j <= Lb; ++j) {
-        const bool node = lane < K && own[j * K + lane] == lane;
+        const bool node = j < Lb && lane < K && own[j * K + lane] == lane;
         const unsigned m = __ballot_sync(0xffffffffu, node);
         int base = 0;
-        if (lane == 0) base = atomicAdd(&pb.ws.ncount[j], __popc(m));
+        if (lane == 0 && m) base = atomicAdd(&pb.ws.ncount[j], __popc(m));
         base = __shfl_sync(0xffffffffu, base, 0);
         const size_t slot = ((size_t)b * (L + 1) + j) * K + lane;
         if (node) pb.ws.nodes[j * BK + base + __popc(m & ((1u << lane) - 1))] = (int)slot;

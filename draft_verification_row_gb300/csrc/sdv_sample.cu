@@ -416,7 +416,7 @@ __device__ void decide_request(const Problem& pb, int b, bool greedy, DecideSmem
             v = __int_as_float(pb.ws.am[s0 + i]);
         else if (token)
             v = pb.ws.a[s0 + i];
-        else  // a leaf's block acceptance is its weight p (the node kernel only checks leaves)
+        else  // a leaf's block acceptance is its weight p (the node kernel skips leaves)
             v = i >= Lb * K ? (Lb == 0 ? 1.f : 1.f - pb.ws.pbar[s0 + i]) : pb.ws.h[s0 + i];
         val[i] = v;
     }
@@ -530,6 +530,23 @@ __device__ void decide_request(const Problem& pb, int b, bool greedy, DecideSmem
         pb.residual_mass[b] = leaf ? (token || Lb == 0 ? 1.f : 1.f - pb.ws.pbar[se]) : pb.ws.S[se];
 }
 
+// A request found invalid after its decision (one warp): the outputs an
+// invalid request gets, and its status bit.
+__device__ __noinline__ void invalidate_request(const Problem& pb, int b, int lane)
+{
+    const int n = pb.K * pb.L;
+    if (pb.accept_prob)
+        for (int i = lane; i < n; i += 32) pb.accept_prob[(size_t)b * n + i] = 0.f;
+    if (lane == 0) {
+        pb.accept_len[b] = 0;
+        pb.accept_draft[b] = 0;
+        pb.out_token[b] = -1;
+        if (pb.residual_mass) pb.residual_mass[b] = 0.f;
+        atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
+        if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
+    }
+}
+
 // One CTA per request: the decision (warp 0), then the correction (or
 // bonus) token at the end node it chose: from the node's final residual R_n
 // (kept by the node kernel), or from P at a leaf or where S_n = 0.
@@ -574,8 +591,11 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy)
         softmax_pass<DT>(d.rowT, V, d.c, false, sm, lane, w);
         __syncthreads();
         float M;
-        if (!row_max(sm, n_seg, lane, M)) {  // checked before; kept for safety
-            if (tid == 0) pb.out_token[b] = -1;
+        if (!row_max(sm, n_seg, lane, M)) {
+            // an unusable row: only a leaf's can be (the node kernel checked
+            // every inner node's rows), and a leaf's row is read here alone,
+            // so the request is found invalid now: its outputs are replaced
+            if (w == 0) invalidate_request(pb, b, lane);
             return;
         }
         d.M = M;

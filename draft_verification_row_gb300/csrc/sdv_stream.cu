@@ -8,8 +8,10 @@
 //           that 1 - P of a dominant token stays exact;
 //   pass 2 (from L2, once per draw): the residual sweep
 //           S_j = sum_x max(p P(x) - C_j Q(x), 0), and, on the last sweep,
-//           the mass per (chunk, warp) for the inverse-CDF sample;
-//   leaf:   one target-only pass for the bonus sample.
+//           the mass per (chunk, warp) for the inverse-CDF sample.
+// Only inner nodes are visited: a leaf has no draws (its residual is p P,
+// of mass p), and its target row is read by the bonus draw alone, after
+// the decision and only if the decision ends there.
 // Warp 0 (metadata) takes nodes from the depth-major list the prep kernel
 // built and fills a descriptor queue: draws, their tokens and logits.
 // Warp 1 (copy) streams each node's rows in 12 KB-per-row chunks through a
@@ -87,7 +89,7 @@ __device__ __forceinline__ void st_release(int* p, int v)
 
 // What the metadata warp prepares for each node, ahead of its rows.
 struct NodeDesc {
-    int slot, b, j, k, leaf, nd;
+    int slot, b, j, k, nd;
     int dk[SDV_MAX_K];            // drafts of the draws, in index order
     int y[SDV_MAX_K];             // their tokens
     float gT[SDV_MAX_K], gD[SDV_MAX_K];  // target / draft logits at those tokens
@@ -109,7 +111,6 @@ struct StreamSmem {
     int uT, uD;
     float S, D, cbar, pbar, Pbs, Qbs, Rs, Ts, Rj, aT, aD, rD;
     int xs, bad;
-    int lbad, lfin;                  // leaf check: NaN or +Inf seen, a finite logit seen
 };
 
 // Online statistics of one row, per thread, in a reference shared by the
@@ -268,13 +269,13 @@ __device__ __forceinline__ void online_finish(Online& s, const uint4 (*stash)[kU
     }
 }
 
-// Pass 1 over one node's rows: OTHER is false for a leaf (target row only).
+// Pass 1 over one node's target and draft rows.
 // Both rows' exponentials sit in one branch-free block.  A chunk can reach
 // the reference only where one of its terms e = 2^(x c - m c) is at least
 // 1, so a lane whose chunk sum is below 1/2 holds no maximum: the chunk
 // maxima, the warp reduction and the reference moves run only when some
 // lane's sum is not (in practice a few chunks per row and warp).
-template <int DT, bool OTHER>
+template <int DT>
 __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, uint32_t& g, bool& timed_out,
                                       int nc, int n_units, int V, float c, int cw, int lane)
 {
@@ -294,19 +295,18 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
             t[i] = d[i] = make_uint4(0u, 0u, 0u, 0u);
             if (!tail || ug0 + i * 32 < n_units) {
                 t[i] = sm->ring[s][0][ul];
-                if (OTHER) d[i] = sm->ring[s][1][ul];
+                d[i] = sm->ring[s][1][ul];
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->empty[s]);  // the units are in registers now
         // nothing finite seen yet: set the reference first (the first chunk,
         // in practice)
-        if (!(sT.m > -INFINITY) || (OTHER && !(sD.m > -INFINITY))) {
+        if (!(sT.m > -INFINITY) || !(sD.m > -INFINITY)) {
             if (!(sT.m > -INFINITY)) online_rebase(sT, warp_max_redux(chunk_max<DT>(t, ug0, n_units, V, tail)), c);
-            if (OTHER && !(sD.m > -INFINITY))
-                online_rebase(sD, warp_max_redux(chunk_max<DT>(d, ug0, n_units, V, tail)), c);
+            if (!(sD.m > -INFINITY)) online_rebase(sD, warp_max_redux(chunk_max<DT>(d, ug0, n_units, V, tail)), c);
         }
-        const bool liveT = sT.m > -INFINITY, liveD = OTHER && sD.m > -INFINITY;
+        const bool liveT = sT.m > -INFINITY, liveD = sD.m > -INFINITY;
         // (a row with nothing finite yet sums against 0: never added)
         const float negT = liveT ? sT.neg : 0.f, negD = liveD ? sD.neg : 0.f;
         float zt = 0.f, zd = 0.f;
@@ -315,7 +315,7 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
             const int ug = ug0 + i * 32;
             if (!tail || ug < n_units) {
                 zt += unit_sum<DT>(t[i], ug * EPU, V, c, negT);
-                if (OTHER) zd += unit_sum<DT>(d[i], ug * EPU, V, c, negD);
+                zd += unit_sum<DT>(d[i], ug * EPU, V, c, negD);
             }
         }
         // a sum of 1/2 or more (or NaN) may hold the maximum
@@ -324,15 +324,15 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
             const float cmT = hotT ? chunk_max<DT>(t, ug0, n_units, V, tail) : -INFINITY;
             const float cmD = hotD ? chunk_max<DT>(d, ug0, n_units, V, tail) : -INFINITY;
             const float wmT = warp_max_redux(cmT);
-            const float wmD = OTHER ? warp_max_redux(cmD) : -INFINITY;
+            const float wmD = warp_max_redux(cmD);
             // a chunk that reaches the reference is not added here
             const bool spT = hotT && cmT >= sT.m, spD = hotD && cmD >= sD.m;
             if (liveT) sT.z += spT ? 0.f : zt;
             if (liveD) sD.z += spD ? 0.f : zd;
-            const bool ovT = set_aside(sT, spT, ch, stashT, t), ovD = OTHER && set_aside(sD, spD, ch, stashD, d);
+            const bool ovT = set_aside(sT, spT, ch, stashT, t), ovD = set_aside(sD, spD, ch, stashD, d);
             // the chunk's sums are in the old reference: move it now
             online_rebase(sT, wmT, c);
-            if (OTHER) online_rebase(sD, wmD, c);
+            online_rebase(sD, wmD, c);
             if (__any_sync(0xffffffffu, ovT || ovD)) {
                 // lanes with no room left: their units, exactly, against
                 // the moved reference (which is at least their maximum)
@@ -350,34 +350,6 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
             if (liveD) sD.z += zd;
         }
     }
-}
-
-// A leaf's target row is only checked (no NaN or +Inf, some finite logit):
-// its bonus token, if the decision ends there, is drawn after the decision.
-template <int DT>
-__device__ __forceinline__ void leaf_check(StreamSmem* sm, uint32_t& g, bool& timed_out, int nc, int n_units, int V,
-                                           int cw, int lane)
-{
-    constexpr int EPU = Elem<DT>::kPerUnit;
-    bool bad = false, fin = false;
-#pragma unroll 1
-    for (int ch = 0; ch < nc; ++ch, ++g) {
-        const int s = g % kStages;
-        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
-#pragma unroll
-        for (int i = 0; i < kUPT; ++i) {
-            const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
-            if (ug < n_units) {
-                const float um = unit_max_masked<DT>(sm->ring[s][0][ul], ug * EPU, V);
-                bad |= (um != um) || um == INFINITY;
-                fin |= um > -INFINITY;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->empty[s]);
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&sm->lbad, 1);
-    if (__any_sync(0xffffffffu, fin) && lane == 0) atomicOr(&sm->lfin, 1);
 }
 
 // The residual term of one token divided by aT = p / Z_T:
@@ -437,11 +409,10 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
 // threads call it; results in shared memory from consumer thread 0): row
 // maximum M, reference -(M c), Z_rest (the sum below M), the count n of
 // maxima, Z = n e(M) + Z_rest, and the index of a unique maximum.
-__device__ __forceinline__ void combine_rows(StreamSmem* sm, const Online& sT, const Online& sD, bool two, float c,
-                                             int ct)
+__device__ __forceinline__ void combine_rows(StreamSmem* sm, const Online& sT, const Online& sD, float c, int ct)
 {
     const int lane = ct & 31, w = ct >> 5;
-    float MT = warp_max_redux(sT.m), MD = two ? warp_max_redux(sD.m) : -INFINITY;
+    float MT = warp_max_redux(sT.m), MD = warp_max_redux(sD.m);
     if (lane == 0) {
         sm->redf[0][w] = MT;
         sm->redf[1][w] = MD;
@@ -456,7 +427,7 @@ __device__ __forceinline__ void combine_rows(StreamSmem* sm, const Online& sT, c
     const float gnegT = -(MT * c), gnegD = -(MD * c);
     // a thread whose reference is the row's adds its sums as they are;
     // another rescales them (its maxima are then ordinary elements)
-    float cT, cD = 0.f;
+    float cT, cD;
     int nT = 0, nD = 0;
     if (sT.m == MT) {
         cT = sT.z;
@@ -466,15 +437,13 @@ __device__ __forceinline__ void combine_rows(StreamSmem* sm, const Online& sT, c
         const float scl = (sT.cnt > 0 || sT.z > 0.f) ? ex2(gnegT - sT.neg) : 0.f;
         cT = sT.cnt > 0 ? scl * (sT.z + (float)sT.cnt * ex2(fmaf(sT.m, c, sT.neg))) : scl * sT.z;
     }
-    if (two) {
-        if (sD.m == MD) {
-            cD = sD.z;
-            nD = sD.cnt;
-            if (nD > 0) atomicMin(&sm->firstD, sD.first);
-        } else {
-            const float scl = (sD.cnt > 0 || sD.z > 0.f) ? ex2(gnegD - sD.neg) : 0.f;
-            cD = sD.cnt > 0 ? scl * (sD.z + (float)sD.cnt * ex2(fmaf(sD.m, c, sD.neg))) : scl * sD.z;
-        }
+    if (sD.m == MD) {
+        cD = sD.z;
+        nD = sD.cnt;
+        if (nD > 0) atomicMin(&sm->firstD, sD.first);
+    } else {
+        const float scl = (sD.cnt > 0 || sD.z > 0.f) ? ex2(gnegD - sD.neg) : 0.f;
+        cD = sD.cnt > 0 ? scl * (sD.z + (float)sD.cnt * ex2(fmaf(sD.m, c, sD.neg))) : scl * sD.z;
     }
     cT = warp_sum(cT);
     cD = warp_sum(cD);
@@ -506,15 +475,13 @@ __device__ __forceinline__ void combine_rows(StreamSmem* sm, const Online& sT, c
         sm->zT = (float)n1 * emT + zT;
         sm->emaxT = emT;
         sm->uT = n1 == 1 ? sm->firstT : -1;
-        if (two) {
-            const float emD = ex2(fmaf(MD, c, gnegD));
-            sm->MD = MD;
-            sm->gnegD = gnegD;
-            sm->zrestD = zD;
-            sm->zD = (float)n2 * emD + zD;
-            sm->emaxD = emD;
-            sm->uD = n2 == 1 ? sm->firstD : -1;
-        }
+        const float emD = ex2(fmaf(MD, c, gnegD));
+        sm->MD = MD;
+        sm->gnegD = gnegD;
+        sm->zrestD = zD;
+        sm->zD = (float)n2 * emD + zD;
+        sm->emaxD = emD;
+        sm->uD = n2 == 1 ? sm->firstD : -1;
     }
 }
 
@@ -603,10 +570,8 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
             NodeDesc& d = sm->qd[q];
             if (slot >= 0) {
                 const int k = slot % K, j = (slot / K) % (L + 1), b = slot / (K * (L + 1));
-                const int Lb = pb.lengths ? pb.lengths[b] : L;
-                const bool leaf = j == Lb;
                 const size_t sbase = (size_t)slot - k;
-                const bool draw = !leaf && lane < K && lane >= k && pb.ws.owner[sbase + lane] == k;
+                const bool draw = lane < K && lane >= k && pb.ws.owner[sbase + lane] == k;
                 const unsigned m = __ballot_sync(0xffffffffu, draw);
                 if (draw) {
                     const int pos = __popc(m & ((1u << lane) - 1));
@@ -625,7 +590,6 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                     d.b = b;
                     d.j = j;
                     d.k = k;
-                    d.leaf = leaf;
                     d.nd = __popc(m);
                 }
             } else if (lane == 0) {
@@ -639,8 +603,8 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
     }
 
     // ---------------------------------------------------------------- copy warp
-    // Streams each node's rows: pass 1 (evict_last), then one pass per draw
-    // (or the leaf's target-only pass), evict_first.
+    // Streams each node's rows: pass 1, then one pass per draw; evict_last
+    // until the last pass, which is evict_first.
     if (tid < 64) {
         if (tid != 32) return;
         const uint64_t pol_last = policy_evict_last();
@@ -654,18 +618,15 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
             }
             const NodeDesc& d = sm->qd[q];
             const int slot = d.slot, b = d.b, j = d.j, k = d.k, nd = d.nd;
-            const bool leaf = d.leaf != 0;
             mbar_arrive(&sm->qempty[q]);
             if (slot < 0) break;
             const char* gT = static_cast<const char*>(pb.target) +
                              (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
-            const char* gD = leaf ? nullptr
-                                  : static_cast<const char*>(pb.draft) +
-                                        (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
-            const int passes = leaf ? 1 : 1 + nd;  // a leaf is only checked
+            const char* gD = static_cast<const char*>(pb.draft) +
+                             (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
+            const int passes = 1 + nd;
             bool ok = true;
             for (int ps = 0; ps < passes && ok; ++ps) {
-                const bool with_d = !leaf;
                 // keep the rows in L2 until the node's last pass over them
                 const uint64_t pol = ps == passes - 1 ? pol_first : pol_last;
                 // passes alternate direction (pass 1 forward, the first
@@ -682,9 +643,9 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                     }
                     const int u0 = ch * kChunk;
                     const uint32_t bytes = (uint32_t)min(kChunk, n_units - u0) * 16u;
-                    mbar_expect_tx(&sm->full[s], with_d ? 2 * bytes : bytes);
+                    mbar_expect_tx(&sm->full[s], 2 * bytes);
                     bulk_g2s_hint(&sm->ring[s][0][0], gT + (size_t)u0 * 16, bytes, &sm->full[s], pol);
-                    if (with_d) bulk_g2s_hint(&sm->ring[s][1][0], gD + (size_t)u0 * 16, bytes, &sm->full[s], pol);
+                    bulk_g2s_hint(&sm->ring[s][1][0], gD + (size_t)u0 * 16, bytes, &sm->full[s], pol);
                 }
             }
             if (!ok) {
@@ -707,7 +668,6 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
         cbar_sync();  // the previous node's readers of sm->cur are done
         if (ct < (int)(sizeof(NodeDesc) / 4))
             reinterpret_cast<int*>(&sm->cur)[ct] = reinterpret_cast<const int*>(&sm->qd[q])[ct];
-        if (ct == 0) sm->lbad = sm->lfin = 0;
         cbar_sync();
         if (ct == 0) mbar_arrive(&sm->qempty[q]);
         const int slot = *static_cast<volatile int*>(&sm->abort) ? -1 : sm->cur.slot;
@@ -715,161 +675,145 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
 
         const int k = sm->cur.k, j = sm->cur.j, b = sm->cur.b;
         const size_t sbase = (size_t)slot - k;
-        const bool leaf = sm->cur.leaf != 0;
         const int nd = sm->cur.nd;
-        const char* gT = static_cast<const char*>(pb.target) +
-                         (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
-        const char* gD = leaf ? nullptr
-                              : static_cast<const char*>(pb.draft) +
-                                    (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
 
-        if (leaf) {
-            // ---- a leaf: its target row is only checked ----
-            leaf_check<DT>(sm, g, timed_out, nc, n_units, V, cw, lane);
-            cbar_sync();
-            if (ct == 0 && (sm->lbad || !sm->lfin)) {
+        // ---- pass 1: online statistics ----
+        Online sT, sD;
+        pass1<DT>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
+        online_finish<DT>(sT, sm->stash[0][ct], cw, lane, n_units, V, c);
+        online_finish<DT>(sD, sm->stash[1][ct], cw, lane, n_units, V, c);
+        combine_rows(sm, sT, sD, c, ct);
+
+        // ---- scalar state ----
+        if (ct == 0) {
+            const bool bad = !(isfinite(sm->MT) && isfinite(sm->zT) && sm->zT > 0.f) ||
+                             !(isfinite(sm->MD) && isfinite(sm->zD) && sm->zD > 0.f);
+            sm->bad = bad;
+            if (bad) {
                 atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
                 if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
             }
-        } else {
-            // ---- pass 1: online statistics ----
-            Online sT, sD;
-            pass1<DT, true>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
-            online_finish<DT>(sT, sm->stash[0][ct], cw, lane, n_units, V, c);
-            online_finish<DT>(sD, sm->stash[1][ct], cw, lane, n_units, V, c);
-            combine_rows(sm, sT, sD, true, c, ct);
-
-            // ---- scalar state ----
-            if (ct == 0) {
-                const bool bad = !(isfinite(sm->MT) && isfinite(sm->zT) && sm->zT > 0.f) ||
-                                 !(isfinite(sm->MD) && isfinite(sm->zD) && sm->zD > 0.f);
-                sm->bad = bad;
-                if (bad) {
-                    atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
-                    if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
-                }
-                // the node weight: from the parent, through its flag
-                float pbar = 0.f;
-                if (j > 0 && pb.mode != SDV_MODE_TOKEN) {
-                    const uint64_t t0 = globaltimer();
-                    while (ld_acquire(&pb.ws.ready[slot]) == 0) {
-                        if (globaltimer() - t0 > 2000000000ull) {
-                            sm->abort = 1;
-                            break;
-                        }
+            // the node weight: from the parent, through its flag
+            float pbar = 0.f;
+            if (j > 0 && pb.mode != SDV_MODE_TOKEN) {
+                const uint64_t t0 = globaltimer();
+                while (ld_acquire(&pb.ws.ready[slot]) == 0) {
+                    if (globaltimer() - t0 > 2000000000ull) {
+                        sm->abort = 1;
+                        break;
                     }
-                    pbar = pb.ws.pbar[slot];
                 }
-                sm->pbar = pbar;
-                const int xs = (sm->uT >= 0 && sm->uT == sm->uD) ? sm->uT : -1;
-                sm->xs = xs;
-                sm->Pbs = xs >= 0 ? sm->zrestT / sm->zT : 0.f;
-                sm->Qbs = xs >= 0 ? sm->zrestD / sm->zD : 0.f;
-                sm->Rs = sm->Ts = 0.f;
-                sm->S = 1.f - pbar;
-                sm->D = 1.f;
-                sm->cbar = 0.f;
+                pbar = pb.ws.pbar[slot];
+            }
+            sm->pbar = pbar;
+            const int xs = (sm->uT >= 0 && sm->uT == sm->uD) ? sm->uT : -1;
+            sm->xs = xs;
+            sm->Pbs = xs >= 0 ? sm->zrestT / sm->zT : 0.f;
+            sm->Qbs = xs >= 0 ? sm->zrestD / sm->zD : 0.f;
+            sm->Rs = sm->Ts = 0.f;
+            sm->S = 1.f - pbar;
+            sm->D = 1.f;
+            sm->cbar = 0.f;
+        }
+        cbar_sync();
+        const float pbar = sm->pbar, p = 1.f - pbar;
+        const float gnegT = sm->gnegT, gnegD = sm->gnegD;
+        const int xs = sm->xs;
+
+        // ---- pass 2: the residual recursion, one sweep per draw ----
+        // R_0 = p P, R_j = max(R_{j-1} - D_{j-1} Q, 0), S_j = sum R_j,
+        // D_j = (1 - p) + S_j.  Scalars are kept as complements (pbar =
+        // 1 - p, cbar = C - 1, Pbs = 1 - P(x*), Qbs = 1 - Q(x*)) so that
+        // nothing cancels when p, P or Q is close to 1.  The shared
+        // dominant token x* (the unique maximum of both rows) is left out
+        // of the sweeps and carried in closed form:
+        //   R_1(x*) = Qbs - Pbs - pbar + pbar Pbs,
+        //   R_j(x*) = R_{j-1}(x*) Qbs - (pbar + T_{j-1}) (1 - Qbs),
+        // with T_{j-1} the sweep's sum over the other tokens.
+        for (int di = 0; di < nd; ++di) {
+            const int k2 = sm->cur.dk[di];
+            const bool first_draw = di == 0;
+            if (ct == 0) {
+                const int y = sm->cur.y[di];
+                const float D = sm->D;
+                const float cnew = first_draw ? 0.f : sm->cbar + D;
+                const float Pbs = sm->Pbs, Qbs = sm->Qbs;
+                const float Rj = first_draw ? ((Qbs - Pbs) - pbar) + pbar * Pbs
+                                            : sm->Rs * Qbs - (pbar + sm->Ts) * (1.f - Qbs);
+                sm->Rj = Rj;
+                float R, Qy, abar_num;
+                if (y == xs) {
+                    Qy = 1.f - Qbs;
+                    R = first_draw ? (1.f - pbar) * (1.f - Pbs) : sm->Rs;
+                    abar_num = fmaxf(-Rj, 0.f);
+                } else {
+                    const ProbS Py = prob_s(sm, true, y, sm->cur.gT[di], c);
+                    const ProbS Qp = prob_s(sm, false, y, sm->cur.gD[di], c);
+                    Qy = Qp.P;
+                    R = first_draw ? p * Py.P : fmaxf((1.f - pbar) * Py.P - (1.f + sm->cbar) * Qp.P, 0.f);
+                    abar_num = fmaxf((1.f + cnew) * Qp.P - (1.f - pbar) * Py.P, 0.f);
+                }
+                float a, abar;
+                const float ratio = (D > 0.f && Qy > 0.f) ? (R / D) / Qy : INFINITY;
+                if (ratio >= 1.f) {
+                    a = 1.f;
+                    abar = 0.f;
+                } else if (!(R > 0.f)) {
+                    a = 0.f;
+                    abar = 1.f;
+                } else {
+                    a = ratio;
+                    abar = fminf((abar_num / D) / Qy, 1.f);
+                }
+                sm->cbar = cnew;
+                pb.ws.a[sbase + k2] = a;
+                bool first_of_token = true;  // this draw's child is new: it owns it
+                for (int e = 0; e < di; ++e) first_of_token &= sm->cur.y[e] != y;
+                if (pb.mode != SDV_MODE_TOKEN) {
+                    const size_t sc = sbase + K + k2;
+                    if (first_of_token) {  // child first reached by this draw
+                        pb.ws.pbar[sc] = abar;
+                        st_release(&pb.ws.ready[sc], 1);
+                    }
+                }
+                sm->aT = p / sm->zT;
+                sm->aD = (1.f + cnew) / sm->zD;
+                sm->rD = sm->aT > 0.f ? sm->aD / sm->aT : 3.402823466e38f;
             }
             cbar_sync();
-            const float pbar = sm->pbar, p = 1.f - pbar;
-            const float gnegT = sm->gnegT, gnegD = sm->gnegD;
-            const int xs = sm->xs;
-
-            // ---- pass 2: the residual recursion, one sweep per draw ----
-            // R_0 = p P, R_j = max(R_{j-1} - D_{j-1} Q, 0), S_j = sum R_j,
-            // D_j = (1 - p) + S_j.  Scalars are kept as complements (pbar =
-            // 1 - p, cbar = C - 1, Pbs = 1 - P(x*), Qbs = 1 - Q(x*)) so that
-            // nothing cancels when p, P or Q is close to 1.  The shared
-            // dominant token x* (the unique maximum of both rows) is left out
-            // of the sweeps and carried in closed form:
-            //   R_1(x*) = Qbs - Pbs - pbar + pbar Pbs,
-            //   R_j(x*) = R_{j-1}(x*) Qbs - (pbar + T_{j-1}) (1 - Qbs),
-            // with T_{j-1} the sweep's sum over the other tokens.
-            for (int di = 0; di < nd; ++di) {
-                const int k2 = sm->cur.dk[di];
-                const bool first_draw = di == 0;
-                if (ct == 0) {
-                    const int y = sm->cur.y[di];
-                    const float D = sm->D;
-                    const float cnew = first_draw ? 0.f : sm->cbar + D;
-                    const float Pbs = sm->Pbs, Qbs = sm->Qbs;
-                    const float Rj = first_draw ? ((Qbs - Pbs) - pbar) + pbar * Pbs
-                                                : sm->Rs * Qbs - (pbar + sm->Ts) * (1.f - Qbs);
-                    sm->Rj = Rj;
-                    float R, Qy, abar_num;
-                    if (y == xs) {
-                        Qy = 1.f - Qbs;
-                        R = first_draw ? (1.f - pbar) * (1.f - Pbs) : sm->Rs;
-                        abar_num = fmaxf(-Rj, 0.f);
-                    } else {
-                        const ProbS Py = prob_s(sm, true, y, sm->cur.gT[di], c);
-                        const ProbS Qp = prob_s(sm, false, y, sm->cur.gD[di], c);
-                        Qy = Qp.P;
-                        R = first_draw ? p * Py.P : fmaxf((1.f - pbar) * Py.P - (1.f + sm->cbar) * Qp.P, 0.f);
-                        abar_num = fmaxf((1.f + cnew) * Qp.P - (1.f - pbar) * Py.P, 0.f);
-                    }
-                    float a, abar;
-                    const float ratio = (D > 0.f && Qy > 0.f) ? (R / D) / Qy : INFINITY;
-                    if (ratio >= 1.f) {
-                        a = 1.f;
-                        abar = 0.f;
-                    } else if (!(R > 0.f)) {
-                        a = 0.f;
-                        abar = 1.f;
-                    } else {
-                        a = ratio;
-                        abar = fminf((abar_num / D) / Qy, 1.f);
-                    }
-                    sm->cbar = cnew;
-                    pb.ws.a[sbase + k2] = a;
-                    bool first_of_token = true;  // this draw's child is new: it owns it
-                    for (int e = 0; e < di; ++e) first_of_token &= sm->cur.y[e] != y;
-                    if (pb.mode != SDV_MODE_TOKEN) {
-                        const size_t sc = sbase + K + k2;
-                        if (first_of_token) {  // child first reached by this draw
-                            pb.ws.pbar[sc] = abar;
-                            st_release(&pb.ws.ready[sc], 1);
-                        }
-                    }
-                    sm->aT = p / sm->zT;
-                    sm->aD = (1.f + cnew) / sm->zD;
-                    sm->rD = sm->aT > 0.f ? sm->aD / sm->aT : 3.402823466e38f;
-                }
-                cbar_sync();
-                // sweep di is pass di + 1 of the node: backward for even di
-                float tot = sweep<DT>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, sm->aT, sm->rD, xs, cw, lane,
-                                      (di & 1) == 0);
-                tot = warp_sum(tot);
-                if (lane == 0) sm->redf[2][cw] = tot;
-                cbar_sync();
-                if (ct == 0) {
-                    float Sj = 0.f;
-                    for (int i = 0; i < kSW; ++i) Sj += sm->redf[2][i];
-                    if (xs >= 0) {  // the sweeps left x* out: their sum is the mass elsewhere
-                        const float Rs = fmaxf(sm->Rj, 0.f);
-                        sm->Ts = Sj;
-                        sm->Rs = Rs;
-                        Sj += Rs;
-                    }
-                    sm->S = fmaxf(Sj, 0.f);
-                    sm->D = pbar + sm->S;
-                }
-            }
+            // sweep di is pass di + 1 of the node: backward for even di
+            float tot = sweep<DT>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, sm->aT, sm->rD, xs, cw, lane,
+                                  (di & 1) == 0);
+            tot = warp_sum(tot);
+            if (lane == 0) sm->redf[2][cw] = tot;
+            cbar_sync();
             if (ct == 0) {
-                // the node's block acceptance and, for the correction draw
-                // should the decision end here, its final residual
-                // R_n = aT max(e_T - (aD / aT) e_D, 0) with R_n(x*) apart
-                const float S = sm->S, D = sm->D;
-                pb.ws.h[slot] = D > 0.f ? S / D : 1.f;
-                pb.ws.S[slot] = S;
-                float* prm = pb.ws.prm + (size_t)slot * 5;
-                prm[0] = gnegT;
-                prm[1] = gnegD;
-                prm[2] = sm->aT;
-                prm[3] = sm->rD;
-                prm[4] = sm->Rs;
-                pb.ws.xs[slot] = xs;
+                float Sj = 0.f;
+                for (int i = 0; i < kSW; ++i) Sj += sm->redf[2][i];
+                if (xs >= 0) {  // the sweeps left x* out: their sum is the mass elsewhere
+                    const float Rs = fmaxf(sm->Rj, 0.f);
+                    sm->Ts = Sj;
+                    sm->Rs = Rs;
+                    Sj += Rs;
+                }
+                sm->S = fmaxf(Sj, 0.f);
+                sm->D = pbar + sm->S;
             }
+        }
+        if (ct == 0) {
+            // the node's block acceptance and, for the correction draw
+            // should the decision end here, its final residual
+            // R_n = aT max(e_T - (aD / aT) e_D, 0) with R_n(x*) apart
+            const float S = sm->S, D = sm->D;
+            pb.ws.h[slot] = D > 0.f ? S / D : 1.f;
+            pb.ws.S[slot] = S;
+            float* prm = pb.ws.prm + (size_t)slot * 5;
+            prm[0] = gnegT;
+            prm[1] = gnegD;
+            prm[2] = sm->aT;
+            prm[3] = sm->rD;
+            prm[4] = sm->Rs;
+            pb.ws.xs[slot] = xs;
         }
         // a timed-out wait anywhere stops every consumer together (the
         // decision is read after the node's last barrier, so it is uniform)
@@ -902,8 +846,9 @@ cudaError_t launch_stream(const Problem& pb, cudaStream_t st)
                                           : reinterpret_cast<const void*>(stream_kernel<SDV_F32>);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StreamSmem));
     if (e != cudaSuccess) return e;
-    // at most one node per request and depth per draft
-    const long long upper = (long long)pb.B * (1 + (long long)pb.K * pb.L);
+    // inner nodes: the root and at most one per draft at depths 1..L-1
+    if (pb.L == 0) return cudaSuccess;
+    const long long upper = (long long)pb.B * (1 + (long long)pb.K * (pb.L - 1));
     const int grid = (int)std::max(1LL, std::min((long long)sms * kCtasPerSm, upper));
     if (pb.dtype == SDV_BF16)
         stream_kernel<SDV_BF16><<<grid, kSThreads, sizeof(StreamSmem), st>>>(pb);

@@ -69,8 +69,8 @@
  * Errors.  The return value reports argument validation and launch errors
  * only (SDV_OK or an SDV_ERR_* code; nothing is launched on error).  Data
  * errors are found on the device: for each request whose length is outside
- * 0..L, whose used tokens are outside [0, V), or one of whose used rows
- * holds NaN or +Inf or no finite value, the outputs are accept_len = 0,
+ * 0..L, whose used tokens are outside [0, V), or one of whose read rows
+ * (see target_logits) holds NaN or +Inf or no finite value, the outputs are accept_len = 0,
  * accept_draft = 0, out_token = -1, residual_mass = 0 and accept_prob = 0,
  * and the request's SDV_REQ_* bit is OR-ed into *device_status.  Other
  * requests are unaffected.  Kernels never trap.
@@ -125,6 +125,10 @@ enum {
  *                conditioned on draft k's first j tokens.  Only the rows of
  *                trie nodes are read: row (b,k,j) with j <= lengths[b] and k
  *                the lowest-index draft with that prefix (row 0: k = 0).
+ *                In the sampling rules a leaf's row (j = lengths[b]) is read
+ *                only if the decision ends at that leaf, for the bonus draw
+ *                (a leaf has no draws; its residual p P has mass p whatever
+ *                P is); greedy reads every node's row.
  *   draft_logits [B][K][L][row_stride], 16-byte aligned; same rule with
  *                j < lengths[b].  May be NULL when L = 0 or for greedy.
  *   draft_tokens [B][K][L] int32; positions j >= lengths[b] are ignored.

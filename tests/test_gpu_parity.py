@@ -131,6 +131,52 @@ def test_invalid_requests_are_isolated():
         assert st[2] == (0 if mode == "greedy" else 4)
 
 
+@pytest.mark.parametrize("name,K", [("multidraft-B32-K4-L4-V32000-f32", 3), ("block-B128-K1-L5-V128256-bf16", 1)])
+def test_leaf_rows_are_read_only_by_the_bonus_draw(name, K):
+    """A leaf's target row enters only the bonus draw, made when the decision
+    ends there.  Requests 0-2 accept everything (accept_u = 0: the decision
+    ends at draft 0's leaf); the others mostly stop short (accept_u = 0.999;
+    a draw still passes where a = 1).  Every leaf row is poisoned except
+    draft 0's in requests 0 and 1.  A request whose clean decision stops
+    short of its leaves must come back unchanged; one that ends at a leaf,
+    invalid; greedy reads every leaf."""
+    lengths = [3, 2, 3, 3, 1, 2, 3, 3, 2, 3]
+    batch = W.make(name, DEV, B=len(lengths), K=K, L=3, V=2003, lengths=lengths, temperature=0.8)
+    batch.accept_u[:3] = 0.0
+    batch.accept_u[3:] = 0.999
+    modes = ["token", "multidraft", "greedy"] if K > 1 else ["token", "block", "greedy"]
+    clean = {mode: P.oracle_run(mode, batch) for mode in modes}
+    for b, Lb in enumerate(lengths):
+        for k in range(K):
+            if b in (0, 1) and k == 0:
+                continue
+            batch.target[b, k, Lb, (7 * b + 3 * k) % batch.V] = float("nan") if k % 2 == 0 else float("inf")
+    for mode in modes:
+        gpu = P.gpu_run(mode, batch)
+        ref = P.oracle_run(mode, batch)
+        P.compare(gpu, ref, f"leaves/{mode}")
+        st, c = ref["req_status"], clean[mode]
+        assert (c["req_status"] == 0).all()
+        if mode == "greedy":  # draft 0 owns its whole path: its poisoned leaves are read
+            assert (st[2:] == 4).all()
+            if K == 1:
+                assert st[0] == 0 and st[1] == 0
+            continue
+        assert st[0] == 0 and st[1] == 0 and st[2] == 4
+        assert gpu["accept_len"][0] == 3 and gpu["accept_len"][1] == 2
+        short = [b for b in range(3, len(lengths)) if c["accept_len"][b] < lengths[b]]
+        assert short, "the fixture should stop short somewhere"
+        for b in range(3, len(lengths)):
+            if b in short:
+                assert st[b] == 0
+                for key in ("accept_len", "accept_draft", "out_token"):
+                    assert ref[key][b] == c[key][b], (mode, b, key)
+            else:
+                assert st[b] == 4
+        for b in np.nonzero(st)[0]:
+            assert gpu["residual_mass"][b] == 0.0 and (gpu["accept_prob"][b] == 0).all()
+
+
 def test_deterministic():
     batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=8, V=30011)
     for mode in ("token", "multidraft"):
