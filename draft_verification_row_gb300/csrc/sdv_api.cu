@@ -24,7 +24,7 @@ bool sizes_ok(int B, int K, int L, int V)
 size_t workspace_size(int B, int K, int L)
 {
     const size_t n = slot_count(B, K, L);
-    return 7 * align_up(n * 4) + align_up(n * 5 * 4) + align_up(n) + align_up((size_t)B * 4) +
+    return 6 * align_up(n * 4) + align_up(n * 5 * 4) + align_up(n) + align_up((size_t)B * 4) +
            align_up((size_t)(L + 1) * B * K * 4) + align_up((size_t)(L + 2) * 4);
 }
 
@@ -51,8 +51,6 @@ Workspace carve(void* base, int B, int K, int L)
     p += align_up(n);
     w.req = reinterpret_cast<int*>(p);
     p += align_up((size_t)B * 4);
-    w.ready = reinterpret_cast<int*>(p);
-    p += align_up(n * 4);
     w.nodes = reinterpret_cast<int*>(p);
     p += align_up((size_t)(L + 1) * B * K * 4);
     w.ncount = reinterpret_cast<int*>(p);

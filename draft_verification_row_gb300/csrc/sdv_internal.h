@@ -20,14 +20,14 @@ struct Workspace {
     float* a;              // draw acceptance probability a (token / multidraft)
     float* h;              // node block acceptance probability h_v
     float* S;              // node residual mass S_n
-    float* pbar;           // node weight complement 1 - p_v
+    float* pbar;           // node weight complement 1 - p_v, written by the parent's draw
+                           //   (below 0 until then: the child's flag)
     float* prm;            // node residual for the correction draw: [slot][5] =
                            //   -(M_T c), -(M_D c), aT = p / Z_T, aD / aT, R_n(x*)
     int* xs;               // node shared dominant token x* (or -1)
     int* am;               // node argmax (greedy)
     unsigned char* owner;  // lowest draft sharing draft k's first j tokens
     int* req;              // [B] request status bits
-    int* ready;            // node weight published by the parent (slot flags)
     int* nodes;            // [L+1][B*K] node slots by depth, listed by the prep kernel
     int* ncount;           // [L+1] nodes per depth, then the streaming kernel's work counter
 };

@@ -58,11 +58,11 @@ __global__ void prep_kernel(Problem pb)
         o = no;
         if (lane < K) own[j * K + lane] = (unsigned char)o;
     }
-    if (lane == 0) pb.ws.pbar[(size_t)b * (L + 1) * K] = 0.f;  // root weight 1
     // list the request's inner nodes by depth (for the node kernel) and
-    // clear the flags through which parents publish their children's
-    // weights.  Leaves are not listed: a leaf has no draws, and its target
-    // row is read by the bonus draw alone, once the decision ends there.
+    // mark every weight below the root unwritten (-1: a parent's draw
+    // writes it, and the child waits for a value of 0 or more).  Leaves are
+    // not listed: a leaf has no draws, and its target row is read by the
+    // bonus draw alone, once the decision ends there.
     const size_t BK = (size_t)pb.B * K;
     for (int j = 0; j <= Lb; ++j) {
         const bool node = j < Lb && lane < K && own[j * K + lane] == lane;
@@ -72,7 +72,7 @@ __global__ void prep_kernel(Problem pb)
         base = __shfl_sync(0xffffffffu, base, 0);
         const size_t slot = ((size_t)b * (L + 1) + j) * K + lane;
         if (node) pb.ws.nodes[j * BK + base + __popc(m & ((1u << lane) - 1))] = (int)slot;
-        if (lane < K) pb.ws.ready[slot] = 0;
+        if (lane < K) pb.ws.pbar[slot] = j == 0 ? 0.f : -1.f;  // the root's weight is 1
     }
 }
 

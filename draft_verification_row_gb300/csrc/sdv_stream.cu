@@ -18,8 +18,8 @@
 // 3-stage ring with 1-D TMA bulk copies (mbarrier full/empty handshake),
 // marked evict_last in L2 until the node's last pass, which is evict_first.
 // Warps 2..13 consume: a warp owns 64 contiguous 16-byte units of each
-// chunk.  A node's weight p comes from its parent through a flag
-// (release/acquire); waiting happens only before pass 2.  Every wait is
+// chunk.  A node's weight p comes from its parent's write of it (a value
+// below 0 means not yet written); waiting happens only before pass 2.  Every wait is
 // bounded and a timeout is reported, never a hang or a trap.
 //
 // The rules computed are stated in include/sdv.h (SpecTr-GBV:
@@ -75,16 +75,18 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
         : "memory");
 }
 
-__device__ __forceinline__ int ld_acquire(const int* p)
+// A node's weight is its own flag: the parent's draw writes it (a value of
+// 0 or more) and the child reads nothing else, so relaxed accesses suffice.
+__device__ __forceinline__ float ld_relaxed(const float* p)
 {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
     return v;
 }
 
-__device__ __forceinline__ void st_release(int* p, int v)
+__device__ __forceinline__ void st_relaxed(float* p, float v)
 {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+    asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 // What the metadata warp prepares for each node, ahead of its rows.
@@ -693,17 +695,21 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
                 if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
             }
-            // the node weight: from the parent, through its flag
+            // the node weight, written by the parent (below 0 until then)
             float pbar = 0.f;
             if (j > 0 && pb.mode != SDV_MODE_TOKEN) {
-                const uint64_t t0 = globaltimer();
-                while (ld_acquire(&pb.ws.ready[slot]) == 0) {
-                    if (globaltimer() - t0 > 2000000000ull) {
-                        sm->abort = 1;
-                        break;
+                const float* f = pb.ws.pbar + slot;
+                pbar = ld_relaxed(f);
+                if (!(pbar >= 0.f)) {
+                    const uint64_t t0 = globaltimer();
+                    while (!((pbar = ld_relaxed(f)) >= 0.f)) {
+                        if (globaltimer() - t0 > 2000000000ull) {
+                            sm->abort = 1;
+                            pbar = 0.f;
+                            break;
+                        }
                     }
                 }
-                pbar = pb.ws.pbar[slot];
             }
             sm->pbar = pbar;
             const int xs = (sm->uT >= 0 && sm->uT == sm->uD) ? sm->uT : -1;
@@ -771,10 +777,9 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 for (int e = 0; e < di; ++e) first_of_token &= sm->cur.y[e] != y;
                 if (pb.mode != SDV_MODE_TOKEN) {
                     const size_t sc = sbase + K + k2;
-                    if (first_of_token) {  // child first reached by this draw
-                        pb.ws.pbar[sc] = abar;
-                        st_release(&pb.ws.ready[sc], 1);
-                    }
+                    // child first reached by this draw: its weight (never NaN:
+                    // the child waits for a value of 0 or more)
+                    if (first_of_token) st_relaxed(&pb.ws.pbar[sc], fmaxf(abar, 0.f));
                 }
                 sm->aT = p / sm->zT;
                 sm->aD = (1.f + cnew) / sm->zD;
