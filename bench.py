@@ -15,7 +15,9 @@ library around those launches, the end-to-end figure through the C-ABI with
 host buffers, the oracle timed on host cores, the launch count and the SM
 clocks sampled during the timed region.  "next_draft_sampling" measures the
 draft-token sampling step (sdv_sample_rows) on the batch's depth-0 draft
-rows.
+rows; "next_psd" the one-GPU emulation of batch-parallel speculative
+decoding (the batch's halves alternating draft and verify phases on two
+streams).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -424,6 +426,16 @@ def run_ours(args, world, rank, local):
                          "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_call": s_bytes,
                          "kernel": "sample_rows_kernel"}}
         del rows
+        # one-GPU PSD emulation: the batch's two halves alternate drafting
+        # (L sampling launches) and verification on two streams
+        from draft_verification_row_gb300 import psd
+        emu = psd.PsdEmulator(batch, steps=8)
+        m = psd.measure(emu, reps=max(5, args.steps // 2), warmup=3)
+        line["next_psd"] = {"what": "two halves of the batch alternate draft (sdv_sample_rows per depth) and "
+                                    "verify (multidraft) phases on two streams of one GPU",
+                            "half_batch": emu.B, **m,
+                            "gpu_launches_per_step": emu.L + 3}  # L sampling launches + prep, node, finish
+        del emu
         if rank == 0:
             rng = np.random.default_rng(1)
             req = sorted(rng.choice(batch.B, size=min(args.cpu_requests, batch.B), replace=False).tolist())

@@ -181,16 +181,18 @@ def sample_rows(logits, n_samples, u, temperature, *, V=None, tokens=None, devic
     """Draft-token sampling: n_samples inverse-CDF draws per row of
     softmax(logits / T).
 
-    logits [n_rows][stride] (float32 or bfloat16, CUDA, contiguous),
-    u [n_rows][n_samples] float32 (may be None when T == 0).  Returns
-    (tokens [n_rows][n_samples] int32, device_status [1] int32); the call is
-    asynchronous.
+    logits [n_rows][width] (float32 or bfloat16, CUDA; each row contiguous,
+    rows evenly spaced by logits.stride(0), e.g. one depth's rows of a
+    [B][K][L][stride] draft tensor), u [n_rows][n_samples] float32 (may be
+    None when T == 0).  Returns (tokens [n_rows][n_samples] int32,
+    device_status [1] int32); the call is asynchronous.
     """
     h = lib()
-    if logits.dim() != 2 or not logits.is_cuda or not logits.is_contiguous():
-        raise ValueError("logits must be a contiguous CUDA [n_rows][stride] tensor")
-    n_rows, stride = logits.shape
-    V = stride if V is None else int(V)
+    if logits.dim() != 2 or not logits.is_cuda or (logits.shape[0] > 1 and logits.stride(1) != 1):
+        raise ValueError("logits must be a CUDA [n_rows][width] tensor with contiguous rows")
+    n_rows, width = logits.shape
+    stride = logits.stride(0) if n_rows > 1 else width
+    V = width if V is None else int(V)
     if u is not None and (u.dtype != torch.float32 or not u.is_cuda or not u.is_contiguous()
                           or tuple(u.shape) != (n_rows, n_samples)):
         raise ValueError("u must be a contiguous CUDA float32 [n_rows][n_samples] tensor")
