@@ -25,7 +25,7 @@ size_t workspace_size(int B, int K, int L)
 {
     const size_t n = slot_count(B, K, L);
     return 6 * align_up(n * 4) + align_up(n * 5 * 4) + align_up(n) + align_up((size_t)B * 4) +
-           align_up((size_t)(L + 1) * B * K * 4) + align_up((size_t)(L + 2) * 4);
+           align_up((size_t)(L + 1) * B * K * 4) + align_up((size_t)(2 * L + 3) * 4);
 }
 
 Workspace carve(void* base, int B, int K, int L)
@@ -149,7 +149,7 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
     pb.ws = carve(workspace, B, K, L);
 
     if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
-    if (cudaMemsetAsync(pb.ws.ncount, 0, sizeof(int) * (L + 2), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (cudaMemsetAsync(pb.ws.ncount, 0, sizeof(int) * (2 * L + 3), st) != cudaSuccess) return SDV_ERR_CUDA;
     if (launch_prep(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
     if (!prof_record(g_prof_start, st)) return SDV_ERR_CUDA;
     if (greedy) {

@@ -28,8 +28,10 @@ struct Workspace {
     int* am;               // node argmax (greedy)
     unsigned char* owner;  // lowest draft sharing draft k's first j tokens
     int* req;              // [B] request status bits
-    int* nodes;            // [L+1][B*K] node slots by depth, listed by the prep kernel
-    int* ncount;           // [L+1] nodes per depth, then the streaming kernel's work counter
+    int* nodes;            // [L+1][B*K] node slots by depth, listed by the prep kernel: nodes
+                           //   with several draws from the front, one-draw nodes from the back
+    int* ncount;           // [2][L+1] nodes per depth (several draws, one draw), then the
+                           //   node kernel's work counter
 };
 
 struct Problem {

@@ -60,18 +60,31 @@ __global__ void prep_kernel(Problem pb)
     }
     // list the request's inner nodes by depth (for the node kernel) and
     // mark every weight below the root unwritten (-1: a parent's draw
-    // writes it, and the child waits for a value of 0 or more).  Leaves are
-    // not listed: a leaf has no draws, and its target row is read by the
-    // bonus draw alone, once the decision ends there.
+    // writes it, and the child waits for a value of 0 or more).  Within a
+    // depth, nodes with several draws (several sweeps) fill the list from
+    // the front and one-draw nodes from the back, so that the longest work
+    // of a depth is handed out first.  Leaves are not listed: a leaf has no
+    // draws, and its target row is read by the bonus draw alone, once the
+    // decision ends there.
     const size_t BK = (size_t)pb.B * K;
+    int* const front = pb.ws.ncount;
+    int* const back = pb.ws.ncount + (L + 1);
     for (int j = 0; j <= Lb; ++j) {
         const bool node = j < Lb && lane < K && own[j * K + lane] == lane;
-        const unsigned m = __ballot_sync(0xffffffffu, node);
-        int base = 0;
-        if (lane == 0 && m) base = atomicAdd(&pb.ws.ncount[j], __popc(m));
-        base = __shfl_sync(0xffffffffu, base, 0);
+        int draws = 0;  // drafts through the node
+        if (node)
+            for (int k2 = 0; k2 < K; ++k2) draws += own[j * K + k2] == lane;
+        const unsigned mh = __ballot_sync(0xffffffffu, node && draws > 1);
+        const unsigned ml = __ballot_sync(0xffffffffu, node && draws == 1);
+        int fb = 0, bb = 0;
+        if (lane == 0 && mh) fb = atomicAdd(&front[j], __popc(mh));
+        if (lane == 0 && ml) bb = atomicAdd(&back[j], __popc(ml));
+        fb = __shfl_sync(0xffffffffu, fb, 0);
+        bb = __shfl_sync(0xffffffffu, bb, 0);
         const size_t slot = ((size_t)b * (L + 1) + j) * K + lane;
-        if (node) pb.ws.nodes[j * BK + base + __popc(m & ((1u << lane) - 1))] = (int)slot;
+        const unsigned below = (1u << lane) - 1;
+        if (node && draws > 1) pb.ws.nodes[j * BK + fb + __popc(mh & below)] = (int)slot;
+        if (node && draws == 1) pb.ws.nodes[j * BK + BK - 1 - (bb + __popc(ml & below))] = (int)slot;
         if (lane < K) pb.ws.pbar[slot] = j == 0 ? 0.f : -1.f;  // the root's weight is 1
     }
 }

@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
     const int n_units = (V + EPU - 1) / EPU;
     const int nc = (n_units + kChunk - 1) / kChunk;
     const float c = pb.c;
-    int* const counter = pb.ws.ncount + (L + 1);
+    int* const counter = pb.ws.ncount + 2 * (L + 1);
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -540,8 +540,10 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
     // ahead: draws, their tokens and logits, the sample uniform.
     if (tid < 32) {
         const int lane = tid;
-        // lane j holds the node count of depth j
-        const int cnt = lane <= L ? pb.ws.ncount[lane] : 0;
+        // lane j holds the node counts of depth j: several-draw nodes (from
+        // the front of the depth's list) and one-draw nodes (from its back)
+        const int cntf = lane <= L ? pb.ws.ncount[lane] : 0;
+        const int cnt = lane <= L ? cntf + pb.ws.ncount[L + 1 + lane] : 0;
         int n_items = cnt;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) n_items += __shfl_xor_sync(0xffffffffu, n_items, o);
@@ -561,7 +563,9 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 }
                 const int j = __ffs(__ballot_sync(0xffffffffu, incl > w)) - 1;
                 const int before = __shfl_sync(0xffffffffu, incl - cnt, j);
-                slot = pb.ws.nodes[(size_t)j * BK + (w - before)];
+                const int nf = __shfl_sync(0xffffffffu, cntf, j);
+                const int i = w - before;
+                slot = pb.ws.nodes[(size_t)j * BK + (i < nf ? i : BK - 1 - (i - nf))];
             }
             bool ok = true;
             if (lane == 0 && it >= kQ) ok = mbar_wait_bounded(&sm->qempty[q], (it / kQ - 1) & 1);
