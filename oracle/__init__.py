@@ -13,7 +13,7 @@ import numpy as np
 
 from . import build as _build
 
-MODE = {"token": 0, "greedy": 1, "block": 2, "multidraft": 3}
+MODE = {"token": 0, "greedy": 1, "block": 2, "multidraft": 3, "kseq": 4}
 F32, BF16 = 0, 1
 REQ_BAD_LENGTH, REQ_BAD_TOKEN, REQ_NONFINITE = 1, 2, 4
 MAX_K = 16

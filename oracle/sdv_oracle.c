@@ -139,6 +139,8 @@ typedef struct {
     double h[SDVO_MAX_L + 1][SDVO_MAX_K];  /* node (j, owner) block acceptance probability */
     double S[SDVO_MAX_L + 1][SDVO_MAX_K];  /* node residual mass S_n */
     int am[SDVO_MAX_L + 1][SDVO_MAX_K];    /* node argmax (greedy) */
+    double rho[SDVO_MAX_L + 1][SDVO_MAX_K];   /* K-SEQ: node scaling factor rho */
+    double gam[SDVO_MAX_L + 1][SDVO_MAX_K];   /* K-SEQ: node factor (1 - (1 - beta)^n) / beta */
     double margin;
     sdvo_trace* tr;
     double *P, *Q, *R;                     /* V-sized scratch */
@@ -457,6 +459,113 @@ static int run_block(req_t* r, float* accept_prob, outcome_t* out, double* resid
     return 0;
 }
 
+/* SpecTr's K-SEQ at a node (the pages name it and its binary search for a
+ * scaling factor rho: SpecTr-GBV page, sections 3-4; the rule is written
+ * here from its published definition).  The n drafts through the node are
+ * i.i.d. candidates from Q.  For rho >= 1 let
+ *   beta(rho) = sum_x min(Q(x), P(x) / rho),
+ *   gamma(rho) = (1 - (1 - beta)^n) / beta   (n when beta = 0).
+ * Candidate i is accepted with probability min(1, P(y_i) / (rho Q(y_i))),
+ * tried in index order; if every one is rejected the token is drawn from
+ * P - gamma min(Q, P / rho).  That residual is nonnegative, and the emitted
+ * token follows P exactly, whenever gamma(rho) <= rho (true at rho = n).
+ * The search for a small such rho (acceptance falls as rho grows) is fixed
+ * here so that a parallel implementation can take the same decisions: rho
+ * = 1 if it qualifies; else, starting from [lo, hi] = [1, n], KSEQ_PASSES
+ * rounds each test the three points lo + (hi - lo) i / 4 (i = 1, 2, 3) and
+ * keep the quarter holding the first that qualifies (the last quarter if
+ * none does).  rho is the final hi, which always qualifies.
+ * Stores a, rho and gamma; leaves P, Q in r->P, r->Q. */
+#define KSEQ_PASSES 10
+
+static double kseq_beta(const req_t* r, double rho)
+{
+    double beta = 0.0;
+    for (int x = 0; x < r->pb->V; ++x) beta += fmin(r->Q[x], r->P[x] / rho);
+    return beta;
+}
+
+static double kseq_gamma(double beta, int n) { return beta > 0.0 ? (1.0 - pow(1.0 - beta, n)) / beta : (double)n; }
+
+static int kseq_ok(const req_t* r, double rho, int n) { return kseq_gamma(kseq_beta(r, rho), n) <= rho; }
+
+static void kseq_node(req_t* r, int j, int o)
+{
+    const sdvo_problem* pb = r->pb;
+    int n = 0;
+    double lo = 1.0, hi;
+    softmax(pb, row_of(pb, 1, r->b, o, j), pb->temperature, r->P);
+    softmax(pb, row_of(pb, 0, r->b, o, j), pb->temperature, r->Q);
+    for (int k = 0; k < pb->K; ++k) n += r->owner[j][k] == o;
+    hi = (double)n;
+    if (kseq_ok(r, 1.0, n)) {
+        hi = 1.0;
+    } else {
+        for (int it = 0; it < KSEQ_PASSES; ++it) {
+            double m[4];
+            int i = 1;
+            m[0] = lo;
+            for (int t = 1; t < 4; ++t) m[t] = lo + (hi - lo) * t / 4.0;
+            while (i < 4 && !kseq_ok(r, m[i], n)) ++i;
+            if (i < 4) {
+                lo = m[i - 1];
+                hi = m[i];
+            } else {
+                lo = m[3];
+            }
+        }
+    }
+    r->rho[j][o] = hi;
+    r->gam[j][o] = kseq_gamma(kseq_beta(r, hi), n);
+    for (int k = 0; k < pb->K; ++k) {
+        if (r->owner[j][k] != o) continue;
+        int y = tok(r, k, j);
+        double den = hi * r->Q[y];
+        r->a[j][k] = den > 0.0 ? fmin(r->P[y] / den, 1.0) : 1.0;
+    }
+}
+
+/* K-SEQ at every node, then the walk of the token rule; the correction
+ * comes from the end node's K-SEQ residual (P where it has no mass), or
+ * P at a leaf. */
+static int run_kseq(req_t* r, float* accept_prob, outcome_t* out, double* residual_out)
+{
+    const sdvo_problem* pb = r->pb;
+    int V = pb->V, j = 0, o = 0;
+    double S = 0.0, tot = 0.0;
+    const double* w;
+    for (int d = 0; d < r->Lb; ++d)
+        for (int v = 0; v < pb->K; ++v)
+            if (r->owner[d][v] == v) kseq_node(r, d, v);
+    if (accept_prob)
+        for (int k = 0; k < pb->K; ++k)
+            for (int d = 0; d < r->Lb; ++d) accept_prob[k * pb->L + d] = (float)r->a[d][k];
+    while (j < r->Lb) {
+        int acc = -1;
+        for (int k = 0; k < pb->K && acc < 0; ++k)
+            if (r->owner[j][k] == o && accept_test(r, k, j, r->a[j][k])) acc = k;
+        if (acc < 0) break;
+        o = r->owner[j + 1][acc];
+        ++j;
+    }
+    if (j == r->Lb) return draw_correction(r, j, o, 1.0, out, residual_out); /* the bonus token */
+    kseq_node(r, j, o);
+    for (int x = 0; x < V; ++x) {
+        r->R[x] = fmax(r->P[x] - r->gam[j][o] * fmin(r->Q[x], r->P[x] / r->rho[j][o]), 0.0);
+        S += r->R[x];
+    }
+    w = S > 0.0 ? r->R : r->P;
+    out->tau = j;
+    out->kstar = o;
+    out->mass = S;
+    out->token = sample_icdf(r, w, o, j);
+    if (residual_out) {
+        for (int x = 0; x < V; ++x) tot += w[x];
+        for (int x = 0; x < V; ++x) residual_out[x] = w[x] / tot;
+    }
+    return 0;
+}
+
 /* Greedy T = 0: a draft position matches when its token is the row's
  * argmax; the longest matching draft wins (lowest k on ties); the
  * correction is the argmax after the accepted prefix. */
@@ -496,7 +605,7 @@ int sdvo_verify(int mode, const sdvo_problem* pb, int* accept_len, int* accept_d
 {
     req_t r;
     int greedy;
-    if (!pb || mode < SDVO_MODE_TOKEN || mode > SDVO_MODE_MULTIDRAFT) return SDVO_ERR_INVALID;
+    if (!pb || mode < SDVO_MODE_TOKEN || mode > SDVO_MODE_KSEQ) return SDVO_ERR_INVALID;
     if (pb->B < 0 || pb->K < 1 || pb->K > SDVO_MAX_K || pb->L < 0 || pb->L > SDVO_MAX_L || pb->V < 1 ||
         pb->row_stride < pb->V || (pb->dtype != SDVO_F32 && pb->dtype != SDVO_BF16))
         return SDVO_ERR_INVALID;
@@ -536,6 +645,7 @@ int sdvo_verify(int mode, const sdvo_problem* pb, int* accept_len, int* accept_d
             if (greedy) run_greedy(&r, ap, &out, ro);
             else if (mode == SDVO_MODE_TOKEN) st = run_token(&r, ap, &out, ro);
             else if (mode == SDVO_MODE_BLOCK) st = run_block(&r, ap, &out, ro);
+            else if (mode == SDVO_MODE_KSEQ) st = run_kseq(&r, ap, &out, ro);
             else st = run_multidraft(&r, ap, &out, ro);
             if (st) { /* the decision ended at a leaf with an unusable row */
                 out.tau = out.kstar = 0;

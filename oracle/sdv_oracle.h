@@ -38,7 +38,7 @@ extern "C" {
 #define SDVO_MAX_L 16
 
 enum { SDVO_F32 = 0, SDVO_BF16 = 1 };
-enum { SDVO_MODE_TOKEN = 0, SDVO_MODE_GREEDY = 1, SDVO_MODE_BLOCK = 2, SDVO_MODE_MULTIDRAFT = 3 };
+enum { SDVO_MODE_TOKEN = 0, SDVO_MODE_GREEDY = 1, SDVO_MODE_BLOCK = 2, SDVO_MODE_MULTIDRAFT = 3, SDVO_MODE_KSEQ = 4 };
 enum { SDVO_OK = 0, SDVO_ERR_INVALID = 1, SDVO_ERR_UNSUPPORTED = 2, SDVO_ERR_NOMEM = 3 };
 /* per-request data status bits (same meaning as the CUDA library's) */
 enum { SDVO_REQ_BAD_LENGTH = 1, SDVO_REQ_BAD_TOKEN = 2, SDVO_REQ_NONFINITE = 4 };
