@@ -314,7 +314,8 @@ MUTANTS = {
                           "h[i] = S / (S + 1.0);"),
     "gbv_residual_without_p": ("r->R[x] = fmax(p[tau] * r->P[x] - r->Q[x], 0.0);",
                                "r->R[x] = fmax(r->P[x] - r->Q[x], 0.0);"),
-    "correction_from_target": ("w = S > 0.0 ? r->R : r->P;", "w = r->P;"),
+    "correction_from_target": ("S = eval_node(r, ej, eo, p);\n        w = S > 0.0 ? r->R : r->P;",
+                               "S = eval_node(r, ej, eo, p);\n        w = r->P;"),
     "leaf_bonus_from_stale_residual": ("S = p;\n        w = r->P;", "S = p;\n        w = r->R;"),
     "no_trie_merge": ("o = k2;\n                    break;", "break;"),
     "merge_only_at_root": ("for (int k2 = 0; k2 < k; ++k2) {", "for (int k2 = 0; k2 < k && j == 0; ++k2) {"),
