@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["multidraft", "token"], default="multidraft")
+    ap.add_argument("--mode", choices=["multidraft", "token", "kseq"], default="multidraft")
     ap.add_argument("--workload", default=None, help="workload name (default: the mixed B=256 batch)")
     ap.add_argument("--B", type=int, default=None, help="override the batch size (profiling runs)")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -362,18 +362,23 @@ def run_ours(args, world, rank, local):
             "clocks": clk}
 
     if not args.no_extras:
-        # the token-level rule on the same batch
-        other = "token" if args.mode == "multidraft" else "multidraft"
-        out2 = binding.Outputs(other, batch.B, batch.K, batch.L, batch.V, dev)
-        call2 = make_call(other, out2)
-        for _ in range(max(2, args.warmup // 2)):
-            call2()
-        t2, r2 = time_calls(call2, args.steps, stream, prof=True)
-        t2 = max_over_ranks(t2, world)
-        r2 = max_over_ranks(r2, world)
-        line["modes"] = {other: {"value": all_positions / (t2 / args.steps / 1000.0), "unit": UNIT,
-                                 "ms_per_step": t2 / args.steps,
-                                 "algorithmic_gbs": alg_bytes / (r2 / args.steps / 1000.0) / 1e9}}
+        # the other rules on the same batch: token-level (per-position
+        # recursive rejection sampling) and SpecTr's K-SEQ, whose search
+        # for rho SpecTr-GBV avoids (the pages' "verification overhead")
+        line["modes"] = {}
+        for other in [m for m in ("multidraft", "token", "kseq") if m != args.mode]:
+            out2 = binding.Outputs(other, batch.B, batch.K, batch.L, batch.V, dev)
+            call2 = make_call(other, out2)
+            for _ in range(max(2, args.warmup // 2)):
+                call2()
+            t2, r2 = time_calls(call2, args.steps, stream, prof=True)
+            t2 = max_over_ranks(t2, world)
+            r2 = max_over_ranks(r2, world)
+            line["modes"][other] = {"value": all_positions / (t2 / args.steps / 1000.0), "unit": UNIT,
+                                    "ms_per_step": t2 / args.steps,
+                                    "node_kernel_ms_per_step": r2 / args.steps,
+                                    "algorithmic_gbs": alg_bytes / (r2 / args.steps / 1000.0) / 1e9}
+            del out2
         # end to end through the C-ABI with host buffers: H2D of every input,
         # the call, D2H of the per-request results
         names = ["target", "draft", "tokens", "lengths", "accept_u", "sample_u"]

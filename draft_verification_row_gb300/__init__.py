@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     verify,
     verify_block,
     verify_greedy,
+    verify_kseq,
     verify_multidraft,
     verify_token,
     workspace_bytes,

@@ -7,9 +7,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsdv.so")
 
-MODES = {"token": 0, "greedy": 1, "block": 2, "multidraft": 3}
+MODES = {"token": 0, "greedy": 1, "block": 2, "multidraft": 3, "kseq": 4}
 _ENTRY = {"token": "sdv_verify_token", "greedy": "sdv_verify_greedy",
-          "block": "sdv_verify_block", "multidraft": "sdv_verify_multidraft"}
+          "block": "sdv_verify_block", "multidraft": "sdv_verify_multidraft", "kseq": "sdv_verify_kseq"}
 SDV_F32, SDV_BF16 = 0, 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "timeout",
           5: "workspace"}
@@ -175,6 +175,10 @@ def verify_block(*args, **kw):
 
 def verify_multidraft(*args, **kw):
     return verify("multidraft", *args, **kw)
+
+
+def verify_kseq(*args, **kw):
+    return verify("kseq", *args, **kw)
 
 
 def sample_rows(logits, n_samples, u, temperature, *, V=None, tokens=None, device_status=None, stream=None):

@@ -24,7 +24,7 @@ bool sizes_ok(int B, int K, int L, int V)
 size_t workspace_size(int B, int K, int L)
 {
     const size_t n = slot_count(B, K, L);
-    return 6 * align_up(n * 4) + align_up(n * 5 * 4) + align_up(n) + align_up((size_t)B * 4) +
+    return 6 * align_up(n * 4) + align_up(n * 6 * 4) + align_up(n) + align_up((size_t)B * 4) +
            align_up((size_t)(L + 1) * B * K * 4) + align_up((size_t)(2 * L + 3) * 4);
 }
 
@@ -42,7 +42,7 @@ Workspace carve(void* base, int B, int K, int L)
     w.pbar = reinterpret_cast<float*>(p);
     p += align_up(n * 4);
     w.prm = reinterpret_cast<float*>(p);
-    p += align_up(n * 5 * 4);
+    p += align_up(n * 6 * 4);
     w.xs = reinterpret_cast<int*>(p);
     p += align_up(n * 4);
     w.am = reinterpret_cast<int*>(p);
@@ -186,10 +186,11 @@ int sdv_verify_token(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_TOKEN); }
 int sdv_verify_greedy(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_GREEDY); }
 int sdv_verify_block(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_BLOCK); }
 int sdv_verify_multidraft(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_MULTIDRAFT); }
+int sdv_verify_kseq(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_KSEQ); }
 
 size_t sdv_workspace_bytes(int mode, int B, int K, int L, int V)
 {
-    if (mode < SDV_MODE_TOKEN || mode > SDV_MODE_MULTIDRAFT || !sdv::sizes_ok(B, K, L, V)) return 0;
+    if (mode < SDV_MODE_TOKEN || mode > SDV_MODE_KSEQ || !sdv::sizes_ok(B, K, L, V)) return 0;
     if (mode == SDV_MODE_BLOCK && K != 1) return 0;
     return sdv::workspace_size(B, K, L);
 }

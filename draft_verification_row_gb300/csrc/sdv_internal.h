@@ -22,8 +22,9 @@ struct Workspace {
     float* S;              // node residual mass S_n
     float* pbar;           // node weight complement 1 - p_v, written by the parent's draw
                            //   (below 0 until then: the child's flag)
-    float* prm;            // node residual for the correction draw: [slot][5] =
-                           //   -(M_T c), -(M_D c), aT = p / Z_T, aD / aT, R_n(x*)
+    float* prm;            // node residual for the correction draw: [slot][6] =
+                           //   -(M_T c), -(M_D c), aT = p / Z_T, aD / aT, R_n(x*), floor
+                           //   (the residual is aT max(e_T - (aD/aT) e_D, floor e_T))
     int* xs;               // node shared dominant token x* (or -1)
     int* am;               // node argmax (greedy)
     unsigned char* owner;  // lowest draft sharing draft k's first j tokens

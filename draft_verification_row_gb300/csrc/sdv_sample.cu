@@ -47,6 +47,7 @@ struct Dist {
     float c;           // log2(e) / T (0: argmax)
     int residual;      // 0: softmax(row / T); 1: aT max(e_T - rD e_D, 0), x* apart
     float negT, negD, aT, rD, Rs;  // residual: references -(M c), scale, ratio, mass at x*
+    float cT;                      // residual: floor, aT cT e_T (0 for SpecTr-GBV; K-SEQ's 1 - gamma/rho)
     int xs;                        // residual: x*, or -1
     float M, negM;                 // softmax, after the pass: row maximum, -(M c)
 };
@@ -79,7 +80,8 @@ __device__ __forceinline__ void masses_of(const Dist& d, const uint4& tu, const 
     }
 #pragma unroll
     for (int e = 0; e < EPU; ++e) {
-        const float r = fmaxf(fmaf(-d.rD, ex2(fmaf(q[e], d.c, d.negD)), ex2(fmaf(t[e], d.c, d.negT))), 0.f);
+        const float eT = ex2(fmaf(t[e], d.c, d.negT));
+        const float r = fmaxf(fmaf(-d.rD, ex2(fmaf(q[e], d.c, d.negD)), eT), d.cT * eT);
         w[e] = ug * EPU + e == d.xs ? d.Rs : d.aT * r;
     }
 }
@@ -346,6 +348,7 @@ __global__ void __launch_bounds__(kRT, 2) sample_rows_kernel(SampleArgs a)
     d.c = a.c;
     d.residual = 0;
     d.xs = -1;
+    d.cT = 0.f;
     softmax_pass<DT>(d.rowT, V, a.c, greedy, sm, lane, w);
     __syncthreads();
     float M;
@@ -404,7 +407,8 @@ __device__ void decide_request(const Problem& pb, int b, bool greedy, DecideSmem
     }
     const int Lb = pb.lengths ? pb.lengths[b] : L;
     const size_t s0 = (size_t)b * (L + 1) * K;
-    const bool token = pb.mode == SDV_MODE_TOKEN;
+    // the token walk: per-position rules (token-level sampling and K-SEQ)
+    const bool token = pb.mode == SDV_MODE_TOKEN || pb.mode == SDV_MODE_KSEQ;
     unsigned char* own = s.own;
     float* val = s.val;
     float* uu = s.u;
@@ -577,13 +581,15 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy)
     d.c = pb.c;
     d.residual = !leaf && pb.ws.S[slot] > 0.f;
     d.xs = -1;
+    d.cT = 0.f;
     if (d.residual) {
-        const float* prm = pb.ws.prm + slot * 5;
+        const float* prm = pb.ws.prm + slot * 6;
         d.negT = prm[0];
         d.negD = prm[1];
         d.aT = prm[2];
         d.rD = prm[3];
         d.Rs = prm[4];
+        d.cT = prm[5];
         d.xs = pb.ws.xs[slot];
         residual_pass<DT>(d, V, sm, lane, w);
         __syncthreads();

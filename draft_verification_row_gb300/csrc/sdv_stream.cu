@@ -44,6 +44,7 @@ constexpr int kStages = 3;               // 3 x 24 KB in flight per CTA
 constexpr int kStash = 1;                // set-aside chunks a lane can hold (at most 2: d0, d1)
 static_assert(kStash >= 1 && kStash <= 2, "a lane keeps at most two set-aside chunk indices");
 constexpr int kQ = 4;                    // node descriptor queue depth
+constexpr int kKseqRounds = 10;          // K-SEQ: search passes of a node with two draws or more
 
 __device__ __forceinline__ void cbar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory"); }
 
@@ -103,7 +104,7 @@ struct StreamSmem {
     uint64_t qfull[kQ], qempty[kQ];
     NodeDesc qd[kQ];
     NodeDesc cur;                    // the consumers' copy of the current node
-    float redf[4][kSW];
+    float redf[5][kSW];
     int redi[4][kSW];
     int firstT, firstD;              // lowest index of each row's maximum
     uint4 stash[2][kCT][kStash][kUPT];  // set-aside units: [row][consumer thread][slot][unit]
@@ -113,6 +114,10 @@ struct StreamSmem {
     int uT, uD;
     float S, D, cbar, pbar, Pbs, Qbs, Rs, Ts, Rj, aT, aD, rD;
     int xs, bad;
+    // K-SEQ search (consumer thread 0): bracket [klo, khi] of rho, beta at
+    // khi, this pass's points and their factors Z_D / (Z_T rho)
+    float klo, khi, kbhi, krho[5], kf[5];
+    int kdone, knp;
 };
 
 // Online statistics of one row, per thread, in a reference shared by the
@@ -407,6 +412,60 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
     return aT * tot;
 }
 
+// One K-SEQ search pass over a node's rows (from the ring): this thread's
+// shares of Z_D beta(rho_k) = sum_x min(e_D(x), e_T(x) Z_D / (Z_T rho_k)),
+// f[k] = Z_D / (Z_T rho_k), for NP points at once.  `back`: the chunks come
+// last to first (the copy warp's order).
+template <int DT, int NP>
+__device__ __forceinline__ void kseq_sweep(StreamSmem* sm, uint32_t& g, bool& timed_out, int nc, int n_units, int V,
+                                           float c, float gnegT, float gnegD, const float (&f)[5], float (&acc)[5],
+                                           int cw, int lane, bool back)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+#pragma unroll
+    for (int k = 0; k < 5; ++k) acc[k] = 0.f;
+#pragma unroll 1
+    for (int it = 0; it < nc; ++it, ++g) {
+        const int ch = back ? nc - 1 - it : it;
+        const int s = g % kStages;
+        if (!timed_out && !mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
+        const bool tail = ch == nc - 1;
+#pragma unroll
+        for (int i = 0; i < kUPT; ++i) {
+            const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
+            if (!tail || ug < n_units) {
+                float t[EPU], d[EPU];
+                unpack_masked<DT>(sm->ring[s][0][ul], ug * EPU, V, t);
+                unpack_masked<DT>(sm->ring[s][1][ul], ug * EPU, V, d);
+                float u[NP];
+#pragma unroll
+                for (int k = 0; k < NP; ++k) u[k] = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPU; ++e) {
+                    const float eT = ex2(fmaf(t[e], c, gnegT)), eD = ex2(fmaf(d[e], c, gnegD));
+#pragma unroll
+                    for (int k = 0; k < NP; ++k) u[k] += fminf(eD, eT * f[k]);
+                }
+#pragma unroll
+                for (int k = 0; k < NP; ++k) acc[k] += u[k];
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->empty[s]);
+    }
+}
+
+// K-SEQ's gamma = (1 - (1 - beta)^n) / beta (n when beta = 0) over n
+// candidates, a rho qualifying when gamma(beta(rho)) <= rho.  The power is
+// taken as -expm1(n log1p(-beta)): the same value without the
+// cancellation of the plain form, which at small beta (nearly disjoint P
+// and Q) costs fp32 several digits of gamma and turns the search.
+__device__ __forceinline__ float kseq_gamma(float beta, int n)
+{
+    beta = fminf(fmaxf(beta, 0.f), 1.f);
+    return beta > 0.f ? -expm1f((float)n * log1pf(-beta)) / beta : (float)n;
+}
+
 // Combine the consumers' online statistics of both rows (all consumer
 // threads call it; results in shared memory from consumer thread 0): row
 // maximum M, reference -(M c), Z_rest (the sum below M), the count n of
@@ -505,7 +564,9 @@ __device__ __forceinline__ ProbS prob_s(const StreamSmem* sm, bool is_t, int x, 
     return o;
 }
 
-template <int DT>
+// KSEQ: the K-SEQ rule's search passes instead of the residual sweeps (a
+// separate instantiation, so that the other rules' code is not affected)
+template <int DT, bool KSEQ>
 __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem pb)
 {
     using E = Elem<DT>;
@@ -630,7 +691,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                              (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
             const char* gD = static_cast<const char*>(pb.draft) +
                              (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
-            const int passes = 1 + nd;
+            const int passes = 1 + (KSEQ ? (nd > 1 ? kKseqRounds : 1) : nd);
             bool ok = true;
             for (int ps = 0; ps < passes && ok; ++ps) {
                 // keep the rows in L2 until the node's last pass over them
@@ -701,7 +762,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
             }
             // the node weight, written by the parent (below 0 until then)
             float pbar = 0.f;
-            if (j > 0 && pb.mode != SDV_MODE_TOKEN) {
+            if (!KSEQ && j > 0 && pb.mode != SDV_MODE_TOKEN) {
                 const float* f = pb.ws.pbar + slot;
                 pbar = ld_relaxed(f);
                 if (!(pbar >= 0.f)) {
@@ -724,6 +785,20 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
             sm->S = 1.f - pbar;
             sm->D = 1.f;
             sm->cbar = 0.f;
+            if constexpr (KSEQ) {
+                // the first pass tests rho = 1, the first round's quarter
+                // points of [1, n], and n (a node with one draw: rho = 1)
+                const float n = (float)nd;
+                sm->klo = 1.f;
+                sm->khi = n;
+                sm->kdone = nd == 1;
+                sm->knp = nd == 1 ? 1 : 5;
+                for (int t = 0; t < 5; ++t) {
+                    const float rho = t == 0 ? 1.f : (t == 4 ? n : 1.f + (n - 1.f) * (float)t / 4.f);
+                    sm->krho[t] = rho;
+                    sm->kf[t] = sm->zD / (sm->zT * rho);
+                }
+            }
         }
         cbar_sync();
         const float pbar = sm->pbar, p = 1.f - pbar;
@@ -740,89 +815,184 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
         //   R_1(x*) = Qbs - Pbs - pbar + pbar Pbs,
         //   R_j(x*) = R_{j-1}(x*) Qbs - (pbar + T_{j-1}) (1 - Qbs),
         // with T_{j-1} the sweep's sum over the other tokens.
-        for (int di = 0; di < nd; ++di) {
-            const int k2 = sm->cur.dk[di];
-            const bool first_draw = di == 0;
-            if (ct == 0) {
-                const int y = sm->cur.y[di];
-                const float D = sm->D;
-                const float cnew = first_draw ? 0.f : sm->cbar + D;
-                const float Pbs = sm->Pbs, Qbs = sm->Qbs;
-                const float Rj = first_draw ? ((Qbs - Pbs) - pbar) + pbar * Pbs
-                                            : sm->Rs * Qbs - (pbar + sm->Ts) * (1.f - Qbs);
-                sm->Rj = Rj;
-                float R, Qy, abar_num;
-                if (y == xs) {
-                    Qy = 1.f - Qbs;
-                    R = first_draw ? (1.f - pbar) * (1.f - Pbs) : sm->Rs;
-                    abar_num = fmaxf(-Rj, 0.f);
-                } else {
-                    const ProbS Py = prob_s(sm, true, y, sm->cur.gT[di], c);
-                    const ProbS Qp = prob_s(sm, false, y, sm->cur.gD[di], c);
-                    Qy = Qp.P;
-                    R = first_draw ? p * Py.P : fmaxf((1.f - pbar) * Py.P - (1.f + sm->cbar) * Qp.P, 0.f);
-                    abar_num = fmaxf((1.f + cnew) * Qp.P - (1.f - pbar) * Py.P, 0.f);
+        if constexpr (!KSEQ) {
+            for (int di = 0; di < nd; ++di) {
+                const int k2 = sm->cur.dk[di];
+                const bool first_draw = di == 0;
+                if (ct == 0) {
+                    const int y = sm->cur.y[di];
+                    const float D = sm->D;
+                    const float cnew = first_draw ? 0.f : sm->cbar + D;
+                    const float Pbs = sm->Pbs, Qbs = sm->Qbs;
+                    const float Rj = first_draw ? ((Qbs - Pbs) - pbar) + pbar * Pbs
+                                                : sm->Rs * Qbs - (pbar + sm->Ts) * (1.f - Qbs);
+                    sm->Rj = Rj;
+                    float R, Qy, abar_num;
+                    if (y == xs) {
+                        Qy = 1.f - Qbs;
+                        R = first_draw ? (1.f - pbar) * (1.f - Pbs) : sm->Rs;
+                        abar_num = fmaxf(-Rj, 0.f);
+                    } else {
+                        const ProbS Py = prob_s(sm, true, y, sm->cur.gT[di], c);
+                        const ProbS Qp = prob_s(sm, false, y, sm->cur.gD[di], c);
+                        Qy = Qp.P;
+                        R = first_draw ? p * Py.P : fmaxf((1.f - pbar) * Py.P - (1.f + sm->cbar) * Qp.P, 0.f);
+                        abar_num = fmaxf((1.f + cnew) * Qp.P - (1.f - pbar) * Py.P, 0.f);
+                    }
+                    float a, abar;
+                    const float ratio = (D > 0.f && Qy > 0.f) ? (R / D) / Qy : INFINITY;
+                    if (ratio >= 1.f) {
+                        a = 1.f;
+                        abar = 0.f;
+                    } else if (!(R > 0.f)) {
+                        a = 0.f;
+                        abar = 1.f;
+                    } else {
+                        a = ratio;
+                        abar = fminf((abar_num / D) / Qy, 1.f);
+                    }
+                    sm->cbar = cnew;
+                    pb.ws.a[sbase + k2] = a;
+                    bool first_of_token = true;  // this draw's child is new: it owns it
+                    for (int e = 0; e < di; ++e) first_of_token &= sm->cur.y[e] != y;
+                    if (pb.mode != SDV_MODE_TOKEN) {
+                        const size_t sc = sbase + K + k2;
+                        // child first reached by this draw: its weight (never NaN:
+                        // the child waits for a value of 0 or more)
+                        if (first_of_token) st_relaxed(&pb.ws.pbar[sc], fmaxf(abar, 0.f));
+                    }
+                    sm->aT = p / sm->zT;
+                    sm->aD = (1.f + cnew) / sm->zD;
+                    sm->rD = sm->aT > 0.f ? sm->aD / sm->aT : 3.402823466e38f;
                 }
-                float a, abar;
-                const float ratio = (D > 0.f && Qy > 0.f) ? (R / D) / Qy : INFINITY;
-                if (ratio >= 1.f) {
-                    a = 1.f;
-                    abar = 0.f;
-                } else if (!(R > 0.f)) {
-                    a = 0.f;
-                    abar = 1.f;
-                } else {
-                    a = ratio;
-                    abar = fminf((abar_num / D) / Qy, 1.f);
+                cbar_sync();
+                // sweep di is pass di + 1 of the node: backward for even di
+                float tot = sweep<DT>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, sm->aT, sm->rD, xs, cw, lane,
+                                      (di & 1) == 0);
+                tot = warp_sum(tot);
+                if (lane == 0) sm->redf[2][cw] = tot;
+                cbar_sync();
+                if (ct == 0) {
+                    float Sj = 0.f;
+                    for (int i = 0; i < kSW; ++i) Sj += sm->redf[2][i];
+                    if (xs >= 0) {  // the sweeps left x* out: their sum is the mass elsewhere
+                        const float Rs = fmaxf(sm->Rj, 0.f);
+                        sm->Ts = Sj;
+                        sm->Rs = Rs;
+                        Sj += Rs;
+                    }
+                    sm->S = fmaxf(Sj, 0.f);
+                    sm->D = pbar + sm->S;
                 }
-                sm->cbar = cnew;
-                pb.ws.a[sbase + k2] = a;
-                bool first_of_token = true;  // this draw's child is new: it owns it
-                for (int e = 0; e < di; ++e) first_of_token &= sm->cur.y[e] != y;
-                if (pb.mode != SDV_MODE_TOKEN) {
-                    const size_t sc = sbase + K + k2;
-                    // child first reached by this draw: its weight (never NaN:
-                    // the child waits for a value of 0 or more)
-                    if (first_of_token) st_relaxed(&pb.ws.pbar[sc], fmaxf(abar, 0.f));
-                }
-                sm->aT = p / sm->zT;
-                sm->aD = (1.f + cnew) / sm->zD;
-                sm->rD = sm->aT > 0.f ? sm->aD / sm->aT : 3.402823466e38f;
             }
-            cbar_sync();
-            // sweep di is pass di + 1 of the node: backward for even di
-            float tot = sweep<DT>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, sm->aT, sm->rD, xs, cw, lane,
-                                  (di & 1) == 0);
-            tot = warp_sum(tot);
-            if (lane == 0) sm->redf[2][cw] = tot;
-            cbar_sync();
             if (ct == 0) {
-                float Sj = 0.f;
-                for (int i = 0; i < kSW; ++i) Sj += sm->redf[2][i];
-                if (xs >= 0) {  // the sweeps left x* out: their sum is the mass elsewhere
-                    const float Rs = fmaxf(sm->Rj, 0.f);
-                    sm->Ts = Sj;
-                    sm->Rs = Rs;
-                    Sj += Rs;
-                }
-                sm->S = fmaxf(Sj, 0.f);
-                sm->D = pbar + sm->S;
+                // the node's block acceptance and, for the correction draw
+                // should the decision end here, its final residual
+                // R_n = aT max(e_T - (aD / aT) e_D, 0) with R_n(x*) apart
+                const float S = sm->S, D = sm->D;
+                pb.ws.h[slot] = D > 0.f ? S / D : 1.f;
+                pb.ws.S[slot] = S;
+                float* prm = pb.ws.prm + (size_t)slot * 6;
+                prm[0] = gnegT;
+                prm[1] = gnegD;
+                prm[2] = sm->aT;
+                prm[3] = sm->rD;
+                prm[4] = sm->Rs;
+                prm[5] = 0.f;
+                pb.ws.xs[slot] = xs;
             }
-        }
-        if (ct == 0) {
-            // the node's block acceptance and, for the correction draw
-            // should the decision end here, its final residual
-            // R_n = aT max(e_T - (aD / aT) e_D, 0) with R_n(x*) apart
-            const float S = sm->S, D = sm->D;
-            pb.ws.h[slot] = D > 0.f ? S / D : 1.f;
-            pb.ws.S[slot] = S;
-            float* prm = pb.ws.prm + (size_t)slot * 5;
-            prm[0] = gnegT;
-            prm[1] = gnegD;
-            prm[2] = sm->aT;
-            prm[3] = sm->rD;
-            prm[4] = sm->Rs;
-            pb.ws.xs[slot] = xs;
+        } else {
+            // ---- K-SEQ: the search for rho, one pass per round ----
+            // beta(rho) = sum_x min(Q(x), P(x) / rho); a rho qualifies when
+            // gamma(beta(rho)) <= rho.  rho = 1 if it qualifies, else each
+            // round keeps the quarter of [lo, hi] ending at the first of its
+            // three points that qualifies (the last quarter if none does);
+            // rho is the final hi.
+            const int rounds = nd > 1 ? kKseqRounds : 1;
+            for (int r = 0; r < rounds; ++r) {
+                float f[5], acc[5];
+#pragma unroll
+                for (int k = 0; k < 5; ++k) f[k] = sm->kf[k];
+                const int np = sm->knp;
+                const bool back = (r & 1) == 0;  // pass r + 1 of the node
+                if (np == 5)
+                    kseq_sweep<DT, 5>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, f, acc, cw, lane, back);
+                else if (np == 3)
+                    kseq_sweep<DT, 3>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, f, acc, cw, lane, back);
+                else
+                    kseq_sweep<DT, 1>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, f, acc, cw, lane, back);
+#pragma unroll
+                for (int k = 0; k < 5; ++k) {
+                    const float v = warp_sum(acc[k]);
+                    if (lane == 0) sm->redf[k][cw] = v;
+                }
+                cbar_sync();
+                if (ct == 0) {
+                    float beta[5];
+                    for (int k = 0; k < np; ++k) {
+                        float z = 0.f;
+                        for (int i = 0; i < kSW; ++i) z += sm->redf[k][i];
+                        beta[k] = z / sm->zD;
+                    }
+                    // the round's three points are beta[first .. first + 2]
+                    int first = 0;
+                    if (r == 0) {
+                        if (nd == 1 || kseq_gamma(beta[0], nd) <= 1.f) {
+                            sm->kdone = 1;
+                            sm->khi = 1.f;
+                            sm->kbhi = beta[0];
+                        } else {
+                            sm->kbhi = beta[4];  // beta at hi = n
+                        }
+                        first = 1;
+                    }
+                    if (!sm->kdone) {
+                        const float lo = sm->klo;
+                        int i = 0;
+                        while (i < 3 && !(kseq_gamma(beta[first + i], nd) <= sm->krho[first + i])) ++i;
+                        if (i < 3) {
+                            sm->klo = i == 0 ? lo : sm->krho[first + i - 1];
+                            sm->khi = sm->krho[first + i];
+                            sm->kbhi = beta[first + i];
+                        } else {
+                            sm->klo = sm->krho[first + 2];
+                        }
+                        // the next round's points
+                        const float l = sm->klo, h = sm->khi;
+                        for (int t = 0; t < 3; ++t) {
+                            const float rho = l + (h - l) * (float)(t + 1) / 4.f;
+                            sm->krho[t] = rho;
+                            sm->kf[t] = sm->zD / (sm->zT * rho);
+                        }
+                    }
+                    sm->knp = 3;
+                }
+                cbar_sync();
+            }
+            if (ct == 0) {
+                // acceptance of each draw, and the residual for the correction
+                // draw should the decision end here:
+                // P - gamma min(Q, P / rho) = (1/Z_T) max(e_T - gamma (Z_T/Z_D) e_D, (1 - gamma/rho) e_T)
+                const float rho = sm->khi, beta = fminf(fmaxf(sm->kbhi, 0.f), 1.f);
+                const float gam = kseq_gamma(beta, nd);
+                for (int di = 0; di < nd; ++di) {
+                    const int y = sm->cur.y[di];
+                    const float Py = prob_s(sm, true, y, sm->cur.gT[di], c).P;
+                    const float Qy = prob_s(sm, false, y, sm->cur.gD[di], c).P;
+                    const float den = rho * Qy;
+                    pb.ws.a[sbase + sm->cur.dk[di]] = den > 0.f ? fminf(Py / den, 1.f) : 1.f;
+                }
+                pb.ws.h[slot] = 0.f;
+                pb.ws.S[slot] = expf((float)nd * log1pf(-beta));  // the residual's mass, (1 - beta)^n
+                float* prm = pb.ws.prm + (size_t)slot * 6;
+                prm[0] = gnegT;
+                prm[1] = gnegD;
+                prm[2] = 1.f / sm->zT;
+                prm[3] = gam * sm->zT / sm->zD;
+                prm[4] = 0.f;
+                prm[5] = fmaxf(1.f - gam / rho, 0.f);
+                pb.ws.xs[slot] = -1;
+            }
         }
         // a timed-out wait anywhere stops every consumer together (the
         // decision is read after the node's last barrier, so it is uniform)
@@ -851,18 +1021,29 @@ cudaError_t launch_stream(const Problem& pb, cudaStream_t st)
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     if (sms <= 0) sms = 1;
-    const void* fn = pb.dtype == SDV_BF16 ? reinterpret_cast<const void*>(stream_kernel<SDV_BF16>)
-                                          : reinterpret_cast<const void*>(stream_kernel<SDV_F32>);
+    const bool kseq = pb.mode == SDV_MODE_KSEQ;
+    const void* fn = pb.dtype == SDV_BF16
+                         ? (kseq ? reinterpret_cast<const void*>(stream_kernel<SDV_BF16, true>)
+                                 : reinterpret_cast<const void*>(stream_kernel<SDV_BF16, false>))
+                         : (kseq ? reinterpret_cast<const void*>(stream_kernel<SDV_F32, true>)
+                                 : reinterpret_cast<const void*>(stream_kernel<SDV_F32, false>));
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StreamSmem));
     if (e != cudaSuccess) return e;
     // inner nodes: the root and at most one per draft at depths 1..L-1
     if (pb.L == 0) return cudaSuccess;
     const long long upper = (long long)pb.B * (1 + (long long)pb.K * (pb.L - 1));
     const int grid = (int)std::max(1LL, std::min((long long)sms * kCtasPerSm, upper));
-    if (pb.dtype == SDV_BF16)
-        stream_kernel<SDV_BF16><<<grid, kSThreads, sizeof(StreamSmem), st>>>(pb);
-    else
-        stream_kernel<SDV_F32><<<grid, kSThreads, sizeof(StreamSmem), st>>>(pb);
+    if (pb.dtype == SDV_BF16) {
+        if (kseq)
+            stream_kernel<SDV_BF16, true><<<grid, kSThreads, sizeof(StreamSmem), st>>>(pb);
+        else
+            stream_kernel<SDV_BF16, false><<<grid, kSThreads, sizeof(StreamSmem), st>>>(pb);
+    } else {
+        if (kseq)
+            stream_kernel<SDV_F32, true><<<grid, kSThreads, sizeof(StreamSmem), st>>>(pb);
+        else
+            stream_kernel<SDV_F32, false><<<grid, kSThreads, sizeof(StreamSmem), st>>>(pb);
+    }
     return cudaGetLastError();
 }
 

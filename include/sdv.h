@@ -93,7 +93,7 @@ extern "C" {
 enum { SDV_F32 = 0, SDV_BF16 = 1 };
 
 /* modes, for sdv_workspace_bytes */
-enum { SDV_MODE_TOKEN = 0, SDV_MODE_GREEDY = 1, SDV_MODE_BLOCK = 2, SDV_MODE_MULTIDRAFT = 3 };
+enum { SDV_MODE_TOKEN = 0, SDV_MODE_GREEDY = 1, SDV_MODE_BLOCK = 2, SDV_MODE_MULTIDRAFT = 3, SDV_MODE_KSEQ = 4 };
 
 /* return codes */
 enum {
@@ -174,6 +174,25 @@ int sdv_verify_block(SDV_VERIFY_ARGS);
 
 /* SpecTr-GBV multi-draft block verification. */
 int sdv_verify_multidraft(SDV_VERIFY_ARGS);
+
+/* SpecTr's K-SEQ, per position: the rule SpecTr-GBV is compared with, and
+ * whose search for a scaling factor rho it avoids (SpecTr-GBV page, sections
+ * 3-4; the rule follows SpecTr's published definition).  At a node with n
+ * drafts through it (i.i.d. candidates from Q):
+ *   beta(rho) = sum_x min(Q(x), P(x) / rho),
+ *   gamma(rho) = (1 - (1 - beta)^n) / beta   (n when beta = 0);
+ * candidate i (index order) is accepted iff accept_u[b][k_i][depth] <=
+ * min(1, P(y_i) / (rho Q(y_i))), the first accepted moves to its child
+ * (as in sdv_verify_token); when all are rejected the correction is drawn
+ * from P - gamma min(Q, P / rho) (P where that has no mass).  rho: 1 if
+ * gamma(1) <= 1, else 10 rounds starting from [lo, hi] = [1, n], each
+ * testing lo + (hi - lo) i / 4 for i = 1, 2, 3 against gamma(rho) <= rho
+ * and keeping the quarter that ends at the first one that passes (the
+ * last quarter if none does); rho is the final hi.  Any such rho keeps the
+ * emitted token distributed as P.  accept_prob holds each draw's
+ * acceptance probability; residual_mass the end node's (1 - beta)^n.  The
+ * search costs one vocabulary pass per round. */
+int sdv_verify_kseq(SDV_VERIFY_ARGS);
 
 /* Workspace bytes a call of `mode` with these sizes needs (0 if the sizes
  * are invalid). */

@@ -485,7 +485,13 @@ static double kseq_beta(const req_t* r, double rho)
     return beta;
 }
 
-static double kseq_gamma(double beta, int n) { return beta > 0.0 ? (1.0 - pow(1.0 - beta, n)) / beta : (double)n; }
+/* gamma with 1 - (1 - beta)^n = -expm1(n log1p(-beta)): the same value,
+ * without the cancellation of the plain form when beta is small */
+static double kseq_gamma(double beta, int n)
+{
+    beta = fmin(fmax(beta, 0.0), 1.0);
+    return beta > 0.0 ? -expm1((double)n * log1p(-beta)) / beta : (double)n;
+}
 
 static int kseq_ok(const req_t* r, double rho, int n) { return kseq_gamma(kseq_beta(r, rho), n) <= rho; }
 

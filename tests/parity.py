@@ -5,8 +5,9 @@ oracle's, except where some decision on the oracle's path had a margin
 |u - threshold| (or distance of u to its CDF interval's ends) below 1e-5;
 such mismatches are counted and must stay at one per comparison or under
 1e-4 of all decisions, whichever is larger.
-accept_prob within 1e-5 absolute everywhere; residual_mass within 1e-5 where
-the end node agrees.  Requests the oracle marks invalid must come back
+accept_prob within 1e-5 absolute everywhere (1e-4 for K-SEQ, whose rho
+comes from a search; see TOL_KSEQ); residual_mass within 1e-5 where the
+end node agrees.  Requests the oracle marks invalid must come back
 invalid with the same status bit.
 """
 import numpy as np
@@ -17,6 +18,14 @@ import oracle
 
 TOL = 1e-5
 MARGIN = 1e-5
+# K-SEQ's acceptance probabilities min(1, P(y) / (rho Q(y))) carry rho from
+# a search whose test gamma(beta(rho)) <= rho is evaluated with an fp32
+# vocabulary sum on the GPU (relative error ~1e-6) and in fp64 by the
+# oracle.  Both test the same dyadic points, but near the crossing the two
+# can decide differently and end on opposite sides of it; rho then differs
+# by the width of that zone, about 1e-6 / |1 - d gamma / d rho|, which a
+# flat crossing widens.  The emitted token follows P for either rho.
+TOL_KSEQ = 1e-4
 
 
 def pad8(a):
@@ -46,6 +55,7 @@ def oracle_run(mode, batch, requests=None):
     prob = oracle.Problem(take(batch.target), take(batch.draft), take(batch.tokens), take(batch.lengths),
                           take(batch.accept_u), take(batch.sample_u), batch.temperature, V=batch.V)
     ref = oracle.verify(mode, prob, trace_cap=1 << 20)
+    ref["mode"] = mode
     ref["decisions"] = len(ref["trace"]) + len(idx)
     ref["requests"] = idx
     return ref
@@ -53,6 +63,7 @@ def oracle_run(mode, batch, requests=None):
 
 def compare(gpu, ref, what=""):
     idx = ref["requests"]
+    ap_tol = TOL_KSEQ if ref.get("mode") == "kseq" else TOL
     mism = 0
     status_or = 0
     for i, b in enumerate(idx):
@@ -74,7 +85,7 @@ def compare(gpu, ref, what=""):
             assert d <= TOL, f"{what} request {b}: residual_mass off by {d:.3g}"
         if gpu.get("accept_prob") is not None:
             d = np.max(np.abs(gpu["accept_prob"][b] - ref["accept_prob"][i]), initial=0.0)
-            assert d <= TOL, f"{what} request {b}: accept_prob off by {d:.3g}"
+            assert d <= ap_tol, f"{what} request {b}: accept_prob off by {d:.3g}"
     # a decision within 1e-5 of its threshold is decided by fp32 rounding
     # (the kernel's summation order): one such flip per comparison is
     # allowed, or 1e-4 of the decisions on large ones

@@ -61,7 +61,8 @@ SMALL = [
 @pytest.mark.parametrize("name,kw,T", SMALL)
 def test_small_parity(name, kw, T):
     batch = W.make(name, DEV, temperature=T, **kw)
-    for mode in _modes(batch):
+    # (K-SEQ at low temperature: test_kseq_low_temperature_rho_is_valid)
+    for mode in _modes(batch) + (["kseq"] if batch.temperature >= 0.4 else []):
         P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"{name}/{mode}")
 
 
@@ -69,13 +70,13 @@ def test_small_parity(name, kw, T):
 @pytest.mark.parametrize("V", [1, 2, 7, 8, 9, 33, 1000, 4097])
 def test_vocabulary_edges(dtype, V):
     batch = W.make("multidraft-B32-K4-L4-V32000-f32", DEV, B=4, K=3, L=3, V=V, dtype=dtype, temperature=0.9)
-    for mode in MODES_K:
+    for mode in MODES_K + ["kseq"]:
         P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"V={V}/{mode}")
 
 
 def test_max_drafts_and_length():
     batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=3, K=16, L=16, V=2053, temperature=1.5)
-    for mode in MODES_K:
+    for mode in MODES_K + ["kseq"]:
         P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch), f"K16L16/{mode}")
 
 
@@ -144,7 +145,7 @@ def test_leaf_rows_are_read_only_by_the_bonus_draw(name, K):
     batch = W.make(name, DEV, B=len(lengths), K=K, L=3, V=2003, lengths=lengths, temperature=0.8)
     batch.accept_u[:3] = 0.0
     batch.accept_u[3:] = 0.999
-    modes = ["token", "multidraft", "greedy"] if K > 1 else ["token", "block", "greedy"]
+    modes = ["token", "multidraft", "greedy", "kseq"] if K > 1 else ["token", "block", "greedy", "kseq"]
     clean = {mode: P.oracle_run(mode, batch) for mode in modes}
     for b, Lb in enumerate(lengths):
         for k in range(K):
@@ -256,6 +257,52 @@ FULL = [
     ("multidraft-B32-K4-L4-V32000-f32", [0.1, 0.4, 0.7], None),
     ("mixed-B256-K8-L8-V151936-bf16", [None], [0, 1, 37, 101, 190, 255]),
 ]
+
+
+def test_kseq_low_temperature_rho_is_valid():
+    """K-SEQ at T = 0.1.  Where P and Q are both nearly one-hot on the same
+    token, gamma(beta(rho)) - rho stays within ~1e-6 over a range of rho, so
+    an fp32 search and the oracle's fp64 search stop at different points of
+    that range.  Check instead that the GPU's rho, recovered from its
+    acceptance probabilities (a = P(y) / (rho Q(y)) when a < 1), qualifies
+    in fp64: gamma(beta(rho)) <= rho to within 1e-6 (the emitted token then
+    follows P up to that clamp)."""
+    batch = W.make("multidraft-B32-K4-L4-V32000-f32", DEV, B=6, V=3203, temperature=0.1)
+    gpu = P.gpu_run("kseq", batch)
+    assert int(gpu["device_status"][0]) == 0
+    T, V = batch.temperature, batch.V
+    checked = 0
+    for b in range(batch.B):
+        Lb = int(batch.lengths[b])
+        tok = batch.tokens[b].cpu().numpy()
+        for j in range(Lb):
+            for k in range(batch.K):
+                if any((tok[k2, :j] == tok[k, :j]).all() for k2 in range(k)):
+                    continue  # not the node's owner
+                n = sum(1 for k2 in range(batch.K) if (tok[k2, :j] == tok[k, :j]).all())
+                lt = batch.target[b, k, j, :V].double().cpu().numpy()
+                ld = batch.draft[b, k, j, :V].double().cpu().numpy()
+                Pd = np.exp((lt - lt.max()) / T); Pd /= Pd.sum()
+                Qd = np.exp((ld - ld.max()) / T); Qd /= Qd.sum()
+                y = int(tok[k, j])
+                a = float(gpu["accept_prob"][b, k, j])
+                if not (1e-6 < a < 1.0) or n == 1:
+                    continue
+                rho = Pd[y] / (a * Qd[y])
+                beta = np.minimum(Qd, Pd / rho).sum()
+                gamma = -np.expm1(n * np.log1p(-min(beta, 1.0))) / beta
+                assert 1.0 - 1e-6 <= rho <= n * (1 + 1e-6), (b, j, k, rho)
+                assert gamma <= rho + 1e-6, (b, j, k, rho, gamma - rho)
+                checked += 1
+    assert checked > 0
+
+
+def test_kseq_full_size_sampled():
+    """K-SEQ on the mixed batch at full size (the launch configuration the
+    bench times); the oracle checks two requests (its search costs 41
+    vocabulary passes per node)."""
+    batch = W.make(W.HEADLINE, DEV)
+    P.compare(P.gpu_run("kseq", batch), P.oracle_run("kseq", batch, [3, 200]), "mixed/kseq")
 
 
 @pytest.mark.parametrize("name,temps,sample", FULL)

@@ -111,7 +111,7 @@ MUTANTS = {
     "residual_without_gamma": ("fmax(r->P[x] - r->gam[j][o] * fmin(r->Q[x], r->P[x] / r->rho[j][o]), 0.0)",
                                "fmax(r->P[x] - fmin(r->Q[x], r->P[x] / r->rho[j][o]), 0.0)"),
     "accept_without_rho": ("double den = hi * r->Q[y];", "double den = r->Q[y];"),
-    "gamma_power_off_by_one": ("(1.0 - pow(1.0 - beta, n)) / beta", "(1.0 - pow(1.0 - beta, n + 1)) / beta"),
+    "gamma_power_off_by_one": ("-expm1((double)n * log1p(-beta)) / beta", "-expm1((double)(n + 1) * log1p(-beta)) / beta"),
     "rho_from_lower_end": ("    r->rho[j][o] = hi;", "    r->rho[j][o] = lo;"),
 }
 
