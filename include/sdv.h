@@ -6,8 +6,7 @@
  * returns per request the accepted prefix length tau, the index k* of the
  * draft whose prefix was accepted, and the correction (or bonus) token.
  *
- * The four entry points are the verification rules named on the source
- * pages:
+ * The verification entry points are the rules named on the source pages:
  *   sdv_verify_token       standard token-level speculative sampling;
  *                          with K > 1 drafts, per-position multi-draft
  *                          verification (recursive rejection sampling over
@@ -27,6 +26,9 @@
  *                          residual correction and target adjustment.
  *                          SpecTr-GBV page, section 2 (algorithmic
  *                          procedure, steps 1-5).
+ *   sdv_verify_kseq        SpecTr's K-SEQ per position, the rule whose
+ *                          search for a scaling factor SpecTr-GBV avoids
+ *                          (SpecTr-GBV page, sections 3-4); stated below.
  *
  * The pages print none of the formulas; the rules computed are:
  *   P_v = softmax(target_row / T), Q_v = softmax(draft_row / T) at a trie
