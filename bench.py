@@ -379,18 +379,24 @@ def run_ours(args, world, rank, local):
                                     "node_kernel_ms_per_step": r2 / args.steps,
                                     "algorithmic_gbs": alg_bytes / (r2 / args.steps / 1000.0) / 1e9}
             del out2
-        # end to end through the C-ABI with host buffers: H2D of every input,
-        # the call, D2H of the per-request results
+        # end to end through the C-ABI with host buffers: the host-to-device
+        # copy of the inputs (of the logits, the rows verification reads,
+        # sdv_copy_read_rows), the call, and the per-request results back
         names = ["target", "draft", "tokens", "lengths", "accept_u", "sample_u"]
+        small = ["tokens", "lengths", "accept_u", "sample_u"]
         host = {n: getattr(batch, n).cpu().pin_memory() for n in names}
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        rows_bytes = binding.read_rows_bytes(host["tokens"], host["lengths"], batch.V, batch.stride,
+                                             batch.target.dtype)
+        h2d = rows_bytes + sum(host[n].numel() * host[n].element_size() for n in small)
         res_host = [torch.empty(batch.B, dtype=torch.int32).pin_memory() for _ in range(3)]
         d2h = 3 * 4 * batch.B
         dev_in = {n: getattr(batch, n) for n in names}
 
         def e2e_step():
-            for n in names:
+            for n in small:
                 dev_in[n].copy_(host[n], non_blocking=True)
+            binding.copy_read_rows(host["target"], host["draft"], host["tokens"], host["lengths"], batch.target,
+                                   batch.draft, V=batch.V, stream=stream)
             call()
             res_host[0].copy_(out.accept_len, non_blocking=True)
             res_host[1].copy_(out.accept_draft, non_blocking=True)
@@ -402,7 +408,26 @@ def run_ours(args, world, rank, local):
         te = max_over_ranks(te, world)
         line["e2e"] = {"value": all_positions / (te / args.e2e_steps / 1000.0), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": te / args.e2e_steps}
+                       "ms_per_step": te / args.e2e_steps,
+                       "inputs": "pinned host tensors; of the logits, the rows verification reads are copied "
+                                 "(sdv_copy_read_rows)"}
+
+        # the same with the whole logit tensors copied
+        def e2e_full_step():
+            for n in names:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            call()
+            res_host[0].copy_(out.accept_len, non_blocking=True)
+            res_host[1].copy_(out.accept_draft, non_blocking=True)
+            res_host[2].copy_(out.out_token, non_blocking=True)
+
+        e2e_full_step()
+        torch.cuda.synchronize()
+        tf, _ = time_calls(e2e_full_step, args.e2e_steps, stream)
+        tf = max_over_ranks(tf, world)
+        line["e2e_whole_tensors"] = {"value": all_positions / (tf / args.e2e_steps / 1000.0), "unit": UNIT,
+                                     "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
+                                     "ms_per_step": tf / args.e2e_steps}
         del host
         # the next row of the path: draft-token sampling, one draw per draft
         # from each request's depth-0 draft rows (B*K rows of V logits)

@@ -11,8 +11,10 @@ compiled library every call raises.
 from .binding import (  # noqa: F401
     MODES,
     SDVError,
+    copy_read_rows,
     launch_shape,
     lib,
+    read_rows_bytes,
     sample_rows,
     set_profile_events,
     verify,

@@ -25,7 +25,8 @@ _VERIFY_ARGTYPES = [
 ]
 
 EXPORTS = list(_ENTRY.values()) + ["sdv_workspace_bytes", "sdv_status_string", "sdv_launch_shape",
-                                   "sdv_set_profile_events", "sdv_sample_rows"]
+                                   "sdv_set_profile_events", "sdv_sample_rows", "sdv_copy_read_rows",
+                                   "sdv_read_rows_bytes"]
 
 
 class SDVError(RuntimeError):
@@ -62,6 +63,12 @@ def lib(path: str = LIB_PATH):
     h.sdv_sample_rows.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_longlong, ctypes.c_int, ctypes.c_float,
                                   ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_void_p, ctypes.c_void_p]
+    h.sdv_copy_read_rows.restype = ctypes.c_int
+    h.sdv_copy_read_rows.argtypes = ([ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int] + [ctypes.c_void_p] * 7
+                                     + [ctypes.POINTER(ctypes.c_longlong)])
+    h.sdv_read_rows_bytes.restype = ctypes.c_int
+    h.sdv_read_rows_bytes.argtypes = ([ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int] + [ctypes.c_void_p] * 2
+                                      + [ctypes.POINTER(ctypes.c_longlong)])
     _lib = h
     return h
 
@@ -213,3 +220,41 @@ def sample_rows(logits, n_samples, u, temperature, *, V=None, tokens=None, devic
         raise SDVError(rc, "sdv_sample_rows")
     return tokens, device_status
 
+
+
+def _host_i32(t):
+    if t is None:
+        return None
+    if t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError("tokens and lengths must be contiguous int32 host tensors")
+    return t
+
+
+def read_rows_bytes(tokens, lengths, V, row_stride, dtype):
+    """Bytes of the rows verification reads (sdv_read_rows_bytes); tokens
+    [B][K][L] and lengths [B] are int32 host tensors."""
+    B, K, L = tokens.shape
+    out = ctypes.c_longlong(0)
+    rc = lib().sdv_read_rows_bytes(B, K, L, int(V), int(row_stride), SDV_BF16 if dtype == torch.bfloat16 else SDV_F32,
+                                   _ptr(_host_i32(tokens)), _ptr(_host_i32(lengths)), ctypes.byref(out))
+    if rc != 0:
+        raise SDVError(rc, "sdv_read_rows_bytes")
+    return out.value
+
+
+def copy_read_rows(host_target, host_draft, tokens, lengths, target, draft, *, V=None, stream=None):
+    """Queue host-to-device copies of the rows verification reads
+    (sdv_copy_read_rows).  host_target / host_draft: full host tensors
+    (pinned); tokens / lengths: int32 host tensors; target / draft: device
+    tensors of the same shapes.  Returns the bytes queued."""
+    B, K, Lp1, stride = host_target.shape
+    V = stride if V is None else int(V)
+    if stream is None:
+        stream = torch.cuda.current_stream(target.device)
+    out = ctypes.c_longlong(0)
+    rc = lib().sdv_copy_read_rows(B, K, Lp1 - 1, V, stride, _dtype_code(host_target), _ptr(host_target),
+                                  _ptr(host_draft), _ptr(_host_i32(tokens)), _ptr(_host_i32(lengths)),
+                                  _ptr(target), _ptr(draft), ctypes.c_void_p(stream.cuda_stream), ctypes.byref(out))
+    if rc != 0:
+        raise SDVError(rc, "sdv_copy_read_rows")
+    return out.value

@@ -173,6 +173,34 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
 
 }  // namespace
 
+// The rows verification reads, as one contiguous range per (request, draft)
+// and tensor: draft k owns its trie nodes from depth f_k on (f_0 = 0; for
+// k > 0, one past the longest prefix it shares with a lower draft, since a
+// node belongs to the lowest draft through it), so it brings target rows
+// [f_k, L_b] and draft rows [f_k, L_b - 1].  Requests with a length outside
+// 0..L get none (they are reported invalid).  Each range goes to fn(target?,
+// offset in rows, rows).
+template <class Fn>
+void for_read_rows(int B, int K, int L, const int* tokens, const int* lengths, Fn fn)
+{
+    for (int b = 0; b < B; ++b) {
+        const int Lb = lengths ? lengths[b] : L;
+        if (Lb < 0 || Lb > L) continue;
+        for (int k = 0; k < K; ++k) {
+            int f = 0;
+            const int* tk = tokens + ((size_t)b * K + k) * L;
+            for (int k2 = 0; k2 < k && f <= Lb; ++k2) {
+                const int* t2 = tokens + ((size_t)b * K + k2) * L;
+                int m = 0;
+                while (m < Lb && tk[m] == t2[m]) ++m;
+                if (m + 1 > f) f = m + 1;
+            }
+            if (f <= Lb) fn(true, ((size_t)b * K + k) * (L + 1) + f, (size_t)(Lb - f + 1));
+            if (f < Lb) fn(false, ((size_t)b * K + k) * L + f, (size_t)(Lb - f));
+        }
+    }
+}
+
 }  // namespace sdv
 
 extern "C" {
@@ -256,6 +284,45 @@ int sdv_launch_shape(int V, int dtype, int* ctas_per_sm, int* threads, int* smem
     if (threads) *threads = sdv::stream_threads();
     if (smem_bytes) *smem_bytes = (int)sdv::stream_smem_bytes();
     return SDV_OK;
+}
+
+int sdv_read_rows_bytes(int B, int K, int L, int V, long long row_stride, int dtype, const int* tokens,
+                        const int* lengths, long long* bytes)
+{
+    if (!sdv::sizes_ok(B, K, L, V) || row_stride < V || row_stride % 8 || (dtype != SDV_F32 && dtype != SDV_BF16) ||
+        !bytes || (B > 0 && L > 0 && !tokens))
+        return SDV_ERR_INVALID;
+    const size_t row = (size_t)row_stride * (dtype == SDV_BF16 ? 2 : 4);
+    size_t n = 0;
+    sdv::for_read_rows(B, K, L, tokens, lengths, [&](bool, size_t, size_t rows) { n += rows * row; });
+    *bytes = (long long)n;
+    return SDV_OK;
+}
+
+int sdv_copy_read_rows(int B, int K, int L, int V, long long row_stride, int dtype, const void* host_target,
+                       const void* host_draft, const int* tokens, const int* lengths, void* target, void* draft,
+                       void* cuda_stream, long long* bytes)
+{
+    if (!sdv::sizes_ok(B, K, L, V) || row_stride < V || row_stride % 8 || (dtype != SDV_F32 && dtype != SDV_BF16) ||
+        (B > 0 && (!host_target || !target || (L > 0 && (!tokens || !host_draft || !draft)))))
+        return SDV_ERR_INVALID;
+    const size_t row = (size_t)row_stride * (dtype == SDV_BF16 ? 2 : 4);
+    const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    size_t n = 0;
+    cudaError_t e = cudaSuccess;
+    sdv::for_read_rows(B, K, L, tokens, lengths, [&](bool is_target, size_t first, size_t rows) {
+        if (e != cudaSuccess) return;
+        const size_t off = first * row, len = rows * row;
+        if (is_target)
+            e = cudaMemcpyAsync(static_cast<char*>(target) + off, static_cast<const char*>(host_target) + off, len,
+                                cudaMemcpyHostToDevice, st);
+        else
+            e = cudaMemcpyAsync(static_cast<char*>(draft) + off, static_cast<const char*>(host_draft) + off, len,
+                                cudaMemcpyHostToDevice, st);
+        n += len;
+    });
+    if (bytes) *bytes = (long long)n;
+    return e == cudaSuccess ? SDV_OK : SDV_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -239,6 +239,32 @@ int sdv_sample_rows(int n_rows, int V, long long row_stride, int dtype, float te
  * range). */
 int sdv_launch_shape(int V, int dtype, int *ctas_per_sm, int *threads, int *smem_bytes);
 
+/* Logits in host memory: verification reads only the rows of trie nodes
+ * (see target_logits), so only those need to be on the device.
+ * sdv_copy_read_rows copies, per request and draft, the one contiguous range
+ * of rows it reads from each tensor: for draft k, target rows f..L_b and
+ * draft rows f..L_b-1, where f is the first depth whose node draft k owns
+ * (0 for k = 0; else one past the longest prefix it shares with a lower
+ * draft).  A leaf's row is among them, since only the decision tells whether
+ * its bonus draw needs it.  Requests whose length is outside 0..L get no
+ * rows.
+ *   host_target, host_draft  the full [B][K][L+1][row_stride] and
+ *                [B][K][L][row_stride] tensors in host memory (pinned, for
+ *                asynchronous copies); tokens [B][K][L] and lengths [B] (or
+ *                NULL) in host memory, read on the host during the call.
+ *   target, draft  device tensors of the same shapes; rows not copied keep
+ *                whatever they held (they are never read).
+ *   cuda_stream  the stream the copies are queued on, one cudaMemcpyAsync
+ *                per range.
+ *   bytes        out, may be NULL: the bytes queued.
+ * Returns SDV_OK, SDV_ERR_INVALID or SDV_ERR_CUDA.  sdv_read_rows_bytes
+ * returns the same byte count without copying (no GPU needed). */
+int sdv_copy_read_rows(int B, int K, int L, int V, long long row_stride, int dtype, const void *host_target,
+                       const void *host_draft, const int *tokens, const int *lengths, void *target, void *draft,
+                       void *cuda_stream, long long *bytes);
+int sdv_read_rows_bytes(int B, int K, int L, int V, long long row_stride, int dtype, const int *tokens,
+                        const int *lengths, long long *bytes);
+
 /* Fixed scratch of sdv_verify_multidraft_static: 4 MiB of device memory
  * that every GPU loading the library reserves until the process exits. */
 #define SDV_STATIC_SCRATCH_BYTES (4u << 20)

@@ -90,3 +90,23 @@ def test_package_fails_loudly_without_library(tmp_path):
             binding.lib(str(tmp_path / "missing.so"))
     finally:
         binding._lib = saved
+
+
+def test_read_rows_bytes_match_the_trie(lib):
+    """The rows verification reads, counted by the library on the host: per
+    request and draft, target rows from the first depth the draft owns to
+    L_b and draft rows to L_b - 1 (the trie rows of the bench's count: one
+    pair per inner node plus a target row per leaf)."""
+    import bench
+    import draft_verification_row_gb300 as sdv
+    from draft_verification_row_gb300 import workloads as W
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", "cpu", B=12, V=997)
+    inner, leaves = bench.trie_nodes(batch.tokens, batch.lengths, batch.K)
+    got = sdv.read_rows_bytes(batch.tokens, batch.lengths, batch.V, batch.stride, batch.target.dtype)
+    assert got == (2 * inner + leaves) * batch.stride * 2
+    # a request with an out-of-range length reads nothing
+    lengths = batch.lengths.clone()
+    lengths[0] = batch.L + 1
+    inner0, leaves0 = bench.trie_nodes(batch.tokens[1:], batch.lengths[1:], batch.K)
+    assert sdv.read_rows_bytes(batch.tokens, lengths, batch.V, batch.stride, batch.target.dtype) == \
+        (2 * inner0 + leaves0) * batch.stride * 2

@@ -315,3 +315,26 @@ def test_full_size_parity(name, temps, sample):
             P.compare(P.gpu_run(mode, batch), P.oracle_run(mode, batch, sample), f"{name}/T={T}/{mode}")
         del batch
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mode", ["multidraft", "token", "greedy", "kseq"])
+def test_copy_read_rows_is_all_verification_needs(mode):
+    """Copy only the rows verification reads (sdv_copy_read_rows) from host
+    memory into NaN-filled device tensors: the results equal those of the
+    fully copied batch, bit for bit."""
+    import dataclasses
+    import draft_verification_row_gb300 as sdv
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=16, V=9001)
+    full = P.gpu_run(mode, batch)
+    ht, hd = batch.target.cpu().pin_memory(), batch.draft.cpu().pin_memory()
+    tok, lens = batch.tokens.cpu(), batch.lengths.cpu()
+    t2 = torch.full_like(batch.target, float("nan"))
+    d2 = torch.full_like(batch.draft, float("nan"))
+    n = sdv.copy_read_rows(ht, hd, tok, lens, t2, d2, V=batch.V)
+    torch.cuda.synchronize()
+    assert n == sdv.read_rows_bytes(tok, lens, batch.V, batch.stride, batch.target.dtype)
+    assert n < batch.target.numel() * 2 + batch.draft.numel() * 2
+    part = P.gpu_run(mode, dataclasses.replace(batch, target=t2, draft=d2))
+    assert int(part["device_status"][0]) == 0
+    for key in ("accept_len", "accept_draft", "out_token", "accept_prob", "residual_mass"):
+        np.testing.assert_array_equal(full[key], part[key])
