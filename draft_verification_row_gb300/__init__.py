@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     MODES,
     SDVError,
     copy_read_rows,
+    gather_read_rows,
     launch_shape,
     lib,
     read_rows_bytes,

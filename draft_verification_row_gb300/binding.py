@@ -26,7 +26,7 @@ _VERIFY_ARGTYPES = [
 
 EXPORTS = list(_ENTRY.values()) + ["sdv_workspace_bytes", "sdv_status_string", "sdv_launch_shape",
                                    "sdv_set_profile_events", "sdv_sample_rows", "sdv_copy_read_rows",
-                                   "sdv_read_rows_bytes"]
+                                   "sdv_read_rows_bytes", "sdv_gather_read_rows"]
 
 
 class SDVError(RuntimeError):
@@ -66,6 +66,8 @@ def lib(path: str = LIB_PATH):
     h.sdv_copy_read_rows.restype = ctypes.c_int
     h.sdv_copy_read_rows.argtypes = ([ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int] + [ctypes.c_void_p] * 7
                                      + [ctypes.POINTER(ctypes.c_longlong)])
+    h.sdv_gather_read_rows.restype = ctypes.c_int
+    h.sdv_gather_read_rows.argtypes = [ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int] + [ctypes.c_void_p] * 7
     h.sdv_read_rows_bytes.restype = ctypes.c_int
     h.sdv_read_rows_bytes.argtypes = ([ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int] + [ctypes.c_void_p] * 2
                                       + [ctypes.POINTER(ctypes.c_longlong)])
@@ -258,3 +260,18 @@ def copy_read_rows(host_target, host_draft, tokens, lengths, target, draft, *, V
     if rc != 0:
         raise SDVError(rc, "sdv_copy_read_rows")
     return out.value
+
+
+def gather_read_rows(host_target, host_draft, tokens, lengths, target, draft, *, V=None, stream=None):
+    """Gather the rows verification reads from pinned, device-mapped host
+    tensors into device tensors with one kernel (sdv_gather_read_rows);
+    tokens / lengths are the device tensors the verification call takes."""
+    B, K, Lp1, stride = host_target.shape
+    V = stride if V is None else int(V)
+    if stream is None:
+        stream = torch.cuda.current_stream(target.device)
+    rc = lib().sdv_gather_read_rows(B, K, Lp1 - 1, V, stride, _dtype_code(host_target), _ptr(host_target),
+                                    _ptr(host_draft), _ptr(tokens), _ptr(lengths), _ptr(target), _ptr(draft),
+                                    ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SDVError(rc, "sdv_gather_read_rows")

@@ -286,6 +286,38 @@ int sdv_launch_shape(int V, int dtype, int* ctas_per_sm, int* threads, int* smem
     return SDV_OK;
 }
 
+int sdv_gather_read_rows(int B, int K, int L, int V, long long row_stride, int dtype, const void* host_target,
+                         const void* host_draft, const int* tokens, const int* lengths, void* target, void* draft,
+                         void* cuda_stream)
+{
+    if (!sdv::sizes_ok(B, K, L, V) || row_stride < V || row_stride % 8 || (dtype != SDV_F32 && dtype != SDV_BF16) ||
+        K > 256)
+        return SDV_ERR_INVALID;
+    if (B == 0) return SDV_OK;
+    // every pointer must be one the device can address: device memory, or
+    // host memory mapped into the device's address space
+    if (!sdv::device_accessible(host_target) || !sdv::device_accessible(target) || !sdv::aligned(host_target, 16) ||
+        !sdv::aligned(target, 16))
+        return SDV_ERR_INVALID;
+    if (L > 0 && (!tokens || !host_draft || !draft || !sdv::device_accessible(tokens) ||
+                  !sdv::device_accessible(host_draft) || !sdv::device_accessible(draft) ||
+                  !sdv::aligned(host_draft, 16) || !sdv::aligned(draft, 16)))
+        return SDV_ERR_INVALID;
+    if (lengths && !sdv::device_accessible(lengths)) return SDV_ERR_INVALID;
+    sdv::GatherArgs a;
+    a.B = B;
+    a.K = K;
+    a.L = L;
+    a.row_bytes = row_stride * (dtype == SDV_BF16 ? 2 : 4);
+    a.host_target = host_target;
+    a.host_draft = host_draft;
+    a.tokens = tokens;
+    a.lengths = lengths;
+    a.target = target;
+    a.draft = draft;
+    return sdv::launch_gather_rows(a, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? SDV_OK : SDV_ERR_CUDA;
+}
+
 int sdv_read_rows_bytes(int B, int K, int L, int V, long long row_stride, int dtype, const int* tokens,
                         const int* lengths, long long* bytes)
 {

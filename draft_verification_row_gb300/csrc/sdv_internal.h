@@ -61,6 +61,20 @@ inline size_t slot_count(int B, int K, int L) { return (size_t)B * (size_t)(L + 
 // Kernel launchers (sdv_kernels.cu, sdv_stream.cu); each returns a cudaError_t.
 cudaError_t launch_prep(const Problem& pb, cudaStream_t st);
 cudaError_t launch_argmax(const Problem& pb, cudaStream_t st);
+
+// The rows verification reads, gathered from host memory the device can
+// address (mapped, pinned) into device tensors (sdv_kernels.cu).
+struct GatherArgs {
+    int B, K, L;
+    long long row_bytes;
+    const void* host_target;
+    const void* host_draft;
+    const int* tokens;   // device
+    const int* lengths;  // device, or NULL
+    void* target;
+    void* draft;
+};
+cudaError_t launch_gather_rows(const GatherArgs& a, cudaStream_t st);
 cudaError_t launch_stream(const Problem& pb, cudaStream_t st);
 
 // Draft-token sampling (sdv_sample.cu): n_samples draws per row.

@@ -5,6 +5,9 @@
 //                 draft-trie owners, the depth-major list of inner trie
 //                 nodes the node kernel works through.
 // argmax_kernel   greedy: one CTA per node, streaming argmax of the target.
+// gather_rows_kernel  one CTA per (request, draft): the rows verification
+//                 reads, from host memory mapped into the device's address
+//                 space into device tensors.
 // (The decision and the correction draw are in sdv_sample.cu.)
 //
 // The rules (SpecTr-GBV: Multi-Draft Block Verification Accelerating
@@ -162,10 +165,73 @@ __global__ void __launch_bounds__(256) argmax_kernel(Problem pb)
     }
 }
 
+// ------------------------------------------------------------------------
+// gather of the rows verification reads: draft k owns its trie nodes from
+// depth f on (f = 0 for k = 0; else one past the longest prefix it shares
+// with a lower draft), so it brings target rows [f, L_b] and draft rows
+// [f, L_b - 1].  The reads cross the host link; many 16-byte loads per
+// thread are kept in flight to cover its latency.
+
+__device__ __forceinline__ void copy_bytes(const void* src, void* dst, size_t n)
+{
+    const uint4* s = static_cast<const uint4*>(src);
+    uint4* d = static_cast<uint4*>(dst);
+    const size_t n16 = n / 16;
+    constexpr int U = 8;
+    size_t i = threadIdx.x;
+    for (; i + (U - 1) * blockDim.x < n16; i += U * blockDim.x) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = s[i + u * blockDim.x];
+#pragma unroll
+        for (int u = 0; u < U; ++u) d[i + u * blockDim.x] = v[u];
+    }
+    for (; i < n16; i += blockDim.x) d[i] = s[i];
+}
+
+__global__ void __launch_bounds__(256) gather_rows_kernel(GatherArgs a)
+{
+    const int K = a.K, L = a.L;
+    const int b = blockIdx.x / K, k = blockIdx.x % K;
+    const int Lb = a.lengths ? a.lengths[b] : L;
+    if (Lb < 0 || Lb > L) return;
+    __shared__ int first;
+    if (threadIdx.x == 0) first = 0;
+    __syncthreads();
+    if ((int)threadIdx.x < k) {  // the prefix shared with lower draft threadIdx.x
+        const int* t1 = a.tokens + ((size_t)b * K + k) * L;
+        const int* t2 = a.tokens + ((size_t)b * K + threadIdx.x) * L;
+        int m = 0;
+        while (m < Lb && t1[m] == t2[m]) ++m;
+        atomicMax(&first, m + 1);
+    }
+    __syncthreads();
+    const int f = first;
+    const size_t rb = (size_t)a.row_bytes;
+    if (f <= Lb) {
+        const size_t off = (((size_t)b * K + k) * (L + 1) + f) * rb;
+        copy_bytes(static_cast<const char*>(a.host_target) + off, static_cast<char*>(a.target) + off,
+                   (size_t)(Lb - f + 1) * rb);
+    }
+    if (f < Lb) {
+        const size_t off = (((size_t)b * K + k) * L + f) * rb;
+        copy_bytes(static_cast<const char*>(a.host_draft) + off, static_cast<char*>(a.draft) + off,
+                   (size_t)(Lb - f) * rb);
+    }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------------
 // launchers
+
+cudaError_t launch_gather_rows(const GatherArgs& a, cudaStream_t st)
+{
+    const long long n = (long long)a.B * a.K;
+    if (n == 0) return cudaSuccess;
+    gather_rows_kernel<<<(unsigned)n, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_prep(const Problem& pb, cudaStream_t st)
 {

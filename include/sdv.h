@@ -265,6 +265,19 @@ int sdv_copy_read_rows(int B, int K, int L, int V, long long row_stride, int dty
 int sdv_read_rows_bytes(int B, int K, int L, int V, long long row_stride, int dtype, const int *tokens,
                         const int *lengths, long long *bytes);
 
+/* The same rows moved by the GPU itself: one kernel launch, one CTA per
+ * (request, draft), reading host memory over the host link with many loads
+ * in flight (no per-range copy calls).  host_target and host_draft must be
+ * host memory mapped into the device's address space (pinned memory on a
+ * UVA system); tokens and lengths (or NULL) device memory, as for the
+ * verification calls; target and draft device tensors; all 16-byte
+ * aligned.  Asynchronous on cuda_stream.  Returns SDV_OK, SDV_ERR_INVALID
+ * (a pointer the device cannot address, misalignment, K > 256) or
+ * SDV_ERR_CUDA. */
+int sdv_gather_read_rows(int B, int K, int L, int V, long long row_stride, int dtype, const void *host_target,
+                         const void *host_draft, const int *tokens, const int *lengths, void *target, void *draft,
+                         void *cuda_stream);
+
 /* Fixed scratch of sdv_verify_multidraft_static: 4 MiB of device memory
  * that every GPU loading the library reserves until the process exits. */
 #define SDV_STATIC_SCRATCH_BYTES (4u << 20)

@@ -338,3 +338,25 @@ def test_copy_read_rows_is_all_verification_needs(mode):
     assert int(part["device_status"][0]) == 0
     for key in ("accept_len", "accept_draft", "out_token", "accept_prob", "residual_mass"):
         np.testing.assert_array_equal(full[key], part[key])
+
+
+def test_gather_read_rows_matches_the_copy():
+    """The GPU-side gather of the rows verification reads (from pinned,
+    device-mapped host tensors) writes exactly the rows the host-side copy
+    does; verification from them equals the full batch's."""
+    import dataclasses
+    import draft_verification_row_gb300 as sdv
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=16, V=9001)
+    ht, hd = batch.target.cpu().pin_memory(), batch.draft.cpu().pin_memory()
+    a_t, a_d = torch.full_like(batch.target, float("nan")), torch.full_like(batch.draft, float("nan"))
+    b_t, b_d = torch.full_like(batch.target, float("nan")), torch.full_like(batch.draft, float("nan"))
+    sdv.copy_read_rows(ht, hd, batch.tokens.cpu(), batch.lengths.cpu(), a_t, a_d, V=batch.V)
+    sdv.gather_read_rows(ht, hd, batch.tokens, batch.lengths, b_t, b_d, V=batch.V)
+    torch.cuda.synchronize()
+    # NaN == NaN for the untouched rows: compare the bits
+    assert torch.equal(a_t.view(torch.int16), b_t.view(torch.int16))
+    assert torch.equal(a_d.view(torch.int16), b_d.view(torch.int16))
+    full = P.gpu_run("multidraft", batch)
+    part = P.gpu_run("multidraft", dataclasses.replace(batch, target=b_t, draft=b_d))
+    for key in ("accept_len", "accept_draft", "out_token", "accept_prob", "residual_mass"):
+        np.testing.assert_array_equal(full[key], part[key])
