@@ -14,7 +14,7 @@ import numpy as np
 from . import build as _build
 
 MODE = {"token": 0, "greedy": 1, "block": 2, "multidraft": 3, "kseq": 4}
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 REQ_BAD_LENGTH, REQ_BAD_TOKEN, REQ_NONFINITE = 1, 2, 4
 MAX_K = 16
 MAX_L = 16
@@ -52,6 +52,7 @@ def lib():
         _lib.sdvo_exact_streams.restype = ctypes.c_int
         _lib.sdvo_prefix_index.restype = ctypes.c_longlong
         _lib.sdvo_sample_rows.restype = ctypes.c_int
+        _lib.sdvo_lm_head_logits.restype = ctypes.c_int
     return _lib
 
 
@@ -96,6 +97,8 @@ class Problem:
             self.dtype = BF16
         elif t.dtype == np.float32:
             self.dtype = F32
+        elif t.dtype == np.float64:
+            self.dtype = F64
         else:
             raise TypeError(f"unsupported logit dtype {t.dtype}")
 
@@ -178,6 +181,29 @@ def sample_rows(logits, n_samples, u, temperature, V=None):
         _ptr(out["tokens"]), _ptr(out["margin"]), _ptr(out["row_status"]))
     out["rc"] = rc
     return out
+
+
+def lm_head_logits(hidden, lm_head):
+    """The target model's LM head in double: hidden [..., d] and lm_head [V][d]
+    as bf16 (CPU torch tensors or uint16 bits).  Returns float64 logits of
+    shape hidden.shape[:-1] + (V,)."""
+    h = _np(hidden)
+    w = _np(lm_head)
+    if h.dtype not in (np.uint16, np.int16) or w.dtype not in (np.uint16, np.int16):
+        raise TypeError("the LM head takes bf16 inputs")
+    d = h.shape[-1]
+    if w.ndim != 2 or w.shape[1] != d:
+        raise ValueError("lm_head must be [V][d] with the hidden size of hidden")
+    lead = h.shape[:-1]
+    M = int(np.prod(lead)) if lead else 1
+    V = w.shape[0]
+    out = np.zeros((M, V), np.float64)
+    rc = lib().sdvo_lm_head_logits(ctypes.c_int(M), ctypes.c_int(V), ctypes.c_int(d),
+                                   _ptr(np.ascontiguousarray(h)), _ptr(np.ascontiguousarray(w)),
+                                   _ptr(out), ctypes.c_longlong(V))
+    if rc != 0:
+        raise RuntimeError(f"sdvo_lm_head_logits failed: {rc}")
+    return out.reshape(tuple(lead) + (V,))
 
 
 def exact_outcomes(mode, prob: Problem):

@@ -61,7 +61,7 @@
 /* ------------------------------------------------------------------------ */
 /* input access                                                              */
 
-static size_t elem_size(int dtype) { return dtype == SDVO_BF16 ? 2u : 4u; }
+static size_t elem_size(int dtype) { return dtype == SDVO_BF16 ? 2u : dtype == SDVO_F64 ? 8u : 4u; }
 
 static const unsigned char* row_of(const sdvo_problem* pb, int is_target, int b, int k, int j)
 {
@@ -71,9 +71,22 @@ static const unsigned char* row_of(const sdvo_problem* pb, int is_target, int b,
     return base + (size_t)r * (size_t)pb->row_stride * elem_size(pb->dtype);
 }
 
+static double bf16_value(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
 static double logit(const sdvo_problem* pb, const unsigned char* row, int x)
 {
     float f;
+    if (pb->dtype == SDVO_F64) {
+        double g;
+        memcpy(&g, row + 8 * (size_t)x, 8);
+        return g;
+    }
     if (pb->dtype == SDVO_BF16) {
         uint16_t h;
         uint32_t u;
@@ -613,7 +626,7 @@ int sdvo_verify(int mode, const sdvo_problem* pb, int* accept_len, int* accept_d
     int greedy;
     if (!pb || mode < SDVO_MODE_TOKEN || mode > SDVO_MODE_KSEQ) return SDVO_ERR_INVALID;
     if (pb->B < 0 || pb->K < 1 || pb->K > SDVO_MAX_K || pb->L < 0 || pb->L > SDVO_MAX_L || pb->V < 1 ||
-        pb->row_stride < pb->V || (pb->dtype != SDVO_F32 && pb->dtype != SDVO_BF16))
+        pb->row_stride < pb->V || (pb->dtype != SDVO_F32 && pb->dtype != SDVO_BF16 && pb->dtype != SDVO_F64))
         return SDVO_ERR_INVALID;
     if (isnan(pb->temperature) || pb->temperature < 0.0 || isinf(pb->temperature)) return SDVO_ERR_INVALID;
     if (mode == SDVO_MODE_BLOCK && pb->K != 1) return SDVO_ERR_INVALID;
@@ -761,3 +774,26 @@ int sdvo_sample_rows(int n_rows, int V, long long row_stride, int dtype, double 
     return SDVO_OK;
 }
 
+
+/* ------------------------------------------------------------------------ */
+/* the target model's LM head                                                */
+
+int sdvo_lm_head_logits(int M, int V, int d, const void* hidden, const void* lm_head, double* logits,
+                        long long out_stride)
+{
+    if (M < 0 || V < 1 || d < 1 || out_stride < V) return SDVO_ERR_INVALID;
+    if (M == 0) return SDVO_OK;
+    if (!hidden || !lm_head || !logits) return SDVO_ERR_INVALID;
+    const uint16_t* h = (const uint16_t*)hidden;
+    const uint16_t* w = (const uint16_t*)lm_head;
+    for (int r = 0; r < M; ++r) {
+        const uint16_t* hr = h + (size_t)r * (size_t)d;
+        for (int x = 0; x < V; ++x) {
+            const uint16_t* wx = w + (size_t)x * (size_t)d;
+            double s = 0.0;
+            for (int i = 0; i < d; ++i) s += bf16_value(hr[i]) * bf16_value(wx[i]);
+            logits[(size_t)r * (size_t)out_stride + x] = s;
+        }
+    }
+    return SDVO_OK;
+}

@@ -37,14 +37,15 @@ extern "C" {
 #define SDVO_MAX_K 16
 #define SDVO_MAX_L 16
 
-enum { SDVO_F32 = 0, SDVO_BF16 = 1 };
+enum { SDVO_F32 = 0, SDVO_BF16 = 1, SDVO_F64 = 2 };
 enum { SDVO_MODE_TOKEN = 0, SDVO_MODE_GREEDY = 1, SDVO_MODE_BLOCK = 2, SDVO_MODE_MULTIDRAFT = 3, SDVO_MODE_KSEQ = 4 };
 enum { SDVO_OK = 0, SDVO_ERR_INVALID = 1, SDVO_ERR_UNSUPPORTED = 2, SDVO_ERR_NOMEM = 3 };
 /* per-request data status bits (same meaning as the CUDA library's) */
 enum { SDVO_REQ_BAD_LENGTH = 1, SDVO_REQ_BAD_TOKEN = 2, SDVO_REQ_NONFINITE = 4 };
 
 /* One batch.  Layouts (row-major, all host memory):
- *   target   [B][K][L+1][row_stride]  f32 or bf16 bits
+ *   target   [B][K][L+1][row_stride]  f32, bf16 bits or f64 (the f64 form
+ *                                     carries the LM head's exact logits)
  *   draft    [B][K][L][row_stride]
  *   tokens   [B][K][L]                int32, drafted token X^k_{j+1} at [b][k][j]
  *   lengths  [B] in 0..L, or NULL (= L for every request)
@@ -127,6 +128,20 @@ int sdvo_exact_streams(int mode, int V, int K, int L, double temperature,
 int sdvo_sample_rows(int n_rows, int V, long long row_stride, int dtype, double temperature,
                      const void* logits, int n_samples, const double* u, int* tokens, double* margin,
                      int* row_status);
+
+/* The target model's LM head, the last step of the target pass whose output
+ * verification consumes ("Speculative Decoding: Performance or Illusion?",
+ * section 3.2: verification is the target model's pass over the drafts):
+ *   logits[r][x] = sum over i < d of hidden[r][i] * lm_head[x][i]
+ * in double.  bf16 inputs are decoded exactly and each product of two bf16
+ * values is exact in double; the sum runs in index order.
+ *   hidden   [M][d]           bf16 bits
+ *   lm_head  [V][d]           bf16 bits (one row per vocabulary entry)
+ *   logits   [M][out_stride]  double; columns >= V are not written
+ * Verification fused into the LM head is sdvo_verify on these logits, passed
+ * as SDVO_F64 rows.  Returns SDVO_OK or SDVO_ERR_INVALID. */
+int sdvo_lm_head_logits(int M, int V, int d, const void* hidden, const void* lm_head, double* logits,
+                        long long out_stride);
 
 /* Index of a prefix of length j: all prefixes of length < j come first,
  * then the base-V number of the tokens (first token most significant). */
