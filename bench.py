@@ -107,7 +107,8 @@ def sum_over_ranks(x, world):
 def rank_seed(name, rank):
     """Seed of rank `rank`'s batch: every rank verifies its own requests."""
     from draft_verification_row_gb300 import workloads as W
-    return W.WORKLOADS[name]["seed"] + 7919 * rank
+    cfg = W.WORKLOADS.get(name) or W.LM_HEAD_WORKLOADS[name]
+    return cfg["seed"] + 7919 * rank
 
 
 def trie_nodes(tokens, lengths, K):
@@ -127,6 +128,84 @@ def trie_nodes(tokens, lengths, K):
             else:
                 leaves += n
     return inner, leaves
+
+
+def measured_bf16_peak():
+    """Dense bf16 TFLOP/s: the measured burst figure (a kernel timed on its
+    own), else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def lm_head_bench(args, dev, stream, rank, world):
+    """Greedy verification fused into the target model's LM head, on the
+    mixed batch's shape with hidden size 4096: the fused call, its tensor-core
+    kernel against the measured bf16 peak, cuBLAS on the same GEMM shape, and
+    the unfused path (cuBLAS logits of every row to HBM, then sdv greedy)."""
+    import draft_verification_row_gb300 as sdv
+    from draft_verification_row_gb300 import binding, workloads as W
+
+    lb = W.make_lm_head(W.LM_HEAD_HEADLINE, dev, seed=rank_seed(W.LM_HEAD_HEADLINE, rank))
+    inner, leaves = trie_nodes(lb.tokens, lb.lengths, lb.K)
+    rows = inner + leaves  # one logit row per trie node, leaves included
+    out = binding.LmHeadOutputs(lb.B, lb.K, lb.L, lb.V, lb.d, dev)
+
+    def fused():
+        sdv.verify_greedy_lm_head(lb.hidden, lb.lm_head, lb.tokens, lb.lengths, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        fused()
+    total, gemm = time_calls(fused, args.steps, stream, prof=True)
+    total, gemm = max_over_ranks(total, world), max_over_ranks(gemm, world)
+    if int(out.device_status.item()):
+        raise RuntimeError(f"fused LM head: device status {int(out.device_status.item())}")
+    ms, gemm_ms = total / args.steps, gemm / args.steps
+    flops = 2.0 * rows * lb.V * lb.d
+    tflops = flops / (gemm_ms / 1000.0) / 1e12
+    peak, kind = measured_bf16_peak()
+    # cuBLAS on the same GEMM shape (rows x V x d, bf16 logits written)
+    a = torch.randn((rows, lb.d), device=dev).to(torch.bfloat16)
+    c = torch.empty((rows, lb.V), dtype=torch.bfloat16, device=dev)
+
+    def cublas():
+        with torch.cuda.stream(stream):
+            torch.mm(a, lb.lm_head.t(), out=c)
+
+    for _ in range(args.warmup):
+        cublas()
+    t_cb, _ = time_calls(cublas, args.steps, stream)
+    del a, c
+    # unfused: logits of every row [B][K][L+1][V] to HBM, then greedy verification
+    logits = torch.empty((lb.B, lb.K, lb.L + 1, lb.V), dtype=torch.bfloat16, device=dev)
+    vout = binding.Outputs("greedy", lb.B, lb.K, lb.L, lb.V, dev)
+
+    def unfused():
+        with torch.cuda.stream(stream):
+            torch.mm(lb.hidden.view(-1, lb.d), lb.lm_head.t(), out=logits.view(-1, lb.V))
+        sdv.verify("greedy", logits, None, lb.tokens, lb.lengths, None, None, 0.0, V=lb.V, out=vout, stream=stream)
+
+    for _ in range(args.warmup):
+        unfused()
+    t_un, _ = time_calls(unfused, args.steps, stream)
+    del logits
+    positions = sum_over_ranks(lb.positions, world)
+    return {
+        "what": "greedy verification fused into the target LM head: logits = hidden . W^T on tcgen05, each "
+                "trie node's row reduced to its argmax in the epilogue (logits never stored)",
+        "workload": W.LM_HEAD_HEADLINE, "rows": rows, "V": lb.V, "d": lb.d,
+        "metric": "verified draft positions/s", "value": positions / (ms / 1000.0), "unit": "positions/s",
+        "ms_per_call": ms, "lm_head_kernel_ms": gemm_ms, "gpu_launches_per_call": 5,
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "peak_kind": f"{kind} bf16_tflops (burst)",
+                     "algorithmic_flops_per_call": flops, "kernel": "lm_head_kernel<ARGMAX>"},
+        "cublas_same_gemm": {"ms": t_cb / args.steps, "tflops": flops / (t_cb / args.steps / 1000.0) / 1e12},
+        "unfused_cublas_all_rows_then_greedy": {
+            "ms": t_un / args.steps, "rows": lb.B * lb.K * (lb.L + 1),
+            "value": positions / (t_un / args.steps / 1000.0)},
+    }
 
 
 def measured_peaks():
@@ -485,6 +564,8 @@ def run_ours(args, world, rank, local):
                             "half_batch": emu.B, **m,
                             "gpu_launches_per_step": emu.L + 3}  # L sampling launches + prep, node, finish
         del emu
+        # the next row: greedy verification fused into the target LM head
+        line["next_lm_head"] = lm_head_bench(args, dev, stream, rank, world)
         if rank == 0:
             rng = np.random.default_rng(1)
             req = sorted(rng.choice(batch.B, size=min(args.cpu_requests, batch.B), replace=False).tolist())

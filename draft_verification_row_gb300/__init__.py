@@ -15,12 +15,15 @@ from .binding import (  # noqa: F401
     gather_read_rows,
     launch_shape,
     lib,
+    lm_head_logits,
+    lm_head_workspace_bytes,
     read_rows_bytes,
     sample_rows,
     set_profile_events,
     verify,
     verify_block,
     verify_greedy,
+    verify_greedy_lm_head,
     verify_kseq,
     verify_multidraft,
     verify_token,

@@ -26,7 +26,8 @@ _VERIFY_ARGTYPES = [
 
 EXPORTS = list(_ENTRY.values()) + ["sdv_workspace_bytes", "sdv_status_string", "sdv_launch_shape",
                                    "sdv_set_profile_events", "sdv_sample_rows", "sdv_copy_read_rows",
-                                   "sdv_read_rows_bytes", "sdv_gather_read_rows"]
+                                   "sdv_read_rows_bytes", "sdv_gather_read_rows", "sdv_verify_greedy_lm_head",
+                                   "sdv_lm_head_workspace_bytes", "sdv_lm_head_logits"]
 
 
 class SDVError(RuntimeError):
@@ -68,6 +69,14 @@ def lib(path: str = LIB_PATH):
                                      + [ctypes.POINTER(ctypes.c_longlong)])
     h.sdv_gather_read_rows.restype = ctypes.c_int
     h.sdv_gather_read_rows.argtypes = [ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int] + [ctypes.c_void_p] * 7
+    h.sdv_verify_greedy_lm_head.restype = ctypes.c_int
+    h.sdv_verify_greedy_lm_head.argtypes = ([ctypes.c_int] * 5 + [ctypes.c_void_p] * 10 + [ctypes.c_size_t]
+                                            + [ctypes.c_void_p])
+    h.sdv_lm_head_workspace_bytes.restype = ctypes.c_size_t
+    h.sdv_lm_head_workspace_bytes.argtypes = [ctypes.c_int] * 5
+    h.sdv_lm_head_logits.restype = ctypes.c_int
+    h.sdv_lm_head_logits.argtypes = ([ctypes.c_int] * 3 + [ctypes.c_void_p] * 3 + [ctypes.c_longlong]
+                                     + [ctypes.c_void_p] * 2)
     h.sdv_read_rows_bytes.restype = ctypes.c_int
     h.sdv_read_rows_bytes.argtypes = ([ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int] + [ctypes.c_void_p] * 2
                                       + [ctypes.POINTER(ctypes.c_longlong)])
@@ -222,6 +231,93 @@ def sample_rows(logits, n_samples, u, temperature, *, V=None, tokens=None, devic
         raise SDVError(rc, "sdv_sample_rows")
     return tokens, device_status
 
+
+
+def _bf16_rows(name, t, d=None):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    if d is not None and t.shape[-1] != d:
+        raise ValueError(f"{name} must have the hidden size {d} as its last dimension")
+
+
+class LmHeadOutputs:
+    """Preallocated outputs and workspace of verify_greedy_lm_head for one shape."""
+
+    def __init__(self, B, K, L, V, d, device, accept_prob=True):
+        self.accept_len = torch.empty(B, dtype=torch.int32, device=device)
+        self.accept_draft = torch.empty(B, dtype=torch.int32, device=device)
+        self.out_token = torch.empty(B, dtype=torch.int32, device=device)
+        self.accept_prob = torch.empty((B, K, L), dtype=torch.float32, device=device) if accept_prob else None
+        self.device_status = torch.empty(1, dtype=torch.int32, device=device)
+        nbytes = max(lib().sdv_lm_head_workspace_bytes(B, K, L, V, d), 256)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k in ("accept_len", "accept_draft", "out_token", "accept_prob",
+                                              "device_status")}
+
+
+def lm_head_workspace_bytes(B, K, L, V, d):
+    return lib().sdv_lm_head_workspace_bytes(B, K, L, V, d)
+
+
+def verify_greedy_lm_head(hidden, lm_head, tokens, lengths, *, out: LmHeadOutputs = None, stream=None,
+                          accept_prob=True):
+    """Greedy verification fused into the target model's LM head.
+
+    hidden [B][K][L+1][d] bfloat16 (the target model's final hidden state of
+    every draft position), lm_head [V][d] bfloat16, tokens [B][K][L] int32,
+    lengths [B] int32 or None.  Returns a dict of output tensors
+    (asynchronous, like verify)."""
+    h = lib()
+    if hidden.dim() != 4 or lm_head.dim() != 2:
+        raise ValueError("hidden must be [B][K][L+1][d] and lm_head [V][d]")
+    B, K, Lp1, d = hidden.shape
+    L, V = Lp1 - 1, lm_head.shape[0]
+    _bf16_rows("hidden", hidden)
+    _bf16_rows("lm_head", lm_head, d)
+    for name, t in (("tokens", tokens), ("lengths", lengths)):
+        if t is not None and (t.dtype != torch.int32 or not t.is_contiguous() or not t.is_cuda):
+            raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+    if out is None:
+        out = LmHeadOutputs(B, K, L, V, d, hidden.device, accept_prob)
+    if stream is None:
+        stream = torch.cuda.current_stream(hidden.device)
+    rc = h.sdv_verify_greedy_lm_head(B, K, L, V, d, _ptr(hidden), _ptr(lm_head), _ptr(tokens), _ptr(lengths),
+                                     _ptr(out.accept_len), _ptr(out.accept_draft), _ptr(out.out_token),
+                                     _ptr(out.accept_prob), _ptr(out.device_status), _ptr(out.workspace),
+                                     out.workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SDVError(rc, "sdv_verify_greedy_lm_head")
+    return out.as_dict()
+
+
+def lm_head_logits(hidden, lm_head, *, logits=None, device_status=None, stream=None):
+    """The target model's LM head alone: fp32 logits [M][V] of hidden [M][d]
+    and lm_head [V][d] (bfloat16).  logits may be a preallocated float32
+    [M][>= V] tensor with contiguous rows (row stride a multiple of 4).
+    Returns (logits, device_status); asynchronous."""
+    h = lib()
+    if hidden.dim() != 2 or lm_head.dim() != 2:
+        raise ValueError("hidden must be [M][d] and lm_head [V][d]")
+    M, d = hidden.shape
+    V = lm_head.shape[0]
+    _bf16_rows("hidden", hidden)
+    _bf16_rows("lm_head", lm_head, d)
+    if logits is None:
+        logits = torch.empty((M, V), dtype=torch.float32, device=hidden.device)
+    if (logits.dtype != torch.float32 or not logits.is_cuda or logits.shape[0] != M or logits.shape[1] < V
+            or logits.stride(1) != 1):
+        raise ValueError("logits must be a CUDA float32 [M][>= V] tensor with contiguous rows")
+    if device_status is None:
+        device_status = torch.empty(1, dtype=torch.int32, device=hidden.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(hidden.device)
+    rc = h.sdv_lm_head_logits(M, V, d, _ptr(hidden), _ptr(lm_head), _ptr(logits), logits.stride(0),
+                              _ptr(device_status), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SDVError(rc, "sdv_lm_head_logits")
+    return logits, device_status
 
 
 def _host_i32(t):

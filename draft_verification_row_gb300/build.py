@@ -12,7 +12,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsdv.so")
-SOURCES = ["sdv_api.cu", "sdv_kernels.cu", "sdv_stream.cu", "sdv_sample.cu", "sdv_static.cu"]
+SOURCES = ["sdv_api.cu", "sdv_kernels.cu", "sdv_stream.cu", "sdv_sample.cu", "sdv_static.cu", "sdv_lmhead.cu"]
 HEADERS = [os.path.join(ROOT, "include", "sdv.h"), os.path.join(CSRC, "sdv_internal.h"),
            os.path.join(CSRC, "sdv_device.cuh")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -28,6 +28,17 @@ size_t workspace_size(int B, int K, int L)
            align_up((size_t)(L + 1) * B * K * 4) + align_up((size_t)(2 * L + 3) * 4);
 }
 
+// The hidden size of the LM head: whole 16-byte units per row (TMA row pitch).
+bool lm_d_ok(int d) { return d >= 8 && d % 8 == 0 && d <= (1 << 16); }
+
+// Fused greedy call: the verification workspace, then the node rows of the
+// LM head (compact map, row count, argmax keys, hidden rows).
+size_t lm_workspace_size(int B, int K, int L, int d)
+{
+    const size_t n = slot_count(B, K, L);
+    return workspace_size(B, K, L) + align_up(n * 4) + align_up(4) + align_up(n * 8) + align_up(n * (size_t)d * 2);
+}
+
 Workspace carve(void* base, int B, int K, int L)
 {
     const size_t n = slot_count(B, K, L);
@@ -171,6 +182,84 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
     return SDV_OK;
 }
 
+int verify_greedy_lm_head(int B, int K, int L, int V, int d, const void* hidden, const void* lm_head,
+                          const int* draft_tokens, const int* lengths, int* accept_len, int* accept_draft,
+                          int* out_token, float* accept_prob, int* device_status, void* workspace,
+                          size_t workspace_bytes, void* cuda_stream)
+{
+    if (!sizes_ok(B, K, L, V) || !lm_d_ok(d)) return SDV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    if (device_status && !device_accessible(device_status)) return SDV_ERR_INVALID;
+    if (B == 0) {
+        if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+        return SDV_OK;
+    }
+    if (!hidden || !lm_head || (L > 0 && !draft_tokens) || !accept_len || !accept_draft || !out_token)
+        return SDV_ERR_INVALID;
+    if (!aligned(hidden, 16) || !aligned(lm_head, 16)) return SDV_ERR_INVALID;
+    const void* ptrs[] = {hidden, lm_head, L > 0 ? draft_tokens : nullptr, lengths, accept_len, accept_draft,
+                          out_token, accept_prob};
+    for (const void* q : ptrs)
+        if (q && !device_accessible(q)) return SDV_ERR_INVALID;
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < lm_workspace_size(B, K, L, d))
+        return SDV_ERR_WORKSPACE;
+    if (!device_accessible(workspace)) return SDV_ERR_WORKSPACE;
+
+    Problem pb;
+    std::memset(&pb, 0, sizeof pb);
+    pb.B = B;
+    pb.K = K;
+    pb.L = L;
+    pb.V = V;
+    pb.stride = V;
+    pb.dtype = SDV_BF16;
+    pb.mode = SDV_MODE_GREEDY;
+    pb.tokens = draft_tokens;
+    pb.lengths = lengths;
+    pb.accept_len = accept_len;
+    pb.accept_draft = accept_draft;
+    pb.out_token = out_token;
+    pb.accept_prob = accept_prob;
+    pb.device_status = device_status;
+    pb.ws = carve(workspace, B, K, L);
+    const size_t n = slot_count(B, K, L);
+    char* p = static_cast<char*>(workspace) + workspace_size(B, K, L);
+    LmRows r;
+    r.d = d;
+    r.hidden = hidden;
+    r.compact = reinterpret_cast<int*>(p);
+    p += align_up(n * 4);
+    r.count = reinterpret_cast<int*>(p);
+    p += align_up(4);
+    r.keys = reinterpret_cast<unsigned long long*>(p);
+    p += align_up(n * 8);
+    r.rows = p;
+    LmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.rows_dev = r.count;
+    a.V = V;
+    a.d = d;
+    a.keys = r.keys;
+    a.device_status = device_status;
+
+    if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (cudaMemsetAsync(pb.ws.ncount, 0, sizeof(int) * (2 * L + 3), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (cudaMemsetAsync(r.count, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_prep(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_lm_rows(pb, r, st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (!prof_record(g_prof_start, st)) return SDV_ERR_CUDA;
+    const cudaError_t e = launch_lm_head(r.rows, (long long)n, lm_head, a, LM_EPI_ARGMAX, st);
+    if (e == cudaErrorInvalidValue) {
+        cudaGetLastError();
+        return SDV_ERR_UNSUPPORTED;  // no tensor-map encoder, or not enough shared memory
+    }
+    if (e != cudaSuccess) return SDV_ERR_CUDA;
+    if (!prof_record(g_prof_stop, st)) return SDV_ERR_CUDA;
+    if (launch_lm_argmax(pb, r, st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_finish(pb, true, st) != cudaSuccess) return SDV_ERR_CUDA;
+    return SDV_OK;
+}
+
 }  // namespace
 
 // The rows verification reads, as one contiguous range per (request, draft)
@@ -221,6 +310,54 @@ size_t sdv_workspace_bytes(int mode, int B, int K, int L, int V)
     if (mode < SDV_MODE_TOKEN || mode > SDV_MODE_KSEQ || !sdv::sizes_ok(B, K, L, V)) return 0;
     if (mode == SDV_MODE_BLOCK && K != 1) return 0;
     return sdv::workspace_size(B, K, L);
+}
+
+int sdv_verify_greedy_lm_head(int B, int K, int L, int V, int d, const void* hidden, const void* lm_head,
+                              const int* draft_tokens, const int* lengths, int* accept_len, int* accept_draft,
+                              int* out_token, float* accept_prob, int* device_status, void* workspace,
+                              size_t workspace_bytes, void* cuda_stream)
+{
+    return sdv::verify_greedy_lm_head(B, K, L, V, d, hidden, lm_head, draft_tokens, lengths, accept_len,
+                                      accept_draft, out_token, accept_prob, device_status, workspace,
+                                      workspace_bytes, cuda_stream);
+}
+
+size_t sdv_lm_head_workspace_bytes(int B, int K, int L, int V, int d)
+{
+    if (!sdv::sizes_ok(B, K, L, V) || !sdv::lm_d_ok(d)) return 0;
+    return sdv::lm_workspace_size(B, K, L, d);
+}
+
+int sdv_lm_head_logits(int M, int V, int d, const void* hidden, const void* lm_head, float* logits,
+                       long long logits_stride, int* device_status, void* cuda_stream)
+{
+    if (M < 0 || V < 1 || V > SDV_MAX_V || !sdv::lm_d_ok(d) || logits_stride < V || logits_stride % 4)
+        return SDV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    if (device_status && !sdv::device_accessible(device_status)) return SDV_ERR_INVALID;
+    if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (M == 0) return SDV_OK;
+    if (!hidden || !lm_head || !logits) return SDV_ERR_INVALID;
+    if (!sdv::aligned(hidden, 16) || !sdv::aligned(lm_head, 16) || !sdv::aligned(logits, 16)) return SDV_ERR_INVALID;
+    const void* ptrs[] = {hidden, lm_head, logits};
+    for (const void* q : ptrs)
+        if (!sdv::device_accessible(q)) return SDV_ERR_INVALID;
+    sdv::LmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.rows = M;
+    a.V = V;
+    a.d = d;
+    a.logits = logits;
+    a.out_stride = logits_stride;
+    a.device_status = device_status;
+    if (!sdv::prof_record(sdv::g_prof_start, st)) return SDV_ERR_CUDA;
+    const cudaError_t e = sdv::launch_lm_head(hidden, M, lm_head, a, sdv::LM_EPI_LOGITS, st);
+    if (e == cudaErrorInvalidValue) {
+        cudaGetLastError();
+        return SDV_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return SDV_ERR_CUDA;
+    return sdv::prof_record(sdv::g_prof_stop, st) ? SDV_OK : SDV_ERR_CUDA;
 }
 
 const char* sdv_status_string(int status)

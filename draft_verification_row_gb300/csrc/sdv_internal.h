@@ -56,7 +56,7 @@ struct Problem {
     Workspace ws;
 };
 
-inline size_t slot_count(int B, int K, int L) { return (size_t)B * (size_t)(L + 1) * (size_t)K; }
+__host__ __device__ inline size_t slot_count(int B, int K, int L) { return (size_t)B * (size_t)(L + 1) * (size_t)K; }
 
 // Kernel launchers (sdv_kernels.cu, sdv_stream.cu); each returns a cudaError_t.
 cudaError_t launch_prep(const Problem& pb, cudaStream_t st);
@@ -92,6 +92,36 @@ cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st);
 // node (sdv_sample.cu).
 cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st);
 int sample_threads();
+
+// The target model's LM head on the tensor cores (sdv_lmhead.cu):
+// logits = hidden . W^T over the hidden size d, bf16 in, fp32 accumulate.
+enum { LM_EPI_ARGMAX = 0, LM_EPI_LOGITS = 1 };
+struct LmArgs {
+    int rows;                  // rows of the A operand (used when rows_dev is NULL)
+    const int* rows_dev;       // device row count, written by an earlier launch, or NULL
+    int V, d;
+    unsigned long long* keys;  // ARGMAX: [rows] (maximum, first index) keys, zeroed beforehand
+    float* logits;             // LOGITS: [rows][out_stride] fp32
+    long long out_stride;
+    int* device_status;
+};
+// hidden: [hidden_rows][d] bf16 (the A operand); lm_head: [V][d] bf16.
+cudaError_t launch_lm_head(const void* hidden, long long hidden_rows, const void* lm_head, const LmArgs& a,
+                           int epi, cudaStream_t st);
+size_t lm_head_smem_bytes();
+
+// Greedy verification fused into the LM head: the trie nodes' hidden rows,
+// gathered into the A operand, and their argmax keys.
+struct LmRows {
+    int d;
+    const void* hidden;        // [B][K][L+1][d] bf16
+    void* rows;                // [slots][d] bf16: the nodes' hidden rows, contiguous
+    int* compact;              // [slots]: node slot -> its row
+    int* count;                // rows listed
+    unsigned long long* keys;  // [slots]
+};
+cudaError_t launch_lm_rows(const Problem& pb, const LmRows& r, cudaStream_t st);
+cudaError_t launch_lm_argmax(const Problem& pb, const LmRows& r, cudaStream_t st);
 
 // The node kernel's launch shape: persistent CTAs per SM, threads per CTA
 // and dynamic shared memory.

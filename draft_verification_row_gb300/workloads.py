@@ -176,3 +176,123 @@ def make(workload, device="cpu", *, seed: Optional[int] = None, temperature: Opt
     return Batch(name=name, B=B_, K=K_, L=L_, V=V_, stride=stride, dtype=cfg["dtype"], temperature=T,
                  target=tgt, draft=dft, tokens=tokens, lengths=lens, accept_u=accept_u,
                  sample_u=sample_u, meta=meta)
+
+
+# ---------------------------------------------------------------------------
+# Greedy verification fused into the target model's LM head: the inputs are
+# the target model's final hidden states and its LM head instead of logits.
+
+LM_HEAD_WORKLOADS = {
+    # the mixed batch's shape with a hidden size of 4096 (8B-class models
+    # with this vocabulary size)
+    "lmhead-greedy-B256-K8-L8-V151936-d4096": dict(
+        B=256, K=8, L=8, V=151936, d=4096, logit_std=3.0, agree=0.6, ragged=True, seed=1006),
+}
+
+LM_HEAD_HEADLINE = "lmhead-greedy-B256-K8-L8-V151936-d4096"
+
+
+@dataclass
+class LmHeadBatch:
+    name: str
+    B: int
+    K: int
+    L: int
+    V: int
+    d: int
+    hidden: torch.Tensor   # [B][K][L+1][d] bf16
+    lm_head: torch.Tensor  # [V][d] bf16
+    tokens: torch.Tensor   # [B][K][L] int32
+    lengths: torch.Tensor  # [B] int32
+    meta: dict = field(default_factory=dict)
+
+    def to(self, device):
+        kw = {k: getattr(self, k) for k in ("name", "B", "K", "L", "V", "d")}
+        for k in ("hidden", "lm_head", "tokens", "lengths"):
+            kw[k] = getattr(self, k).to(device)
+        return LmHeadBatch(meta=dict(self.meta), **kw)
+
+    @property
+    def positions(self) -> int:
+        return int(self.lengths.to(torch.int64).sum().item()) * self.K
+
+
+def make_lm_head(workload, device="cpu", *, seed: Optional[int] = None, B: Optional[int] = None,
+                 K: Optional[int] = None, L: Optional[int] = None, V: Optional[int] = None,
+                 d: Optional[int] = None, lengths=None, integer: int = 0, poison_unread: bool = False,
+                 agree: Optional[float] = None) -> LmHeadBatch:
+    """One batch for greedy verification fused into the LM head.
+
+    W ~ N(0, logit_std^2 / d) and hidden ~ N(0, 1), so logits have std about
+    logit_std.  Drafts are built depth by depth like a greedy draft model
+    that agrees with the target: draft k's next token is the target row's
+    argmax (found with torch) with probability ``agree``, else a uniform
+    token; drafts sharing a prefix share its hidden row.  ``integer`` > 0
+    draws every entry of hidden and W uniformly from -integer..integer
+    instead (exact logits, many ties).  With ``poison_unread`` the rows the
+    method never reads (past a request's length, duplicate copies of a
+    shared prefix's row) hold NaN.
+    """
+    cfg = dict(LM_HEAD_WORKLOADS[workload]) if isinstance(workload, str) else dict(workload)
+    name = workload if isinstance(workload, str) else cfg.get("name", "custom")
+    for k, v in (("B", B), ("K", K), ("L", L), ("V", V), ("d", d), ("agree", agree)):
+        if v is not None:
+            cfg[k] = v
+    B_, K_, L_, V_, d_ = cfg["B"], cfg["K"], cfg["L"], cfg["V"], cfg["d"]
+    seed = cfg["seed"] if seed is None else seed
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed))
+
+    def draw(*shape, scale=1.0):
+        if integer:
+            return torch.randint(-integer, integer + 1, shape, generator=g, device=dev).to(torch.float32)
+        return torch.randn(*shape, generator=g, device=dev) * scale
+
+    W = draw(V_, d_, scale=cfg["logit_std"] / d_ ** 0.5).to(torch.bfloat16)
+    Wf = W.to(torch.float32)
+    hidden = torch.empty((B_, K_, L_ + 1, d_), dtype=torch.bfloat16, device=dev)
+    tokens = torch.zeros((B_, K_, L_), dtype=torch.int32, device=dev)
+    if lengths is not None:
+        lens = torch.as_tensor(lengths, dtype=torch.int32, device=dev).clone()
+    elif cfg["ragged"] and L_ > 0:
+        lens = torch.randint(1, L_ + 1, (B_,), generator=g, device=dev, dtype=torch.int64).to(torch.int32)
+    else:
+        lens = torch.full((B_,), L_, dtype=torch.int32, device=dev)
+    owners = []
+    for j in range(L_ + 1):
+        h = draw(B_, K_, d_).to(torch.bfloat16)
+        if j == 0:
+            owner = torch.zeros((B_, K_), dtype=torch.int64, device=dev)
+        else:
+            pre = tokens[:, :, :j]
+            same = (pre[:, :, None, :] == pre[:, None, :, :]).all(dim=-1)
+            owner = same.to(torch.int8).argmax(dim=-1)
+        owners.append(owner)
+        h = h.gather(1, owner[:, :, None].expand(B_, K_, d_))
+        hidden[:, :, j] = h
+        if j < L_:
+            rows = h.reshape(B_ * K_, d_).to(torch.float32)
+            am = torch.zeros(0, dtype=torch.int64, device=dev)
+            if B_ * K_:
+                am = torch.cat([(rows[i:i + 512] @ Wf.T).argmax(dim=-1) for i in range(0, B_ * K_, 512)])
+            pick = torch.rand(B_ * K_, generator=g, device=dev) < cfg["agree"]
+            other = torch.randint(0, V_, (B_ * K_,), generator=g, device=dev)
+            tokens[:, :, j] = torch.where(pick, am, other).view(B_, K_).to(torch.int32)
+
+    if poison_unread:
+        nan = float("nan")
+        ar = torch.arange(L_ + 1, device=dev)
+        past = ar[None, :] > lens[:, None].to(torch.int64)
+        hidden[past[:, None, :, None].expand_as(hidden)] = nan
+        if L_ > 0:
+            past_d = ar[None, :L_] >= lens[:, None].to(torch.int64)
+            tokens[past_d[:, None, :].expand_as(tokens)] = -1
+        for j, owner in enumerate(owners):
+            dup = owner != torch.arange(K_, device=dev)[None, :]
+            hidden[:, :, j][dup] = nan
+
+    meta = {k: cfg[k] for k in ("logit_std", "agree", "ragged")}
+    meta.update(seed=int(seed), integer=int(integer))
+    return LmHeadBatch(name=name, B=B_, K=K_, L=L_, V=V_, d=d_, hidden=hidden, lm_head=W, tokens=tokens,
+                       lengths=lens, meta=meta)

@@ -26,6 +26,10 @@
  *                          residual correction and target adjustment.
  *                          SpecTr-GBV page, section 2 (algorithmic
  *                          procedure, steps 1-5).
+ *   sdv_verify_greedy_lm_head  greedy verification fused into the target
+ *                          model's LM head: the logits are computed on the
+ *                          tensor cores and reduced to argmaxes without
+ *                          being stored (declared below).
  *   sdv_verify_kseq        SpecTr's K-SEQ per position, the rule whose
  *                          search for a scaling factor SpecTr-GBV avoids
  *                          (SpecTr-GBV page, sections 3-4); stated below.
@@ -307,6 +311,55 @@ int sdv_verify_multidraft_static(int B, int K, int L, int V, long long row_strid
                                  const int *lengths, const float *accept_u, const float *sample_u,
                                  int *accept_len, int *accept_draft, int *out_token, float *accept_prob,
                                  float *residual_mass, int *device_status, void *cuda_stream);
+
+/* ---------------------------------------------------------------------------
+ * The target model's LM head, and greedy verification fused into it.
+ *
+ * Verification consumes the target model's pass over the drafts
+ * ("Speculative Decoding: Performance or Illusion?", section 3.2: that pass
+ * is the verification step), and the pass ends in the LM head,
+ *   logits[r][x] = sum over i < d of hidden[r][i] * lm_head[x][i],
+ * a dense contraction over the hidden size d.  Both calls below compute it
+ * on the tensor cores from bf16 inputs with fp32 accumulation; the order in
+ * which the d products are summed is the hardware's, so a logit can differ
+ * from the exact sum by a few fp32 rounding steps of the products' sizes.
+ *
+ * sdv_verify_greedy_lm_head applies the greedy rule (as sdv_verify_greedy)
+ * to these logits without storing them: each trie node's row (one per
+ * distinct draft prefix of length 0..L_b) is computed once and reduced in
+ * the tensor-core epilogue to its maximum and first index.
+ *   B, K, L, V   as for sdv_verify_greedy; d hidden size, a multiple of 8 in
+ *                8..65536.
+ *   hidden       [B][K][L+1][d] bf16: row (b,k,j) is the target model's
+ *                final hidden state after draft k's first j tokens (rows of
+ *                drafts sharing those tokens are read from the lowest such
+ *                draft; rows past L_b are never read).  16-byte aligned.
+ *   lm_head      [V][d] bf16, one row per vocabulary entry; 16-byte aligned.
+ *   draft_tokens, lengths, accept_len, accept_draft, out_token, accept_prob,
+ *   device_status  as for sdv_verify_greedy.  A node whose logits hold NaN
+ *                or +Inf marks its request SDV_REQ_NONFINITE.
+ *   workspace    device scratch of at least sdv_lm_head_workspace_bytes(B,
+ *                K, L, V, d) bytes, 256-byte aligned (it holds the nodes'
+ *                hidden rows: about B*K*(L+1)*d*2 bytes).
+ * Returns SDV_OK, SDV_ERR_INVALID, SDV_ERR_WORKSPACE, SDV_ERR_UNSUPPORTED (no
+ * tensor-map encoder in the driver, or not enough shared memory) or
+ * SDV_ERR_CUDA.  The profiling hook brackets the LM-head kernel. */
+int sdv_verify_greedy_lm_head(int B, int K, int L, int V, int d, const void *hidden, const void *lm_head,
+                              const int *draft_tokens, const int *lengths, int *accept_len, int *accept_draft,
+                              int *out_token, float *accept_prob, int *device_status, void *workspace,
+                              size_t workspace_bytes, void *cuda_stream);
+
+/* Workspace bytes of sdv_verify_greedy_lm_head; 0 for invalid sizes. */
+size_t sdv_lm_head_workspace_bytes(int B, int K, int L, int V, int d);
+
+/* The LM head alone: logits [M][logits_stride] fp32 (columns >= V are not
+ * written) from hidden [M][d] and lm_head [V][d], both bf16 and 16-byte
+ * aligned; logits_stride >= V and a multiple of 4, logits 16-byte aligned;
+ * d as above; V in 1..SDV_MAX_V.  device_status (or NULL) is zeroed and
+ * gets SDV_DEV_TIMEOUT if a device wait gave up.  Returns SDV_OK,
+ * SDV_ERR_INVALID, SDV_ERR_UNSUPPORTED or SDV_ERR_CUDA. */
+int sdv_lm_head_logits(int M, int V, int d, const void *hidden, const void *lm_head, float *logits,
+                       long long logits_stride, int *device_status, void *cuda_stream);
 
 /* Profiling hook.  With start and stop both cudaEvent_t handles, every
  * later call made from the calling host thread records `start` on its
