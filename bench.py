@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, token mode and CPU baseline")
     ap.add_argument("--cpu-requests", type=int, default=8, help="requests in the oracle's timed sample")
+    ap.add_argument("--lm-head-only", action="store_true",
+                    help="only the LM-head-fused greedy measurement (--B sets its batch size)")
     return ap.parse_args()
 
 
@@ -148,7 +150,7 @@ def lm_head_bench(args, dev, stream, rank, world):
     import draft_verification_row_gb300 as sdv
     from draft_verification_row_gb300 import binding, workloads as W
 
-    lb = W.make_lm_head(W.LM_HEAD_HEADLINE, dev, seed=rank_seed(W.LM_HEAD_HEADLINE, rank))
+    lb = W.make_lm_head(W.LM_HEAD_HEADLINE, dev, seed=rank_seed(W.LM_HEAD_HEADLINE, rank), B=args.B)
     inner, leaves = trie_nodes(lb.tokens, lb.lengths, lb.K)
     rows = inner + leaves  # one logit row per trie node, leaves included
     out = binding.LmHeadOutputs(lb.B, lb.K, lb.L, lb.V, lb.d, dev)
@@ -376,6 +378,11 @@ def run_ours(args, world, rank, local):
     from draft_verification_row_gb300 import binding, workloads as W
 
     dev = torch.device(f"cuda:{local}")
+    if args.lm_head_only:
+        r = lm_head_bench(args, dev, torch.cuda.current_stream(dev), rank, world)
+        if rank == 0:
+            print(json.dumps(r), flush=True)
+        return
     name = args.workload or W.HEADLINE
     seed = rank_seed(name, rank)
     batch = W.make(name, dev, seed=seed, B=args.B)
@@ -565,7 +572,7 @@ def run_ours(args, world, rank, local):
                             "gpu_launches_per_step": emu.L + 3}  # L sampling launches + prep, node, finish
         del emu
         # the next row: greedy verification fused into the target LM head
-        line["next_lm_head"] = lm_head_bench(args, dev, stream, rank, world)
+        line["next_lm_head"] = lm_head_bench(args, dev, stream, rank, world) if args.B is None else None
         if rank == 0:
             rng = np.random.default_rng(1)
             req = sorted(rng.choice(batch.B, size=min(args.cpu_requests, batch.B), replace=False).tolist())
