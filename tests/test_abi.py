@@ -110,3 +110,34 @@ def test_read_rows_bytes_match_the_trie(lib):
     inner0, leaves0 = bench.trie_nodes(batch.tokens[1:], batch.lengths[1:], batch.K)
     assert sdv.read_rows_bytes(batch.tokens, lengths, batch.V, batch.stride, batch.target.dtype) == \
         (2 * inner0 + leaves0) * batch.stride * 2
+
+
+def test_lm_head_workspace_bytes(lib):
+    n = 256 * 8 * 9
+    ws = lib.sdv_lm_head_workspace_bytes(256, 8, 8, 151936, 4096)
+    # the verification workspace, the nodes' hidden rows, their keys and map
+    assert ws >= lib.sdv_workspace_bytes(1, 256, 8, 8, 151936) + n * (4096 * 2 + 8 + 4)
+    for bad in [(1, 1, 1, 16, 0), (1, 1, 1, 16, 12), (1, 1, 1, 16, 1 << 17), (1, 0, 1, 16, 64),
+                (1, 1, 17, 16, 64), (1, 1, 1, 262145, 64), (-1, 1, 1, 16, 64)]:
+        assert lib.sdv_lm_head_workspace_bytes(*bad) == 0, bad
+
+
+@pytest.mark.parametrize("over", [dict(d=0), dict(d=12), dict(d=1 << 17), dict(K=0), dict(K=17), dict(L=17),
+                                  dict(V=0), dict(V=262145), dict(B=-1)])
+def test_lm_head_invalid_sizes_rejected_without_gpu(lib, over):
+    a = dict(B=2, K=1, L=2, V=16, d=64)
+    a.update(over)
+    assert lib.sdv_verify_greedy_lm_head(a["B"], a["K"], a["L"], a["V"], a["d"], *([None] * 10), 0, None) == 1
+
+
+@pytest.mark.parametrize("over", [dict(M=-1), dict(V=0), dict(V=262145, stride=262148), dict(d=4), dict(d=20),
+                                  dict(stride=12), dict(stride=18)])
+def test_lm_head_logits_invalid_rejected_without_gpu(lib, over):
+    a = dict(M=2, V=16, d=64, stride=16)
+    a.update(over)
+    assert lib.sdv_lm_head_logits(a["M"], a["V"], a["d"], None, None, None, a["stride"], None, None) == 1
+
+
+def test_lm_head_empty_is_a_no_op(lib):
+    assert lib.sdv_verify_greedy_lm_head(0, 2, 2, 16, 64, *([None] * 10), 0, None) == 0
+    assert lib.sdv_lm_head_logits(0, 16, 64, None, None, None, 16, None, None) == 0
