@@ -245,12 +245,12 @@ static void build_trie(req_t* r)
 }
 
 /* Request status: bad length, else bad token, else an unusable row among
- * the rows every decision reads: each trie node's target and draft rows,
- * except a leaf's target row in the sampling rules.  A leaf's P enters
- * nothing but its bonus draw (its residual is p P, of mass p), so its row
- * is read, and checked, only when the decision ends at that leaf
- * (draw_correction), just as rows past L_b are never read.  Greedy
- * matching takes every node's argmax, leaves included. */
+ * the rows every decision reads: each inner trie node's target row, and its
+ * draft row in the sampling rules.  A leaf's row enters nothing but the
+ * token drawn there (in the sampling rules its residual is p P, of mass p;
+ * greedy takes its argmax as the correction), so it is read, and checked,
+ * only when the decision ends at that leaf (draw_correction, run_greedy),
+ * just as rows past L_b are never read. */
 static int request_status(req_t* r)
 {
     const sdvo_problem* pb = r->pb;
@@ -264,7 +264,7 @@ static int request_status(req_t* r)
     for (int j = 0; j <= r->Lb; ++j)
         for (int o = 0; o < pb->K; ++o) {
             if (r->owner[j][o] != o) continue;
-            if ((r->greedy || j < r->Lb) && !row_usable(pb, row_of(pb, 1, r->b, o, j)))
+            if (j < r->Lb && !row_usable(pb, row_of(pb, 1, r->b, o, j)))
                 st = SDVO_REQ_NONFINITE;
             if (!r->greedy && j < r->Lb && !row_usable(pb, row_of(pb, 0, r->b, o, j)))
                 st = SDVO_REQ_NONFINITE;
@@ -588,11 +588,11 @@ static int run_kseq(req_t* r, float* accept_prob, outcome_t* out, double* residu
 /* Greedy T = 0: a draft position matches when its token is the row's
  * argmax; the longest matching draft wins (lowest k on ties); the
  * correction is the argmax after the accepted prefix. */
-static void run_greedy(req_t* r, float* accept_prob, outcome_t* out, double* residual_out)
+static int run_greedy(req_t* r, float* accept_prob, outcome_t* out, double* residual_out)
 {
     const sdvo_problem* pb = r->pb;
     int best = -1, bestk = 0;
-    for (int d = 0; d <= r->Lb; ++d)
+    for (int d = 0; d < r->Lb; ++d) /* the inner nodes' argmaxes decide the matches */
         for (int v = 0; v < pb->K; ++v)
             if (r->owner[d][v] == v) r->am[d][v] = argmax_row(pb, row_of(pb, 1, r->b, v, d));
     for (int k = 0; k < pb->K; ++k) {
@@ -608,12 +608,19 @@ static void run_greedy(req_t* r, float* accept_prob, outcome_t* out, double* res
     }
     out->tau = best;
     out->kstar = bestk;
-    out->token = r->am[best][r->owner[best][bestk]];
+    if (best == r->Lb) { /* a leaf: its row is read only now, for the correction */
+        const unsigned char* row = row_of(pb, 1, r->b, r->owner[best][bestk], best);
+        if (!row_usable(pb, row)) return SDVO_REQ_NONFINITE;
+        out->token = argmax_row(pb, row);
+    } else {
+        out->token = r->am[best][r->owner[best][bestk]];
+    }
     out->mass = 1.0;
     if (residual_out) {
         for (int x = 0; x < pb->V; ++x) residual_out[x] = 0.0;
         residual_out[out->token] = 1.0;
     }
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -661,7 +668,7 @@ int sdvo_verify(int mode, const sdvo_problem* pb, int* accept_len, int* accept_d
         if (ro) memset(ro, 0, sizeof(double) * (size_t)pb->V);
         st = request_status(&r);
         if (st == 0) {
-            if (greedy) run_greedy(&r, ap, &out, ro);
+            if (greedy) st = run_greedy(&r, ap, &out, ro);
             else if (mode == SDVO_MODE_TOKEN) st = run_token(&r, ap, &out, ro);
             else if (mode == SDVO_MODE_BLOCK) st = run_block(&r, ap, &out, ro);
             else if (mode == SDVO_MODE_KSEQ) st = run_kseq(&r, ap, &out, ro);

@@ -196,14 +196,46 @@ def test_leaf_rows_are_unread_when_a_draft_position_is_rejected(mode, K):
         np.testing.assert_array_equal(o[key], base[key])
 
 
-def test_greedy_reads_every_leaf_row():
-    """Greedy matching takes each node's argmax, a leaf's included."""
-    d = _problem()
+def test_greedy_reads_a_leaf_row_only_where_the_decision_ends():
+    """Greedy's matches use the inner nodes' argmaxes; a leaf's argmax is the
+    correction only when the decision ends there.  Draft 0 follows its rows'
+    argmax path, so every request ends at draft 0's leaf: the other leaves
+    are never read, and poisoning draft 0's leaf invalidates that request
+    alone."""
+    d = _problem(K=3)
     for b in range(3):
-        e = _problem()
-        leaves = _leaves(e, b)
-        e["target"][b, leaves[-1], e["lengths"][b], 0] = np.nan
-        o = _run("greedy", e)
-        assert o["req_status"][b] == oracle.REQ_NONFINITE
-        assert o["out_token"][b] == -1
-    assert (_run("greedy", d)["req_status"] == 0).all()
+        for j in range(d["lengths"][b]):
+            d["tokens"][b, 0, j] = np.argmax(d["target"][b, 0, j])
+        d["tokens"][b, 1, 0] = d["tokens"][b, 0, 0]  # the fixture's shared first token
+    base = _run("greedy", d)
+    assert (base["req_status"] == 0).all()
+    np.testing.assert_array_equal(base["accept_len"], d["lengths"])
+    np.testing.assert_array_equal(base["accept_draft"], 0)
+    for b in range(3):
+        np.testing.assert_equal(base["out_token"][b], np.argmax(d["target"][b, 0, d["lengths"][b]]))
+        for k in _leaves(d, b)[1:]:
+            d["target"][b, k, d["lengths"][b], 1] = np.nan
+    o = _run("greedy", d)
+    assert (o["req_status"] == 0).all()
+    for key in ("accept_len", "accept_draft", "out_token", "accept_prob"):
+        np.testing.assert_array_equal(o[key], base[key])
+    d["target"][2, 0, d["lengths"][2], 4] = np.inf
+    o = _run("greedy", d)
+    assert o["req_status"].tolist() == [0, 0, oracle.REQ_NONFINITE]
+    assert o["accept_len"][2] == 0 and o["accept_draft"][2] == 0 and o["out_token"][2] == -1
+    assert (o["accept_prob"][2] == 0).all()
+    for key in ("accept_len", "out_token", "accept_prob"):
+        np.testing.assert_array_equal(o[key][:2], base[key][:2])
+
+
+def test_greedy_that_stops_short_reads_no_leaf():
+    d = _problem(K=2, seed=5)
+    base = _run("greedy", d)
+    short = [b for b in range(3) if base["accept_len"][b] < d["lengths"][b]]
+    assert short, "the fixture should stop short somewhere"
+    for b in short:
+        d["target"][b, :, d["lengths"][b]] = np.nan
+    o = _run("greedy", d)
+    assert (o["req_status"] == 0).all()
+    for key in ("accept_len", "accept_draft", "out_token", "accept_prob"):
+        np.testing.assert_array_equal(o[key], base[key])
