@@ -152,7 +152,7 @@ def lm_head_bench(args, dev, stream, rank, world):
 
     lb = W.make_lm_head(W.LM_HEAD_HEADLINE, dev, seed=rank_seed(W.LM_HEAD_HEADLINE, rank), B=args.B)
     inner, leaves = trie_nodes(lb.tokens, lb.lengths, lb.K)
-    rows = inner + leaves  # one logit row per trie node, leaves included
+    rows = inner  # the main LM-head pass: one logit row per inner trie node
     out = binding.LmHeadOutputs(lb.B, lb.K, lb.L, lb.V, lb.d, dev)
 
     def fused():
@@ -166,6 +166,8 @@ def lm_head_bench(args, dev, stream, rank, world):
         raise RuntimeError(f"fused LM head: device status {int(out.device_status.item())}")
     ms, gemm_ms = total / args.steps, gemm / args.steps
     flops = 2.0 * rows * lb.V * lb.d
+    # the leaf pass: one row per request whose decision ends at a leaf
+    ended_at_leaf = int((out.accept_len == lb.lengths).sum().item())
     tflops = flops / (gemm_ms / 1000.0) / 1e12
     peak, kind = measured_bf16_peak()
     # cuBLAS on the same GEMM shape (rows x V x d, bf16 logits written)
@@ -196,10 +198,12 @@ def lm_head_bench(args, dev, stream, rank, world):
     positions = sum_over_ranks(lb.positions, world)
     return {
         "what": "greedy verification fused into the target LM head: logits = hidden . W^T on tcgen05, each "
-                "trie node's row reduced to its argmax in the epilogue (logits never stored)",
-        "workload": W.LM_HEAD_HEADLINE, "rows": rows, "V": lb.V, "d": lb.d,
+                "inner trie node's row reduced to its argmax in the epilogue (logits never stored); after the "
+                "decision, a second pass over the leaves the decisions end at",
+        "workload": W.LM_HEAD_HEADLINE, "rows": rows, "leaf_rows": ended_at_leaf, "leaves_in_trie": leaves,
+        "V": lb.V, "d": lb.d,
         "metric": "verified draft positions/s", "value": positions / (ms / 1000.0), "unit": "positions/s",
-        "ms_per_call": ms, "lm_head_kernel_ms": gemm_ms, "gpu_launches_per_call": 5,
+        "ms_per_call": ms, "lm_head_kernel_ms": gemm_ms, "gpu_launches_per_call": 8,
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "peak_kind": f"{kind} bf16_tflops (burst)",
                      "algorithmic_flops_per_call": flops, "kernel": "lm_head_kernel<ARGMAX>"},

@@ -32,11 +32,14 @@ size_t workspace_size(int B, int K, int L)
 bool lm_d_ok(int d) { return d >= 8 && d % 8 == 0 && d <= (1 << 16); }
 
 // Fused greedy call: the verification workspace, then the node rows of the
-// LM head (compact map, row count, argmax keys, hidden rows).
+// LM head (compact map, row count, argmax keys, hidden rows), then the end
+// leaves (pending slot and request per leaf, count, keys, hidden rows).
 size_t lm_workspace_size(int B, int K, int L, int d)
 {
     const size_t n = slot_count(B, K, L);
-    return workspace_size(B, K, L) + align_up(n * 4) + align_up(4) + align_up(n * 8) + align_up(n * (size_t)d * 2);
+    const size_t nb = (size_t)B;
+    return workspace_size(B, K, L) + align_up(n * 4) + align_up(4) + align_up(n * 8) + align_up(n * (size_t)d * 2) +
+           2 * align_up(nb * 4) + align_up(4) + align_up(nb * 8) + align_up(nb * (size_t)d * 2);
 }
 
 Workspace carve(void* base, int B, int K, int L)
@@ -234,6 +237,16 @@ int verify_greedy_lm_head(int B, int K, int L, int V, int d, const void* hidden,
     r.keys = reinterpret_cast<unsigned long long*>(p);
     p += align_up(n * 8);
     r.rows = p;
+    p += align_up(n * (size_t)d * 2);
+    pb.leaf_pending = reinterpret_cast<int*>(p);
+    p += align_up((size_t)B * 4);
+    r.leaf_req = reinterpret_cast<int*>(p);
+    p += align_up((size_t)B * 4);
+    r.leaf_count = reinterpret_cast<int*>(p);
+    p += align_up(4);
+    r.leaf_keys = reinterpret_cast<unsigned long long*>(p);
+    p += align_up((size_t)B * 8);
+    r.leaf_rows = p;
     LmArgs a;
     std::memset(&a, 0, sizeof a);
     a.rows_dev = r.count;
@@ -245,6 +258,7 @@ int verify_greedy_lm_head(int B, int K, int L, int V, int d, const void* hidden,
     if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
     if (cudaMemsetAsync(pb.ws.ncount, 0, sizeof(int) * (2 * L + 3), st) != cudaSuccess) return SDV_ERR_CUDA;
     if (cudaMemsetAsync(r.count, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (cudaMemsetAsync(r.leaf_count, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
     if (launch_prep(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
     if (launch_lm_rows(pb, r, st) != cudaSuccess) return SDV_ERR_CUDA;
     if (!prof_record(g_prof_start, st)) return SDV_ERR_CUDA;
@@ -256,7 +270,14 @@ int verify_greedy_lm_head(int B, int K, int L, int V, int d, const void* hidden,
     if (e != cudaSuccess) return SDV_ERR_CUDA;
     if (!prof_record(g_prof_stop, st)) return SDV_ERR_CUDA;
     if (launch_lm_argmax(pb, r, st) != cudaSuccess) return SDV_ERR_CUDA;
+    // the decision; where it ends at a leaf, that leaf's row is computed now
     if (launch_finish(pb, true, st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_lm_leaf_rows(pb, r, st) != cudaSuccess) return SDV_ERR_CUDA;
+    LmArgs la = a;
+    la.rows_dev = r.leaf_count;
+    la.keys = r.leaf_keys;
+    if (launch_lm_head(r.leaf_rows, (long long)B, lm_head, la, LM_EPI_ARGMAX, st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_lm_leaf_token(pb, r, st) != cudaSuccess) return SDV_ERR_CUDA;
     return SDV_OK;
 }
 

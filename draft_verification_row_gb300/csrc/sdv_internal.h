@@ -53,6 +53,7 @@ struct Problem {
     float* accept_prob;
     float* residual_mass;
     int* device_status;
+    int* leaf_pending;  // greedy with the LM head: [B] end leaf slot whose argmax is still to come, or -1
     Workspace ws;
 };
 
@@ -119,9 +120,16 @@ struct LmRows {
     int* compact;              // [slots]: node slot -> its row
     int* count;                // rows listed
     unsigned long long* keys;  // [slots]
+    // the end leaves the decision reached, one per request at most
+    void* leaf_rows;                // [B][d] bf16
+    int* leaf_req;                  // [B]: request of each listed leaf
+    int* leaf_count;
+    unsigned long long* leaf_keys;  // [B]
 };
 cudaError_t launch_lm_rows(const Problem& pb, const LmRows& r, cudaStream_t st);
 cudaError_t launch_lm_argmax(const Problem& pb, const LmRows& r, cudaStream_t st);
+cudaError_t launch_lm_leaf_rows(const Problem& pb, const LmRows& r, cudaStream_t st);
+cudaError_t launch_lm_leaf_token(const Problem& pb, const LmRows& r, cudaStream_t st);
 
 // The node kernel's launch shape: persistent CTAs per SM, threads per CTA
 // and dynamic shared memory.

@@ -93,7 +93,7 @@ __global__ void prep_kernel(Problem pb)
 }
 
 // ------------------------------------------------------------------------
-// greedy argmax: one CTA per node, streaming
+// greedy argmax: one CTA per inner node, streaming
 
 template <int DT>
 __global__ void __launch_bounds__(256) argmax_kernel(Problem pb)
@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(256) argmax_kernel(Problem pb)
     const int b = slot / (K * (L + 1));
     if (pb.ws.req[b] & (SDV_REQ_BAD_LENGTH | SDV_REQ_BAD_TOKEN)) return;
     const int Lb = pb.lengths ? pb.lengths[b] : L;
-    if (j > Lb || pb.ws.owner[slot] != k) return;
+    // inner nodes only: a leaf's argmax is taken where the decision ends there
+    if (j >= Lb || pb.ws.owner[slot] != k) return;
     const size_t row = ((size_t)b * K + k) * (L + 1) + j;
     const uint4* g = reinterpret_cast<const uint4*>(static_cast<const char*>(pb.target) +
                                                     row * (size_t)pb.stride * E::kBytes);

@@ -21,11 +21,16 @@
 //                   Epilogues: ARGMAX folds the tile's maximum and its first
 //                   index into one 64-bit atomicMax per row (the logits
 //                   never reach memory); LOGITS stores the fp32 logits.
-// lm_rows_kernel    one CTA per request: numbers the request's trie nodes
-//                   (one per distinct draft prefix of length 0..L_b) and
-//                   copies their hidden rows into one contiguous block, the
-//                   GEMM's A operand.
+// lm_rows_kernel    one CTA per request: numbers the request's inner trie
+//                   nodes (one per distinct draft prefix of length
+//                   0..L_b - 1) and copies their hidden rows into one
+//                   contiguous block, the GEMM's A operand.
 // lm_argmax_kernel  one thread per node: its argmax out of the 64-bit key.
+// Leaves (depth L_b) are not listed: greedy matching uses the inner nodes'
+// argmaxes only, and a leaf's argmax is the correction only where the
+// decision ends there.  After the decision, lm_leaf_rows_kernel lists those
+// leaves (one per request at most), the LM head runs again over them, and
+// lm_leaf_token_kernel writes their tokens.
 //
 // Tiles are ordered vocabulary-major (consecutive tiles share a W tile), so
 // the CTAs running at one time read the same few MB of W from L2 while all
@@ -352,7 +357,7 @@ __global__ void __launch_bounds__(256) lm_rows_kernel(Problem pb, LmRows r)
     if (pb.ws.req[b] & (SDV_REQ_BAD_LENGTH | SDV_REQ_BAD_TOKEN)) return;
     const int K = pb.K, L = pb.L;
     const int Lb = pb.lengths ? pb.lengths[b] : L;
-    const int n = K * (Lb + 1);  // slots of depths 0..L_b, depth-major
+    const int n = K * Lb;  // slots of depths 0..L_b - 1 (inner nodes), depth-major
     const size_t s0 = (size_t)b * (L + 1) * K;
     __shared__ short local[SDV_MAX_K * (SDV_MAX_L + 1)];
     __shared__ int cnt, base;
@@ -392,7 +397,7 @@ __global__ void lm_argmax_kernel(Problem pb, LmRows r)
     const int b = (int)(slot / ((size_t)K * (L + 1)));
     if (pb.ws.req[b] & (SDV_REQ_BAD_LENGTH | SDV_REQ_BAD_TOKEN)) return;
     const int Lb = pb.lengths ? pb.lengths[b] : L;
-    if (j > Lb || pb.ws.owner[slot] != k) return;
+    if (j >= Lb || pb.ws.owner[slot] != k) return;
     const unsigned long long key = r.keys[r.compact[slot]];
     const float v = key_value(key);
     int am = (int)(0xffffffffu - (uint32_t)key);
@@ -402,6 +407,51 @@ __global__ void lm_argmax_kernel(Problem pb, LmRows r)
         am = -1;
     }
     pb.ws.am[slot] = am;
+}
+
+// The end leaves the decision reached: one CTA per request copies its
+// leaf's hidden row, if it has one, into the leaf block.
+__global__ void __launch_bounds__(128) lm_leaf_rows_kernel(Problem pb, LmRows r)
+{
+    const int b = blockIdx.x;
+    const int slot = pb.leaf_pending[b];
+    if (slot < 0) return;
+    const int K = pb.K, L = pb.L;
+    const int k = slot % K, j = (slot / K) % (L + 1);
+    __shared__ int c;
+    if (threadIdx.x == 0) {
+        c = atomicAdd(r.leaf_count, 1);
+        r.leaf_req[c] = b;
+        r.leaf_keys[c] = 0ull;
+    }
+    __syncthreads();
+    const int units = r.d / 8;
+    const uint4* src = reinterpret_cast<const uint4*>(r.hidden) + (((size_t)b * K + k) * (L + 1) + j) * units;
+    uint4* dst = reinterpret_cast<uint4*>(r.leaf_rows) + (size_t)c * units;
+    for (int e = threadIdx.x; e < units; e += blockDim.x) dst[e] = src[e];
+}
+
+// The reached leaves' tokens: the argmax, or the request made invalid when
+// the leaf's logits hold NaN or +Inf (or nothing finite).
+__global__ void lm_leaf_token_kernel(Problem pb, LmRows r)
+{
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= *r.leaf_count) return;
+    const int b = r.leaf_req[c];
+    const unsigned long long key = r.leaf_keys[c];
+    const float v = key_value(key);
+    if (v > -INFINITY && v < INFINITY) {
+        pb.out_token[b] = (int)(0xffffffffu - (uint32_t)key);
+        return;
+    }
+    const int n = pb.K * pb.L;
+    if (pb.accept_prob)
+        for (int i = 0; i < n; ++i) pb.accept_prob[(size_t)b * n + i] = 0.f;
+    pb.accept_len[b] = 0;
+    pb.accept_draft[b] = 0;
+    pb.out_token[b] = -1;
+    atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
+    if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
 }
 
 // ------------------------------------------------------------------------
@@ -486,6 +536,18 @@ cudaError_t launch_lm_head(const void* hidden, long long hidden_rows, const void
 cudaError_t launch_lm_rows(const Problem& pb, const LmRows& r, cudaStream_t st)
 {
     lm_rows_kernel<<<pb.B, 256, 0, st>>>(pb, r);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lm_leaf_rows(const Problem& pb, const LmRows& r, cudaStream_t st)
+{
+    lm_leaf_rows_kernel<<<pb.B, 128, 0, st>>>(pb, r);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_lm_leaf_token(const Problem& pb, const LmRows& r, cudaStream_t st)
+{
+    lm_leaf_token_kernel<<<(pb.B + 127) / 128, 128, 0, st>>>(pb, r);
     return cudaGetLastError();
 }
 

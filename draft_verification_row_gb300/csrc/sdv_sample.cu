@@ -390,7 +390,10 @@ struct DecideSmem {
 __device__ void decide_request(const Problem& pb, int b, bool greedy, DecideSmem& s, int lane)
 {
     const int K = pb.K, L = pb.L;
-    if (lane == 0) s.endn = -1;
+    if (lane == 0) {
+        s.endn = -1;
+        if (pb.leaf_pending) pb.leaf_pending[b] = -1;
+    }
     const int st = pb.ws.req[b];
     float* ap = pb.accept_prob ? pb.accept_prob + (size_t)b * K * L : nullptr;
     if (st) {
@@ -461,8 +464,16 @@ __device__ void decide_request(const Problem& pb, int b, bool greedy, DecideSmem
         eo = own[best * K + bestk];
         pb.accept_len[b] = best;
         pb.accept_draft[b] = bestk;
-        pb.out_token[b] = __float_as_int(val[ej * K + eo]);
         if (pb.residual_mass) pb.residual_mass[b] = 1.f;
+        const size_t se = s0 + (size_t)ej * K + eo;
+        if (ej < Lb) {
+            pb.out_token[b] = __float_as_int(val[ej * K + eo]);
+        } else if (pb.leaf_pending) {  // the LM head computes this leaf's row afterwards
+            pb.out_token[b] = -1;
+            pb.leaf_pending[b] = (int)se;
+        } else {  // a leaf: its row is read now, by the CTA (its argmax is the correction)
+            s.endn = (int)(se | (1u << 30));
+        }
         return;
     }
     if (token) {
@@ -572,7 +583,7 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy)
     const size_t slot = (size_t)(e & ((1 << 30) - 1));
     const bool leaf = (e >> 30) != 0;
     const int k = (int)(slot % K), j = (int)((slot / K) % (L + 1));
-    const float u = pb.sample_u[((size_t)b * K + k) * (L + 1) + j];
+    const float u = greedy ? 0.f : pb.sample_u[((size_t)b * K + k) * (L + 1) + j];
     const int n_seg = ((V + EPU - 1) / EPU + kRSeg - 1) / kRSeg;
     Dist d;
     d.rowT = static_cast<const char*>(pb.target) + (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
@@ -594,7 +605,7 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy)
         residual_pass<DT>(d, V, sm, lane, w);
         __syncthreads();
     } else {
-        softmax_pass<DT>(d.rowT, V, d.c, false, sm, lane, w);
+        softmax_pass<DT>(d.rowT, V, d.c, greedy != 0, sm, lane, w);
         __syncthreads();
         float M;
         if (!row_max(sm, n_seg, lane, M)) {
@@ -608,7 +619,7 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy)
         d.negM = -(M * d.c);
     }
     if (w == 0) {
-        const int x = draw<DT>(d, sm, V, u, false, lane);
+        const int x = draw<DT>(d, sm, V, u, greedy != 0, lane);
         if (lane == 0) pb.out_token[b] = x;
     }
 }

@@ -131,10 +131,11 @@ enum {
  *                conditioned on draft k's first j tokens.  Only the rows of
  *                trie nodes are read: row (b,k,j) with j <= lengths[b] and k
  *                the lowest-index draft with that prefix (row 0: k = 0).
- *                In the sampling rules a leaf's row (j = lengths[b]) is read
- *                only if the decision ends at that leaf, for the bonus draw
- *                (a leaf has no draws; its residual p P has mass p whatever
- *                P is); greedy reads every node's row.
+ *                A leaf's row (j = lengths[b]) is read only if the decision
+ *                ends at that leaf, for the token drawn there: a leaf has
+ *                no draws (in the sampling rules its residual p P has mass
+ *                p whatever P is; greedy matching uses the inner nodes'
+ *                argmaxes, and the leaf's is the correction).
  *   draft_logits [B][K][L][row_stride], 16-byte aligned; same rule with
  *                j < lengths[b].  May be NULL when L = 0 or for greedy.
  *   draft_tokens [B][K][L] int32; positions j >= lengths[b] are ignored.
@@ -325,9 +326,11 @@ int sdv_verify_multidraft_static(int B, int K, int L, int V, long long row_strid
  * from the exact sum by a few fp32 rounding steps of the products' sizes.
  *
  * sdv_verify_greedy_lm_head applies the greedy rule (as sdv_verify_greedy)
- * to these logits without storing them: each trie node's row (one per
- * distinct draft prefix of length 0..L_b) is computed once and reduced in
- * the tensor-core epilogue to its maximum and first index.
+ * to these logits without storing them: each inner trie node's row (one per
+ * distinct draft prefix of length 0..L_b - 1) is computed once and reduced
+ * in the tensor-core epilogue to its maximum and first index; after the
+ * decision, the one leaf row a request ends at (if any) is computed the
+ * same way for its correction token.
  *   B, K, L, V   as for sdv_verify_greedy; d hidden size, a multiple of 8 in
  *                8..65536.
  *   hidden       [B][K][L+1][d] bf16: row (b,k,j) is the target model's

@@ -120,8 +120,9 @@ def _oracle(batch, exact=False):
     if not exact:
         bound = _err_bound(host.hidden, host.lm_head)
         top2 = np.sort(np.nan_to_num(lg, nan=-np.inf), axis=-1)[..., -2:]
-        with np.errstate(invalid="ignore"):  # unread NaN rows
+        with np.errstate(invalid="ignore", over="ignore"):  # NaN or Inf rows
             ok = top2[..., 1] - top2[..., 0] > 2 * np.nan_to_num(bound, nan=0.0).max(axis=-1)  # [B][K][L+1]
+        ok |= ~np.isfinite(lg).all(axis=-1)  # an unusable row decides by its status, not its argmax
         read = _read_rows(host.tokens.numpy(), host.lengths.numpy(), batch.L)
         unique = (ok | ~read).all(axis=(1, 2))
     return ref, unique
@@ -198,6 +199,40 @@ def test_fused_greedy_edge_cases():
     for i, b in enumerate(keep):
         if unique[i]:
             assert (al[b], ot[b]) == (ref["accept_len"][i], ref["out_token"][i])
+
+
+def test_fused_greedy_reads_only_the_leaves_it_ends_at():
+    # leaves are computed only where the decision ends there: poisoning the
+    # others changes nothing; poisoning those makes just their requests invalid
+    V, d = 1000, 64
+    batch = W.make_lm_head(WL, DEV, B=12, K=3, L=3, V=V, d=d, agree=0.6, poison_unread=True)
+    clean = {k: v.cpu().numpy() for k, v in _run(batch).items() if v is not None}
+    lens = batch.lengths.cpu().numpy()
+    tok = batch.tokens.cpu().numpy()
+    ends = []  # requests whose decision ends at a leaf, with that leaf's draft
+    for b in range(batch.B):
+        if clean["accept_len"][b] == lens[b]:
+            ks = int(clean["accept_draft"][b])
+            ends.append((b, min(k2 for k2 in range(batch.K) if (tok[b, k2, :lens[b]] == tok[b, ks, :lens[b]]).all())))
+    assert 0 < len(ends) < batch.B
+    end_set = set(ends)
+    for b in range(batch.B):
+        for k in range(batch.K):
+            if (b, k) not in end_set:
+                batch.hidden[b, k, lens[b]] = float("nan")
+    got = _run(batch)
+    assert int(got["device_status"].item()) == 0
+    for key in ("accept_len", "accept_draft", "out_token", "accept_prob"):
+        assert np.array_equal(got[key].cpu().numpy(), clean[key]), key
+    for b, k in ends:
+        batch.hidden[b, k, lens[b], 3] = float("inf")
+    got = _run(batch)
+    ref, unique = _oracle(batch)
+    _compare(batch, got, ref, unique, "poisoned end leaves")
+    assert int(got["device_status"].item()) == 4
+    ot = got["out_token"].cpu().numpy()
+    for b in range(batch.B):
+        assert (ot[b] == -1) == (b in {e[0] for e in ends})
 
 
 def test_fused_greedy_is_deterministic():

@@ -140,7 +140,7 @@ def test_leaf_rows_are_read_only_by_the_bonus_draw(name, K):
     a draw still passes where a = 1).  Every leaf row is poisoned except
     draft 0's in requests 0 and 1.  A request whose clean decision stops
     short of its leaves must come back unchanged; one that ends at a leaf,
-    invalid; greedy reads every leaf."""
+    invalid.  Greedy, too, reads a leaf only where its decision ends."""
     lengths = [3, 2, 3, 3, 1, 2, 3, 3, 2, 3]
     batch = W.make(name, DEV, B=len(lengths), K=K, L=3, V=2003, lengths=lengths, temperature=0.8)
     batch.accept_u[:3] = 0.0
@@ -158,10 +158,21 @@ def test_leaf_rows_are_read_only_by_the_bonus_draw(name, K):
         P.compare(gpu, ref, f"leaves/{mode}")
         st, c = ref["req_status"], clean[mode]
         assert (c["req_status"] == 0).all()
-        if mode == "greedy":  # draft 0 owns its whole path: its poisoned leaves are read
-            assert (st[2:] == 4).all()
-            if K == 1:
-                assert st[0] == 0 and st[1] == 0
+        if mode == "greedy":
+            # greedy ends at a leaf only where a draft matches to its end,
+            # and reads that leaf alone
+            tok = batch.tokens.cpu().numpy()
+            ended = 0
+            for b, Lb in enumerate(lengths):
+                if c["accept_len"][b] < Lb:
+                    assert st[b] == 0
+                    for key in ("accept_len", "accept_draft", "out_token"):
+                        assert ref[key][b] == c[key][b], (mode, b, key)
+                else:
+                    ended += 1
+                    ks = int(c["accept_draft"][b])
+                    owner = min(k2 for k2 in range(K) if (tok[b, k2, :Lb] == tok[b, ks, :Lb]).all())
+                    assert st[b] == (0 if b in (0, 1) and owner == 0 else 4), (b, owner)
             continue
         assert st[0] == 0 and st[1] == 0 and st[2] == 4
         assert gpu["accept_len"][0] == 3 and gpu["accept_len"][1] == 2
