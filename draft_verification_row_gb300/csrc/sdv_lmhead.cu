@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 // ------------------------------------------------------------------------
 // trie nodes of the fused greedy call
 
-__global__ void __launch_bounds__(256) lm_rows_kernel(Problem pb, LmRows r)
+__global__ void __launch_bounds__(512) lm_rows_kernel(Problem pb, LmRows r)
 {
     const int b = blockIdx.x;
     if (pb.ws.req[b] & (SDV_REQ_BAD_LENGTH | SDV_REQ_BAD_TOKEN)) return;
@@ -374,16 +374,29 @@ __global__ void __launch_bounds__(256) lm_rows_kernel(Problem pb, LmRows r)
         r.compact[s0 + i] = c0 + local[i];
         r.keys[c0 + local[i]] = 0ull;
     }
-    // copy the nodes' hidden rows, 16 bytes per thread and step
+    // copy the nodes' hidden rows: 16 bytes per thread and load, four loads
+    // in flight per thread
+    constexpr int U = 4;
     const int units = r.d / 8;
     const int total = n * units;
-    for (int u = threadIdx.x; u < total; u += blockDim.x) {
-        const int i = u / units, e = u % units;
-        if (local[i] < 0) continue;
-        const int j = i / K, k = i % K;
-        const uint4* src = reinterpret_cast<const uint4*>(r.hidden) + (((size_t)b * K + k) * (L + 1) + j) * units;
-        uint4* dst = reinterpret_cast<uint4*>(r.rows) + (size_t)(c0 + local[i]) * units;
-        dst[e] = src[e];
+    const uint4* hid = reinterpret_cast<const uint4*>(r.hidden);
+    uint4* rows = reinterpret_cast<uint4*>(r.rows);
+    for (int u0 = threadIdx.x; u0 < total; u0 += U * blockDim.x) {
+        uint4 v[U];
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int u = u0 + q * blockDim.x;
+            if (u < total && local[u / units] >= 0) {
+                const int i = u / units, j = i / K, k = i % K;
+                v[q] = hid[(((size_t)b * K + k) * (L + 1) + j) * units + u % units];
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int u = u0 + q * blockDim.x;
+            if (u < total && local[u / units] >= 0)
+                rows[(size_t)(c0 + local[u / units]) * units + u % units] = v[q];
+        }
     }
 }
 
@@ -535,7 +548,7 @@ cudaError_t launch_lm_head(const void* hidden, long long hidden_rows, const void
 
 cudaError_t launch_lm_rows(const Problem& pb, const LmRows& r, cudaStream_t st)
 {
-    lm_rows_kernel<<<pb.B, 256, 0, st>>>(pb, r);
+    lm_rows_kernel<<<pb.B, 512, 0, st>>>(pb, r);
     return cudaGetLastError();
 }
 
