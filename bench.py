@@ -456,7 +456,7 @@ def run_ours(args, world, rank, local):
         # recursive rejection sampling) and SpecTr's K-SEQ, whose search
         # for rho SpecTr-GBV avoids (the pages' "verification overhead")
         line["modes"] = {}
-        for other in [m for m in ("multidraft", "token", "kseq") if m != args.mode]:
+        for other in [m for m in ("multidraft", "token", "kseq", "greedy") if m != args.mode]:
             out2 = binding.Outputs(other, batch.B, batch.K, batch.L, batch.V, dev)
             call2 = make_call(other, out2)
             for _ in range(max(2, args.warmup // 2)):
@@ -467,7 +467,9 @@ def run_ours(args, world, rank, local):
             line["modes"][other] = {"value": all_positions / (t2 / args.steps / 1000.0), "unit": UNIT,
                                     "ms_per_step": t2 / args.steps,
                                     "node_kernel_ms_per_step": r2 / args.steps,
-                                    "algorithmic_gbs": alg_bytes / (r2 / args.steps / 1000.0) / 1e9}
+                                    # greedy reads target rows only: one V esz per position
+                                    "algorithmic_gbs": (alg_bytes // 2 if other == "greedy" else alg_bytes)
+                                    / (r2 / args.steps / 1000.0) / 1e9}
             del out2
         # end to end through the C-ABI with host buffers: the host-to-device
         # copy of the inputs (of the logits, the rows verification reads,
