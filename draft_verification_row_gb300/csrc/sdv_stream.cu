@@ -182,6 +182,41 @@ __device__ __forceinline__ float tree_sum(float (&a)[N])
     return a[0];
 }
 
+
+// Packed pairs of fp32 (f32x2): one instruction for two independent FMAs or
+// adds, each rounded as its scalar form.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Pairwise sum of a unit's 4 or 8 terms with packed adds.
+template <int N>
+__device__ __forceinline__ float tree_sum2(const float (&a)[N])
+{
+    static_assert(N == 4 || N == 8, "a unit holds 4 or 8 elements");
+    float2 s = fadd2(make_float2(a[0], a[1]), make_float2(a[2], a[3]));
+    if constexpr (N == 8) s = fadd2(s, fadd2(make_float2(a[4], a[5]), make_float2(a[6], a[7])));
+    return s.x + s.y;
+}
+
 // Sum of one unit's elements below the reference, counting those equal to
 // it apart (cnt, first).
 template <int DT>
@@ -209,9 +244,14 @@ __device__ __forceinline__ float unit_sum(const uint4& u, int x0, int V, float c
     constexpr int EPU = Elem<DT>::kPerUnit;
     float v[EPU];
     unpack_masked<DT>(u, x0, V, v);
+    const float2 c2 = make_float2(c, c), n2 = make_float2(neg, neg);
 #pragma unroll
-    for (int e = 0; e < EPU; ++e) v[e] = ex2(fmaf(v[e], c, neg));
-    return tree_sum(v);
+    for (int e = 0; e < EPU; e += 2) {
+        const float2 x = ffma2(make_float2(v[e], v[e + 1]), c2, n2);
+        v[e] = ex2(x.x);
+        v[e + 1] = ex2(x.y);
+    }
+    return tree_sum2(v);
 }
 
 // Unit index of (chunk, warp, sub-unit, lane): a warp's units of a chunk
@@ -359,15 +399,14 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
     }
 }
 
-// The residual term of one token divided by aT = p / Z_T:
-// max(aT e_T - aD e_D, 0) / aT = max(e_T - r e_D, 0), r = aD / aT.  One FMA
-// per token; the sums are scaled by aT once.  (With p = 0, aT = 0 and r is
-// the largest float: every term is finite and scaled to 0.)
-__device__ __forceinline__ float res_unscaled(float eT, float eD, float r) { return fmaxf(fmaf(-r, eD, eT), 0.f); }
-
 // One residual sweep over a node's rows (from the ring): returns this
 // thread's share of S_j = sum over x != x* of max(aT e_T(x) - aD e_D(x), 0).
-// `back`: the chunks come last to first (the copy warp's order).
+// Each token's term is taken divided by aT = p / Z_T:
+// max(aT e_T - aD e_D, 0) / aT = max(e_T - r e_D, 0), r = aD / aT, one FMA
+// per token (two tokens per packed FMA); the sums are scaled by aT once.
+// (With p = 0, aT = 0 and r is the largest float: every term is finite and
+// scaled to 0.)  `back`: the chunks come last to first (the copy warp's
+// order).
 template <int DT>
 __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_out, int nc, int n_units, int V,
                                        float c, float gnegT, float gnegD, float aT, float r, int xs, int cw,
@@ -395,14 +434,22 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
                     Elem<DT>::unpack(sm->ring[s][0][ul], t);
                     Elem<DT>::unpack(sm->ring[s][1][ul], d);
                 }
+                const float2 c2 = make_float2(c, c), nT = make_float2(gnegT, gnegT), nD = make_float2(gnegD, gnegD);
+                const float2 mr = make_float2(-r, -r);
 #pragma unroll
-                for (int e = 0; e < EPU; ++e) d[e] = res_unscaled(ex2(fmaf(t[e], c, gnegT)), ex2(fmaf(d[e], c, gnegD)), r);
+                for (int e = 0; e < EPU; e += 2) {
+                    const float2 xt = ffma2(make_float2(t[e], t[e + 1]), c2, nT);
+                    const float2 xd = ffma2(make_float2(d[e], d[e + 1]), c2, nD);
+                    const float2 v = ffma2(mr, make_float2(ex2(xd.x), ex2(xd.y)), make_float2(ex2(xt.x), ex2(xt.y)));
+                    d[e] = fmaxf(v.x, 0.f);
+                    d[e + 1] = fmaxf(v.y, 0.f);
+                }
                 if (ch == xs_ch) {
 #pragma unroll
                     for (int e = 0; e < EPU; ++e)
                         if (ug * EPU + e == xs) d[e] = 0.f;
                 }
-                w += tree_sum(d);
+                w += tree_sum2(d);
             }
         }
         __syncwarp();
