@@ -78,11 +78,18 @@ __device__ __forceinline__ void masses_of(const Dist& d, const uint4& tu, const 
 #pragma unroll
         for (int e = 0; e < EPU; ++e) q[e] = -INFINITY;
     }
+    const float2 c2 = make_float2(d.c, d.c), nT = make_float2(d.negT, d.negT), nD = make_float2(d.negD, d.negD);
+    const float2 mr = make_float2(-d.rD, -d.rD), ct = make_float2(d.cT, d.cT), at = make_float2(d.aT, d.aT);
 #pragma unroll
-    for (int e = 0; e < EPU; ++e) {
-        const float eT = ex2(fmaf(t[e], d.c, d.negT));
-        const float r = fmaxf(fmaf(-d.rD, ex2(fmaf(q[e], d.c, d.negD)), eT), d.cT * eT);
-        w[e] = ug * EPU + e == d.xs ? d.Rs : d.aT * r;
+    for (int e = 0; e < EPU; e += 2) {
+        const float2 xt = ffma2(make_float2(t[e], t[e + 1]), c2, nT);
+        const float2 xq = ffma2(make_float2(q[e], q[e + 1]), c2, nD);
+        const float2 eT = make_float2(ex2(xt.x), ex2(xt.y));
+        const float2 v = ffma2(mr, make_float2(ex2(xq.x), ex2(xq.y)), eT);
+        const float2 fl = fmul2(ct, eT);
+        const float2 r = fmul2(at, make_float2(fmaxf(v.x, fl.x), fmaxf(v.y, fl.y)));
+        w[e] = ug * EPU + e == d.xs ? d.Rs : r.x;
+        w[e + 1] = ug * EPU + e + 1 == d.xs ? d.Rs : r.y;
     }
 }
 
@@ -200,8 +207,13 @@ __device__ void softmax_pass(const char* row, int V, float c, bool greedy, RowSm
                 if (ug < n_units) {
                     float v[EPU];
                     unpack_masked<DT>(u[i], ug * EPU, V, v);
+                    const float2 c2 = make_float2(c, c), n2 = make_float2(negm, negm);
 #pragma unroll
-                    for (int e = 0; e < EPU; ++e) v[e] = ex2(fmaf(v[e], c, negm));
+                    for (int e = 0; e < EPU; e += 2) {
+                        const float2 x = ffma2(make_float2(v[e], v[e + 1]), c2, n2);
+                        v[e] = ex2(x.x);
+                        v[e + 1] = ex2(x.y);
+                    }
 #pragma unroll
                     for (int s2 = 1; s2 < EPU; s2 *= 2)
 #pragma unroll

@@ -183,30 +183,6 @@ __device__ __forceinline__ float tree_sum(float (&a)[N])
 }
 
 
-// Packed pairs of fp32 (f32x2): one instruction for two independent FMAs or
-// adds, each rounded as its scalar form.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
-{
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
 // Pairwise sum of a unit's 4 or 8 terms with packed adds.
 template <int N>
 __device__ __forceinline__ float tree_sum2(const float (&a)[N])
@@ -484,17 +460,23 @@ __device__ __forceinline__ void kseq_sweep(StreamSmem* sm, uint32_t& g, bool& ti
                 float t[EPU], d[EPU];
                 unpack_masked<DT>(sm->ring[s][0][ul], ug * EPU, V, t);
                 unpack_masked<DT>(sm->ring[s][1][ul], ug * EPU, V, d);
-                float u[NP];
+                float2 u[NP];
 #pragma unroll
-                for (int k = 0; k < NP; ++k) u[k] = 0.f;
+                for (int k = 0; k < NP; ++k) u[k] = make_float2(0.f, 0.f);
+                const float2 c2 = make_float2(c, c), nT = make_float2(gnegT, gnegT), nD = make_float2(gnegD, gnegD);
 #pragma unroll
-                for (int e = 0; e < EPU; ++e) {
-                    const float eT = ex2(fmaf(t[e], c, gnegT)), eD = ex2(fmaf(d[e], c, gnegD));
+                for (int e = 0; e < EPU; e += 2) {
+                    const float2 xt = ffma2(make_float2(t[e], t[e + 1]), c2, nT);
+                    const float2 xd = ffma2(make_float2(d[e], d[e + 1]), c2, nD);
+                    const float2 eT = make_float2(ex2(xt.x), ex2(xt.y)), eD = make_float2(ex2(xd.x), ex2(xd.y));
 #pragma unroll
-                    for (int k = 0; k < NP; ++k) u[k] += fminf(eD, eT * f[k]);
+                    for (int k = 0; k < NP; ++k) {
+                        const float2 m = fmul2(eT, make_float2(f[k], f[k]));
+                        u[k] = fadd2(u[k], make_float2(fminf(eD.x, m.x), fminf(eD.y, m.y)));
+                    }
                 }
 #pragma unroll
-                for (int k = 0; k < NP; ++k) acc[k] += u[k];
+                for (int k = 0; k < NP; ++k) acc[k] += u[k].x + u[k].y;
             }
         }
         __syncwarp();
