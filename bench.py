@@ -514,11 +514,39 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         te, _ = time_calls(e2e_gather_step, args.e2e_steps, stream)
         te = max_over_ranks(te, world)
-        line["e2e"] = {"value": all_positions / (te / args.e2e_steps / 1000.0), "unit": UNIT,
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": te / args.e2e_steps,
-                       "inputs": "pinned host tensors; of the logits, the rows verification reads are gathered "
-                                 "by the GPU over the host link (sdv_gather_read_rows)"}
+
+        # the inner rows gathered; the leaf rows the decisions end at read by
+        # the verification call from the host tensor itself
+        def e2e_inner_step():
+            for n in small:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            binding.gather_read_rows(host["target"], host["draft"], dev_in["tokens"], dev_in["lengths"],
+                                     batch.target, batch.draft, V=batch.V, stream=stream, leaves=False)
+            sdv.verify(args.mode, batch.target, batch.draft, batch.tokens, batch.lengths, batch.accept_u,
+                       batch.sample_u, batch.temperature, V=batch.V, out=out, stream=stream, leaf_target=host["target"])
+            res_host[0].copy_(out.accept_len, non_blocking=True)
+            res_host[1].copy_(out.accept_draft, non_blocking=True)
+            res_host[2].copy_(out.out_token, non_blocking=True)
+
+        e2e_inner_step()
+        torch.cuda.synchronize()
+        ti, _ = time_calls(e2e_inner_step, args.e2e_steps, stream)
+        ti = max_over_ranks(ti, world)
+        row_b = batch.stride * esz
+        ended_at_leaf = int((out.accept_len == batch.lengths).sum().item())  # one leaf row read each
+        h2d_inner = 2 * inner * row_b + ended_at_leaf * row_b + sum(host[n].numel() * host[n].element_size()
+                                                                   for n in small)
+        line["e2e"] = {"value": all_positions / (ti / args.e2e_steps / 1000.0), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d_inner, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": ti / args.e2e_steps,
+                       "inputs": "pinned host tensors; of the logits, the inner trie nodes' rows are gathered by "
+                                 "the GPU over the host link (sdv_gather_inner_rows) and the leaf rows the "
+                                 "decisions end at are read from the host tensor by the call itself "
+                                 "(sdv_verify_leaves_apart)"}
+        line["e2e_all_read_rows"] = {"value": all_positions / (te / args.e2e_steps / 1000.0), "unit": UNIT,
+                                     "h2d_bytes_per_step": h2d, "ms_per_step": te / args.e2e_steps,
+                                     "inputs": "every row verification may read, leaves included, gathered by the "
+                                               "GPU (sdv_gather_read_rows)"}
         line["e2e_copy_calls"] = {"value": all_positions / (tc / args.e2e_steps / 1000.0), "unit": UNIT,
                                   "h2d_bytes_per_step": h2d, "ms_per_step": tc / args.e2e_steps,
                                   "inputs": "the same rows, one cudaMemcpyAsync per range (sdv_copy_read_rows)"}

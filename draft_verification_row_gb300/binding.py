@@ -27,7 +27,8 @@ _VERIFY_ARGTYPES = [
 EXPORTS = list(_ENTRY.values()) + ["sdv_workspace_bytes", "sdv_status_string", "sdv_launch_shape",
                                    "sdv_set_profile_events", "sdv_sample_rows", "sdv_copy_read_rows",
                                    "sdv_read_rows_bytes", "sdv_gather_read_rows", "sdv_verify_greedy_lm_head",
-                                   "sdv_lm_head_workspace_bytes", "sdv_lm_head_logits"]
+                                   "sdv_lm_head_workspace_bytes", "sdv_lm_head_logits", "sdv_gather_inner_rows",
+                                   "sdv_verify_leaves_apart"]
 
 
 class SDVError(RuntimeError):
@@ -77,6 +78,10 @@ def lib(path: str = LIB_PATH):
     h.sdv_lm_head_logits.restype = ctypes.c_int
     h.sdv_lm_head_logits.argtypes = ([ctypes.c_int] * 3 + [ctypes.c_void_p] * 3 + [ctypes.c_longlong]
                                      + [ctypes.c_void_p] * 2)
+    h.sdv_gather_inner_rows.restype = ctypes.c_int
+    h.sdv_gather_inner_rows.argtypes = h.sdv_gather_read_rows.argtypes
+    h.sdv_verify_leaves_apart.restype = ctypes.c_int
+    h.sdv_verify_leaves_apart.argtypes = [ctypes.c_int] + _VERIFY_ARGTYPES + [ctypes.c_void_p]
     h.sdv_read_rows_bytes.restype = ctypes.c_int
     h.sdv_read_rows_bytes.argtypes = ([ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int] + [ctypes.c_void_p] * 2
                                       + [ctypes.POINTER(ctypes.c_longlong)])
@@ -139,13 +144,15 @@ class Outputs:
 
 
 def verify(mode, target, draft, tokens, lengths, accept_u, sample_u, temperature, *, V=None,
-           out: Outputs = None, stream=None, accept_prob=True, residual_mass=True):
+           out: Outputs = None, stream=None, accept_prob=True, residual_mass=True, leaf_target=None):
     """Run one verification call on the current CUDA stream.
 
     target [B][K][L+1][stride], draft [B][K][L][stride] (float32 or bfloat16),
     tokens [B][K][L] int32, lengths [B] int32 or None, accept_u [B][K][L],
     sample_u [B][K][L+1] float32.  Returns a dict of output tensors; the call
-    is asynchronous (read them after a synchronize).
+    is asynchronous (read them after a synchronize).  leaf_target: a tensor of
+    target's shape and dtype (e.g. pinned host memory) the leaves' rows are
+    read from instead (sdv_verify_leaves_apart).
     """
     if mode not in _ENTRY:
         raise ValueError(f"unknown mode {mode!r}")
@@ -168,14 +175,19 @@ def verify(mode, target, draft, tokens, lengths, accept_u, sample_u, temperature
         out = Outputs(mode, B, K, L, V, target.device, accept_prob, residual_mass)
     if stream is None:
         stream = torch.cuda.current_stream(target.device)
-    rc = getattr(h, _ENTRY[mode])(
-        B, K, L, V, stride, _dtype_code(target), float(temperature),
-        _ptr(target), _ptr(draft), _ptr(tokens), _ptr(lengths), _ptr(accept_u), _ptr(sample_u),
-        _ptr(out.accept_len), _ptr(out.accept_draft), _ptr(out.out_token), _ptr(out.accept_prob),
-        _ptr(out.residual_mass), _ptr(out.device_status), _ptr(out.workspace),
-        out.workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    args = (B, K, L, V, stride, _dtype_code(target), float(temperature),
+            _ptr(target), _ptr(draft), _ptr(tokens), _ptr(lengths), _ptr(accept_u), _ptr(sample_u),
+            _ptr(out.accept_len), _ptr(out.accept_draft), _ptr(out.out_token), _ptr(out.accept_prob),
+            _ptr(out.residual_mass), _ptr(out.device_status), _ptr(out.workspace),
+            out.workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if leaf_target is None:
+        rc = getattr(h, _ENTRY[mode])(*args)
+    else:
+        if leaf_target.shape != target.shape or leaf_target.dtype != target.dtype or not leaf_target.is_contiguous():
+            raise ValueError("leaf_target must be contiguous, with target's shape and dtype")
+        rc = h.sdv_verify_leaves_apart(MODES[mode], *args, _ptr(leaf_target))
     if rc != 0:
-        raise SDVError(rc, _ENTRY[mode])
+        raise SDVError(rc, _ENTRY[mode] if leaf_target is None else "sdv_verify_leaves_apart")
     return out.as_dict()
 
 
@@ -358,16 +370,21 @@ def copy_read_rows(host_target, host_draft, tokens, lengths, target, draft, *, V
     return out.value
 
 
-def gather_read_rows(host_target, host_draft, tokens, lengths, target, draft, *, V=None, stream=None):
+def gather_read_rows(host_target, host_draft, tokens, lengths, target, draft, *, V=None, stream=None,
+                     leaves=True):
     """Gather the rows verification reads from pinned, device-mapped host
     tensors into device tensors with one kernel (sdv_gather_read_rows);
-    tokens / lengths are the device tensors the verification call takes."""
+    tokens / lengths are the device tensors the verification call takes.
+    leaves=False leaves out the leaves' target rows (sdv_gather_inner_rows):
+    verify(..., leaf_target=host_target) then reads the few it needs from
+    the host tensor."""
     B, K, Lp1, stride = host_target.shape
     V = stride if V is None else int(V)
     if stream is None:
         stream = torch.cuda.current_stream(target.device)
-    rc = lib().sdv_gather_read_rows(B, K, Lp1 - 1, V, stride, _dtype_code(host_target), _ptr(host_target),
-                                    _ptr(host_draft), _ptr(tokens), _ptr(lengths), _ptr(target), _ptr(draft),
-                                    ctypes.c_void_p(stream.cuda_stream))
+    name = "sdv_gather_read_rows" if leaves else "sdv_gather_inner_rows"
+    rc = getattr(lib(), name)(B, K, Lp1 - 1, V, stride, _dtype_code(host_target), _ptr(host_target),
+                              _ptr(host_draft), _ptr(tokens), _ptr(lengths), _ptr(target), _ptr(draft),
+                              ctypes.c_void_p(stream.cuda_stream))
     if rc != 0:
-        raise SDVError(rc, "sdv_gather_read_rows")
+        raise SDVError(rc, name)

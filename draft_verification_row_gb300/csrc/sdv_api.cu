@@ -103,7 +103,7 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
            const void* target_logits, const void* draft_logits, const int* draft_tokens, const int* lengths,
            const float* accept_u, const float* sample_u, int* accept_len, int* accept_draft, int* out_token,
            float* accept_prob, float* residual_mass, int* device_status, void* workspace,
-           size_t workspace_bytes, void* cuda_stream)
+           size_t workspace_bytes, void* cuda_stream, const void* leaf_target = nullptr)
 {
     if (!sizes_ok(B, K, L, V)) return SDV_ERR_INVALID;
     if (row_stride < V || row_stride % 8 != 0) return SDV_ERR_INVALID;
@@ -134,6 +134,7 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
                           accept_len, accept_draft, out_token, accept_prob, residual_mass};
     for (const void* q : ptrs)
         if (q && !device_accessible(q)) return SDV_ERR_INVALID;
+    if (leaf_target && (!aligned(leaf_target, 16) || !device_accessible(leaf_target))) return SDV_ERR_INVALID;
     if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < workspace_size(B, K, L))
         return SDV_ERR_WORKSPACE;
     if (!device_accessible(workspace)) return SDV_ERR_WORKSPACE;
@@ -149,6 +150,7 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
     pb.mode = greedy ? SDV_MODE_GREEDY : mode;
     pb.c = c;
     pb.target = target_logits;
+    pb.leaf_target = leaf_target;
     pb.draft = draft_logits;
     pb.tokens = draft_tokens;
     pb.lengths = lengths;
@@ -326,6 +328,14 @@ int sdv_verify_block(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_BLOCK); }
 int sdv_verify_multidraft(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_MULTIDRAFT); }
 int sdv_verify_kseq(SDV_VERIFY_ARGS) { return SDV_FORWARD(SDV_MODE_KSEQ); }
 
+int sdv_verify_leaves_apart(int mode, SDV_VERIFY_ARGS, const void* leaf_target_logits)
+{
+    if (mode < SDV_MODE_TOKEN || mode > SDV_MODE_KSEQ) return SDV_ERR_INVALID;
+    return sdv::verify(mode, B, K, L, V, row_stride, dtype, temperature, target_logits, draft_logits, draft_tokens,
+                       lengths, accept_u, sample_u, accept_len, accept_draft, out_token, accept_prob, residual_mass,
+                       device_status, workspace, workspace_bytes, cuda_stream, leaf_target_logits);
+}
+
 size_t sdv_workspace_bytes(int mode, int B, int K, int L, int V)
 {
     if (mode < SDV_MODE_TOKEN || mode > SDV_MODE_KSEQ || !sdv::sizes_ok(B, K, L, V)) return 0;
@@ -444,9 +454,9 @@ int sdv_launch_shape(int V, int dtype, int* ctas_per_sm, int* threads, int* smem
     return SDV_OK;
 }
 
-int sdv_gather_read_rows(int B, int K, int L, int V, long long row_stride, int dtype, const void* host_target,
-                         const void* host_draft, const int* tokens, const int* lengths, void* target, void* draft,
-                         void* cuda_stream)
+static int gather_rows(int B, int K, int L, int V, long long row_stride, int dtype, const void* host_target,
+                       const void* host_draft, const int* tokens, const int* lengths, void* target, void* draft,
+                       void* cuda_stream, int leaves)
 {
     if (!sdv::sizes_ok(B, K, L, V) || row_stride < V || row_stride % 8 || (dtype != SDV_F32 && dtype != SDV_BF16) ||
         K > 256)
@@ -466,6 +476,7 @@ int sdv_gather_read_rows(int B, int K, int L, int V, long long row_stride, int d
     a.B = B;
     a.K = K;
     a.L = L;
+    a.leaves = leaves;
     a.row_bytes = row_stride * (dtype == SDV_BF16 ? 2 : 4);
     a.host_target = host_target;
     a.host_draft = host_draft;
@@ -474,6 +485,22 @@ int sdv_gather_read_rows(int B, int K, int L, int V, long long row_stride, int d
     a.target = target;
     a.draft = draft;
     return sdv::launch_gather_rows(a, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? SDV_OK : SDV_ERR_CUDA;
+}
+
+int sdv_gather_read_rows(int B, int K, int L, int V, long long row_stride, int dtype, const void* host_target,
+                         const void* host_draft, const int* tokens, const int* lengths, void* target, void* draft,
+                         void* cuda_stream)
+{
+    return gather_rows(B, K, L, V, row_stride, dtype, host_target, host_draft, tokens, lengths, target, draft,
+                       cuda_stream, 1);
+}
+
+int sdv_gather_inner_rows(int B, int K, int L, int V, long long row_stride, int dtype, const void* host_target,
+                          const void* host_draft, const int* tokens, const int* lengths, void* target, void* draft,
+                          void* cuda_stream)
+{
+    return gather_rows(B, K, L, V, row_stride, dtype, host_target, host_draft, tokens, lengths, target, draft,
+                       cuda_stream, 0);
 }
 
 int sdv_read_rows_bytes(int B, int K, int L, int V, long long row_stride, int dtype, const int* tokens,

@@ -42,6 +42,7 @@ struct Problem {
     int mode;       // SDV_MODE_*; greedy when temperature == 0
     float c;        // log2(e) / T
     const void* target;
+    const void* leaf_target;  // where leaf rows (depth L_b) are read from, if not target (may be mapped host memory)
     const void* draft;
     const int* tokens;
     const int* lengths;
@@ -67,6 +68,7 @@ cudaError_t launch_argmax(const Problem& pb, cudaStream_t st);
 // address (mapped, pinned) into device tensors (sdv_kernels.cu).
 struct GatherArgs {
     int B, K, L;
+    int leaves;  // 1: target rows down to depth L_b; 0: inner rows only (depth < L_b)
     long long row_bytes;
     const void* host_target;
     const void* host_draft;

@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(256) argmax_kernel(Problem pb)
 // gather of the rows verification reads: draft k owns its trie nodes from
 // depth f on (f = 0 for k = 0; else one past the longest prefix it shares
 // with a lower draft), so it brings target rows [f, L_b] and draft rows
-// [f, L_b - 1].  The reads cross the host link; many 16-byte loads per
+// [f, L_b - 1]; without leaves, target rows [f, L_b - 1].  The reads cross the host link; many 16-byte loads per
 // thread are kept in flight to cover its latency.
 
 __device__ __forceinline__ void copy_bytes(const void* src, void* dst, size_t n)
@@ -209,10 +209,11 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(GatherArgs a)
     __syncthreads();
     const int f = first;
     const size_t rb = (size_t)a.row_bytes;
-    if (f <= Lb) {
+    const int last = a.leaves ? Lb : Lb - 1;  // the deepest target row brought
+    if (f <= last) {
         const size_t off = (((size_t)b * K + k) * (L + 1) + f) * rb;
         copy_bytes(static_cast<const char*>(a.host_target) + off, static_cast<char*>(a.target) + off,
-                   (size_t)(Lb - f + 1) * rb);
+                   (size_t)(last - f + 1) * rb);
     }
     if (f < Lb) {
         const size_t off = (((size_t)b * K + k) * L + f) * rb;

@@ -598,7 +598,9 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy)
     const float u = greedy ? 0.f : pb.sample_u[((size_t)b * K + k) * (L + 1) + j];
     const int n_seg = ((V + EPU - 1) / EPU + kRSeg - 1) / kRSeg;
     Dist d;
-    d.rowT = static_cast<const char*>(pb.target) + (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
+    // a leaf's row may live elsewhere (e.g. host memory the device can read)
+    const void* tsrc = leaf && pb.leaf_target ? pb.leaf_target : pb.target;
+    d.rowT = static_cast<const char*>(tsrc) + (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
     d.rowD = leaf ? nullptr
                   : static_cast<const char*>(pb.draft) + (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
     d.c = pb.c;

@@ -283,6 +283,28 @@ int sdv_gather_read_rows(int B, int K, int L, int V, long long row_stride, int d
                          const void *host_draft, const int *tokens, const int *lengths, void *target, void *draft,
                          void *cuda_stream);
 
+/* As sdv_gather_read_rows, without the leaves' target rows: draft k brings
+ * target rows [f_k, L_b - 1] and draft rows [f_k, L_b - 1], the rows every
+ * decision reads.  A leaf's row (depth L_b) is read only where the decision
+ * ends there; sdv_verify_leaves_apart can read those few rows from the host
+ * tensor itself. */
+int sdv_gather_inner_rows(int B, int K, int L, int V, long long row_stride, int dtype, const void *host_target,
+                          const void *host_draft, const int *tokens, const int *lengths, void *target, void *draft,
+                          void *cuda_stream);
+
+/* The verification of `mode` (SDV_MODE_*), as its sdv_verify_* entry, with
+ * the leaves' target rows (depth lengths[b]) read from leaf_target_logits
+ * instead of target_logits.  leaf_target_logits has target_logits' layout
+ * ([B][K][L+1][row_stride], same dtype), is 16-byte aligned, and may be
+ * host memory mapped into the device's address space: only the leaf rows
+ * the decisions end at are read from it (at most one per request), and
+ * target_logits' rows at depth lengths[b] are never read.  With the inner
+ * rows gathered by sdv_gather_inner_rows, a batch whose logits live in host
+ * memory crosses the host link once, without its leaves.  Returns as the
+ * sdv_verify_* calls; SDV_ERR_INVALID also for a mode out of range or a
+ * leaf_target_logits the device cannot address. */
+int sdv_verify_leaves_apart(int mode, SDV_VERIFY_ARGS, const void *leaf_target_logits);
+
 /* Fixed scratch of sdv_verify_multidraft_static: 4 MiB of device memory
  * that every GPU loading the library reserves until the process exits. */
 #define SDV_STATIC_SCRATCH_BYTES (4u << 20)

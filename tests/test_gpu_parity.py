@@ -371,3 +371,31 @@ def test_gather_read_rows_matches_the_copy():
     part = P.gpu_run("multidraft", dataclasses.replace(batch, target=b_t, draft=b_d))
     for key in ("accept_len", "accept_draft", "out_token", "accept_prob", "residual_mass"):
         np.testing.assert_array_equal(full[key], part[key])
+
+
+@pytest.mark.parametrize("mode", ["multidraft", "token", "greedy", "kseq"])
+def test_inner_rows_with_leaves_read_from_the_host(mode):
+    """sdv_gather_inner_rows brings every row but the leaves' target rows;
+    sdv_verify_leaves_apart reads the leaf rows the decisions end at from the
+    pinned host tensor itself.  The results equal the full batch's, bit for
+    bit, and the device tensor's leaf rows (NaN here) are never read."""
+    import draft_verification_row_gb300 as sdv
+    lengths = [3, 1, 2, 3, 0, 3, 2, 1, 3, 3, 2, 3]
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=len(lengths), K=4, L=3, V=9001, lengths=lengths)
+    batch.accept_u[:4] = 0.0  # these requests accept everything: their decisions end at leaves
+    ht, hd = batch.target.cpu().pin_memory(), batch.draft.cpu().pin_memory()
+    t = torch.full_like(batch.target, float("nan"))
+    d = torch.full_like(batch.draft, float("nan"))
+    sdv.gather_read_rows(ht, hd, batch.tokens, batch.lengths, t, d, V=batch.V, leaves=False)
+    torch.cuda.synchronize()
+    for b, Lb in enumerate(lengths):  # no leaf row was brought
+        assert torch.isnan(t[b, :, Lb].float()).all()
+    full = P.gpu_run(mode, batch)
+    out = sdv.verify(mode, t, d, batch.tokens, batch.lengths, batch.accept_u, batch.sample_u, batch.temperature,
+                     V=batch.V, leaf_target=ht)
+    torch.cuda.synchronize()
+    assert int(out["device_status"].item()) == 0
+    for key in ("accept_len", "accept_draft", "out_token", "accept_prob", "residual_mass"):
+        np.testing.assert_array_equal(full[key], out[key].cpu().numpy(), err_msg=key)
+    ends_at_leaf = int((full["accept_len"] == np.array(lengths)).sum())
+    assert ends_at_leaf >= (1 if mode == "greedy" else 4)  # greedy: at least the length-0 request
