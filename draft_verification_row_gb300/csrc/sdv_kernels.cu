@@ -116,15 +116,29 @@ __global__ void __launch_bounds__(256) argmax_kernel(Problem pb)
     float best = -INFINITY;
     int bidx = 0x7fffffff;
     bool bad = false;
-    for (int uu = threadIdx.x; uu < n_units; uu += blockDim.x) {
-        float v[EPU];
-        unpack_masked<DT>(__ldg(g + uu), uu * EPU, V, v);
+    // four 16-byte loads in flight per thread; a thread's units increase,
+    // so the first maximum it sees is its lowest index
+    constexpr int U = 4;
+    for (int u0 = threadIdx.x; u0 < n_units; u0 += U * blockDim.x) {
+        uint4 w[U];
 #pragma unroll
-        for (int e = 0; e < EPU; ++e) {
-            bad |= (v[e] != v[e]) || (v[e] == INFINITY);
-            if (v[e] > best) {
-                best = v[e];
-                bidx = uu * EPU + e;
+        for (int q = 0; q < U; ++q) {
+            const int uu = u0 + q * blockDim.x;
+            w[q] = uu < n_units ? __ldg(g + uu) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int uu = u0 + q * blockDim.x;
+            if (uu >= n_units) break;
+            float v[EPU];
+            unpack_masked<DT>(w[q], uu * EPU, V, v);
+#pragma unroll
+            for (int e = 0; e < EPU; ++e) {
+                bad |= (v[e] != v[e]) || (v[e] == INFINITY);
+                if (v[e] > best) {
+                    best = v[e];
+                    bidx = uu * EPU + e;
+                }
             }
         }
     }

@@ -141,3 +141,23 @@ def test_lm_head_logits_invalid_rejected_without_gpu(lib, over):
 def test_lm_head_empty_is_a_no_op(lib):
     assert lib.sdv_verify_greedy_lm_head(0, 2, 2, 16, 64, *([None] * 10), 0, None) == 0
     assert lib.sdv_lm_head_logits(0, 16, 64, None, None, None, 16, None, None) == 0
+
+
+@pytest.mark.parametrize("mode", [-1, 5])
+def test_leaves_apart_rejects_unknown_modes_without_gpu(lib, mode):
+    args = [2, 1, 2, 16, 16, 0, 1.0] + [None] * 13 + [0, None]
+    assert lib.sdv_verify_leaves_apart(mode, *args, None) == 1
+
+
+def test_leaves_apart_checks_sizes_without_gpu(lib):
+    args = [2, 0, 2, 16, 16, 0, 1.0] + [None] * 13 + [0, None]  # K = 0
+    assert lib.sdv_verify_leaves_apart(3, *args, None) == 1
+    args = [0, 1, 2, 16, 16, 0, 1.0] + [None] * 13 + [0, None]  # B = 0: nothing to do
+    assert lib.sdv_verify_leaves_apart(3, *args, None) == 0
+
+
+def test_gather_inner_rows_rejects_bad_sizes_without_gpu(lib):
+    f = lib.sdv_gather_inner_rows
+    assert f(2, 0, 2, 16, 16, 1, None, None, None, None, None, None, None) == 1   # K = 0
+    assert f(2, 1, 2, 16, 12, 1, None, None, None, None, None, None, None) == 1   # stride < V
+    assert f(0, 1, 2, 16, 16, 1, None, None, None, None, None, None, None) == 0   # B = 0
