@@ -24,7 +24,7 @@ bool sizes_ok(int B, int K, int L, int V)
 size_t workspace_size(int B, int K, int L)
 {
     const size_t n = slot_count(B, K, L);
-    return 6 * align_up(n * 4) + align_up(n * 6 * 4) + align_up(n) + align_up((size_t)B * 4) +
+    return 6 * align_up(n * 4) + align_up(n * 6 * 4) + align_up(n) + 2 * align_up((size_t)B * 4) +
            align_up((size_t)(L + 1) * B * K * 4) + align_up((size_t)(2 * L + 3) * 4);
 }
 
@@ -64,6 +64,8 @@ Workspace carve(void* base, int B, int K, int L)
     w.owner = reinterpret_cast<unsigned char*>(p);
     p += align_up(n);
     w.req = reinterpret_cast<int*>(p);
+    p += align_up((size_t)B * 4);
+    w.left = reinterpret_cast<int*>(p);
     p += align_up((size_t)B * 4);
     w.nodes = reinterpret_cast<int*>(p);
     p += align_up((size_t)(L + 1) * B * K * 4);
@@ -182,8 +184,12 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
     }
     if (!prof_record(g_prof_stop, st)) return SDV_ERR_CUDA;
     // per request: the decision, then the correction (or bonus) token drawn
-    // at its end node only
-    if (launch_finish(pb, greedy, st) != cudaSuccess) return SDV_ERR_CUDA;
+    // at its end node only.  After the node kernel it is launched as that
+    // kernel's programmatic dependent, each CTA waiting for its request's
+    // nodes; a profiling event between the two would serialize them, so
+    // with the hook on it is an ordinary launch.
+    const bool overlap = !greedy && !g_prof_stop;
+    if (launch_finish(pb, greedy, st, overlap) != cudaSuccess) return SDV_ERR_CUDA;
     return SDV_OK;
 }
 

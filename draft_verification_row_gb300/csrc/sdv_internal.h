@@ -29,6 +29,7 @@ struct Workspace {
     int* am;               // node argmax (greedy)
     unsigned char* owner;  // lowest draft sharing draft k's first j tokens
     int* req;              // [B] request status bits
+    int* left;             // [B] inner nodes the node kernel has still to finish (set by the prep kernel)
     int* nodes;            // [L+1][B*K] node slots by depth, listed by the prep kernel: nodes
                            //   with several draws from the front, one-draw nodes from the back
     int* ncount;           // [2][L+1] nodes per depth (several draws, one draw), then the
@@ -93,7 +94,9 @@ struct SampleArgs {
 cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st);
 // Per request: the decision, then the correction (or bonus) draw at its end
 // node (sdv_sample.cu).
-cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st);
+// after_nodes: launched right after the node kernel, as its programmatic
+// dependent; each CTA waits for its request's nodes (Workspace::left).
+cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st, bool after_nodes = false);
 int sample_threads();
 
 // The target model's LM head on the tensor cores (sdv_lmhead.cu):

@@ -28,19 +28,23 @@ __global__ void prep_kernel(Problem pb)
     if (b >= pb.B) return;
     const int K = pb.K, L = pb.L, V = pb.V;
     const int Lb = pb.lengths ? pb.lengths[b] : L;
+    // lane k < K holds draft k's tokens, all loaded at once (L <= 16)
+    int tk[SDV_MAX_L];
     int st = 0;
     if (Lb < 0 || Lb > L) {
         st = SDV_REQ_BAD_LENGTH;
     } else {
+        const int* row = pb.tokens + ((size_t)b * K + lane) * L;
+#pragma unroll
+        for (int j = 0; j < SDV_MAX_L; ++j) tk[j] = lane < K && j < Lb ? row[j] : 0;
         int bad = 0;
-        for (int i = lane; i < K * Lb; i += 32) {
-            const int t = pb.tokens[((size_t)b * K + i / Lb) * L + i % Lb];
-            bad |= (t < 0 || t >= V);
-        }
+#pragma unroll
+        for (int j = 0; j < SDV_MAX_L; ++j) bad |= j < Lb && lane < K && (tk[j] < 0 || tk[j] >= V);
         if (__any_sync(0xffffffffu, bad)) st = SDV_REQ_BAD_TOKEN;
     }
     if (lane == 0) {
         pb.ws.req[b] = st;
+        pb.ws.left[b] = 0;  // the node count below, for a valid request
         if (st && pb.device_status) atomicOr(pb.device_status, st);
     }
     if (st) return;
@@ -50,13 +54,15 @@ __global__ void prep_kernel(Problem pb)
     unsigned char* own = pb.ws.owner + (size_t)b * (L + 1) * K;
     int o = 0;
     if (lane < K) own[lane] = 0;
-    for (int j = 1; j <= Lb; ++j) {
-        const int tk = lane < K ? pb.tokens[((size_t)b * K + lane) * L + j - 1] : -1;
+#pragma unroll
+    for (int j = 1; j <= SDV_MAX_L; ++j) {
+        if (j > Lb) break;
+        const int t = lane < K ? tk[j - 1] : -1;
         int no = lane;
         for (int k2 = K - 1; k2 >= 0; --k2) {
             const int o2 = __shfl_sync(0xffffffffu, o, k2);
-            const int t2 = __shfl_sync(0xffffffffu, tk, k2);
-            if (k2 <= lane && o2 == o && t2 == tk) no = k2;
+            const int t2 = __shfl_sync(0xffffffffu, t, k2);
+            if (k2 <= lane && o2 == o && t2 == t) no = k2;
         }
         o = no;
         if (lane < K) own[j * K + lane] = (unsigned char)o;
@@ -72,6 +78,7 @@ __global__ void prep_kernel(Problem pb)
     const size_t BK = (size_t)pb.B * K;
     int* const front = pb.ws.ncount;
     int* const back = pb.ws.ncount + (L + 1);
+    int listed = 0;  // the request's inner nodes: the node kernel counts them down
     for (int j = 0; j <= Lb; ++j) {
         const bool node = j < Lb && lane < K && own[j * K + lane] == lane;
         int draws = 0;  // drafts through the node
@@ -89,7 +96,9 @@ __global__ void prep_kernel(Problem pb)
         if (node && draws > 1) pb.ws.nodes[j * BK + fb + __popc(mh & below)] = (int)slot;
         if (node && draws == 1) pb.ws.nodes[j * BK + BK - 1 - (bb + __popc(ml & below))] = (int)slot;
         if (lane < K) pb.ws.pbar[slot] = j == 0 ? 0.f : -1.f;  // the root's weight is 1
+        listed += __popc(mh) + __popc(ml);
     }
+    if (lane == 0) pb.ws.left[b] = listed;
 }
 
 // ------------------------------------------------------------------------

@@ -578,7 +578,7 @@ __device__ __noinline__ void invalidate_request(const Problem& pb, int b, int la
 // bonus) token at the end node it chose: from the node's final residual R_n
 // (kept by the node kernel), or from P at a leaf or where S_n = 0.
 template <int DT>
-__global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy)
+__global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy, int wait_nodes)
 {
     using E = Elem<DT>;
     constexpr int EPU = E::kPerUnit;
@@ -586,6 +586,27 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy)
     __shared__ DecideSmem ds;
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (wait_nodes) {
+        // launched while the node kernel still runs: wait (bounded) until it
+        // has finished every node of this request (its release, our acquire)
+        if (tid == 0) {
+            const int* left = pb.ws.left + b;
+            int n;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(n) : "l"(left) : "memory");
+            if (n > 0) {
+                const uint64_t t0 = globaltimer();
+                do {
+                    __nanosleep(256);  // leave issue slots to the node kernel's CTAs on this SM
+                    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(n) : "l"(left) : "memory");
+                } while (n > 0 && globaltimer() - t0 <= kWaitNs);
+                if (n > 0) {
+                    atomicOr(&pb.ws.req[b], SDV_DEV_TIMEOUT);
+                    if (pb.device_status) atomicOr(pb.device_status, SDV_DEV_TIMEOUT);
+                }
+            }
+        }
+        __syncthreads();
+    }
     if (w == 0) decide_request(pb, b, greedy != 0, ds, lane);
     if (tid == 0) sm.bad = 0;
     __syncthreads();
@@ -642,14 +663,24 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy)
 
 int sample_threads() { return kRT; }
 
-cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st)
+cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st, bool after_nodes)
 {
     if (pb.B == 0) return cudaSuccess;
-    if (pb.dtype == SDV_BF16)
-        finish_kernel<SDV_BF16><<<pb.B, kRT, 0, st>>>(pb, greedy ? 1 : 0);
-    else
-        finish_kernel<SDV_F32><<<pb.B, kRT, 0, st>>>(pb, greedy ? 1 : 0);
-    return cudaGetLastError();
+    // after the node kernel: a programmatic dependent launch, so that the
+    // decisions of finished requests overlap the node kernel's last nodes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pb.B);
+    cfg.blockDim = dim3(kRT);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_nodes ? 1 : 0;
+    const int g = greedy ? 1 : 0, wait = after_nodes ? 1 : 0;
+    if (pb.dtype == SDV_BF16) return cudaLaunchKernelEx(&cfg, finish_kernel<SDV_BF16>, pb, g, wait);
+    return cudaLaunchKernelEx(&cfg, finish_kernel<SDV_F32>, pb, g, wait);
 }
 
 cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st)

@@ -603,6 +603,9 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
     extern __shared__ __align__(128) unsigned char smem_raw[];
     StreamSmem* sm = reinterpret_cast<StreamSmem*>(smem_raw);
     const int tid = threadIdx.x;
+    // the finish kernel may be scheduled now: its CTAs take SMs only as this
+    // kernel's CTAs leave them, and each waits for its own request's nodes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int K = pb.K, L = pb.L, V = pb.V;
     const int BK = pb.B * K;
     const int n_units = (V + EPU - 1) / EPU;
@@ -1033,6 +1036,12 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 if (pb.device_status) atomicOr(pb.device_status, SDV_DEV_TIMEOUT);
             }
             break;
+        }
+        // the node's records are complete (all written by this thread): a
+        // release, then one node fewer for the request's decision to wait on
+        if (ct == 0) {
+            __threadfence();
+            atomicSub(&pb.ws.left[b], 1);
         }
     }
 }

@@ -388,9 +388,12 @@ int sdv_lm_head_logits(int M, int V, int d, const void *hidden, const void *lm_h
 
 /* Profiling hook.  With start and stop both cudaEvent_t handles, every
  * later call made from the calling host thread records `start` on its
- * stream just before its first vocabulary-row kernel and `stop` just after
- * its last one, so that cudaEventElapsedTime gives the time of those
- * kernels alone; NULL, NULL turns it off.  The events stay owned by the
+ * stream just before its first vocabulary-row kernel (the node kernel, the
+ * greedy argmax or the LM head) and `stop` just after it, so that
+ * cudaEventElapsedTime gives the time of that kernel alone; NULL, NULL turns
+ * it off.  Without the hook, the decision kernel of the sampling rules is
+ * launched as the node kernel's programmatic dependent and overlaps its
+ * last nodes; with the hook on, the two run one after the other.  The events stay owned by the
  * caller.  Returns SDV_OK, or SDV_ERR_INVALID if exactly one is NULL. */
 int sdv_set_profile_events(void *start, void *stop);
 
