@@ -61,7 +61,9 @@ def parse():
     ap.add_argument("--B", type=int, default=None, help="override the batch size (profiling runs)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, token mode and CPU baseline")
-    ap.add_argument("--cpu-requests", type=int, default=8, help="requests in the oracle's timed sample")
+    ap.add_argument("--cpu-requests", type=int, default=160,
+                    help="requests in the oracle's timed sample (cpu_baseline; about 10 s on one core)")
+    ap.add_argument("--ref-requests", type=int, default=4, help="requests per step of --impl reference")
     ap.add_argument("--lm-head-only", action="store_true",
                     help="only the LM-head-fused greedy measurement (--B sets its batch size)")
     return ap.parse_args()
@@ -357,7 +359,7 @@ def run_reference(args, world, rank):
     name = args.workload or W.HEADLINE
     dev = "cuda:0" if torch.cuda.is_available() else "cpu"
     batch = W.make(name, dev, B=args.B)
-    n = max(1, min(args.cpu_requests // 4 or 1, batch.B))
+    n = max(1, min(args.ref_requests, batch.B))
     rng = np.random.default_rng(0)
     times, positions = [], []
     for i in range(args.warmup + args.steps):
