@@ -153,6 +153,16 @@ def test_fused_greedy_matches_the_oracle(B, K, L, V, d):
     _compare(batch, got, ref, unique, f"B{B} K{K} L{L} V{V} d{d}")
 
 
+def test_fused_greedy_at_the_maximum_sizes():
+    # K = 16 drafts of L = 16 tokens: up to 272 trie nodes per request
+    batch = W.make_lm_head(WL, DEV, B=4, K=16, L=16, V=1000, d=64, agree=0.9, poison_unread=True)
+    got = _run(batch)
+    ref, unique = _oracle(batch)
+    assert int(got["device_status"].item()) == 0
+    _compare(batch, got, ref, unique, "K16 L16")
+    assert (got["accept_len"].cpu().numpy() > 4).any()  # long accepted runs happen
+
+
 def test_fused_greedy_ties_across_tiles_take_the_lowest_index():
     # integer logits in -64..64 over 1500 entries: the maximum repeats in about
     # a quarter of the rows, mostly in different 256-wide vocabulary tiles;
