@@ -197,6 +197,22 @@ def lm_head_bench(args, dev, stream, rank, world):
         unfused()
     t_un, _ = time_calls(unfused, args.steps, stream)
     del logits
+    # for the sampling rules: every trie node's row (leaves included) written
+    # once in bf16 into the verification layout
+    tgt = torch.empty((lb.B, lb.K, lb.L + 1, (lb.V + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(binding.lm_head_workspace_bytes(lb.B, lb.K, lb.L, lb.V, lb.d), 256), dtype=torch.uint8,
+                     device=dev)
+    tst = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def trie():
+        sdv.lm_head_trie_logits(lb.hidden, lb.lm_head, lb.tokens, lb.lengths, target=tgt, workspace=ws,
+                                device_status=tst, stream=stream)
+
+    for _ in range(args.warmup):
+        trie()
+    t_tr, g_tr = time_calls(trie, args.steps, stream, prof=True)
+    del tgt, ws
+    trie_flops = 2.0 * (inner + leaves) * lb.V * lb.d
     positions = sum_over_ranks(lb.positions, world)
     return {
         "what": "greedy verification fused into the target LM head: logits = hidden . W^T on tcgen05, each "
@@ -213,6 +229,11 @@ def lm_head_bench(args, dev, stream, rank, world):
         "unfused_cublas_all_rows_then_greedy": {
             "ms": t_un / args.steps, "rows": lb.B * lb.K * (lb.L + 1),
             "value": positions / (t_un / args.steps / 1000.0)},
+        "trie_logits_for_sampling_rules": {
+            "what": "sdv_lm_head_trie_logits: each trie node's row, leaves included, computed once and written "
+                    "in bf16 into the verification layout",
+            "ms": t_tr / args.steps, "rows": inner + leaves, "lm_head_kernel_ms": g_tr / args.steps,
+            "tflops": trie_flops / (g_tr / args.steps / 1000.0) / 1e12},
     }
 
 

@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     launch_shape,
     lib,
     lm_head_logits,
+    lm_head_trie_logits,
     lm_head_workspace_bytes,
     read_rows_bytes,
     sample_rows,

@@ -28,7 +28,7 @@ EXPORTS = list(_ENTRY.values()) + ["sdv_workspace_bytes", "sdv_status_string", "
                                    "sdv_set_profile_events", "sdv_sample_rows", "sdv_copy_read_rows",
                                    "sdv_read_rows_bytes", "sdv_gather_read_rows", "sdv_verify_greedy_lm_head",
                                    "sdv_lm_head_workspace_bytes", "sdv_lm_head_logits", "sdv_gather_inner_rows",
-                                   "sdv_verify_leaves_apart"]
+                                   "sdv_verify_leaves_apart", "sdv_lm_head_trie_logits"]
 
 
 class SDVError(RuntimeError):
@@ -75,6 +75,9 @@ def lib(path: str = LIB_PATH):
                                             + [ctypes.c_void_p])
     h.sdv_lm_head_workspace_bytes.restype = ctypes.c_size_t
     h.sdv_lm_head_workspace_bytes.argtypes = [ctypes.c_int] * 5
+    h.sdv_lm_head_trie_logits.restype = ctypes.c_int
+    h.sdv_lm_head_trie_logits.argtypes = ([ctypes.c_int] * 5 + [ctypes.c_void_p] * 5 + [ctypes.c_longlong]
+                                          + [ctypes.c_void_p] * 2 + [ctypes.c_size_t, ctypes.c_void_p])
     h.sdv_lm_head_logits.restype = ctypes.c_int
     h.sdv_lm_head_logits.argtypes = ([ctypes.c_int] * 3 + [ctypes.c_void_p] * 3 + [ctypes.c_longlong]
                                      + [ctypes.c_void_p] * 2)
@@ -302,6 +305,39 @@ def verify_greedy_lm_head(hidden, lm_head, tokens, lengths, *, out: LmHeadOutput
     if rc != 0:
         raise SDVError(rc, "sdv_verify_greedy_lm_head")
     return out.as_dict()
+
+
+def lm_head_trie_logits(hidden, lm_head, tokens, lengths, *, target=None, workspace=None, device_status=None,
+                        stream=None):
+    """The target logits of every trie node (leaves included), computed once
+    by the LM head and written in bf16 into target [B][K][L+1][stride] (a
+    new NaN-filled tensor with stride V rounded up to 8 when None): the rows
+    the sampling rules read (sdv_lm_head_trie_logits).  Returns (target,
+    device_status); asynchronous."""
+    h = lib()
+    if hidden.dim() != 4 or lm_head.dim() != 2:
+        raise ValueError("hidden must be [B][K][L+1][d] and lm_head [V][d]")
+    B, K, Lp1, d = hidden.shape
+    L, V = Lp1 - 1, lm_head.shape[0]
+    _bf16_rows("hidden", hidden)
+    _bf16_rows("lm_head", lm_head, d)
+    if target is None:
+        target = torch.full((B, K, Lp1, (V + 7) // 8 * 8), float("nan"), dtype=torch.bfloat16, device=hidden.device)
+    if target.dtype != torch.bfloat16 or not target.is_contiguous() or tuple(target.shape[:3]) != (B, K, Lp1):
+        raise ValueError("target must be a contiguous bfloat16 [B][K][L+1][stride] tensor")
+    if workspace is None:
+        workspace = torch.empty(max(h.sdv_lm_head_workspace_bytes(B, K, L, V, d), 256), dtype=torch.uint8,
+                                device=hidden.device)
+    if device_status is None:
+        device_status = torch.empty(1, dtype=torch.int32, device=hidden.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(hidden.device)
+    rc = h.sdv_lm_head_trie_logits(B, K, L, V, d, _ptr(hidden), _ptr(lm_head), _ptr(tokens), _ptr(lengths),
+                                   _ptr(target), target.shape[3], _ptr(device_status), _ptr(workspace),
+                                   workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise SDVError(rc, "sdv_lm_head_trie_logits")
+    return target, device_status
 
 
 def lm_head_logits(hidden, lm_head, *, logits=None, device_status=None, stream=None):

@@ -31,15 +31,16 @@ size_t workspace_size(int B, int K, int L)
 // The hidden size of the LM head: whole 16-byte units per row (TMA row pitch).
 bool lm_d_ok(int d) { return d >= 8 && d % 8 == 0 && d <= (1 << 16); }
 
-// Fused greedy call: the verification workspace, then the node rows of the
-// LM head (compact map, row count, argmax keys, hidden rows), then the end
-// leaves (pending slot and request per leaf, count, keys, hidden rows).
+// LM-head calls: the verification workspace, then the node rows of the LM
+// head (compact map, row count, argmax keys, hidden rows, row indices),
+// then the end leaves (pending slot and request per leaf, count, keys,
+// hidden rows).
 size_t lm_workspace_size(int B, int K, int L, int d)
 {
     const size_t n = slot_count(B, K, L);
     const size_t nb = (size_t)B;
     return workspace_size(B, K, L) + align_up(n * 4) + align_up(4) + align_up(n * 8) + align_up(n * (size_t)d * 2) +
-           2 * align_up(nb * 4) + align_up(4) + align_up(nb * 8) + align_up(nb * (size_t)d * 2);
+           align_up(n * 4) + 2 * align_up(nb * 4) + align_up(4) + align_up(nb * 8) + align_up(nb * (size_t)d * 2);
 }
 
 Workspace carve(void* base, int B, int K, int L)
@@ -193,6 +194,39 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
     return SDV_OK;
 }
 
+// The LM-head part of the workspace (after carve's), and pb.ws itself.
+LmRows carve_lm(void* workspace, Problem& pb, int d, const void* hidden)
+{
+    const int B = pb.B, K = pb.K, L = pb.L;
+    pb.ws = carve(workspace, B, K, L);
+    const size_t n = slot_count(B, K, L);
+    char* p = static_cast<char*>(workspace) + workspace_size(B, K, L);
+    LmRows r;
+    std::memset(&r, 0, sizeof r);
+    r.d = d;
+    r.hidden = hidden;
+    r.compact = reinterpret_cast<int*>(p);
+    p += align_up(n * 4);
+    r.count = reinterpret_cast<int*>(p);
+    p += align_up(4);
+    r.keys = reinterpret_cast<unsigned long long*>(p);
+    p += align_up(n * 8);
+    r.rows = p;
+    p += align_up(n * (size_t)d * 2);
+    r.row_of = reinterpret_cast<int*>(p);
+    p += align_up(n * 4);
+    pb.leaf_pending = reinterpret_cast<int*>(p);
+    p += align_up((size_t)B * 4);
+    r.leaf_req = reinterpret_cast<int*>(p);
+    p += align_up((size_t)B * 4);
+    r.leaf_count = reinterpret_cast<int*>(p);
+    p += align_up(4);
+    r.leaf_keys = reinterpret_cast<unsigned long long*>(p);
+    p += align_up((size_t)B * 8);
+    r.leaf_rows = p;
+    return r;
+}
+
 int verify_greedy_lm_head(int B, int K, int L, int V, int d, const void* hidden, const void* lm_head,
                           const int* draft_tokens, const int* lengths, int* accept_len, int* accept_draft,
                           int* out_token, float* accept_prob, int* device_status, void* workspace,
@@ -232,29 +266,9 @@ int verify_greedy_lm_head(int B, int K, int L, int V, int d, const void* hidden,
     pb.out_token = out_token;
     pb.accept_prob = accept_prob;
     pb.device_status = device_status;
-    pb.ws = carve(workspace, B, K, L);
     const size_t n = slot_count(B, K, L);
-    char* p = static_cast<char*>(workspace) + workspace_size(B, K, L);
-    LmRows r;
-    r.d = d;
-    r.hidden = hidden;
-    r.compact = reinterpret_cast<int*>(p);
-    p += align_up(n * 4);
-    r.count = reinterpret_cast<int*>(p);
-    p += align_up(4);
-    r.keys = reinterpret_cast<unsigned long long*>(p);
-    p += align_up(n * 8);
-    r.rows = p;
-    p += align_up(n * (size_t)d * 2);
-    pb.leaf_pending = reinterpret_cast<int*>(p);
-    p += align_up((size_t)B * 4);
-    r.leaf_req = reinterpret_cast<int*>(p);
-    p += align_up((size_t)B * 4);
-    r.leaf_count = reinterpret_cast<int*>(p);
-    p += align_up(4);
-    r.leaf_keys = reinterpret_cast<unsigned long long*>(p);
-    p += align_up((size_t)B * 8);
-    r.leaf_rows = p;
+    LmRows r = carve_lm(workspace, pb, d, hidden);
+    r.leaves = 0;
     LmArgs a;
     std::memset(&a, 0, sizeof a);
     a.rows_dev = r.count;
@@ -357,6 +371,62 @@ int sdv_verify_greedy_lm_head(int B, int K, int L, int V, int d, const void* hid
     return sdv::verify_greedy_lm_head(B, K, L, V, d, hidden, lm_head, draft_tokens, lengths, accept_len,
                                       accept_draft, out_token, accept_prob, device_status, workspace,
                                       workspace_bytes, cuda_stream);
+}
+
+int sdv_lm_head_trie_logits(int B, int K, int L, int V, int d, const void* hidden, const void* lm_head,
+                            const int* draft_tokens, const int* lengths, void* target_logits, long long row_stride,
+                            int* device_status, void* workspace, size_t workspace_bytes, void* cuda_stream)
+{
+    using namespace sdv;
+    if (!sizes_ok(B, K, L, V) || !lm_d_ok(d) || row_stride < V || row_stride % 8) return SDV_ERR_INVALID;
+    cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+    if (device_status && !device_accessible(device_status)) return SDV_ERR_INVALID;
+    if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (B == 0) return SDV_OK;
+    if (!hidden || !lm_head || !target_logits || (L > 0 && !draft_tokens)) return SDV_ERR_INVALID;
+    if (!aligned(hidden, 16) || !aligned(lm_head, 16) || !aligned(target_logits, 16)) return SDV_ERR_INVALID;
+    const void* ptrs[] = {hidden, lm_head, target_logits, L > 0 ? draft_tokens : nullptr, lengths};
+    for (const void* q : ptrs)
+        if (q && !device_accessible(q)) return SDV_ERR_INVALID;
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < lm_workspace_size(B, K, L, d))
+        return SDV_ERR_WORKSPACE;
+    if (!device_accessible(workspace)) return SDV_ERR_WORKSPACE;
+
+    Problem pb;
+    std::memset(&pb, 0, sizeof pb);
+    pb.B = B;
+    pb.K = K;
+    pb.L = L;
+    pb.V = V;
+    pb.stride = row_stride;
+    pb.dtype = SDV_BF16;
+    pb.mode = SDV_MODE_MULTIDRAFT;
+    pb.tokens = draft_tokens;
+    pb.lengths = lengths;
+    pb.device_status = device_status;
+    LmRows r = carve_lm(workspace, pb, d, hidden);
+    r.leaves = 1;  // every trie node's row, leaves included
+    LmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.rows_dev = r.count;
+    a.V = V;
+    a.d = d;
+    a.out_bf16 = target_logits;
+    a.dest_row = r.row_of;
+    a.out_stride = row_stride;
+    a.device_status = device_status;
+    if (cudaMemsetAsync(pb.ws.ncount, 0, sizeof(int) * (2 * L + 3), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (cudaMemsetAsync(r.count, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_prep(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (launch_lm_rows(pb, r, st) != cudaSuccess) return SDV_ERR_CUDA;
+    if (!prof_record(g_prof_start, st)) return SDV_ERR_CUDA;
+    const cudaError_t e = launch_lm_head(r.rows, (long long)slot_count(B, K, L), lm_head, a, LM_EPI_ROWS_BF16, st);
+    if (e == cudaErrorInvalidValue) {
+        cudaGetLastError();
+        return SDV_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return SDV_ERR_CUDA;
+    return prof_record(g_prof_stop, st) ? SDV_OK : SDV_ERR_CUDA;
 }
 
 size_t sdv_lm_head_workspace_bytes(int B, int K, int L, int V, int d)

@@ -101,13 +101,15 @@ int sample_threads();
 
 // The target model's LM head on the tensor cores (sdv_lmhead.cu):
 // logits = hidden . W^T over the hidden size d, bf16 in, fp32 accumulate.
-enum { LM_EPI_ARGMAX = 0, LM_EPI_LOGITS = 1 };
+enum { LM_EPI_ARGMAX = 0, LM_EPI_LOGITS = 1, LM_EPI_ROWS_BF16 = 2 };
 struct LmArgs {
     int rows;                  // rows of the A operand (used when rows_dev is NULL)
     const int* rows_dev;       // device row count, written by an earlier launch, or NULL
     int V, d;
     unsigned long long* keys;  // ARGMAX: [rows] (maximum, first index) keys, zeroed beforehand
     float* logits;             // LOGITS: [rows][out_stride] fp32
+    void* out_bf16;            // ROWS_BF16: bf16 rows of out_stride elements; row r goes to row dest_row[r]
+    const int* dest_row;
     long long out_stride;
     int* device_status;
 };
@@ -125,6 +127,8 @@ struct LmRows {
     int* compact;              // [slots]: node slot -> its row
     int* count;                // rows listed
     unsigned long long* keys;  // [slots]
+    int leaves;                // 1: list the leaves (depth L_b) too
+    int* row_of;               // [slots] or NULL: each listed row's index in [B][K][L+1]
     // the end leaves the decision reached, one per request at most
     void* leaf_rows;                // [B][d] bf16
     int* leaf_req;                  // [B]: request of each listed leaf

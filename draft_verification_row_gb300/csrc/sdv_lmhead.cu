@@ -36,6 +36,7 @@
 // the CTAs running at one time read the same few MB of W from L2 while all
 // hidden rows stay L2-resident.
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 #include "sdv_internal.h"
 #include "sdv_device.cuh"
@@ -299,6 +300,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN);
             const int row = m0 + q * 32 + lane;
+            const int dest = EPI == LM_EPI_ROWS_BF16 && row < M ? a.dest_row[row] : 0;
             float best = -INFINITY;
             int bidx = n0;
             bool bad = false;
@@ -317,6 +319,28 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                                 best = f;
                                 bidx = x0 + e;
                             }
+                        }
+                    }
+                } else if (EPI == LM_EPI_ROWS_BF16) {
+                    if (row < M) {  // rounded to bf16 (nearest even) into the row's place
+                        __nv_bfloat16* out =
+                            static_cast<__nv_bfloat16*>(a.out_bf16) + (size_t)dest * (size_t)a.out_stride + x0;
+                        if (x0 + 32 <= a.V) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 8) {
+                                uint32_t p[4];
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                                        __uint_as_float(v[e + 2 * h]), __uint_as_float(v[e + 2 * h + 1]));
+                                    p[h] = *reinterpret_cast<const uint32_t*>(&b2);
+                                }
+                                *reinterpret_cast<uint4*>(out + e) = make_uint4(p[0], p[1], p[2], p[3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (x0 + e < a.V) out[e] = __float2bfloat16_rn(__uint_as_float(v[e]));
                         }
                     }
                 } else if (row < M) {
@@ -357,7 +381,7 @@ __global__ void __launch_bounds__(512) lm_rows_kernel(Problem pb, LmRows r)
     if (pb.ws.req[b] & (SDV_REQ_BAD_LENGTH | SDV_REQ_BAD_TOKEN)) return;
     const int K = pb.K, L = pb.L;
     const int Lb = pb.lengths ? pb.lengths[b] : L;
-    const int n = K * Lb;  // slots of depths 0..L_b - 1 (inner nodes), depth-major
+    const int n = K * (r.leaves ? Lb + 1 : Lb);  // slots of depths 0..L_b - 1 (and L_b), depth-major
     const size_t s0 = (size_t)b * (L + 1) * K;
     __shared__ short local[SDV_MAX_K * (SDV_MAX_L + 1)];
     __shared__ int cnt, base;
@@ -373,6 +397,7 @@ __global__ void __launch_bounds__(512) lm_rows_kernel(Problem pb, LmRows r)
         if (local[i] < 0) continue;
         r.compact[s0 + i] = c0 + local[i];
         r.keys[c0 + local[i]] = 0ull;
+        if (r.row_of) r.row_of[c0 + local[i]] = (b * K + i % K) * (L + 1) + i / K;
     }
     // copy the nodes' hidden rows: 16 bytes per thread and load, four loads
     // in flight per thread
@@ -532,7 +557,12 @@ cudaError_t launch_lm_head(const void* hidden, long long hidden_rows, const void
         grid = grid < tiles ? grid : tiles;
     }
     cudaError_t e;
-    if (epi == LM_EPI_ARGMAX) {
+    if (epi == LM_EPI_ROWS_BF16) {
+        e = cudaFuncSetAttribute(lm_head_kernel<LM_EPI_ROWS_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kLmSmem);
+        if (e != cudaSuccess) return e;
+        lm_head_kernel<LM_EPI_ROWS_BF16><<<(unsigned)grid, kLmThreads, kLmSmem, st>>>(ma, mb, a);
+    } else if (epi == LM_EPI_ARGMAX) {
         e = cudaFuncSetAttribute(lm_head_kernel<LM_EPI_ARGMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kLmSmem);
         if (e != cudaSuccess) return e;

@@ -374,7 +374,31 @@ int sdv_verify_greedy_lm_head(int B, int K, int L, int V, int d, const void *hid
                               int *out_token, float *accept_prob, int *device_status, void *workspace,
                               size_t workspace_bytes, void *cuda_stream);
 
-/* Workspace bytes of sdv_verify_greedy_lm_head; 0 for invalid sizes. */
+/* The LM head for the sampling rules, which cannot be fused into it (each
+ * residual sweep needs the row's normaliser first, and recomputing a row
+ * costs far more than reading it back): every trie node's row, leaves
+ * included, is computed once on the tensor cores and written, rounded to
+ * bf16 (nearest even), into the verification layout, where any
+ * sdv_verify_* call can read it.
+ *   B, K, L, V, d, hidden, lm_head, draft_tokens, lengths  as for
+ *                sdv_verify_greedy_lm_head.
+ *   target_logits [B][K][L+1][row_stride] bf16, 16-byte aligned; row_stride
+ *                >= V and a multiple of 8.  Row (b,k,j) is written for each
+ *                trie node (j <= lengths[b], k the lowest draft with that
+ *                prefix); every other row and the columns past V are left
+ *                as they were.
+ *   device_status [1] or NULL: zeroed, then SDV_REQ_* bits of requests
+ *                with a bad length or token (their rows are not written),
+ *                or SDV_DEV_TIMEOUT.
+ *   workspace    as for sdv_verify_greedy_lm_head.
+ * Returns SDV_OK, SDV_ERR_INVALID, SDV_ERR_WORKSPACE, SDV_ERR_UNSUPPORTED or
+ * SDV_ERR_CUDA.  The profiling hook brackets the LM-head kernel. */
+int sdv_lm_head_trie_logits(int B, int K, int L, int V, int d, const void *hidden, const void *lm_head,
+                            const int *draft_tokens, const int *lengths, void *target_logits, long long row_stride,
+                            int *device_status, void *workspace, size_t workspace_bytes, void *cuda_stream);
+
+/* Workspace bytes of sdv_verify_greedy_lm_head and sdv_lm_head_trie_logits;
+ * 0 for invalid sizes. */
 size_t sdv_lm_head_workspace_bytes(int B, int K, int L, int V, int d);
 
 /* The LM head alone: logits [M][logits_stride] fp32 (columns >= V are not

@@ -286,3 +286,32 @@ def test_fused_greedy_full_size_sampled():
     best = max(range(batch.K), key=lambda k: (int(sub.tokens[0, k, 0].item()) == am[k, 0], -k))
     m = int(int(sub.tokens[0, best, 0].item()) == am[best, 0])
     assert (al[b], ad[b], ot[b]) == (m, best, am[best, m])
+
+
+def test_trie_logits_for_the_sampling_rules():
+    # every trie node's row, leaves included, written once in bf16 into the
+    # verification layout: within bf16 rounding (2^-9 relative) of the fp32
+    # sum, itself within the summation allowance of the exact logits; every
+    # other row and the padding stay untouched
+    B, K, L, V, d = 7, 4, 3, 1003, 136
+    batch = W.make_lm_head(WL, DEV, B=B, K=K, L=L, V=V, d=d, poison_unread=True)
+    batch.lengths[6] = L + 1  # an invalid request: its rows are not written
+    target, status = sdv.lm_head_trie_logits(batch.hidden, batch.lm_head, batch.tokens, batch.lengths)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    host = batch.to("cpu")
+    ref = oracle.lm_head_logits(host.hidden, host.lm_head)
+    bound = _err_bound(host.hidden, host.lm_head)
+    got = target.float().cpu().numpy()
+    assert np.isnan(got[..., V:]).all()
+    read = _read_rows(host.tokens.numpy(), host.lengths.numpy(), L)
+    assert not read[6].any() and read.sum() > B * 2
+    for b in range(B):
+        for k in range(K):
+            for j in range(L + 1):
+                g = got[b, k, j, :V]
+                if not read[b, k, j]:
+                    assert np.isnan(g).all(), (b, k, j)
+                    continue
+                tol = bound[b, k, j] + 2.0 ** -8 * np.abs(ref[b, k, j]) + 1e-30
+                assert (np.abs(g - ref[b, k, j]) <= tol).all(), (b, k, j)
