@@ -69,7 +69,14 @@ struct LmBars {
     uint32_t tmem_base;
 };
 
-constexpr size_t kLmSmem = 1024 + (size_t)kStages * (kTileA + kTileB) + sizeof(LmBars);
+constexpr size_t kBarsBytes = (sizeof(LmBars) + 127) / 128 * 128;
+// ROWS_BF16 epilogue: each epilogue warp stages its 32 rows x 64 columns of
+// bf16 (rows 128 B apart plus 16 B of padding against bank conflicts), then
+// writes whole 128-byte row segments.
+constexpr int kStageCols = 64;
+constexpr int kStagePitch = kStageCols * 2 + 16;   // 144 B
+constexpr int kStageWarpBytes = 32 * kStagePitch;  // 4608 B
+constexpr size_t kLmSmem = 1024 + (size_t)kStages * (kTileA + kTileB) + kBarsBytes + 4 * kStageWarpBytes;
 
 // ------------------------------------------------------------------------
 // PTX: TMA, tcgen05
@@ -291,6 +298,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         }
     } else {  // epilogue: warp w may read TMEM lanes 32 (w % 4) .. + 31
         const int q = warp & 3;
+        unsigned char* const stage =
+            tiles + (size_t)kStages * (kTileA + kTileB) + kBarsBytes + (size_t)(warp - 2) * kStageWarpBytes;
         int i = 0;
         for (long long t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
             const int acc = i & 1;
@@ -322,26 +331,45 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                         }
                     }
                 } else if (EPI == LM_EPI_ROWS_BF16) {
-                    if (row < M) {  // rounded to bf16 (nearest even) into the row's place
-                        __nv_bfloat16* out =
-                            static_cast<__nv_bfloat16*>(a.out_bf16) + (size_t)dest * (size_t)a.out_stride + x0;
-                        if (x0 + 32 <= a.V) {
+                    // this lane's 32 columns, rounded to bf16 (nearest even),
+                    // into its staging row
+                    const int half = c & 1;
 #pragma unroll
-                            for (int e = 0; e < 32; e += 8) {
-                                uint32_t p[4];
+                    for (int e = 0; e < 32; e += 8) {
+                        uint32_t p[4];
 #pragma unroll
-                                for (int h = 0; h < 4; ++h) {
-                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                                        __uint_as_float(v[e + 2 * h]), __uint_as_float(v[e + 2 * h + 1]));
-                                    p[h] = *reinterpret_cast<const uint32_t*>(&b2);
-                                }
-                                *reinterpret_cast<uint4*>(out + e) = make_uint4(p[0], p[1], p[2], p[3]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                if (x0 + e < a.V) out[e] = __float2bfloat16_rn(__uint_as_float(v[e]));
+                        for (int h = 0; h < 4; ++h) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[e + 2 * h]),
+                                                                            __uint_as_float(v[e + 2 * h + 1]));
+                            p[h] = *reinterpret_cast<const uint32_t*>(&b2);
                         }
+                        *reinterpret_cast<uint4*>(stage + lane * kStagePitch + half * 64 + e * 2) =
+                            make_uint4(p[0], p[1], p[2], p[3]);
+                    }
+                    if (half == 1) {
+                        // 32 rows x 64 columns staged: 8 lanes per row, four
+                        // rows per store, each row's 128 bytes in one piece
+                        __syncwarp();
+                        const int xs = n0 + (c - 1) * 32;
+                        const int seg = lane & 7;
+#pragma unroll 1
+                        for (int it = 0; it < 8; ++it) {
+                            const int rl = it * 4 + (lane >> 3);
+                            const int drow = __shfl_sync(0xffffffffu, dest, rl);
+                            const int col = xs + seg * 8;
+                            if (m0 + q * 32 + rl < M && col < a.V) {
+                                const unsigned char* src = stage + rl * kStagePitch + seg * 16;
+                                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out_bf16) +
+                                                     (size_t)drow * (size_t)a.out_stride + col;
+                                if (col + 8 <= a.V) {
+                                    *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(src);
+                                } else {
+                                    for (int e = 0; e < 8 && col + e < a.V; ++e)
+                                        out[e] = reinterpret_cast<const __nv_bfloat16*>(src)[e];
+                                }
+                            }
+                        }
+                        __syncwarp();
                     }
                 } else if (row < M) {
                     float* out = a.logits + (size_t)row * (size_t)a.out_stride + x0;
