@@ -361,8 +361,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                                 const unsigned char* src = stage + rl * kStagePitch + seg * 16;
                                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out_bf16) +
                                                      (size_t)drow * (size_t)a.out_stride + col;
-                                if (col + 8 <= a.V) {
-                                    *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(src);
+                                if (col + 8 <= a.V) {  // streaming: the logits should not evict W from L2
+                                    __stcs(reinterpret_cast<uint4*>(out), *reinterpret_cast<const uint4*>(src));
                                 } else {
                                     for (int e = 0; e < 8 && col + e < a.V; ++e)
                                         out[e] = reinterpret_cast<const __nv_bfloat16*>(src)[e];
