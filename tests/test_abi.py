@@ -161,3 +161,16 @@ def test_gather_inner_rows_rejects_bad_sizes_without_gpu(lib):
     assert f(2, 0, 2, 16, 16, 1, None, None, None, None, None, None, None) == 1   # K = 0
     assert f(2, 1, 2, 16, 12, 1, None, None, None, None, None, None, None) == 1   # stride < V
     assert f(0, 1, 2, 16, 16, 1, None, None, None, None, None, None, None) == 0   # B = 0
+
+
+@pytest.mark.parametrize("over", [dict(d=12), dict(K=0), dict(L=17), dict(V=0), dict(stride=12), dict(stride=20),
+                                  dict(B=-1)])
+def test_trie_logits_invalid_sizes_rejected_without_gpu(lib, over):
+    a = dict(B=2, K=1, L=2, V=16, d=64, stride=16)
+    a.update(over)
+    assert lib.sdv_lm_head_trie_logits(a["B"], a["K"], a["L"], a["V"], a["d"], None, None, None, None, None,
+                                       a["stride"], None, None, 0, None) == 1
+
+
+def test_trie_logits_empty_batch_is_a_no_op(lib):
+    assert lib.sdv_lm_head_trie_logits(0, 2, 2, 16, 64, None, None, None, None, None, 16, None, None, 0, None) == 0
