@@ -170,20 +170,9 @@ __device__ __forceinline__ void online_rebase(Online& s, float wm, float c)
     }
 }
 
-// Pairwise sum of a unit's terms: a dependency chain of depth log2(N)
-// instead of N (the exponentials of a unit are independent).
-template <int N>
-__device__ __forceinline__ float tree_sum(float (&a)[N])
-{
-#pragma unroll
-    for (int w = 1; w < N; w *= 2)
-#pragma unroll
-        for (int i = 0; i + w < N; i += 2 * w) a[i] += a[i + w];
-    return a[0];
-}
-
-
-// Pairwise sum of a unit's 4 or 8 terms with packed adds.
+// Pairwise sum of a unit's 4 or 8 terms with packed adds: a dependency
+// chain of depth log2(N) instead of N (the exponentials of a unit are
+// independent).
 template <int N>
 __device__ __forceinline__ float tree_sum2(const float (&a)[N])
 {
