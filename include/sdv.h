@@ -120,7 +120,7 @@ enum {
 };
 
 /*
- * Arguments shared by the four entry points.
+ * Arguments shared by the sdv_verify_* entry points.
  *   B, K, L, V   batch size (>= 0), drafts per request (1..SDV_MAX_K), draft
  *                length (0..SDV_MAX_L), vocabulary size (1..SDV_MAX_V).
  *   row_stride   elements between consecutive rows; >= V and a multiple
