@@ -346,17 +346,24 @@ def time_calls(fn, steps, stream, prof=None):
     return total, rows
 
 
-def oracle_sample(batch, mode, requests):
-    """Time the oracle, as it stands, on the given requests (host copies)."""
-    import oracle
+def sample_arrays(batch, requests):
+    """Host numpy copies of the given requests' inputs (bf16 logits as int16 bits)."""
     sel = torch.as_tensor(requests, dtype=torch.long, device=batch.target.device)
 
     def take(t):
-        return t.index_select(0, sel).cpu()
+        t = t.index_select(0, sel).cpu()
+        return (t.view(torch.int16) if t.dtype == torch.bfloat16 else t).numpy()
 
-    prob = oracle.Problem(take(batch.target), take(batch.draft), take(batch.tokens), take(batch.lengths),
-                          take(batch.accept_u), take(batch.sample_u), batch.temperature, V=batch.V)
-    positions = int(take(batch.lengths).sum().item()) * batch.K
+    return {k: take(getattr(batch, k)) for k in ("target", "draft", "tokens", "lengths", "accept_u", "sample_u")}
+
+
+def oracle_sample(batch, mode, requests, arrays=None):
+    """Time the oracle, as it stands, on the given requests (host copies)."""
+    import oracle
+    a = arrays if arrays is not None else sample_arrays(batch, requests)
+    prob = oracle.Problem(a["target"], a["draft"], a["tokens"], a["lengths"], a["accept_u"], a["sample_u"],
+                          batch.temperature, V=batch.V)
+    positions = int(a["lengths"].astype(np.int64).sum()) * batch.K
     t0 = time.perf_counter()
     out = oracle.verify(mode, prob)
     dt = time.perf_counter() - t0
@@ -642,10 +649,18 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             rng = np.random.default_rng(1)
             req = sorted(rng.choice(batch.B, size=min(args.cpu_requests, batch.B), replace=False).tolist())
-            p, dt = oracle_sample(batch, args.mode, req)
+            arrays = sample_arrays(batch, req)
+            p, dt = oracle_sample(batch, args.mode, req, arrays)
             line["cpu_baseline"] = {"value": p / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
                                     "sample": f"{len(req)} random requests of the batch ({p} positions, "
                                               f"{dt:.1f} s, single thread)"}
+            # the same sample across every host core, one oracle process each
+            from oracle import pool
+            _, dta, procs = pool.verify_all_cores(arrays, args.mode, batch.temperature, batch.V)
+            line["cpu_baseline_all_cores"] = {"value": p / dta, "unit": UNIT, "cores": procs, "kind": "oracle",
+                                              "sample": f"the same {len(req)} requests split over {procs} "
+                                                        f"processes ({dta:.2f} s wall)"}
+            del arrays
     if rank == 0:
         print(json.dumps(line), flush=True)
 
