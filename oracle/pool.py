@@ -61,6 +61,12 @@ def verify_all_cores(arrays, mode, temperature, V, procs=None):
     from multiprocessing import shared_memory
     B = arrays["target"].shape[0]
     procs = max(1, min(procs or os.cpu_count() or 1, B))
+    # shared memory is a tmpfs: writing past its size would kill this
+    # process, so check the room first
+    need = sum(np.asarray(a).nbytes for a in arrays.values()) + 3 * 4 * B
+    st = os.statvfs("/dev/shm")
+    if st.f_bavail * st.f_frsize < need + (64 << 20):
+        raise RuntimeError(f"/dev/shm has {st.f_bavail * st.f_frsize >> 20} MiB free, {need >> 20} MiB needed")
     shms, specs, workers = [], {}, []
     try:
         for k in _INPUTS + _OUTPUTS:

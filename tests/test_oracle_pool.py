@@ -32,3 +32,17 @@ def test_more_processes_than_requests():
     batch = W.make("mixed-B256-K8-L8-V151936-bf16", "cpu", B=2, K=2, L=2, V=101)
     out, dt, used = pool.verify_all_cores(_arrays(batch), "multidraft", batch.temperature, batch.V, procs=8)
     assert used == 2 and out["accept_len"].shape == (2,)
+
+
+def test_refuses_when_shared_memory_is_too_small(monkeypatch):
+    # a tmpfs written past its size would kill the process: the pool checks
+    # the room first and raises instead
+    import os
+
+    class Small:
+        f_bavail, f_frsize = 1024, 4096  # 4 MiB free
+
+    monkeypatch.setattr(os, "statvfs", lambda path: Small())
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", "cpu", B=2, K=2, L=2, V=101)
+    with pytest.raises(RuntimeError, match="/dev/shm"):
+        pool.verify_all_cores(_arrays(batch), "token", batch.temperature, batch.V, procs=2)
