@@ -50,6 +50,7 @@ def lib():
         _lib.sdvo_verify.restype = ctypes.c_int
         _lib.sdvo_exact_outcomes.restype = ctypes.c_int
         _lib.sdvo_exact_streams.restype = ctypes.c_int
+        _lib.sdvo_exact_accept_len.restype = ctypes.c_int
         _lib.sdvo_prefix_index.restype = ctypes.c_longlong
         _lib.sdvo_sample_rows.restype = ctypes.c_int
         _lib.sdvo_lm_head_logits.restype = ctypes.c_int
@@ -115,16 +116,20 @@ class Problem:
 
     def request(self, b):
         """The same problem restricted to request b (a contiguous slab)."""
+        return self.requests(b, b + 1)
+
+    def requests(self, lo, hi):
+        """The same problem restricted to requests lo..hi-1 (views, no copy)."""
         sub = object.__new__(Problem)
         sub.__dict__.update(self.__dict__)
-        sl = slice(b, b + 1)
+        sl = slice(lo, hi)
         sub.target = self.target[sl]
         sub.draft = None if self.draft is None else self.draft[sl]
         sub.tokens = self.tokens[sl]
         sub.lengths = None if self.lengths is None else self.lengths[sl]
         sub.accept_u = None if self.accept_u is None else self.accept_u[sl]
         sub.sample_u = None if self.sample_u is None else self.sample_u[sl]
-        sub.B = 1
+        sub.B = hi - lo
         return sub
 
 
@@ -158,6 +163,63 @@ def verify(mode, prob: Problem, residual_out=False, trace_cap=0):
     if tr is not None:
         out["trace"] = [(entries[i].kind, entries[i].index, entries[i].lo, entries[i].hi)
                         for i in range(min(tr.n, trace_cap))]
+    return out
+
+
+def trace_counts(prob: Problem, trace, margin=1e-5):
+    """Per request: the decisions the oracle took (comparisons of a uniform
+    with a threshold, and inverse-CDF draws) and how many of them were
+    within `margin` of flipping: |u - threshold| for an accept test, the
+    distance of u to the ends of the chosen token's CDF interval for a draw.
+    Returns two int arrays of shape [B]."""
+    K, L = prob.K, prob.L
+    dec = np.zeros(prob.B, np.int64)
+    near = np.zeros(prob.B, np.int64)
+    au = None if prob.accept_u is None else prob.accept_u.reshape(-1)
+    su = None if prob.sample_u is None else prob.sample_u.reshape(-1)
+    for kind, idx, lo, hi in trace:
+        if kind == 0:
+            b, m = idx // (K * L), abs(au[idx] - lo)
+        else:
+            b, m = idx // (K * (L + 1)), min(su[idx] - lo, hi - su[idx])
+        dec[b] += 1
+        near[b] += m < margin
+    return dec, near
+
+
+def verify_threads(mode, prob: Problem, threads=None, residual_out=False, trace_cap_per_request=4096):
+    """verify() with the requests split into contiguous shares run on
+    `threads` host threads (the oracle holds no global state, and ctypes
+    releases the interpreter lock during each call).  Returns verify()'s
+    outputs for the whole batch plus per-request 'decisions' and
+    'near_margin' counts (trace_counts)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    B = prob.B
+    threads = max(1, min(threads or os.cpu_count() or 1, B)) if B else 1
+    bounds = np.linspace(0, B, 4 * threads + 1).astype(int) if B else np.array([0, 0])
+    shares = [(int(lo), int(hi)) for lo, hi in zip(bounds[:-1], bounds[1:]) if hi > lo]
+
+    def run(share):
+        lo, hi = share
+        sub = prob.requests(lo, hi)
+        out = verify(mode, sub, residual_out=residual_out, trace_cap=trace_cap_per_request * (hi - lo))
+        out["decisions"], out["near_margin"] = trace_counts(sub, out["trace"])
+        return out
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(run, shares))
+    if any(p["rc"] != 0 for p in parts):
+        raise RuntimeError("oracle verify failed")
+    keys = ["accept_len", "accept_draft", "out_token", "accept_prob", "residual_mass", "margin", "req_status",
+            "decisions", "near_margin"] + (["residual_out"] if residual_out else [])
+    if not parts:
+        empty = verify(mode, prob, residual_out=residual_out)
+        empty["decisions"] = np.zeros(0, np.int64)
+        empty["near_margin"] = np.zeros(0, np.int64)
+        return empty
+    out = {k: np.concatenate([p[k] for p in parts]) for k in keys}
+    out["rc"] = 0
     return out
 
 
@@ -215,6 +277,31 @@ def exact_outcomes(mode, prob: Problem):
     if rc != 0:
         raise RuntimeError(f"sdvo_exact_outcomes failed: {rc}")
     return out
+
+
+def exact_accept_len(mode, prob: Problem):
+    """Exact P(tau = i) of a one-request problem over its accept uniforms:
+    array [L+1]."""
+    assert prob.B == 1
+    out = np.zeros(prob.L + 1, np.float64)
+    s = prob.struct()
+    rc = lib().sdvo_exact_accept_len(ctypes.c_int(MODE[mode]), ctypes.byref(s), _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"sdvo_exact_accept_len failed: {rc}")
+    return out
+
+
+def expected_accept_len(mode, prob: Problem, threads=None):
+    """E[tau | drafts] of every request (exact over its accept uniforms),
+    computed on host threads: array [B]."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    if prob.B == 0:
+        return np.zeros(0)
+    threads = max(1, min(threads or os.cpu_count() or 1, prob.B))
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        dists = list(ex.map(lambda b: exact_accept_len(mode, prob.request(b)), range(prob.B)))
+    return np.array([float(np.dot(np.arange(d.size), d)) for d in dists])
 
 
 def prefix_index(tokens, V):
