@@ -34,6 +34,7 @@ typedef struct {
     sink_fn sink;
     void* ctx;
     int err;
+    int accept_only; /* split at accept-test thresholds only (the draws' uniforms stay whole) */
 } integ_t;
 
 static void run_box(integ_t* g, double w);
@@ -64,6 +65,7 @@ static void run_box(integ_t* g, double w)
     for (int i = 0; i < g->tr.n; ++i) {
         sdvo_trace_entry e = g->tr.e[i];
         int c = e.kind == 0 ? e.index : g->n_acc + e.index;
+        if (e.kind == 1 && g->accept_only) continue;
         if (g->lo[c] < e.lo && e.lo < g->hi[c]) {
             split_at(g, c, e.lo, w);
             return;
@@ -143,6 +145,42 @@ int sdvo_exact_outcomes(int mode, const sdvo_problem* pb, double* out_prob)
         s.V = pb->V;
         g.sink = outcome_sink;
         g.ctx = &s;
+        integ_reset_box(&g);
+        run_box(&g, 1.0);
+        rc = g.err;
+    }
+    integ_free(&g);
+    return rc;
+}
+
+/* ---- accepted length only ------------------------------------------------ */
+
+/* The accepted length is settled by the accept tests alone: every rule
+ * takes them all before it draws the correction.  Integrating over the
+ * accept uniforms only, with the draws' uniforms left whole, gives
+ * P(tau = i) exactly at the cost of one oracle run per decision path. */
+static void tau_sink(void* ctx, const int* tokens, int K, int L, int tau, int kstar, int token, double w)
+{
+    double* out = (double*)ctx;
+    (void)tokens;
+    (void)K;
+    (void)L;
+    (void)kstar;
+    (void)token;
+    out[tau] += w;
+}
+
+int sdvo_exact_accept_len(int mode, const sdvo_problem* pb, double* tau_prob)
+{
+    integ_t g;
+    int rc;
+    if (!pb || pb->B != 1 || !tau_prob) return SDVO_ERR_INVALID;
+    rc = integ_init(&g, mode, pb);
+    if (rc == SDVO_OK) {
+        memset(tau_prob, 0, sizeof(double) * (size_t)(pb->L + 1));
+        g.sink = tau_sink;
+        g.ctx = tau_prob;
+        g.accept_only = 1;
         integ_reset_box(&g);
         run_box(&g, 1.0);
         rc = g.err;

@@ -95,6 +95,13 @@ int sdvo_verify(int mode, const sdvo_problem* pb,
  * [tau][k*][token].  Returns SDVO_OK or an error code. */
 int sdvo_exact_outcomes(int mode, const sdvo_problem* pb, double* out_prob);
 
+/* Exact P(tau = i), i = 0..L, of one request (B == 1) over its accept
+ * uniforms: the integration of sdvo_exact_outcomes with the draws'
+ * uniforms left whole (tau is settled before the correction is drawn).
+ * E[tau] = sum_i i tau_prob[i] is the expected accepted length for the
+ * request's fixed drafts.  Returns SDVO_OK or an error code. */
+int sdvo_exact_accept_len(int mode, const sdvo_problem* pb, double* tau_prob);
+
 /* Exact distribution of the emitted stream (accepted prefix + correction
  * token) of a prefix-consistent toy model, over all K-tuples of i.i.d.
  * drafts of length L and over the uniforms.

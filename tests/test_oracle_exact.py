@@ -373,3 +373,36 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
                     and all(e[K] >= ref[K] - TOL and abs(et[K] - ref[K]) < 1e-9 for K in (1, 2, 3))):
                 caught.append(("invariant", seed))
         assert caught, f"mutant {name} not caught by the stream-validity pin"
+
+
+@pytest.mark.parametrize("mode,K", [("token", 1), ("token", 3), ("block", 1), ("multidraft", 3), ("kseq", 3),
+                                    ("greedy", 2)])
+@pytest.mark.parametrize("seed", [0, 4])
+def test_exact_accept_len_is_the_outcome_marginal(mode, K, seed):
+    """sdvo_exact_accept_len integrates over the accept uniforms alone: its
+    P(tau = i) equals the marginal of the full exact outcome law, and the
+    token rule at K = 1 gives the closed-form tail prod_{j<i} r_j."""
+    V, L, T = 4, 3, 0.8
+    prob, tgt, dft, tok = _fixed_problem(V, K, L, seed, T)
+    ex = oracle.exact_outcomes(mode, prob)
+    tau = oracle.exact_accept_len(mode, prob)
+    assert abs(tau.sum() - 1.0) < TOL
+    assert np.max(np.abs(tau - ex.sum(axis=(1, 2)))) < TOL
+    if mode == "token" and K == 1:
+        P = tm.softmax_rows(tgt[0, 0], T)
+        Q = tm.softmax_rows(dft[0, 0], T)
+        r = [min(1.0, P[j, tok[0, 0, j]] / Q[j, tok[0, 0, j]]) for j in range(L)]
+        tail = [np.prod(r[:i]) for i in range(L + 1)]
+        assert np.max(np.abs(np.cumsum(tau[::-1])[::-1] - tail)) < TOL
+
+
+def test_expected_accept_len_over_requests():
+    """expected_accept_len: per request E[tau] = sum_i i P(tau = i), one
+    request at a time on host threads."""
+    V, K, L, T = 4, 2, 3, 1.0
+    probs = [_fixed_problem(V, K, L, s, T)[0] for s in range(3)]
+    for mode in ("token", "multidraft"):
+        for p in probs:
+            want = float(np.dot(np.arange(L + 1), oracle.exact_accept_len(mode, p)))
+            got = oracle.expected_accept_len(mode, p, threads=2)
+            assert got.shape == (1,) and abs(got[0] - want) < TOL
