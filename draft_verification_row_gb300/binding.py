@@ -28,7 +28,9 @@ EXPORTS = list(_ENTRY.values()) + ["sdv_workspace_bytes", "sdv_status_string", "
                                    "sdv_set_profile_events", "sdv_sample_rows", "sdv_copy_read_rows",
                                    "sdv_read_rows_bytes", "sdv_gather_read_rows", "sdv_verify_greedy_lm_head",
                                    "sdv_lm_head_workspace_bytes", "sdv_lm_head_logits", "sdv_gather_inner_rows",
-                                   "sdv_verify_leaves_apart", "sdv_lm_head_trie_logits"]
+                                   "sdv_verify_leaves_apart", "sdv_lm_head_trie_logits", "sdv_verify_residual",
+                                   "sdv_verify_multidraft_static", "sdv_testing_set_wait_limit",
+                                   "sdv_testing_verify_without_roots"]
 
 
 class SDVError(RuntimeError):
@@ -85,6 +87,12 @@ def lib(path: str = LIB_PATH):
     h.sdv_gather_inner_rows.argtypes = h.sdv_gather_read_rows.argtypes
     h.sdv_verify_leaves_apart.restype = ctypes.c_int
     h.sdv_verify_leaves_apart.argtypes = [ctypes.c_int] + _VERIFY_ARGTYPES + [ctypes.c_void_p]
+    h.sdv_verify_residual.restype = ctypes.c_int
+    h.sdv_verify_residual.argtypes = [ctypes.c_int] + _VERIFY_ARGTYPES + [ctypes.c_void_p]
+    h.sdv_testing_set_wait_limit.restype = ctypes.c_int
+    h.sdv_testing_set_wait_limit.argtypes = [ctypes.c_ulonglong]
+    h.sdv_testing_verify_without_roots.restype = ctypes.c_int
+    h.sdv_testing_verify_without_roots.argtypes = [ctypes.c_int] + _VERIFY_ARGTYPES
     h.sdv_read_rows_bytes.restype = ctypes.c_int
     h.sdv_read_rows_bytes.argtypes = ([ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int] + [ctypes.c_void_p] * 2
                                       + [ctypes.POINTER(ctypes.c_longlong)])
@@ -131,7 +139,8 @@ def _dtype_code(t):
 class Outputs:
     """Preallocated outputs (and workspace) for repeated calls of one shape."""
 
-    def __init__(self, mode, B, K, L, V, device, accept_prob=True, residual_mass=True):
+    def __init__(self, mode, B, K, L, V, device, accept_prob=True, residual_mass=True, residual_out=False):
+        self.residual_out = torch.empty((B, V), dtype=torch.float32, device=device) if residual_out else None
         self.accept_len = torch.empty(B, dtype=torch.int32, device=device)
         self.accept_draft = torch.empty(B, dtype=torch.int32, device=device)
         self.out_token = torch.empty(B, dtype=torch.int32, device=device)
@@ -142,12 +151,16 @@ class Outputs:
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
 
     def as_dict(self):
-        return {k: getattr(self, k) for k in ("accept_len", "accept_draft", "out_token", "accept_prob",
-                                              "residual_mass", "device_status")}
+        d = {k: getattr(self, k) for k in ("accept_len", "accept_draft", "out_token", "accept_prob",
+                                           "residual_mass", "device_status")}
+        if self.residual_out is not None:
+            d["residual_out"] = self.residual_out
+        return d
 
 
 def verify(mode, target, draft, tokens, lengths, accept_u, sample_u, temperature, *, V=None,
-           out: Outputs = None, stream=None, accept_prob=True, residual_mass=True, leaf_target=None):
+           out: Outputs = None, stream=None, accept_prob=True, residual_mass=True, leaf_target=None,
+           residual_out=False):
     """Run one verification call on the current CUDA stream.
 
     target [B][K][L+1][stride], draft [B][K][L][stride] (float32 or bfloat16),
@@ -155,7 +168,9 @@ def verify(mode, target, draft, tokens, lengths, accept_u, sample_u, temperature
     sample_u [B][K][L+1] float32.  Returns a dict of output tensors; the call
     is asynchronous (read them after a synchronize).  leaf_target: a tensor of
     target's shape and dtype (e.g. pinned host memory) the leaves' rows are
-    read from instead (sdv_verify_leaves_apart).
+    read from instead (sdv_verify_leaves_apart).  residual_out: also return
+    [B][V] float32 rows, the normalised distribution each correction was
+    drawn from (sdv_verify_residual).
     """
     if mode not in _ENTRY:
         raise ValueError(f"unknown mode {mode!r}")
@@ -175,7 +190,11 @@ def verify(mode, target, draft, tokens, lengths, accept_u, sample_u, temperature
         if t is not None and (t.dtype != dt or not t.is_contiguous() or not t.is_cuda):
             raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
     if out is None:
-        out = Outputs(mode, B, K, L, V, target.device, accept_prob, residual_mass)
+        out = Outputs(mode, B, K, L, V, target.device, accept_prob, residual_mass, residual_out)
+    if residual_out and (out.residual_out is None or tuple(out.residual_out.shape) != (B, V)):
+        raise ValueError("residual_out needs Outputs holding a [B][V] residual_out tensor")
+    if residual_out and leaf_target is not None:
+        raise ValueError("residual_out and leaf_target cannot be combined")
     if stream is None:
         stream = torch.cuda.current_stream(target.device)
     args = (B, K, L, V, stride, _dtype_code(target), float(temperature),
@@ -183,6 +202,11 @@ def verify(mode, target, draft, tokens, lengths, accept_u, sample_u, temperature
             _ptr(out.accept_len), _ptr(out.accept_draft), _ptr(out.out_token), _ptr(out.accept_prob),
             _ptr(out.residual_mass), _ptr(out.device_status), _ptr(out.workspace),
             out.workspace.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if residual_out:
+        rc = h.sdv_verify_residual(MODES[mode], *args, _ptr(out.residual_out))
+        if rc != 0:
+            raise SDVError(rc, "sdv_verify_residual")
+        return out.as_dict()
     if leaf_target is None:
         rc = getattr(h, _ENTRY[mode])(*args)
     else:

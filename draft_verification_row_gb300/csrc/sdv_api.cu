@@ -100,13 +100,19 @@ bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) %
 thread_local cudaEvent_t g_prof_start = nullptr;
 thread_local cudaEvent_t g_prof_stop = nullptr;
 
+// limit of the bounded device waits (sdv_testing_set_wait_limit): per host
+// thread; 0 means the default of 2 s
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+thread_local unsigned long long g_wait_ns = 0;
+
 bool prof_record(cudaEvent_t e, cudaStream_t st) { return !e || cudaEventRecord(e, st) == cudaSuccess; }
 
 int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype, float temperature,
            const void* target_logits, const void* draft_logits, const int* draft_tokens, const int* lengths,
            const float* accept_u, const float* sample_u, int* accept_len, int* accept_draft, int* out_token,
            float* accept_prob, float* residual_mass, int* device_status, void* workspace,
-           size_t workspace_bytes, void* cuda_stream, const void* leaf_target = nullptr)
+           size_t workspace_bytes, void* cuda_stream, const void* leaf_target = nullptr,
+           float* residual_out = nullptr, bool skip_roots = false)
 {
     if (!sizes_ok(B, K, L, V)) return SDV_ERR_INVALID;
     if (row_stride < V || row_stride % 8 != 0) return SDV_ERR_INVALID;
@@ -134,9 +140,10 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
     const void* ptrs[] = {target_logits,  need_draft ? draft_logits : nullptr,
                           L > 0 ? draft_tokens : nullptr, lengths,
                           need_draft ? accept_u : nullptr, greedy ? nullptr : sample_u,
-                          accept_len, accept_draft, out_token, accept_prob, residual_mass};
+                          accept_len, accept_draft, out_token, accept_prob, residual_mass, residual_out};
     for (const void* q : ptrs)
         if (q && !device_accessible(q)) return SDV_ERR_INVALID;
+    if (residual_out && !aligned(residual_out, 4)) return SDV_ERR_INVALID;
     if (leaf_target && (!aligned(leaf_target, 16) || !device_accessible(leaf_target))) return SDV_ERR_INVALID;
     if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < workspace_size(B, K, L))
         return SDV_ERR_WORKSPACE;
@@ -165,11 +172,19 @@ int verify(int mode, int B, int K, int L, int V, long long row_stride, int dtype
     pb.accept_prob = accept_prob;
     pb.residual_mass = residual_mass;
     pb.device_status = device_status;
+    pb.residual_out = residual_out;
+    pb.wait_ns = g_wait_ns ? g_wait_ns : kDefaultWaitNs;
     pb.ws = carve(workspace, B, K, L);
 
     if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int), st) != cudaSuccess) return SDV_ERR_CUDA;
     if (cudaMemsetAsync(pb.ws.ncount, 0, sizeof(int) * (2 * L + 3), st) != cudaSuccess) return SDV_ERR_CUDA;
     if (launch_prep(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
+    // test hook: take the roots (depth 0) out of the node kernel's work list,
+    // so that nothing writes their children's weights nor finishes their
+    // requests, and every wait on them runs out
+    if (skip_roots && (cudaMemsetAsync(pb.ws.ncount, 0, sizeof(int), st) != cudaSuccess ||
+                       cudaMemsetAsync(pb.ws.ncount + (L + 1), 0, sizeof(int), st) != cudaSuccess))
+        return SDV_ERR_CUDA;
     if (!prof_record(g_prof_start, st)) return SDV_ERR_CUDA;
     if (greedy) {
         if (launch_argmax(pb, st) != cudaSuccess) return SDV_ERR_CUDA;
@@ -266,6 +281,7 @@ int verify_greedy_lm_head(int B, int K, int L, int V, int d, const void* hidden,
     pb.out_token = out_token;
     pb.accept_prob = accept_prob;
     pb.device_status = device_status;
+    pb.wait_ns = g_wait_ns ? g_wait_ns : kDefaultWaitNs;
     const size_t n = slot_count(B, K, L);
     LmRows r = carve_lm(workspace, pb, d, hidden);
     r.leaves = 0;
@@ -356,6 +372,29 @@ int sdv_verify_leaves_apart(int mode, SDV_VERIFY_ARGS, const void* leaf_target_l
                        device_status, workspace, workspace_bytes, cuda_stream, leaf_target_logits);
 }
 
+int sdv_verify_residual(int mode, SDV_VERIFY_ARGS, float* residual_out)
+{
+    if (mode < SDV_MODE_TOKEN || mode > SDV_MODE_KSEQ) return SDV_ERR_INVALID;
+    if (!residual_out && B > 0) return SDV_ERR_INVALID;
+    return sdv::verify(mode, B, K, L, V, row_stride, dtype, temperature, target_logits, draft_logits, draft_tokens,
+                       lengths, accept_u, sample_u, accept_len, accept_draft, out_token, accept_prob, residual_mass,
+                       device_status, workspace, workspace_bytes, cuda_stream, nullptr, residual_out);
+}
+
+int sdv_testing_set_wait_limit(unsigned long long wait_ns)
+{
+    sdv::g_wait_ns = wait_ns;
+    return SDV_OK;
+}
+
+int sdv_testing_verify_without_roots(int mode, SDV_VERIFY_ARGS)
+{
+    if (mode != SDV_MODE_BLOCK && mode != SDV_MODE_MULTIDRAFT) return SDV_ERR_INVALID;
+    return sdv::verify(mode, B, K, L, V, row_stride, dtype, temperature, target_logits, draft_logits, draft_tokens,
+                       lengths, accept_u, sample_u, accept_len, accept_draft, out_token, accept_prob, residual_mass,
+                       device_status, workspace, workspace_bytes, cuda_stream, nullptr, nullptr, true);
+}
+
 size_t sdv_workspace_bytes(int mode, int B, int K, int L, int V)
 {
     if (mode < SDV_MODE_TOKEN || mode > SDV_MODE_KSEQ || !sdv::sizes_ok(B, K, L, V)) return 0;
@@ -404,6 +443,7 @@ int sdv_lm_head_trie_logits(int B, int K, int L, int V, int d, const void* hidde
     pb.tokens = draft_tokens;
     pb.lengths = lengths;
     pb.device_status = device_status;
+    pb.wait_ns = g_wait_ns ? g_wait_ns : kDefaultWaitNs;
     LmRows r = carve_lm(workspace, pb, d, hidden);
     r.leaves = 1;  // every trie node's row, leaves included
     LmArgs a;

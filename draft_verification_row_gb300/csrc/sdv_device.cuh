@@ -115,13 +115,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase)
     return ok != 0;
 }
 
-// Waits for phase `phase` of the barrier for at most kWaitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase)
+// Waits for phase `phase` of the barrier for at most limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, uint64_t limit_ns = kWaitNs)
 {
     if (mbar_try_wait(bar, phase)) return true;  // the common case reads no clock
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, phase)) {
-        if (globaltimer() - t0 > kWaitNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
     return true;
 }

@@ -56,6 +56,8 @@ struct Problem {
     float* residual_mass;
     int* device_status;
     int* leaf_pending;  // greedy with the LM head: [B] end leaf slot whose argmax is still to come, or -1
+    float* residual_out;  // [B][V] or NULL: the normalised distribution each correction was drawn from
+    unsigned long long wait_ns;  // limit of every bounded device wait, in nanoseconds
     Workspace ws;
 };
 

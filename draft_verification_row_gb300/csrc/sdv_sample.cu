@@ -395,6 +395,7 @@ struct DecideSmem {
     int tok[SDV_MAX_K * SDV_MAX_L];
     signed char sib[kSlotsMax];  // next sibling's draft, or -1
     int endn;                    // the end node: slot | leaf << 30, or -1 (no draw)
+    int token;                   // the correction token once known (greedy, no draw), else -1
 };
 
 // Decide request b (one warp): accept_len, accept_draft, accept_prob,
@@ -404,6 +405,7 @@ __device__ void decide_request(const Problem& pb, int b, bool greedy, DecideSmem
     const int K = pb.K, L = pb.L;
     if (lane == 0) {
         s.endn = -1;
+        s.token = -1;
         if (pb.leaf_pending) pb.leaf_pending[b] = -1;
     }
     const int st = pb.ws.req[b];
@@ -479,7 +481,7 @@ __device__ void decide_request(const Problem& pb, int b, bool greedy, DecideSmem
         if (pb.residual_mass) pb.residual_mass[b] = 1.f;
         const size_t se = s0 + (size_t)ej * K + eo;
         if (ej < Lb) {
-            pb.out_token[b] = __float_as_int(val[ej * K + eo]);
+            pb.out_token[b] = s.token = __float_as_int(val[ej * K + eo]);
         } else if (pb.leaf_pending) {  // the LM head computes this leaf's row afterwards
             pb.out_token[b] = -1;
             pb.leaf_pending[b] = (int)se;
@@ -574,6 +576,44 @@ __device__ __noinline__ void invalidate_request(const Problem& pb, int b, int la
     }
 }
 
+// The debug output residual_out[b][0..V): the normalised distribution the
+// correction (or bonus) token was drawn from, written by every thread of
+// the CTA after the draw.  tok >= 0 with one_hot: a one-hot row at tok
+// (greedy); tok < 0 with one_hot: a zero row (an invalid request);
+// otherwise each element's mass under d over the total the draw used.
+template <int DT>
+__device__ void write_residual_row(const Problem& pb, int b, const Dist& d, const RowSmem& sm, bool one_hot, int tok,
+                                   int tid, int lane)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+    const int V = pb.V;
+    float* row = pb.residual_out + (size_t)b * V;
+    if (one_hot) {
+        for (int x = tid; x < V; x += kRT) row[x] = x == tok ? 1.f : 0.f;
+        return;
+    }
+    const int n_units = (V + EPU - 1) / EPU;
+    const int n_seg = (n_units + kRSeg - 1) / kRSeg;
+    // the total, summed as the draw sums it (every warp for itself)
+    float tot = 0.f;
+    for (int i = lane; i < n_seg; i += 32) {
+        if (d.residual) {
+            tot += sm.mass[i];
+        } else {
+            const float ref = sm.ref[i];
+            tot += ref > -INFINITY ? sm.mass[i] * ex2((ref - d.M) * d.c) : 0.f;
+        }
+    }
+    tot = warp_sum(tot);
+    for (int ug = tid; ug < n_units; ug += kRT) {
+        float v[EPU];
+        unit_masses<DT>(d, ug, n_units, V, false, v);
+#pragma unroll
+        for (int e = 0; e < EPU; ++e)
+            if (ug * EPU + e < V) row[ug * EPU + e] = v[e] / tot;
+    }
+}
+
 // One CTA per request: the decision (warp 0), then the correction (or
 // bonus) token at the end node it chose: from the node's final residual R_n
 // (kept by the node kernel), or from P at a leaf or where S_n = 0.
@@ -598,7 +638,7 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy, 
                 do {
                     __nanosleep(256);  // leave issue slots to the node kernel's CTAs on this SM
                     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(n) : "l"(left) : "memory");
-                } while (n > 0 && globaltimer() - t0 <= kWaitNs);
+                } while (n > 0 && globaltimer() - t0 <= pb.wait_ns);
                 if (n > 0) {
                     atomicOr(&pb.ws.req[b], SDV_DEV_TIMEOUT);
                     if (pb.device_status) atomicOr(pb.device_status, SDV_DEV_TIMEOUT);
@@ -611,7 +651,13 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy, 
     if (tid == 0) sm.bad = 0;
     __syncthreads();
     const int e = ds.endn;
-    if (e < 0) return;  // greedy, or an invalid request: the decision wrote the outputs
+    if (e < 0) {  // greedy, or an invalid request: the decision wrote the outputs
+        if (pb.residual_out) {
+            Dist none = {};
+            write_residual_row<DT>(pb, b, none, sm, true, ds.token, tid, lane);
+        }
+        return;
+    }
     const int K = pb.K, L = pb.L, V = pb.V;
     const size_t slot = (size_t)(e & ((1 << 30) - 1));
     const bool leaf = (e >> 30) != 0;
@@ -648,6 +694,7 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy, 
             // every inner node's rows), and a leaf's row is read here alone,
             // so the request is found invalid now: its outputs are replaced
             if (w == 0) invalidate_request(pb, b, lane);
+            if (pb.residual_out) write_residual_row<DT>(pb, b, d, sm, true, -1, tid, lane);
             return;
         }
         d.M = M;
@@ -655,7 +702,11 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy, 
     }
     if (w == 0) {
         const int x = draw<DT>(d, sm, V, u, greedy != 0, lane);
-        if (lane == 0) pb.out_token[b] = x;
+        if (lane == 0) pb.out_token[b] = ds.token = x;
+    }
+    if (pb.residual_out) {
+        __syncthreads();
+        write_residual_row<DT>(pb, b, d, sm, greedy != 0, ds.token, tid, lane);
     }
 }
 

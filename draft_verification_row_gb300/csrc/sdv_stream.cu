@@ -289,7 +289,7 @@ __device__ __forceinline__ void online_finish(Online& s, const uint4 (*stash)[kU
 // lane's sum is not (in practice a few chunks per row and warp).
 template <int DT>
 __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, uint32_t& g, bool& timed_out,
-                                      int nc, int n_units, int V, float c, int cw, int lane)
+                                      int nc, int n_units, int V, float c, int cw, int lane, uint64_t lim)
 {
     uint4(*const stashT)[kUPT] = sm->stash[0][cw * 32 + lane];
     uint4(*const stashD)[kUPT] = sm->stash[1][cw * 32 + lane];
@@ -297,7 +297,7 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
 #pragma unroll 1
     for (int ch = 0; ch < nc; ++ch, ++g) {
         const int s = g % kStages;
-        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
+        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim)) timed_out = true;
         const bool tail = ch == nc - 1;
         const int ug0 = ch * kChunk + unit_local(cw, 0, lane);
         uint4 t[kUPT], d[kUPT];
@@ -375,7 +375,7 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
 template <int DT>
 __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_out, int nc, int n_units, int V,
                                        float c, float gnegT, float gnegD, float aT, float r, int xs, int cw,
-                                       int lane, bool back)
+                                       int lane, bool back, uint64_t lim)
 {
     constexpr int EPU = Elem<DT>::kPerUnit;
     const int xs_ch = xs >= 0 ? xs / EPU / kChunk : -1;  // x* is carried apart: its chunk skips it
@@ -384,7 +384,7 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
     for (int it = 0; it < nc; ++it, ++g) {
         const int ch = back ? nc - 1 - it : it;
         const int s = g % kStages;
-        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
+        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim)) timed_out = true;
         const bool tail = ch == nc - 1;
         float w = 0.f;
 #pragma unroll
@@ -431,7 +431,7 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
 template <int DT, int NP>
 __device__ __forceinline__ void kseq_sweep(StreamSmem* sm, uint32_t& g, bool& timed_out, int nc, int n_units, int V,
                                            float c, float gnegT, float gnegD, const float (&f)[5], float (&acc)[5],
-                                           int cw, int lane, bool back)
+                                           int cw, int lane, bool back, uint64_t lim)
 {
     constexpr int EPU = Elem<DT>::kPerUnit;
 #pragma unroll
@@ -440,7 +440,7 @@ __device__ __forceinline__ void kseq_sweep(StreamSmem* sm, uint32_t& g, bool& ti
     for (int it = 0; it < nc; ++it, ++g) {
         const int ch = back ? nc - 1 - it : it;
         const int s = g % kStages;
-        if (!timed_out && !mbar_wait_bounded(&sm->full[s], (g / kStages) & 1)) timed_out = true;
+        if (!timed_out && !mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim)) timed_out = true;
         const bool tail = ch == nc - 1;
 #pragma unroll
         for (int i = 0; i < kUPT; ++i) {
@@ -600,6 +600,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
     const int n_units = (V + EPU - 1) / EPU;
     const int nc = (n_units + kChunk - 1) / kChunk;
     const float c = pb.c;
+    const uint64_t lim = pb.wait_ns;
     int* const counter = pb.ws.ncount + 2 * (L + 1);
 
     if (tid == 0) {
@@ -650,7 +651,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 slot = pb.ws.nodes[(size_t)j * BK + (i < nf ? i : BK - 1 - (i - nf))];
             }
             bool ok = true;
-            if (lane == 0 && it >= kQ) ok = mbar_wait_bounded(&sm->qempty[q], (it / kQ - 1) & 1);
+            if (lane == 0 && it >= kQ) ok = mbar_wait_bounded(&sm->qempty[q], (it / kQ - 1) & 1, lim);
             if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
                 sm->abort = 1;
                 break;
@@ -700,7 +701,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
         uint32_t g = 0;
         for (uint32_t it = 0;; ++it) {
             const int q = it % kQ;
-            if (!mbar_wait_bounded(&sm->qfull[q], (it / kQ) & 1)) {
+            if (!mbar_wait_bounded(&sm->qfull[q], (it / kQ) & 1, lim)) {
                 sm->abort = 1;
                 break;
             }
@@ -725,7 +726,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                     const int ch = back ? nc - 1 - i : i;
                     const int s = g % kStages;
                     const uint32_t use = g / kStages;
-                    if (use > 0 && !mbar_wait_bounded(&sm->empty[s], (use - 1) & 1)) {
+                    if (use > 0 && !mbar_wait_bounded(&sm->empty[s], (use - 1) & 1, lim)) {
                         ok = false;
                         break;
                     }
@@ -741,6 +742,15 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 break;
             }
         }
+        // before the CTA may exit: every copy this warp issued has landed
+        // (at once in a normal run, where the consumers waited for each;
+        // after an abort they may not have)
+        for (int s = 0; s < kStages; ++s) {
+            if (g > (uint32_t)s) {
+                const uint32_t last_use = (g - 1 - (uint32_t)s) / kStages;
+                mbar_wait_bounded(&sm->full[s], last_use & 1, lim);
+            }
+        }
         return;
     }
 
@@ -751,7 +761,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
     for (uint32_t it = 0;; ++it) {
         const int q = it % kQ;
         // copy the descriptor, then hand the queue slot back
-        const bool got = mbar_wait_bounded(&sm->qfull[q], (it / kQ) & 1);
+        const bool got = mbar_wait_bounded(&sm->qfull[q], (it / kQ) & 1, lim);
         if (!got) atomicExch(&sm->abort, 1);
         cbar_sync();  // the previous node's readers of sm->cur are done
         if (ct < (int)(sizeof(NodeDesc) / 4))
@@ -767,7 +777,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
 
         // ---- pass 1: online statistics ----
         Online sT, sD;
-        pass1<DT>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane);
+        pass1<DT>(sm, sT, sD, g, timed_out, nc, n_units, V, c, cw, lane, lim);
         online_finish<DT>(sT, sm->stash[0][ct], cw, lane, n_units, V, c);
         online_finish<DT>(sD, sm->stash[1][ct], cw, lane, n_units, V, c);
         combine_rows(sm, sT, sD, c, ct);
@@ -789,7 +799,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 if (!(pbar >= 0.f)) {
                     const uint64_t t0 = globaltimer();
                     while (!((pbar = ld_relaxed(f)) >= 0.f)) {
-                        if (globaltimer() - t0 > 2000000000ull) {
+                        if (globaltimer() - t0 > lim) {
                             sm->abort = 1;
                             pbar = 0.f;
                             break;
@@ -889,7 +899,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 cbar_sync();
                 // sweep di is pass di + 1 of the node: backward for even di
                 float tot = sweep<DT>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, sm->aT, sm->rD, xs, cw, lane,
-                                      (di & 1) == 0);
+                                      (di & 1) == 0, lim);
                 tot = warp_sum(tot);
                 if (lane == 0) sm->redf[2][cw] = tot;
                 cbar_sync();
@@ -937,11 +947,11 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 const int np = sm->knp;
                 const bool back = (r & 1) == 0;  // pass r + 1 of the node
                 if (np == 5)
-                    kseq_sweep<DT, 5>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, f, acc, cw, lane, back);
+                    kseq_sweep<DT, 5>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, f, acc, cw, lane, back, lim);
                 else if (np == 3)
-                    kseq_sweep<DT, 3>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, f, acc, cw, lane, back);
+                    kseq_sweep<DT, 3>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, f, acc, cw, lane, back, lim);
                 else
-                    kseq_sweep<DT, 1>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, f, acc, cw, lane, back);
+                    kseq_sweep<DT, 1>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, f, acc, cw, lane, back, lim);
 #pragma unroll
                 for (int k = 0; k < 5; ++k) {
                     const float v = warp_sum(acc[k]);

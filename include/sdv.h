@@ -305,6 +305,24 @@ int sdv_gather_inner_rows(int B, int K, int L, int V, long long row_stride, int 
  * leaf_target_logits the device cannot address. */
 int sdv_verify_leaves_apart(int mode, SDV_VERIFY_ARGS, const void *leaf_target_logits);
 
+/* The verification of `mode` (SDV_MODE_*), as its sdv_verify_* entry, that
+ * also writes, per request, the normalised distribution its correction (or
+ * bonus) token was drawn from: the residual of the end node after the
+ * target adjustment, R_n / S_n (SpecTr-GBV page, section 2, steps 4-5: the
+ * residual distribution of Eq. 4 and Algorithm 2's adjusted target); P_v at
+ * a leaf or where S_n = 0; for K-SEQ, P - gamma min(Q, P / rho) normalised;
+ * for greedy (or T = 0), the one-hot row of the correction token.  An
+ * invalid request (see Errors above) gets a row of zeros.
+ *   residual_out [B][V] fp32, device memory, 4-byte aligned, written in
+ *                full (no other column); row b is each element's mass over
+ *                the total mass the draw used, so it sums to 1 up to fp32
+ *                rounding.
+ * A debug and test output: it costs one more pass over the end node's rows
+ * per request, after the draw.  Returns as the sdv_verify_* calls;
+ * SDV_ERR_INVALID also for a mode out of range or a NULL residual_out with
+ * B > 0. */
+int sdv_verify_residual(int mode, SDV_VERIFY_ARGS, float *residual_out);
+
 /* Fixed scratch of sdv_verify_multidraft_static: 4 MiB of device memory
  * that every GPU loading the library reserves until the process exits. */
 #define SDV_STATIC_SCRATCH_BYTES (4u << 20)
@@ -322,9 +340,10 @@ int sdv_verify_leaves_apart(int mode, SDV_VERIFY_ARGS, const void *leaf_target_l
  *   rejected with SDV_ERR_WORKSPACE before anything is launched (e.g.
  *   B = 256, K = 8, L = 8 needs about 0.5 MiB).
  *   The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current and keeps it; make that
- *   first call before any stream capture.  Nothing is allocated, then or
- *   later.
+ *   (cudaGetSymbolAddress) with that device current and keeps it; the first
+ *   call after the device's context was destroyed and created again (e.g.
+ *   by cudaDeviceReset) looks it up again.  Make those calls before any
+ *   stream capture.  Nothing is allocated, then or later.
  *   Every call on a device shares the one array: two calls whose kernels
  *   overlap on the GPU (different streams without ordering, or different
  *   host threads) race and give wrong results.  Nothing in the array needs

@@ -18,7 +18,8 @@ def lib():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "sdv.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(sdv_\w+)\s*\(", src)))
 
