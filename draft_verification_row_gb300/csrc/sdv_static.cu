@@ -12,6 +12,8 @@
 // per-request status) comes from g_scratch below.
 #include <mutex>
 
+#include <cuda.h>
+
 #include "sdv_internal.h"
 
 namespace {
@@ -23,11 +25,47 @@ static __device__ __align__(256) unsigned char g_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};  // device address of g_scratch, per device
+struct Cached {
+    void* addr;               // device address of g_scratch
+    unsigned long long ctx;   // id of the context it belongs to (0: unknown)
+};
+Cached g_addr[kMaxDevices] = {};  // per device
 
-// Device address of g_scratch on the current device, looked up once per
-// device.  The host-side symbol g_scratch is not a device address; only
-// the pointer cudaGetSymbolAddress returns may be handed to a kernel.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (the device's primary
+// context for runtime callers), or false when there is none yet or the
+// driver lacks the query.  The id changes when the context is destroyed
+// and created again (cudaDeviceReset), and the array's address with it.
+bool context_id(unsigned long long* id)
+{
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static bool looked = false;
+    if (!looked) {  // called with g_mu held
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+        cudaGetLastError();
+        looked = true;
+    }
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_scratch on the current device.  The host-side
+// symbol g_scratch is not a device address; only the pointer
+// cudaGetSymbolAddress returns may be handed to a kernel.  It is looked up
+// once per device and context, with that device current: on the first
+// call, and again on the first call after the context was reset.
 int scratch_address(void** out)
 {
     int dev = -1;
@@ -36,15 +74,20 @@ int scratch_address(void** out)
         return SDV_ERR_CUDA;
     }
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
+    Cached& c = g_addr[dev];
+    unsigned long long id = 0;
+    const bool have_id = context_id(&id);
+    if (!c.addr || (have_id && c.ctx != id)) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
             return SDV_ERR_CUDA;
         }
-        g_addr[dev] = p;
+        c.addr = p;
+        // the lookup made the context current if it was not yet
+        c.ctx = context_id(&id) ? id : 0;
     }
-    *out = g_addr[dev];
+    *out = c.addr;
     return SDV_OK;
 }
 
