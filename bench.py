@@ -134,6 +134,32 @@ def trie_nodes(tokens, lengths, K):
     return inner, leaves
 
 
+def table_rows(lengths, K, greedy=False):
+    """Rows per call as the hot-path size table counts them: per request,
+    the root's target and draft rows once, then each draft's own rows at
+    depths 1..L_b (L_b target rows, L_b - 1 draft rows): 2 + K (2 L_b - 1);
+    target rows only for greedy: 1 + K L_b."""
+    n = 0
+    for Lb in lengths.cpu().numpy().tolist():
+        if greedy:
+            n += 1 + K * Lb
+        else:
+            n += 1 if Lb == 0 else 2 + K * (2 * Lb - 1)
+    return n
+
+
+def row_bytes_of(batch, inner, leaves, greedy=False, ended_at_leaf=0):
+    """Bytes per call of the method's own rows: each distinct trie node's
+    target row (leaves included) and each inner node's draft row.  Greedy
+    matching needs target rows only, every inner node's (its argmax decides
+    the matches) and the leaves its decisions end at (their argmax is the
+    correction)."""
+    row = batch.V * (2 if batch.dtype == "bf16" else 4)
+    if greedy:
+        return (inner + ended_at_leaf) * row
+    return (2 * inner + leaves) * row
+
+
 def measured_bf16_peak():
     """Dense bf16 TFLOP/s: the measured burst figure (a kernel timed on its
     own), else the fallback."""
@@ -255,13 +281,15 @@ def kernel_sha():
 
 
 def recorded_traffic():
-    """DRAM bytes per launch of the node kernel from a committed ncu capture:
-    (bytes while the kernel's sources are unchanged, else None; the last
-    capture's bytes, or None without a record)."""
+    """DRAM bytes of the node kernel per inner trie node, from a committed
+    one-pass ncu capture of a smaller batch of the same workload (the
+    kernel's traffic grows with the nodes it visits): (bytes per node while
+    the kernel's sources are unchanged, else None; the last capture's
+    figure, or None without a record)."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
-        last = float(d["dram_bytes_per_call"])
+        last = float(d["dram_bytes_per_inner_node"])
         return (last if d.get("kernel_source_sha256") == kernel_sha() else None), last
     except (OSError, KeyError, ValueError):
         return None, None
@@ -378,6 +406,182 @@ def config_of(batch, mode, world):
             "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}
 
 
+def numa_placement(t, dev):
+    """Where a pinned host tensor's pages sit (NUMA node -> pages, from
+    /proc/self/numa_maps) and the GPU's NUMA node (sysfs): reading only."""
+    info = {}
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bus = f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        with open(f"/sys/bus/pci/devices/{bus}/numa_node") as f:
+            info["gpu_numa_node"] = int(f.read().strip())
+        info["gpu_pci"] = bus
+    except (AttributeError, OSError, ValueError):
+        info["gpu_numa_node"] = None
+    addr = t.data_ptr()
+    try:
+        with open("/proc/self/numa_maps") as f:
+            for line in f:
+                start = int(line.split()[0], 16)
+                if start <= addr < start + t.numel() * t.element_size():
+                    info["buffer_pages"] = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in line.split()
+                                            if kv.startswith("N") and "=" in kv}
+                    info["policy"] = line.split()[1]
+                    break
+    except (OSError, ValueError):
+        pass
+    info["process_cpus"] = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else None
+    return info
+
+
+def host_link(src, nbytes, dev, stream, reps):
+    """The host link's own rate: one cudaMemcpyAsync of nbytes from pinned
+    host memory (the e2e step's input bytes) to the device, CUDA events on
+    the stream, best of reps; plus where the host buffer sits."""
+    flat = src.view(-1).view(torch.uint8)
+    nbytes = min(int(nbytes), flat.numel())
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = None
+    for _ in range(reps + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            dst.copy_(flat[:nbytes], non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    del dst
+    return {"what": "one pinned host-to-device cudaMemcpyAsync of the e2e step's input bytes", "bytes": nbytes,
+            "ms": best, "gbs": nbytes / (best / 1000.0) / 1e9, "numa": numa_placement(src, dev)}
+
+
+# The other workloads, as extras beside the headline: (workload, T, rule).
+CONFIG_RUNS = [
+    ("token-B4-K1-L4-V1024-f32", 1.0, "token"),
+    ("token-greedy-B64-K1-L5-V32000-bf16", 1.0, "token"),
+    ("token-greedy-B64-K1-L5-V32000-bf16", 0.0, "greedy"),
+    ("block-B128-K1-L5-V128256-bf16", 0.7, "block"),
+    ("multidraft-B32-K4-L4-V32000-f32", 0.1, "multidraft"),
+    ("multidraft-B32-K4-L4-V32000-f32", 0.4, "multidraft"),
+    ("multidraft-B32-K4-L4-V32000-f32", 0.7, "multidraft"),
+    ("multidraft-B32-K4-L4-V32000-f32", 0.7, "token"),
+    ("multidraft-B32-K4-L4-V32000-f32", 0.7, "kseq"),
+]
+# SpecTr-GBV against the rules it is compared with, on the multi-draft
+# workload: (label, rule, drafts used)
+ACCEPT_RULES = [("SpecTr-GBV K=4", "multidraft", 4), ("GBV K=1", "multidraft", 1),
+                ("per-position K=4", "token", 4), ("K-SEQ K=4", "kseq", 4)]
+
+
+def first_drafts(batch, K):
+    """The batch with only its first K drafts (the same rows and tokens)."""
+    import dataclasses
+    if K == batch.K:
+        return batch
+    cut = lambda t: t[:, :K].contiguous()
+    return dataclasses.replace(batch, K=K, target=cut(batch.target), draft=cut(batch.draft),
+                               tokens=cut(batch.tokens), accept_u=cut(batch.accept_u), sample_u=cut(batch.sample_u))
+
+
+def time_flushed(fn, reps, stream, flush, prof=False):
+    """Mean ms of fn between CUDA events on `stream`, L2 flushed (a write
+    larger than L2) before every call and outside the timed pair; with prof,
+    the mean ms between the library's profiling events instead."""
+    import draft_verification_row_gb300 as sdv
+    pairs, rows = [], []
+    for _ in range(reps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if prof:
+            c, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c.record(stream)
+            d.record(stream)
+            sdv.set_profile_events(c, d)
+            rows.append((c, d))
+        a.record(stream)
+        fn()
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    sdv.set_profile_events(None, None)
+    use = rows if prof else pairs
+    return sum(x.elapsed_time(y) for x, y in use) / reps
+
+
+def config_lines(args, dev, stream, peak, rank):
+    """Positions/s, the row kernel's fraction of HBM peak and the oracle
+    timed on the host (one core, the whole batch) for each other workload;
+    and, on the multi-draft workload, SpecTr-GBV's acceptance against the
+    rules it is compared with (E[tau] and BE = E[tau] + 1, means over many
+    independent draws of the uniforms, same drafts)."""
+    import draft_verification_row_gb300 as sdv
+    from draft_verification_row_gb300 import binding, workloads as W
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # twice the L2
+    reps = max(20, args.steps)
+    res = {}
+    for name, T, mode in CONFIG_RUNS:
+        batch = W.make(name, dev, temperature=T)
+        inner, leaves = trie_nodes(batch.tokens, batch.lengths, batch.K)
+        greedy = mode == "greedy" or T == 0.0
+        out = binding.Outputs(mode, batch.B, batch.K, batch.L, batch.V, dev)
+
+        def call():
+            sdv.verify(mode, batch.target, batch.draft, batch.tokens, batch.lengths, batch.accept_u,
+                       batch.sample_u, batch.temperature, V=batch.V, out=out, stream=stream)
+
+        for _ in range(3):
+            call()
+        ms = time_flushed(call, reps, stream, flush)
+        kms = time_flushed(call, reps, stream, flush, prof=True)
+        if int(out.device_status.item()):
+            raise RuntimeError(f"{name} {mode}: device status {int(out.device_status.item())}")
+        nbytes = row_bytes_of(batch, inner, leaves, greedy=greedy,
+                              ended_at_leaf=int((out.accept_len == batch.lengths).sum().item()))
+        gbs = nbytes / (kms / 1000.0) / 1e9
+        entry = {"workload": name, "rule": mode, "temperature": T, "B": batch.B, "K": batch.K, "L": batch.L,
+                 "V": batch.V, "positions": batch.positions, "ms_per_call": ms,
+                 "value": batch.positions / (ms / 1000.0), "unit": UNIT, "row_kernel_ms": kms,
+                 "algorithmic_bytes": nbytes, "achieved_gbs": gbs, "frac": gbs / peak,
+                 "size_table_bytes": table_rows(batch.lengths, batch.K, greedy) * batch.V * (
+                     2 if batch.dtype == "bf16" else 4),
+                 "gpu_launches_per_call": 3, "l2": "flushed before every call"}
+        if rank == 0:
+            p, dt = oracle_sample(batch, "greedy" if greedy else mode, list(range(batch.B)))
+            entry["cpu_baseline"] = {"value": p / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                     "sample": f"all {batch.B} requests ({p} positions, {dt:.2f} s, single thread)"}
+        res[f"{name} T={T} {mode}"] = entry
+        del batch, out
+    # acceptance on the multi-draft workload (GPU path)
+    acc = {}
+    draws = 64
+    for T in (0.1, 0.4, 0.7):
+        batch = W.make("multidraft-B32-K4-L4-V32000-f32", dev, temperature=T)
+        acc[f"T={T}"] = {}
+        for label, mode, K in ACCEPT_RULES:
+            b = first_drafts(batch, K)
+            out = binding.Outputs(mode, b.B, b.K, b.L, b.V, dev)
+            g = torch.Generator(device=dev).manual_seed(11 + K)
+            taus = []
+            for _ in range(draws):
+                au = torch.rand(b.accept_u.shape, generator=g, device=dev)
+                su = torch.rand(b.sample_u.shape, generator=g, device=dev)
+                sdv.verify(mode, b.target, b.draft, b.tokens, b.lengths, au, su, b.temperature, V=b.V, out=out,
+                           stream=stream)
+                taus.append(out.accept_len.clone())
+            t = torch.stack(taus).double()
+            m = float(t.mean())
+            se = float((t.var(dim=0).sum() / b.B ** 2 / draws).sqrt())
+            acc[f"T={T}"][label] = {"E_tau": m, "BE": m + 1.0, "stderr": se, "draws": draws * b.B}
+        del batch
+    res["acceptance multidraft-B32-K4-L4-V32000-f32"] = {
+        "what": "mean accepted length over 64 independent draws of every request's uniforms (same drafts); "
+                "BE = E[tau] + 1", **acc}
+    del flush
+    return res
+
+
 def run_reference(args, world, rank):
     """The oracle on the host cores: each step times a bounded sample."""
     from draft_verification_row_gb300 import workloads as W
@@ -424,11 +628,16 @@ def run_ours(args, world, rank, local):
     esz = 2 if batch.dtype == "bf16" else 4
     inner, leaves = trie_nodes(batch.tokens, batch.lengths, batch.K)
     positions = batch.positions
-    # algorithmic bytes per call: a target and a draft row per draft
-    # position (2 V esz each); the rows the node kernel has to read are
-    # fewer, one pair per distinct inner trie node
-    alg_bytes = 2 * positions * batch.V * esz
-    read_bytes = 2 * inner * batch.V * esz
+    row_b = batch.V * esz
+    # algorithmic bytes per call: the method's own rows, each distinct trie
+    # node's target row (leaves included) and each inner node's draft row;
+    # beside it, the size table's count (per-draft rows, the root once), the
+    # rows the node kernel has to read (a pair per inner node: leaves wait
+    # for the decision), and a row pair per draft position (dense, no trie)
+    trie_bytes = row_bytes_of(batch, inner, leaves)
+    table_bytes = table_rows(batch.lengths, batch.K) * row_b
+    read_bytes = 2 * inner * row_b
+    dense_bytes = 2 * positions * row_b
 
     def make_call(mode, out):
         def call():
@@ -462,32 +671,40 @@ def run_ours(args, world, rank, local):
 
     peak, peak_kind = measured_peaks()
     row_step_s = row_ms / args.steps / 1000.0
-    achieved = alg_bytes / row_step_s / 1e9
-    achieved_read = read_bytes / row_step_s / 1e9
-    traffic, last_traffic = recorded_traffic()
+    gbs = lambda nbytes: nbytes / row_step_s / 1e9
+    per_node, last_per_node = recorded_traffic()
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config_of(batch, args.mode, world),
             "positions_per_step": all_positions,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_kind": f"{peak_kind} hbm_gbs",
-                         "traffic": traffic, "kernel": "stream_kernel",
-                         "algorithmic_bytes_per_step": alg_bytes,
+            "roofline": {"bound": "hbm", "achieved": gbs(trie_bytes), "peak": peak, "unit": "GB/s",
+                         "frac": gbs(trie_bytes) / peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                         "traffic": None if per_node is None else per_node * inner,
+                         "kernel": "stream_kernel",
+                         "algorithmic_bytes_per_step": trie_bytes,
+                         "algorithmic_bytes": "each distinct trie node's target row (leaves included) and each "
+                                              "inner node's draft row",
+                         "trie_rows_per_step": {"target": inner + leaves, "draft": inner},
                          "kernel_ms_per_step": row_ms / args.steps,
+                         "size_table_bytes_per_step": table_bytes,
+                         "size_table_frac": gbs(table_bytes) / peak,
                          "rows_read_bytes_per_step": read_bytes,
-                         "rows_read_achieved": achieved_read,
-                         "rows_read_frac": achieved_read / peak,
-                         "rows_read_per_step": {"target": inner, "draft": inner},
+                         "rows_read_frac": gbs(read_bytes) / peak,
+                         "dense_bytes_per_step": dense_bytes,
+                         "dense_frac": gbs(dense_bytes) / peak,
+                         "dense": "a target and a draft row per draft position, no row shared",
                          "leaves": leaves,
                          "bonus_leaf_rows_per_step": int((out.accept_len == batch.lengths).sum().item())},
             "gpu_launches": launches,
             "clocks": clk}
-    if traffic is None and last_traffic is not None:
+    if per_node is not None:
+        line["roofline"]["traffic_note"] = ("dram__bytes_read.sum + dram__bytes_write.sum of one launch of a "
+                                            "smaller batch of this workload, scaled by inner trie nodes")
+    elif last_per_node is not None:
         # the sources changed since the capture: its figure for reference
-        line["roofline"]["traffic_last_capture"] = {
-            "bytes_per_launch": last_traffic, "sources_changed_since": True,
-            "summary": "profiles/stream_kernel_mixed_B256_dram.md"}
+        line["roofline"]["traffic_last_capture"] = {"bytes_per_inner_node": last_per_node,
+                                                    "sources_changed_since": True}
 
     if not args.no_extras:
         # the other rules on the same batch: token-level (per-position
@@ -503,12 +720,13 @@ def run_ours(args, world, rank, local):
             _, r2 = time_calls(call2, args.steps, stream, prof=True)
             t2 = max_over_ranks(t2, world)
             r2 = max_over_ranks(r2, world)
+            ob = row_bytes_of(batch, inner, leaves, greedy=other == "greedy",
+                              ended_at_leaf=int((out2.accept_len == batch.lengths).sum().item()))
+            og = ob / (r2 / args.steps / 1000.0) / 1e9
             line["modes"][other] = {"value": all_positions / (t2 / args.steps / 1000.0), "unit": UNIT,
                                     "ms_per_step": t2 / args.steps,
-                                    "node_kernel_ms_per_step": r2 / args.steps,
-                                    # greedy reads target rows only: one V esz per position
-                                    "algorithmic_gbs": (alg_bytes // 2 if other == "greedy" else alg_bytes)
-                                    / (r2 / args.steps / 1000.0) / 1e9}
+                                    "row_kernel_ms_per_step": r2 / args.steps,
+                                    "algorithmic_bytes_per_step": ob, "achieved_gbs": og, "frac": og / peak}
             del out2
         # end to end through the C-ABI with host buffers: the host-to-device
         # copy of the inputs (of the logits, the rows verification reads,
@@ -571,13 +789,17 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         ti, _ = time_calls(e2e_inner_step, args.e2e_steps, stream)
         ti = max_over_ranks(ti, world)
-        row_b = batch.stride * esz
+        row_h2d = batch.stride * esz
         ended_at_leaf = int((out.accept_len == batch.lengths).sum().item())  # one leaf row read each
-        h2d_inner = 2 * inner * row_b + ended_at_leaf * row_b + sum(host[n].numel() * host[n].element_size()
-                                                                   for n in small)
-        line["e2e"] = {"value": all_positions / (ti / args.e2e_steps / 1000.0), "unit": UNIT,
+        h2d_inner = 2 * inner * row_h2d + ended_at_leaf * row_h2d + sum(host[n].numel() * host[n].element_size()
+                                                                       for n in small)
+        link = host_link(host["target"], h2d_inner, dev, stream, args.e2e_steps)
+        e2e_ms = ti / args.e2e_steps
+        line["e2e"] = {"value": all_positions / (e2e_ms / 1000.0), "unit": UNIT,
                        "h2d_bytes_per_step": h2d_inner, "d2h_bytes_per_step": d2h,
-                       "ms_per_step": ti / args.e2e_steps,
+                       "ms_per_step": e2e_ms,
+                       "link_frac": (h2d_inner / link["gbs"] / 1e6) / e2e_ms if link.get("gbs") else None,
+                       "link": link,
                        "inputs": "pinned host tensors; of the logits, the inner trie nodes' rows are gathered by "
                                  "the GPU over the host link (sdv_gather_inner_rows) and the leaf rows the "
                                  "decisions end at are read from the host tensor by the call itself "
@@ -646,6 +868,9 @@ def run_ours(args, world, rank, local):
         del emu
         # the next row: greedy verification fused into the target LM head
         line["next_lm_head"] = lm_head_bench(args, dev, stream, rank, world) if args.B is None else None
+        # the other workloads beside the headline
+        if args.B is None:
+            line["configs"] = config_lines(args, dev, stream, peak, rank)
         if rank == 0:
             rng = np.random.default_rng(1)
             req = sorted(rng.choice(batch.B, size=min(args.cpu_requests, batch.B), replace=False).tolist())
