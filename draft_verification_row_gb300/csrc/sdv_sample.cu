@@ -671,7 +671,12 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy, 
     d.rowD = leaf ? nullptr
                   : static_cast<const char*>(pb.draft) + (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
     d.c = pb.c;
-    d.residual = !leaf && pb.ws.S[slot] > 0.f;
+    // the end node's residual mass S_n; below 0 when the node kernel left it
+    // to this pass (the token rule's last sweep): it is then the residual's
+    // total here, and the residual, or P where it has no mass, is drawn from
+    const float Sn = leaf ? 0.f : pb.ws.S[slot];
+    const bool sum_here = !leaf && Sn < 0.f;
+    d.residual = !leaf && (Sn > 0.f || sum_here);
     d.xs = -1;
     d.cT = 0.f;
     if (d.residual) {
@@ -685,7 +690,15 @@ __global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy, 
         d.xs = pb.ws.xs[slot];
         residual_pass<DT>(d, V, sm, lane, w);
         __syncthreads();
-    } else {
+        if (sum_here) {
+            float tot = 0.f;  // summed as the draw sums it (every warp for itself)
+            for (int i = lane; i < n_seg; i += 32) tot += sm.mass[i];
+            tot = fmaxf(warp_sum(tot), 0.f);
+            if (tid == 0 && pb.residual_mass) pb.residual_mass[b] = tot;
+            d.residual = tot > 0.f;
+        }
+    }
+    if (!d.residual) {
         softmax_pass<DT>(d.rowT, V, d.c, greedy != 0, sm, lane, w);
         __syncthreads();
         float M;

@@ -602,6 +602,9 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
     const float c = pb.c;
     const uint64_t lim = pb.wait_ns;
     int* const counter = pb.ws.ncount + 2 * (L + 1);
+    // token rule: a node's last draw needs no sweep here (its S_n enters only
+    // the end node's residual, summed by the decision kernel's draw pass)
+    const bool lazy_last = !KSEQ && pb.mode == SDV_MODE_TOKEN;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -713,7 +716,9 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                              (((size_t)b * K + k) * (L + 1) + j) * (size_t)pb.stride * E::kBytes;
             const char* gD = static_cast<const char*>(pb.draft) +
                              (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
-            const int passes = 1 + (KSEQ ? (nd > 1 ? kKseqRounds : 1) : nd);
+            // the token rule's last sweep of a node only feeds the residual
+            // the walk may end at: the decision kernel takes it then
+            const int passes = 1 + (KSEQ ? (nd > 1 ? kKseqRounds : 1) : nd - (lazy_last ? 1 : 0));
             bool ok = true;
             for (int ps = 0; ps < passes && ok; ++ps) {
                 // keep the rows in L2 until the node's last pass over them
@@ -897,6 +902,12 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                     sm->rD = sm->aT > 0.f ? sm->aD / sm->aT : 3.402823466e38f;
                 }
                 cbar_sync();
+                if (lazy_last && di == nd - 1) {
+                    // no sweep: R_n(x*) is known in closed form, and the
+                    // rest of S_n is summed where it is needed
+                    if (ct == 0) sm->Rs = xs >= 0 ? fmaxf(sm->Rj, 0.f) : 0.f;
+                    break;
+                }
                 // sweep di is pass di + 1 of the node: backward for even di
                 float tot = sweep<DT>(sm, g, timed_out, nc, n_units, V, c, gnegT, gnegD, sm->aT, sm->rD, xs, cw, lane,
                                       (di & 1) == 0, lim);
@@ -921,8 +932,8 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 // should the decision end here, its final residual
                 // R_n = aT max(e_T - (aD / aT) e_D, 0) with R_n(x*) apart
                 const float S = sm->S, D = sm->D;
-                pb.ws.h[slot] = D > 0.f ? S / D : 1.f;
-                pb.ws.S[slot] = S;
+                pb.ws.h[slot] = lazy_last ? 0.f : (D > 0.f ? S / D : 1.f);
+                pb.ws.S[slot] = lazy_last ? -1.f : S;  // (below 0: to be summed by the decision kernel)
                 float* prm = pb.ws.prm + (size_t)slot * 6;
                 prm[0] = gnegT;
                 prm[1] = gnegD;
