@@ -102,6 +102,7 @@ struct StreamSmem {
     uint4 ring[kStages][2][kChunk];  // [stage][target, draft][units]
     uint64_t full[kStages], empty[kStages];
     uint64_t qfull[kQ], qempty[kQ];
+    uint64_t lastdec;                // the consumers' word on a node's last sweep (block rules)
     NodeDesc qd[kQ];
     NodeDesc cur;                    // the consumers' copy of the current node
     float redf[5][kSW];
@@ -114,6 +115,7 @@ struct StreamSmem {
     int uT, uD;
     float S, D, cbar, pbar, Pbs, Qbs, Rs, Ts, Rj, aT, aD, rD;
     int xs, bad;
+    int skip_last, last_go;          // the node's last sweep: skipped here / issued by the copy warp
     // K-SEQ search (consumer thread 0): bracket [klo, khi] of rho, beta at
     // khi, this pass's points and their factors Z_D / (Z_T rho)
     float klo, khi, kbhi, krho[5], kf[5];
@@ -605,6 +607,15 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
     // token rule: a node's last draw needs no sweep here (its S_n enters only
     // the end node's residual, summed by the decision kernel's draw pass)
     const bool lazy_last = !KSEQ && pb.mode == SDV_MODE_TOKEN;
+    // block rules, when the caller does not ask for every node's h (accept_prob):
+    // a node's last sweep gives S_n, which enters only h_v = S_n / D_n, read
+    // when the decision tests v (accepted iff u_v <= h_v), and the residual
+    // of the end node.  The root is never tested, and its residual is summed
+    // by the decision kernel's draw pass; another node is skipped when its
+    // test must fail: S_n <= S_{n-1}, so h_v <= S_{n-1} / D_{n-1} (p for one
+    // draw), and u_v above that bound rejects v whatever S_n is.
+    const bool lazy_block =
+        !KSEQ && (pb.mode == SDV_MODE_BLOCK || pb.mode == SDV_MODE_MULTIDRAFT) && pb.accept_prob == nullptr;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -615,6 +626,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
             mbar_init(&sm->qfull[i], 1);
             mbar_init(&sm->qempty[i], 2);  // read by the copy warp and by the consumers
         }
+        mbar_init(&sm->lastdec, 1);
         mbar_fence_init();
         sm->abort = 0;
     }
@@ -702,6 +714,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
         const uint64_t pol_last = policy_evict_last();
         const uint64_t pol_first = policy_evict_first();
         uint32_t g = 0;
+        uint32_t dec_par = 0;  // parity of the next last-sweep decision
         for (uint32_t it = 0;; ++it) {
             const int q = it % kQ;
             if (!mbar_wait_bounded(&sm->qfull[q], (it / kQ) & 1, lim)) {
@@ -717,10 +730,19 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
             const char* gD = static_cast<const char*>(pb.draft) +
                              (((size_t)b * K + k) * L + j) * (size_t)pb.stride * E::kBytes;
             // the token rule's last sweep of a node only feeds the residual
-            // the walk may end at: the decision kernel takes it then
-            const int passes = 1 + (KSEQ ? (nd > 1 ? kKseqRounds : 1) : nd - (lazy_last ? 1 : 0));
+            // the walk may end at: the decision kernel takes it then; so does
+            // a root's under the block rules; another node's last sweep under
+            // the block rules is issued only if the consumers ask for it
+            const bool root_skip = lazy_block && j == 0;
+            const bool ask_last = lazy_block && j > 0;
+            const int passes = 1 + (KSEQ ? (nd > 1 ? kKseqRounds : 1) : nd - (lazy_last || root_skip ? 1 : 0));
             bool ok = true;
             for (int ps = 0; ps < passes && ok; ++ps) {
+                if (ask_last && ps == passes - 1) {
+                    ok = mbar_wait_bounded(&sm->lastdec, dec_par, lim);
+                    dec_par ^= 1u;
+                    if (!ok || !*static_cast<volatile int*>(&sm->last_go)) break;
+                }
                 // keep the rows in L2 until the node's last pass over them
                 const uint64_t pol = ps == passes - 1 ? pol_first : pol_last;
                 // passes alternate direction (pass 1 forward, the first
@@ -900,9 +922,26 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                     sm->aT = p / sm->zT;
                     sm->aD = (1.f + cnew) / sm->zD;
                     sm->rD = sm->aT > 0.f ? sm->aD / sm->aT : 3.402823466e38f;
+                    if (di == nd - 1) {
+                        bool skip = lazy_last;
+                        if (lazy_block) {
+                            if (j == 0) {
+                                skip = true;  // (the copy warp knows: no word)
+                            } else {
+                                // the bound on h_v from S_{n-1}, D_{n-1} (held since the
+                                // previous sweep; p and 1 before the first)
+                                const float hhi = sm->D > 0.f ? sm->S / sm->D : 1.f;
+                                const float uv = pb.accept_u[((size_t)b * K + k) * L + (j - 1)];
+                                skip = uv > hhi * (1.f + 1e-6f) + 1e-7f;
+                                sm->last_go = !skip;
+                                mbar_arrive(&sm->lastdec);
+                            }
+                        }
+                        sm->skip_last = skip;
+                    }
                 }
                 cbar_sync();
-                if (lazy_last && di == nd - 1) {
+                if (di == nd - 1 && sm->skip_last) {
                     // no sweep: R_n(x*) is known in closed form, and the
                     // rest of S_n is summed where it is needed
                     if (ct == 0) sm->Rs = xs >= 0 ? fmaxf(sm->Rj, 0.f) : 0.f;
@@ -932,8 +971,12 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 // should the decision end here, its final residual
                 // R_n = aT max(e_T - (aD / aT) e_D, 0) with R_n(x*) apart
                 const float S = sm->S, D = sm->D;
-                pb.ws.h[slot] = lazy_last ? 0.f : (D > 0.f ? S / D : 1.f);
-                pb.ws.S[slot] = lazy_last ? -1.f : S;  // (below 0: to be summed by the decision kernel)
+                const bool skipped = nd > 0 && sm->skip_last;
+                // a skipped node's test fails for sure (h below any uniform);
+                // its S_n, below 0, is summed by the decision kernel should the
+                // node end the decision (only a root or a token-rule node can)
+                pb.ws.h[slot] = skipped ? -1.f : (D > 0.f ? S / D : 1.f);
+                pb.ws.S[slot] = skipped ? -1.f : S;
                 float* prm = pb.ws.prm + (size_t)slot * 6;
                 prm[0] = gnegT;
                 prm[1] = gnegD;
