@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--cpu-requests", type=int, default=160,
                     help="requests in the oracle's timed sample (cpu_baseline; about 10 s on one core)")
     ap.add_argument("--ref-requests", type=int, default=4, help="requests per step of --impl reference")
+    ap.add_argument("--sampling-only", action="store_true",
+                    help="only the draft-token sampling measurement (--B sets the batch size)")
     ap.add_argument("--lm-head-only", action="store_true",
                     help="only the LM-head-fused greedy measurement (--B sets its batch size)")
     return ap.parse_args()
@@ -525,7 +527,7 @@ def config_lines(args, dev, stream, peak, rank):
         batch = W.make(name, dev, temperature=T)
         inner, leaves = trie_nodes(batch.tokens, batch.lengths, batch.K)
         greedy = mode == "greedy" or T == 0.0
-        out = binding.Outputs(mode, batch.B, batch.K, batch.L, batch.V, dev)
+        out = binding.Outputs(mode, batch.B, batch.K, batch.L, batch.V, dev, accept_prob=False)
 
         def call():
             sdv.verify(mode, batch.target, batch.draft, batch.tokens, batch.lengths, batch.accept_u,
@@ -561,7 +563,7 @@ def config_lines(args, dev, stream, peak, rank):
         acc[f"T={T}"] = {}
         for label, mode, K in ACCEPT_RULES:
             b = first_drafts(batch, K)
-            out = binding.Outputs(mode, b.B, b.K, b.L, b.V, dev)
+            out = binding.Outputs(mode, b.B, b.K, b.L, b.V, dev, accept_prob=False)
             g = torch.Generator(device=dev).manual_seed(11 + K)
             taus = []
             for _ in range(draws):
@@ -580,6 +582,35 @@ def config_lines(args, dev, stream, peak, rank):
                 "BE = E[tau] + 1", **acc}
     del flush
     return res
+
+
+def sampling_bench(args, batch, dev, stream, world, peak, peak_kind):
+    """Draft-token sampling (sdv_sample_rows): one draw per draft from each
+    request's depth-0 draft rows (B*K rows of V logits)."""
+    import draft_verification_row_gb300 as sdv
+    esz = 2 if batch.dtype == "bf16" else 4
+    rows = batch.draft[:, :, 0, :].reshape(batch.B * batch.K, batch.stride).contiguous()
+    n_rows = rows.shape[0]
+    su = torch.rand((n_rows, 1), device=dev, generator=torch.Generator(device=dev).manual_seed(17))
+    toks = torch.empty((n_rows, 1), dtype=torch.int32, device=dev)
+    dst = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def sample_call():
+        sdv.sample_rows(rows, 1, su, batch.temperature, V=batch.V, tokens=toks, device_status=dst, stream=stream)
+
+    for _ in range(args.warmup):
+        sample_call()
+    ts, _ = time_calls(sample_call, args.steps, stream)
+    ts = max_over_ranks(ts, world)
+    ms_s = ts / args.steps
+    s_bytes = n_rows * batch.V * esz
+    s_gbs = s_bytes / (ms_s / 1000.0) / 1e9
+    return {"metric": "sampled draft tokens/s", "value": sum_over_ranks(n_rows, world) / (ms_s / 1000.0),
+            "unit": "tokens/s", "ms_per_call": ms_s, "rows": n_rows, "draws_per_row": 1, "V": batch.V,
+            "gpu_launches_per_call": 1,
+            "roofline": {"bound": "hbm", "achieved": s_gbs, "peak": peak, "unit": "GB/s", "frac": s_gbs / peak,
+                         "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_call": s_bytes,
+                         "kernel": "sample_rows_kernel"}}
 
 
 def run_reference(args, world, rank):
@@ -625,6 +656,12 @@ def run_ours(args, world, rank, local):
     batch = W.make(name, dev, seed=seed, B=args.B)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
+    if args.sampling_only:
+        peak, peak_kind = measured_peaks()
+        r = sampling_bench(args, batch, dev, stream, world, peak, peak_kind)
+        if rank == 0:
+            print(json.dumps(r), flush=True)
+        return
     esz = 2 if batch.dtype == "bf16" else 4
     inner, leaves = trie_nodes(batch.tokens, batch.lengths, batch.K)
     positions = batch.positions
@@ -645,7 +682,10 @@ def run_ours(args, world, rank, local):
                        batch.sample_u, batch.temperature, V=batch.V, out=out, stream=stream)
         return call
 
-    out = binding.Outputs(args.mode, batch.B, batch.K, batch.L, batch.V, dev)
+    # the outputs the method defines (tau, k*, the token) and the residual's
+    # mass; accept_prob, every node's threshold, is a diagnostic a caller asks
+    # for apart (timed below as modes["<mode> with accept_prob"])
+    out = binding.Outputs(args.mode, batch.B, batch.K, batch.L, batch.V, dev, accept_prob=False)
     call = make_call(args.mode, out)
     for _ in range(args.warmup):
         call()
@@ -677,6 +717,7 @@ def run_ours(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config_of(batch, args.mode, world),
+            "outputs": "accept_len, accept_draft, out_token, residual_mass per request (accept_prob not requested)",
             "positions_per_step": all_positions,
             "roofline": {"bound": "hbm", "achieved": gbs(trie_bytes), "peak": peak, "unit": "GB/s",
                          "frac": gbs(trie_bytes) / peak, "peak_kind": f"{peak_kind} hbm_gbs",
@@ -711,8 +752,10 @@ def run_ours(args, world, rank, local):
         # recursive rejection sampling) and SpecTr's K-SEQ, whose search
         # for rho SpecTr-GBV avoids (the pages' "verification overhead")
         line["modes"] = {}
-        for other in [m for m in ("multidraft", "token", "kseq", "greedy") if m != args.mode]:
-            out2 = binding.Outputs(other, batch.B, batch.K, batch.L, batch.V, dev)
+        runs = [(m, False) for m in ("multidraft", "token", "kseq", "greedy") if m != args.mode]
+        runs.append((args.mode, True))
+        for other, with_ap in runs:
+            out2 = binding.Outputs(other, batch.B, batch.K, batch.L, batch.V, dev, accept_prob=with_ap)
             call2 = make_call(other, out2)
             for _ in range(max(2, args.warmup // 2)):
                 call2()
@@ -723,7 +766,8 @@ def run_ours(args, world, rank, local):
             ob = row_bytes_of(batch, inner, leaves, greedy=other == "greedy",
                               ended_at_leaf=int((out2.accept_len == batch.lengths).sum().item()))
             og = ob / (r2 / args.steps / 1000.0) / 1e9
-            line["modes"][other] = {"value": all_positions / (t2 / args.steps / 1000.0), "unit": UNIT,
+            line["modes"][other + (" with accept_prob" if with_ap else "")] = {
+                                    "value": all_positions / (t2 / args.steps / 1000.0), "unit": UNIT,
                                     "ms_per_step": t2 / args.steps,
                                     "row_kernel_ms_per_step": r2 / args.steps,
                                     "algorithmic_bytes_per_step": ob, "achieved_gbs": og, "frac": og / peak}
@@ -829,33 +873,8 @@ def run_ours(args, world, rank, local):
                                      "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
                                      "ms_per_step": tf / args.e2e_steps}
         del host
-        # the next row of the path: draft-token sampling, one draw per draft
-        # from each request's depth-0 draft rows (B*K rows of V logits)
-        rows = batch.draft[:, :, 0, :].reshape(batch.B * batch.K, batch.stride).contiguous()
-        n_rows = rows.shape[0]
-        su = torch.rand((n_rows, 1), device=dev, generator=torch.Generator(device=dev).manual_seed(17))
-        toks = torch.empty((n_rows, 1), dtype=torch.int32, device=dev)
-        dst = torch.empty(1, dtype=torch.int32, device=dev)
-
-        def sample_call():
-            sdv.sample_rows(rows, 1, su, batch.temperature, V=batch.V, tokens=toks, device_status=dst,
-                            stream=stream)
-
-        for _ in range(args.warmup):
-            sample_call()
-        ts, _ = time_calls(sample_call, args.steps, stream)
-        ts = max_over_ranks(ts, world)
-        ms_s = ts / args.steps
-        s_bytes = n_rows * batch.V * esz
-        s_gbs = s_bytes / (ms_s / 1000.0) / 1e9
-        line["next_draft_sampling"] = {
-            "metric": "sampled draft tokens/s", "value": sum_over_ranks(n_rows, world) / (ms_s / 1000.0),
-            "unit": "tokens/s", "ms_per_call": ms_s, "rows": n_rows, "draws_per_row": 1, "V": batch.V,
-            "gpu_launches_per_call": 1,
-            "roofline": {"bound": "hbm", "achieved": s_gbs, "peak": peak, "unit": "GB/s", "frac": s_gbs / peak,
-                         "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_call": s_bytes,
-                         "kernel": "sample_rows_kernel"}}
-        del rows
+        # the next row of the path: draft-token sampling
+        line["next_draft_sampling"] = sampling_bench(args, batch, dev, stream, world, peak, peak_kind)
         # one-GPU PSD emulation: the batch's two halves alternate drafting
         # (L sampling launches) and verification on two streams
         from draft_verification_row_gb300 import psd
