@@ -135,9 +135,9 @@ def test_invalid_requests_are_isolated():
     batch.lengths[4] = 4                              # length > L
     batch.target[5, 0, 0, :] = float("-inf")          # no finite value
     for mode in MODES_K:
-        gpu = P.gpu_run(mode, batch)
         ref = P.oracle_run(mode, batch)
-        P.compare(gpu, ref, f"invalid/{mode}")
+        _compare_both(mode, batch, ref, f"invalid/{mode}")
+        gpu = P.gpu_run(mode, batch)
         st = ref["req_status"]
         assert st[0] == 0 and st[3] == 2 and st[4] == 1
         assert st[1] == 4 and st[5] == 4
@@ -167,7 +167,7 @@ def test_leaf_rows_are_read_only_by_the_bonus_draw(name, K):
     for mode in modes:
         gpu = P.gpu_run(mode, batch)
         ref = P.oracle_run(mode, batch)
-        P.compare(gpu, ref, f"leaves/{mode}")
+        _compare_both(mode, batch, ref, f"leaves/{mode}")
         st, c = ref["req_status"], clean[mode]
         assert (c["req_status"] == 0).all()
         if mode == "greedy":
@@ -203,11 +203,27 @@ def test_leaf_rows_are_read_only_by_the_bonus_draw(name, K):
 
 def test_deterministic():
     batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=8, V=30011)
-    for mode in ("token", "multidraft"):
-        a, b = P.gpu_run(mode, batch), P.gpu_run(mode, batch)
+    for mode, kw in (("token", {}), ("multidraft", {}), ("multidraft", dict(accept_prob=False))):
+        a, b = P.gpu_run(mode, batch, **kw), P.gpu_run(mode, batch, **kw)
         for key in a:
             if a[key] is not None:
                 np.testing.assert_array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("name,kw,T", SMALL[3:])
+def test_skipping_last_sweeps_keeps_every_output(name, kw, T):
+    """Without accept_prob the block rules skip the last sweep of nodes whose
+    test must fail and of the root: every other output is bit for bit the
+    one of the call with accept_prob, except residual_mass where the end
+    node is the root (summed in another order by the draw pass)."""
+    batch = W.make(name, DEV, temperature=T, **kw)
+    for mode in ("block", "multidraft") if batch.K == 1 else ("multidraft",):
+        full, lazy = P.gpu_run(mode, batch), P.gpu_run(mode, batch, accept_prob=False)
+        for key in ("accept_len", "accept_draft", "out_token", "device_status"):
+            np.testing.assert_array_equal(full[key], lazy[key], err_msg=key)
+        at_root = full["accept_len"] == 0
+        np.testing.assert_array_equal(full["residual_mass"][~at_root], lazy["residual_mass"][~at_root])
+        np.testing.assert_allclose(full["residual_mass"][at_root], lazy["residual_mass"][at_root], atol=1e-6, rtol=0)
 
 
 # The node kernel streams rows in chunks of 1024 16-byte units (8192 bf16 or
