@@ -221,6 +221,24 @@ __device__ __forceinline__ float unit_sum(const uint4& u, int x0, int V, float c
     return tree_sum2(v);
 }
 
+// The same over a whole unit (every element below V: any chunk but the
+// last), without the masking test.
+template <int DT>
+__device__ __forceinline__ float unit_sum_full(const uint4& u, float c, float neg)
+{
+    constexpr int EPU = Elem<DT>::kPerUnit;
+    float v[EPU];
+    Elem<DT>::unpack(u, v);
+    const float2 c2 = make_float2(c, c), n2 = make_float2(neg, neg);
+#pragma unroll
+    for (int e = 0; e < EPU; e += 2) {
+        const float2 x = ffma2(make_float2(v[e], v[e + 1]), c2, n2);
+        v[e] = ex2(x.x);
+        v[e + 1] = ex2(x.y);
+    }
+    return tree_sum2(v);
+}
+
 // Unit index of (chunk, warp, sub-unit, lane): a warp's units of a chunk
 // are contiguous, consecutive lanes on consecutive units.
 __device__ __forceinline__ int unit_local(int cw, int i, int lane) { return cw * kWU + i * 32 + lane; }
@@ -302,14 +320,25 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
         if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim)) timed_out = true;
         const bool tail = ch == nc - 1;
         const int ug0 = ch * kChunk + unit_local(cw, 0, lane);
+        // (only the last chunk has units past V, or none: the others take no
+        // test per unit; this loop and the sums below are the hot path)
         uint4 t[kUPT], d[kUPT];
+        if (!tail) {
 #pragma unroll
-        for (int i = 0; i < kUPT; ++i) {
-            const int ul = unit_local(cw, i, lane);
-            t[i] = d[i] = make_uint4(0u, 0u, 0u, 0u);
-            if (!tail || ug0 + i * 32 < n_units) {
+            for (int i = 0; i < kUPT; ++i) {
+                const int ul = unit_local(cw, i, lane);
                 t[i] = sm->ring[s][0][ul];
                 d[i] = sm->ring[s][1][ul];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kUPT; ++i) {
+                const int ul = unit_local(cw, i, lane);
+                t[i] = d[i] = make_uint4(0u, 0u, 0u, 0u);
+                if (ug0 + i * 32 < n_units) {
+                    t[i] = sm->ring[s][0][ul];
+                    d[i] = sm->ring[s][1][ul];
+                }
             }
         }
         __syncwarp();
@@ -324,12 +353,20 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
         // (a row with nothing finite yet sums against 0: never added)
         const float negT = liveT ? sT.neg : 0.f, negD = liveD ? sD.neg : 0.f;
         float zt = 0.f, zd = 0.f;
+        if (!tail) {
 #pragma unroll
-        for (int i = 0; i < kUPT; ++i) {
-            const int ug = ug0 + i * 32;
-            if (!tail || ug < n_units) {
-                zt += unit_sum<DT>(t[i], ug * EPU, V, c, negT);
-                zd += unit_sum<DT>(d[i], ug * EPU, V, c, negD);
+            for (int i = 0; i < kUPT; ++i) {
+                zt += unit_sum_full<DT>(t[i], c, negT);
+                zd += unit_sum_full<DT>(d[i], c, negD);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kUPT; ++i) {
+                const int ug = ug0 + i * 32;
+                if (ug < n_units) {
+                    zt += unit_sum<DT>(t[i], ug * EPU, V, c, negT);
+                    zd += unit_sum<DT>(d[i], ug * EPU, V, c, negD);
+                }
             }
         }
         // a sum of 1/2 or more (or NaN) may hold the maximum
@@ -389,6 +426,27 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
         if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim)) timed_out = true;
         const bool tail = ch == nc - 1;
         float w = 0.f;
+        if (!tail && ch != xs_ch) {
+            // the hot path: whole units, no x* (no test per unit or element)
+            const float2 c2 = make_float2(c, c), nT = make_float2(gnegT, gnegT), nD = make_float2(gnegD, gnegD);
+            const float2 mr = make_float2(-r, -r);
+#pragma unroll
+            for (int i = 0; i < kUPT; ++i) {
+                const int ul = unit_local(cw, i, lane);
+                float t[EPU], d[EPU];
+                Elem<DT>::unpack(sm->ring[s][0][ul], t);
+                Elem<DT>::unpack(sm->ring[s][1][ul], d);
+#pragma unroll
+                for (int e = 0; e < EPU; e += 2) {
+                    const float2 xt = ffma2(make_float2(t[e], t[e + 1]), c2, nT);
+                    const float2 xd = ffma2(make_float2(d[e], d[e + 1]), c2, nD);
+                    const float2 v = ffma2(mr, make_float2(ex2(xd.x), ex2(xd.y)), make_float2(ex2(xt.x), ex2(xt.y)));
+                    d[e] = fmaxf(v.x, 0.f);
+                    d[e + 1] = fmaxf(v.y, 0.f);
+                }
+                w += tree_sum2(d);
+            }
+        } else
 #pragma unroll
         for (int i = 0; i < kUPT; ++i) {
             const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
@@ -449,8 +507,13 @@ __device__ __forceinline__ void kseq_sweep(StreamSmem* sm, uint32_t& g, bool& ti
             const int ul = unit_local(cw, i, lane), ug = ch * kChunk + ul;
             if (!tail || ug < n_units) {
                 float t[EPU], d[EPU];
-                unpack_masked<DT>(sm->ring[s][0][ul], ug * EPU, V, t);
-                unpack_masked<DT>(sm->ring[s][1][ul], ug * EPU, V, d);
+                if (tail) {
+                    unpack_masked<DT>(sm->ring[s][0][ul], ug * EPU, V, t);
+                    unpack_masked<DT>(sm->ring[s][1][ul], ug * EPU, V, d);
+                } else {  // (whole units: no masking test)
+                    Elem<DT>::unpack(sm->ring[s][0][ul], t);
+                    Elem<DT>::unpack(sm->ring[s][1][ul], d);
+                }
                 float2 u[NP];
 #pragma unroll
                 for (int k = 0; k < NP; ++k) u[k] = make_float2(0.f, 0.f);
