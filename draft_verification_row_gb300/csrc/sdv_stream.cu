@@ -16,7 +16,8 @@
 // built and fills a descriptor queue: draws, their tokens and logits.
 // Warp 1 (copy) streams each node's rows in 12 KB-per-row chunks through a
 // 3-stage ring with 1-D TMA bulk copies (mbarrier full/empty handshake),
-// marked evict_last in L2 until the node's last pass, which is evict_first.
+// marked evict_last in L2 until the node's last pass, which is evict_first
+// (so is the pass before a last sweep that may not be asked for).
 // Warps 2..13 consume: a warp owns 64 contiguous 16-byte units of each
 // chunk.  A node's weight p comes from its parent's write of it (a value
 // below 0 means not yet written); waiting happens only before pass 2.  Every wait is
@@ -771,7 +772,8 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
 
     // ---------------------------------------------------------------- copy warp
     // Streams each node's rows: pass 1, then one pass per draw; evict_last
-    // until the last pass, which is evict_first.
+    // until the last pass, which is evict_first (as is the one before a
+    // last sweep that waits for the consumers' word).
     if (tid < 64) {
         if (tid != 32) return;
         const uint64_t pol_last = policy_evict_last();
@@ -806,8 +808,13 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                     dec_par ^= 1u;
                     if (!ok || !*static_cast<volatile int*>(&sm->last_go)) break;
                 }
-                // keep the rows in L2 until the node's last pass over them
-                const uint64_t pol = ps == passes - 1 ? pol_first : pol_last;
+                // keep the rows in L2 until the node's last pass over them;
+                // where that last pass is a sweep the consumers may not ask
+                // for (most are not asked for), the pass before it is
+                // already evict_first: L2 space is kept for the rows that
+                // are surely read again
+                const bool final_pass = ps == passes - 1 || (ask_last && ps == passes - 2);
+                const uint64_t pol = final_pass ? pol_first : pol_last;
                 // passes alternate direction (pass 1 forward, the first
                 // sweep backward, ...): each pass starts on the chunks the
                 // one before just brought into L2
