@@ -68,6 +68,8 @@ def parse():
                     help="only the draft-token sampling measurement (--B sets the batch size)")
     ap.add_argument("--lm-head-only", action="store_true",
                     help="only the LM-head-fused greedy measurement (--B sets its batch size)")
+    ap.add_argument("--lm-head-parts", default="fused,cublas,unfused,trie",
+                    help="parts of the LM-head measurement to run (profiling runs time one part alone)")
     return ap.parse_args()
 
 
@@ -188,81 +190,86 @@ def lm_head_bench(args, dev, stream, rank, world):
     def fused():
         sdv.verify_greedy_lm_head(lb.hidden, lb.lm_head, lb.tokens, lb.lengths, out=out, stream=stream)
 
-    for _ in range(args.warmup):
-        fused()
-    total, gemm = time_calls(fused, args.steps, stream, prof=True)
-    total, gemm = max_over_ranks(total, world), max_over_ranks(gemm, world)
-    if int(out.device_status.item()):
-        raise RuntimeError(f"fused LM head: device status {int(out.device_status.item())}")
-    ms, gemm_ms = total / args.steps, gemm / args.steps
+    parts = set(getattr(args, "lm_head_parts", "fused,cublas,unfused,trie").split(","))
     flops = 2.0 * rows * lb.V * lb.d
-    # the leaf pass: one row per request whose decision ends at a leaf
-    ended_at_leaf = int((out.accept_len == lb.lengths).sum().item())
-    tflops = flops / (gemm_ms / 1000.0) / 1e12
-    peak, kind = measured_bf16_peak()
-    # cuBLAS on the same GEMM shape (rows x V x d, bf16 logits written)
-    a = torch.randn((rows, lb.d), device=dev).to(torch.bfloat16)
-    c = torch.empty((rows, lb.V), dtype=torch.bfloat16, device=dev)
-
-    def cublas():
-        with torch.cuda.stream(stream):
-            torch.mm(a, lb.lm_head.t(), out=c)
-
-    for _ in range(args.warmup):
-        cublas()
-    t_cb, _ = time_calls(cublas, args.steps, stream)
-    del a, c
-    # unfused: logits of every row [B][K][L+1][V] to HBM, then greedy verification
-    logits = torch.empty((lb.B, lb.K, lb.L + 1, lb.V), dtype=torch.bfloat16, device=dev)
-    vout = binding.Outputs("greedy", lb.B, lb.K, lb.L, lb.V, dev)
-
-    def unfused():
-        with torch.cuda.stream(stream):
-            torch.mm(lb.hidden.view(-1, lb.d), lb.lm_head.t(), out=logits.view(-1, lb.V))
-        sdv.verify("greedy", logits, None, lb.tokens, lb.lengths, None, None, 0.0, V=lb.V, out=vout, stream=stream)
-
-    for _ in range(args.warmup):
-        unfused()
-    t_un, _ = time_calls(unfused, args.steps, stream)
-    del logits
-    # for the sampling rules: every trie node's row (leaves included) written
-    # once in bf16 into the verification layout
-    tgt = torch.empty((lb.B, lb.K, lb.L + 1, (lb.V + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(max(binding.lm_head_workspace_bytes(lb.B, lb.K, lb.L, lb.V, lb.d), 256), dtype=torch.uint8,
-                     device=dev)
-    tst = torch.empty(1, dtype=torch.int32, device=dev)
-
-    def trie():
-        sdv.lm_head_trie_logits(lb.hidden, lb.lm_head, lb.tokens, lb.lengths, target=tgt, workspace=ws,
-                                device_status=tst, stream=stream)
-
-    for _ in range(args.warmup):
-        trie()
-    t_tr, g_tr = time_calls(trie, args.steps, stream, prof=True)
-    del tgt, ws
-    trie_flops = 2.0 * (inner + leaves) * lb.V * lb.d
     positions = sum_over_ranks(lb.positions, world)
-    return {
-        "what": "greedy verification fused into the target LM head: logits = hidden . W^T on tcgen05, each "
-                "inner trie node's row reduced to its argmax in the epilogue (logits never stored); after the "
-                "decision, a second pass over the leaves the decisions end at",
-        "workload": W.LM_HEAD_HEADLINE, "rows": rows, "leaf_rows": ended_at_leaf, "leaves_in_trie": leaves,
-        "V": lb.V, "d": lb.d,
-        "metric": "verified draft positions/s", "value": positions / (ms / 1000.0), "unit": "positions/s",
-        "ms_per_call": ms, "lm_head_kernel_ms": gemm_ms, "gpu_launches_per_call": 8,
-        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops / peak, "peak_kind": f"{kind} bf16_tflops (burst)",
-                     "algorithmic_flops_per_call": flops, "kernel": "lm_head_kernel<ARGMAX>"},
-        "cublas_same_gemm": {"ms": t_cb / args.steps, "tflops": flops / (t_cb / args.steps / 1000.0) / 1e12},
-        "unfused_cublas_all_rows_then_greedy": {
-            "ms": t_un / args.steps, "rows": lb.B * lb.K * (lb.L + 1),
-            "value": positions / (t_un / args.steps / 1000.0)},
-        "trie_logits_for_sampling_rules": {
+    r = {"what": "greedy verification fused into the target LM head: logits = hidden . W^T on tcgen05, each "
+                 "inner trie node's row reduced to its argmax in the epilogue (logits never stored); after the "
+                 "decision, a second pass over the leaves the decisions end at",
+         "workload": W.LM_HEAD_HEADLINE, "rows": rows, "leaves_in_trie": leaves, "V": lb.V, "d": lb.d}
+    if "fused" in parts:
+        for _ in range(args.warmup):
+            fused()
+        total, gemm = time_calls(fused, args.steps, stream, prof=True)
+        total, gemm = max_over_ranks(total, world), max_over_ranks(gemm, world)
+        if int(out.device_status.item()):
+            raise RuntimeError(f"fused LM head: device status {int(out.device_status.item())}")
+        ms, gemm_ms = total / args.steps, gemm / args.steps
+        # the leaf pass: one row per request whose decision ends at a leaf
+        ended_at_leaf = int((out.accept_len == lb.lengths).sum().item())
+        tflops = flops / (gemm_ms / 1000.0) / 1e12
+        peak, kind = measured_bf16_peak()
+        r.update({
+            "leaf_rows": ended_at_leaf,
+            "metric": "verified draft positions/s", "value": positions / (ms / 1000.0), "unit": "positions/s",
+            "ms_per_call": ms, "lm_head_kernel_ms": gemm_ms, "gpu_launches_per_call": 8,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "peak_kind": f"{kind} bf16_tflops (burst)",
+                         "algorithmic_flops_per_call": flops, "kernel": "lm_head_pair_kernel<ARGMAX>"}})
+    if "cublas" in parts:
+        # cuBLAS on the same GEMM shape (rows x V x d, bf16 logits written)
+        a = torch.randn((rows, lb.d), device=dev).to(torch.bfloat16)
+        c = torch.empty((rows, lb.V), dtype=torch.bfloat16, device=dev)
+
+        def cublas():
+            with torch.cuda.stream(stream):
+                torch.mm(a, lb.lm_head.t(), out=c)
+
+        for _ in range(args.warmup):
+            cublas()
+        t_cb, _ = time_calls(cublas, args.steps, stream)
+        del a, c
+        r["cublas_same_gemm"] = {"ms": t_cb / args.steps, "tflops": flops / (t_cb / args.steps / 1000.0) / 1e12}
+    if "unfused" in parts:
+        # unfused: logits of every row [B][K][L+1][V] to HBM, then greedy verification
+        logits = torch.empty((lb.B, lb.K, lb.L + 1, lb.V), dtype=torch.bfloat16, device=dev)
+        vout = binding.Outputs("greedy", lb.B, lb.K, lb.L, lb.V, dev)
+
+        def unfused():
+            with torch.cuda.stream(stream):
+                torch.mm(lb.hidden.view(-1, lb.d), lb.lm_head.t(), out=logits.view(-1, lb.V))
+            sdv.verify("greedy", logits, None, lb.tokens, lb.lengths, None, None, 0.0, V=lb.V, out=vout,
+                       stream=stream)
+
+        for _ in range(args.warmup):
+            unfused()
+        t_un, _ = time_calls(unfused, args.steps, stream)
+        del logits
+        r["unfused_cublas_all_rows_then_greedy"] = {
+            "ms": t_un / args.steps, "rows": lb.B * lb.K * (lb.L + 1), "value": positions / (t_un / args.steps / 1000.0)}
+    if "trie" in parts:
+        # for the sampling rules: every trie node's row (leaves included)
+        # written once in bf16 into the verification layout
+        tgt = torch.empty((lb.B, lb.K, lb.L + 1, (lb.V + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(max(binding.lm_head_workspace_bytes(lb.B, lb.K, lb.L, lb.V, lb.d), 256), dtype=torch.uint8,
+                         device=dev)
+        tst = torch.empty(1, dtype=torch.int32, device=dev)
+
+        def trie():
+            sdv.lm_head_trie_logits(lb.hidden, lb.lm_head, lb.tokens, lb.lengths, target=tgt, workspace=ws,
+                                    device_status=tst, stream=stream)
+
+        for _ in range(args.warmup):
+            trie()
+        t_tr, g_tr = time_calls(trie, args.steps, stream, prof=True)
+        del tgt, ws
+        trie_flops = 2.0 * (inner + leaves) * lb.V * lb.d
+        r["trie_logits_for_sampling_rules"] = {
             "what": "sdv_lm_head_trie_logits: each trie node's row, leaves included, computed once and written "
                     "in bf16 into the verification layout",
             "ms": t_tr / args.steps, "rows": inner + leaves, "lm_head_kernel_ms": g_tr / args.steps,
-            "tflops": trie_flops / (g_tr / args.steps / 1000.0) / 1e12},
-    }
+            "tflops": trie_flops / (g_tr / args.steps / 1000.0) / 1e12}
+    return r
 
 
 def measured_peaks():

@@ -30,7 +30,7 @@ EXPORTS = list(_ENTRY.values()) + ["sdv_workspace_bytes", "sdv_status_string", "
                                    "sdv_lm_head_workspace_bytes", "sdv_lm_head_logits", "sdv_gather_inner_rows",
                                    "sdv_verify_leaves_apart", "sdv_lm_head_trie_logits", "sdv_verify_residual",
                                    "sdv_verify_multidraft_static", "sdv_testing_set_wait_limit",
-                                   "sdv_testing_verify_without_roots"]
+                                   "sdv_testing_verify_without_roots", "sdv_testing_set_lm_head_single_cta"]
 
 
 class SDVError(RuntimeError):
@@ -91,6 +91,8 @@ def lib(path: str = LIB_PATH):
     h.sdv_verify_residual.argtypes = [ctypes.c_int] + _VERIFY_ARGTYPES + [ctypes.c_void_p]
     h.sdv_testing_set_wait_limit.restype = ctypes.c_int
     h.sdv_testing_set_wait_limit.argtypes = [ctypes.c_ulonglong]
+    h.sdv_testing_set_lm_head_single_cta.restype = ctypes.c_int
+    h.sdv_testing_set_lm_head_single_cta.argtypes = [ctypes.c_int]
     h.sdv_testing_verify_without_roots.restype = ctypes.c_int
     h.sdv_testing_verify_without_roots.argtypes = [ctypes.c_int] + _VERIFY_ARGTYPES
     h.sdv_read_rows_bytes.restype = ctypes.c_int

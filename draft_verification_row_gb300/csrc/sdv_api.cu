@@ -387,6 +387,12 @@ int sdv_testing_set_wait_limit(unsigned long long wait_ns)
     return SDV_OK;
 }
 
+int sdv_testing_set_lm_head_single_cta(int on)
+{
+    sdv::g_lm_single_cta = on ? 1 : 0;
+    return SDV_OK;
+}
+
 int sdv_testing_verify_without_roots(int mode, SDV_VERIFY_ARGS)
 {
     if (mode != SDV_MODE_BLOCK && mode != SDV_MODE_MULTIDRAFT) return SDV_ERR_INVALID;

@@ -119,6 +119,9 @@ struct LmArgs {
 cudaError_t launch_lm_head(const void* hidden, long long hidden_rows, const void* lm_head, const LmArgs& a,
                            int epi, cudaStream_t st);
 size_t lm_head_smem_bytes();
+// 1: the LM head runs as one CTA per tile even where CTA pairs fit (a test
+// hook: the pair form is the default, the one-CTA form its fallback).
+extern int g_lm_single_cta;
 
 // Greedy verification fused into the LM head: the trie nodes' hidden rows,
 // gathered into the A operand, and their argmax keys.

@@ -23,6 +23,15 @@ extern "C" {
  * SDV_OK. */
 int sdv_testing_set_wait_limit(unsigned long long wait_ns);
 
+/* The LM-head kernels (sdv_verify_greedy_lm_head, sdv_lm_head_logits,
+ * sdv_lm_head_trie_logits) run as CTA pairs (tcgen05 cta_group::2, 256-row
+ * tiles over two SMs) wherever a cluster of two CTAs fits, and as one CTA
+ * per 128-row tile otherwise.  on = 1 makes every later launch in the
+ * process take the one-CTA form, so that tests cover it on a device where
+ * pairs fit; on = 0 restores the default.  Not thread-safe against
+ * concurrent launches.  Returns SDV_OK. */
+int sdv_testing_set_lm_head_single_cta(int on);
+
 /* sdv_verify_block or sdv_verify_multidraft (mode SDV_MODE_BLOCK or
  * SDV_MODE_MULTIDRAFT; arguments as there) with the trie roots taken out of
  * the node kernel's work list.  Every node below a root then waits for a

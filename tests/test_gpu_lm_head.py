@@ -34,6 +34,18 @@ def _built():
     __graft_entry__.build()
 
 
+@pytest.fixture(autouse=True, params=["cta_pair", "one_cta"])
+def lm_form(request):
+    """Every test runs on both forms of the LM-head kernel: CTA pairs
+    (tcgen05 cta_group::2, the default where a cluster of two CTAs fits) and
+    one CTA per tile (the fallback), chosen through the library's test hook."""
+    from draft_verification_row_gb300 import binding
+    h = binding.lib()
+    assert h.sdv_testing_set_lm_head_single_cta(1 if request.param == "one_cta" else 0) == 0
+    yield request.param
+    h.sdv_testing_set_lm_head_single_cta(0)
+
+
 def _err_bound(hidden, lm_head):
     """Per-logit error allowance d * 2^-22 * sum_i |h_i w_i| (numpy, float64)."""
     h = np.abs(hidden.to(torch.float64).numpy())
