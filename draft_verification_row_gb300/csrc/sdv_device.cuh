@@ -115,10 +115,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase)
     return ok != 0;
 }
 
-// Waits for phase `phase` of the barrier for at most limit_ns.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, uint64_t limit_ns = kWaitNs)
+// Waits for phase `phase` of the barrier for at most limit_ns; once a wait
+// of the caller has run out (gave_up), only one try is made.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase, uint64_t limit_ns = kWaitNs,
+                                                  bool gave_up = false)
 {
     if (mbar_try_wait(bar, phase)) return true;  // the common case reads no clock
+    if (gave_up) return false;
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, phase)) {
         if (globaltimer() - t0 > limit_ns) return false;

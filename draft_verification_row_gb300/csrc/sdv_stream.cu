@@ -318,7 +318,7 @@ __device__ __forceinline__ void pass1(StreamSmem* sm, Online& sT, Online& sD, ui
 #pragma unroll 1
     for (int ch = 0; ch < nc; ++ch, ++g) {
         const int s = g % kStages;
-        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim)) timed_out = true;
+        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim, timed_out)) timed_out = true;
         const bool tail = ch == nc - 1;
         const int ug0 = ch * kChunk + unit_local(cw, 0, lane);
         // (only the last chunk has units past V, or none: the others take no
@@ -424,7 +424,7 @@ __device__ __forceinline__ float sweep(StreamSmem* sm, uint32_t& g, bool& timed_
     for (int it = 0; it < nc; ++it, ++g) {
         const int ch = back ? nc - 1 - it : it;
         const int s = g % kStages;
-        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim)) timed_out = true;
+        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim, timed_out)) timed_out = true;
         const bool tail = ch == nc - 1;
         float w = 0.f;
         if (!tail && ch != xs_ch) {
@@ -501,7 +501,7 @@ __device__ __forceinline__ void kseq_sweep(StreamSmem* sm, uint32_t& g, bool& ti
     for (int it = 0; it < nc; ++it, ++g) {
         const int ch = back ? nc - 1 - it : it;
         const int s = g % kStages;
-        if (!timed_out && !mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim)) timed_out = true;
+        if (!mbar_wait_bounded(&sm->full[s], (g / kStages) & 1, lim, timed_out)) timed_out = true;
         const bool tail = ch == nc - 1;
 #pragma unroll
         for (int i = 0; i < kUPT; ++i) {
