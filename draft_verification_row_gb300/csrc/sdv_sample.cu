@@ -31,7 +31,6 @@ constexpr int kRW = 16;                                   // warps per CTA
 constexpr int kRT = 32 * kRW;                             // threads per CTA
 constexpr int kRU = 8;                                    // units per lane per step
 constexpr int kRSeg = 32 * kRU;                           // units per segment (one warp, one step)
-constexpr int kRStep = kRW * kRSeg;                       // units per step
 constexpr int kRMaxSeg = (SDV_MAX_V / 4 + kRSeg - 1) / kRSeg;  // segments of the longest row
 
 struct RowSmem {
@@ -170,11 +169,12 @@ __device__ void softmax_pass(const char* row, int V, float c, bool greedy, RowSm
     constexpr int EPU = E::kPerUnit;
     const int n_units = (V + EPU - 1) / EPU;
     const int n_seg = (n_units + kRSeg - 1) / kRSeg;
-    const int n_steps = (n_units + kRStep - 1) / kRStep;
+    const int nw = blockDim.x >> 5;  // warps per CTA (one segment each per step)
+    const int n_steps = (n_units + nw * kRSeg - 1) / (nw * kRSeg);
     bool bad = false;
 #pragma unroll 1
     for (int st = 0; st < n_steps; ++st) {
-        const int seg = st * kRW + w;
+        const int seg = st * nw + w;
         const int ug0 = seg * kRSeg + lane;
         uint4 u[kRU];
 #pragma unroll
@@ -239,11 +239,12 @@ __device__ void residual_pass(const Dist& d, int V, RowSmem& sm, int lane, int w
     constexpr int EPU = Elem<DT>::kPerUnit;
     const int n_units = (V + EPU - 1) / EPU;
     const int n_seg = (n_units + kRSeg - 1) / kRSeg;
-    const int n_steps = (n_units + kRStep - 1) / kRStep;
+    const int nw = blockDim.x >> 5;  // warps per CTA (one segment each per step)
+    const int n_steps = (n_units + nw * kRSeg - 1) / (nw * kRSeg);
     constexpr int kHalf = kRU / 2;  // units of both rows loaded before they are used
 #pragma unroll 1
     for (int st = 0; st < n_steps; ++st) {
-        const int seg = st * kRW + w;
+        const int seg = st * nw + w;
         float z = 0.f;
 #pragma unroll
         for (int h = 0; h < kRU; h += kHalf) {
@@ -589,7 +590,7 @@ __device__ void write_residual_row(const Problem& pb, int b, const Dist& d, cons
     const int V = pb.V;
     float* row = pb.residual_out + (size_t)b * V;
     if (one_hot) {
-        for (int x = tid; x < V; x += kRT) row[x] = x == tok ? 1.f : 0.f;
+        for (int x = tid; x < V; x += (int)blockDim.x) row[x] = x == tok ? 1.f : 0.f;
         return;
     }
     const int n_units = (V + EPU - 1) / EPU;
@@ -605,7 +606,7 @@ __device__ void write_residual_row(const Problem& pb, int b, const Dist& d, cons
         }
     }
     tot = warp_sum(tot);
-    for (int ug = tid; ug < n_units; ug += kRT) {
+    for (int ug = tid; ug < n_units; ug += (int)blockDim.x) {
         float v[EPU];
         unit_masses<DT>(d, ug, n_units, V, false, v);
 #pragma unroll
@@ -617,8 +618,8 @@ __device__ void write_residual_row(const Problem& pb, int b, const Dist& d, cons
 // One CTA per request: the decision (warp 0), then the correction (or
 // bonus) token at the end node it chose: from the node's final residual R_n
 // (kept by the node kernel), or from P at a leaf or where S_n = 0.
-template <int DT>
-__global__ void __launch_bounds__(kRT, 2) finish_kernel(Problem pb, int greedy, int wait_nodes)
+template <int DT, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) finish_kernel(Problem pb, int greedy, int wait_nodes)
 {
     using E = Elem<DT>;
     constexpr int EPU = E::kPerUnit;
@@ -730,11 +731,27 @@ int sample_threads() { return kRT; }
 cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st, bool after_nodes)
 {
     if (pb.B == 0) return cudaSuccess;
+    // One CTA per request; its passes over the end node's rows are bound by
+    // instruction issue within the CTA, so when the requests are no more
+    // than the SMs (one CTA per SM) each CTA takes 32 warps, else 16 (two
+    // CTAs per SM).
+    constexpr int kDevs = 64;
+    static int sms[kDevs];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int n_sm = dev >= 0 && dev < kDevs ? sms[dev] : 0;
+    if (n_sm == 0) {
+        e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kDevs) sms[dev] = n_sm;
+    }
+    const bool wide = pb.B <= n_sm;
     // after the node kernel: a programmatic dependent launch, so that the
     // decisions of finished requests overlap the node kernel's last nodes
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pb.B);
-    cfg.blockDim = dim3(kRT);
+    cfg.blockDim = dim3(wide ? 1024 : 512);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -743,8 +760,11 @@ cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st, bool 
     cfg.attrs = attr;
     cfg.numAttrs = after_nodes ? 1 : 0;
     const int g = greedy ? 1 : 0, wait = after_nodes ? 1 : 0;
-    if (pb.dtype == SDV_BF16) return cudaLaunchKernelEx(&cfg, finish_kernel<SDV_BF16>, pb, g, wait);
-    return cudaLaunchKernelEx(&cfg, finish_kernel<SDV_F32>, pb, g, wait);
+    if (pb.dtype == SDV_BF16)
+        return wide ? cudaLaunchKernelEx(&cfg, finish_kernel<SDV_BF16, 1024>, pb, g, wait)
+                    : cudaLaunchKernelEx(&cfg, finish_kernel<SDV_BF16, 512>, pb, g, wait);
+    return wide ? cudaLaunchKernelEx(&cfg, finish_kernel<SDV_F32, 1024>, pb, g, wait)
+                : cudaLaunchKernelEx(&cfg, finish_kernel<SDV_F32, 512>, pb, g, wait);
 }
 
 cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st)
