@@ -99,7 +99,6 @@ cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st);
 // after_nodes: launched right after the node kernel, as its programmatic
 // dependent; each CTA waits for its request's nodes (Workspace::left).
 cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st, bool after_nodes = false);
-int sample_threads();
 
 // The target model's LM head on the tensor cores (sdv_lmhead.cu):
 // logits = hidden . W^T over the hidden size d, bf16 in, fp32 accumulate.

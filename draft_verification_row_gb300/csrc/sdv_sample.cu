@@ -27,8 +27,6 @@
 namespace sdv {
 namespace {
 
-constexpr int kRW = 16;                                   // warps per CTA
-constexpr int kRT = 32 * kRW;                             // threads per CTA
 constexpr int kRU = 8;                                    // units per lane per step
 constexpr int kRSeg = 32 * kRU;                           // units per segment (one warp, one step)
 constexpr int kRMaxSeg = (SDV_MAX_V / 4 + kRSeg - 1) / kRSeg;  // segments of the longest row
@@ -342,8 +340,8 @@ __device__ __forceinline__ bool row_max(const RowSmem& sm, int n_seg, int lane, 
     return sm.bad == 0 && M > -INFINITY && M == M;
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kRT, 2) sample_rows_kernel(SampleArgs a)
+template <int DT, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) sample_rows_kernel(SampleArgs a)
 {
     using E = Elem<DT>;
     constexpr int EPU = E::kPerUnit;
@@ -368,15 +366,15 @@ __global__ void __launch_bounds__(kRT, 2) sample_rows_kernel(SampleArgs a)
     const bool ok = row_max(sm, n_seg, lane, M);
     int* const out = a.tokens + (size_t)r * a.n_samples;
     if (!ok) {
-        for (int s = tid; s < a.n_samples; s += kRT) out[s] = -1;
+        for (int s = tid; s < a.n_samples; s += NT) out[s] = -1;
         if (tid == 0 && a.device_status) atomicOr(a.device_status, SDV_REQ_NONFINITE);
         return;
     }
     d.M = M;
     d.negM = -(M * a.c);
-    // warp w takes draws w, w + 16, ...
+    // warp w takes draws w, w + NT / 32, ...
 #pragma unroll 1
-    for (int s = w; s < a.n_samples; s += kRW) {
+    for (int s = w; s < a.n_samples; s += NT / 32) {
         const float u = greedy ? 0.f : a.u[(size_t)r * a.n_samples + s];
         const int x = draw<DT>(d, sm, V, u, greedy, lane);
         if (lane == 0) out[s] = x;
@@ -726,7 +724,6 @@ __global__ void __launch_bounds__(NT, 1024 / NT) finish_kernel(Problem pb, int g
 
 }  // namespace
 
-int sample_threads() { return kRT; }
 
 cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st, bool after_nodes)
 {
@@ -770,10 +767,24 @@ cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st, bool 
 cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st)
 {
     if (a.n_rows == 0 || a.n_samples == 0) return cudaSuccess;
-    if (a.dtype == SDV_BF16)
-        sample_rows_kernel<SDV_BF16><<<a.n_rows, kRT, 0, st>>>(a);
-    else
-        sample_rows_kernel<SDV_F32><<<a.n_rows, kRT, 0, st>>>(a);
+    // One CTA per row; its warps share the row's pass, then take one draw
+    // each at a time.  Few draws per row: small CTAs, many per SM, so that
+    // while one CTA draws (a serial scan and a 4 KB re-read) the others
+    // stream their rows.  Measured on 2048 rows of V = 151936 bf16, one
+    // draw each, single calls alternated in one process: 128 threads 5.5%
+    // faster than 512, 64 threads 1% faster again.
+    const int nt = a.n_samples <= 2 ? 64 : a.n_samples <= 4 ? 128 : a.n_samples <= 8 ? 256 : 512;
+    if (a.dtype == SDV_BF16) {
+        if (nt == 64) sample_rows_kernel<SDV_BF16, 64><<<a.n_rows, 64, 0, st>>>(a);
+        else if (nt == 128) sample_rows_kernel<SDV_BF16, 128><<<a.n_rows, 128, 0, st>>>(a);
+        else if (nt == 256) sample_rows_kernel<SDV_BF16, 256><<<a.n_rows, 256, 0, st>>>(a);
+        else sample_rows_kernel<SDV_BF16, 512><<<a.n_rows, 512, 0, st>>>(a);
+    } else {
+        if (nt == 64) sample_rows_kernel<SDV_F32, 64><<<a.n_rows, 64, 0, st>>>(a);
+        else if (nt == 128) sample_rows_kernel<SDV_F32, 128><<<a.n_rows, 128, 0, st>>>(a);
+        else if (nt == 256) sample_rows_kernel<SDV_F32, 256><<<a.n_rows, 256, 0, st>>>(a);
+        else sample_rows_kernel<SDV_F32, 512><<<a.n_rows, 512, 0, st>>>(a);
+    }
     return cudaGetLastError();
 }
 

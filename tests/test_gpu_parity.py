@@ -5,6 +5,8 @@ import numpy as np
 import pytest
 import torch
 
+import draft_verification_row_gb300 as sdv
+from draft_verification_row_gb300 import binding
 from draft_verification_row_gb300 import workloads as W
 from tests import goldens
 from tests import parity as P
@@ -208,6 +210,31 @@ def test_deterministic():
         for key in a:
             if a[key] is not None:
                 np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_full_size_calls_repeat_bit_for_bit():
+    """The headline batch at full size, in the launch configuration the bench
+    times (the decision kernel overlapping the node kernel's tail, nodes
+    handed out by a global counter): repeated calls on the same inputs give
+    the same bits, in every rule that runs the node kernel.  A dependence on
+    which CTA took which node, or on the timing of the weights' flags and
+    the node counts, would show here."""
+    batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV)
+    stream = torch.cuda.current_stream()
+    for mode, ap in (("multidraft", False), ("multidraft", True), ("token", True), ("kseq", True)):
+        out = binding.Outputs(mode, batch.B, batch.K, batch.L, batch.V, DEV, accept_prob=ap)
+        ref = None
+        for _ in range(8):
+            sdv.verify(mode, batch.target, batch.draft, batch.tokens, batch.lengths, batch.accept_u, batch.sample_u,
+                       batch.temperature, V=batch.V, out=out, stream=stream)
+            torch.cuda.synchronize()
+            got = {k: v.cpu().numpy().copy() for k, v in out.as_dict().items() if v is not None}
+            assert int(got["device_status"][0]) == 0, mode
+            if ref is None:
+                ref = got
+            else:
+                for k in ref:
+                    np.testing.assert_array_equal(ref[k], got[k], err_msg=f"{mode} accept_prob={ap} {k}")
 
 
 @pytest.mark.parametrize("name,kw,T", SMALL[3:])
