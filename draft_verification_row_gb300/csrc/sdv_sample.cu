@@ -725,6 +725,29 @@ __global__ void __launch_bounds__(NT, 1024 / NT) finish_kernel(Problem pb, int g
 }  // namespace
 
 
+namespace {
+
+// The device's SM count, asked once per device.
+cudaError_t sm_count_cached(int* n_sm)
+{
+    constexpr int kDevs = 64;
+    static int sms[kDevs];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int n = dev >= 0 && dev < kDevs ? sms[dev] : 0;
+    if (n == 0) {
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (n <= 0) n = 1;
+        if (dev >= 0 && dev < kDevs) sms[dev] = n;
+    }
+    *n_sm = n;
+    return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st, bool after_nodes)
 {
     if (pb.B == 0) return cudaSuccess;
@@ -732,17 +755,9 @@ cudaError_t launch_finish(const Problem& pb, bool greedy, cudaStream_t st, bool 
     // instruction issue within the CTA, so when the requests are no more
     // than the SMs (one CTA per SM) each CTA takes 32 warps, else 16 (two
     // CTAs per SM).
-    constexpr int kDevs = 64;
-    static int sms[kDevs];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    int n_sm = 0;
+    const cudaError_t e = sm_count_cached(&n_sm);
     if (e != cudaSuccess) return e;
-    int n_sm = dev >= 0 && dev < kDevs ? sms[dev] : 0;
-    if (n_sm == 0) {
-        e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kDevs) sms[dev] = n_sm;
-    }
     const bool wide = pb.B <= n_sm;
     // after the node kernel: a programmatic dependent launch, so that the
     // decisions of finished requests overlap the node kernel's last nodes
@@ -768,12 +783,22 @@ cudaError_t launch_sample_rows(const SampleArgs& a, cudaStream_t st)
 {
     if (a.n_rows == 0 || a.n_samples == 0) return cudaSuccess;
     // One CTA per row; its warps share the row's pass, then take one draw
-    // each at a time.  Few draws per row: small CTAs, many per SM, so that
+    // each at a time.  The CTAs are sized so that the launch holds about
+    // 32 warps per SM: with many rows, small CTAs, many per SM, so that
     // while one CTA draws (a serial scan and a 4 KB re-read) the others
-    // stream their rows.  Measured on 2048 rows of V = 151936 bf16, one
-    // draw each, single calls alternated in one process: 128 threads 5.5%
-    // faster than 512, 64 threads 1% faster again.
-    const int nt = a.n_samples <= 2 ? 64 : a.n_samples <= 4 ? 128 : a.n_samples <= 8 ? 256 : 512;
+    // stream their rows; with few rows, larger CTAs, so that each row's
+    // pass has warps enough to keep its loads in flight.  At least one warp
+    // per draw, up to 16.  Measured on rows of V = 151936 bf16, one draw
+    // each, single calls alternated in one process (against 16 warps):
+    // 512 rows 8 warps 4% faster (4 warps 19% slower), 1024 rows 4 warps
+    // 10.5% faster, 2048 rows 2 warps 6.5% faster.
+    int n_sm = 0;
+    const cudaError_t e = sm_count_cached(&n_sm);
+    if (e != cudaSuccess) return e;
+    int warps = 2;
+    while (warps < 16 && (long long)warps * 2 * a.n_rows <= 32LL * n_sm) warps *= 2;
+    while (warps < 16 && warps < a.n_samples) warps *= 2;
+    const int nt = 32 * warps;
     if (a.dtype == SDV_BF16) {
         if (nt == 64) sample_rows_kernel<SDV_BF16, 64><<<a.n_rows, 64, 0, st>>>(a);
         else if (nt == 128) sample_rows_kernel<SDV_BF16, 128><<<a.n_rows, 128, 0, st>>>(a);
