@@ -634,6 +634,21 @@ struct ProbS {
     float P, Pbar;
 };
 
+// 2^(logit c + gneg) for one gathered token.  For a tail token the
+// argument is 20 to 30 in size, where rounding it to fp32 alone moves the
+// result by up to 7e-7 relative; in a row sum such errors average out,
+// but a draw's own P(y) and Q(y) meet in R = P - C Q, whose cancellation
+// multiplies it.  The product of two floats is exact in double, so the
+// argument is formed there, split into a float and its remainder, and
+// raised with the accurate exp2f and a first-order term for the remainder.
+__device__ __forceinline__ float exp2_gathered(float logit, float c, float gneg)
+{
+    const double a = fma((double)logit, (double)c, (double)gneg);
+    const float hi = (float)a;
+    const float lo = (float)(a - (double)hi);
+    return exp2f(hi) * fmaf(lo, 0.693147180559945309f, 1.f);
+}
+
 __device__ __forceinline__ ProbS prob_s(const StreamSmem* sm, bool is_t, int x, float logit, float c)
 {
     ProbS o;
@@ -642,7 +657,7 @@ __device__ __forceinline__ ProbS prob_s(const StreamSmem* sm, bool is_t, int x, 
         o.P = (is_t ? sm->emaxT : sm->emaxD) / z;
         o.Pbar = (is_t ? sm->zrestT : sm->zrestD) / z;
     } else {
-        o.P = ex2(fmaf(logit, c, is_t ? sm->gnegT : sm->gnegD)) / (is_t ? sm->zT : sm->zD);
+        o.P = exp2_gathered(logit, c, is_t ? sm->gnegT : sm->gnegD) / (is_t ? sm->zT : sm->zD);
         o.Pbar = 1.f - o.P;
     }
     return o;
