@@ -32,10 +32,35 @@ constexpr int kRSeg = 32 * kRU;                           // units per segment (
 constexpr int kRMaxSeg = (SDV_MAX_V / 4 + kRSeg - 1) / kRSeg;  // segments of the longest row
 
 struct RowSmem {
-    float mass[kRMaxSeg];  // per segment: sum of its masses (softmax: against ref)
+    float mass[kRMaxSeg];  // per segment: sum of its masses (softmax: against its maximum)
     float ref[kRMaxSeg];   // softmax: the segment's maximum; residual: unused
     int bad;
 };
+
+// A draw compares u times the row's total with running sums over the
+// segments, of the same size as the total; in fp32 their rounding alone
+// (half an ulp: 3e-8 near 0.5) would settle a draw whose u lies that close
+// to an interval's end.  The total and the running sums over segments are
+// therefore kept in double (a few dozen additions a draw); a segment's own
+// mass and the running sum inside one are fp32, at most 1/32 of the total
+// for a row of 65536 elements or more.
+__device__ __forceinline__ double warp_sum_d(double v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Inclusive prefix sum over the warp's lanes.
+__device__ __forceinline__ double warp_scan_d(double v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
 
 // The distribution a draw is taken from.
 struct Dist {
@@ -272,6 +297,33 @@ __device__ void residual_pass(const Dist& d, int V, RowSmem& sm, int lane, int w
     }
 }
 
+// Segment i's mass against the row's reference.  A softmax pass summed the
+// segment's elements as 2^(x c + negm) with its own offset negm = -(m c)
+// rounded to float, and a draw's elements are taken as 2^(x c + negM); the
+// factor between the two is 2 to the difference of those float offsets.
+// The difference of two floats is exact as a float plus a remainder
+// (TwoSum); the factor is exp2f of the first times a first-order term for
+// the second.
+__device__ __forceinline__ float seg_mass(const Dist& d, const RowSmem& sm, int i)
+{
+    if (d.residual) return sm.mass[i];
+    const float ref = sm.ref[i];
+    if (!(ref > -INFINITY)) return 0.f;
+    const float a = d.negM, b = ref * d.c;  // delta = a + b, b = -negm
+    const float hi = a + b;
+    const float bb = hi - a;
+    const float lo = (a - (hi - bb)) + (b - bb);
+    return sm.mass[i] * (exp2f(hi) * fmaf(lo, 0.693147180559945309f, 1.f));
+}
+
+// The row's total mass as every draw sums it (per warp, lanes in order).
+__device__ __forceinline__ double row_total(const Dist& d, const RowSmem& sm, int n_seg, int lane)
+{
+    double tot = 0.0;
+    for (int i = lane; i < n_seg; i += 32) tot += (double)seg_mass(d, sm, i);
+    return warp_sum_d(tot);
+}
+
 // One draw with uniform u (warp-wide).  Softmax distributions rescale each
 // segment from its own maximum to the row's.
 template <int DT>
@@ -280,13 +332,8 @@ __device__ int draw(const Dist& d, const RowSmem& sm, int V, float u, bool greed
     constexpr int EPU = Elem<DT>::kPerUnit;
     const int n_units = (V + EPU - 1) / EPU;
     const int n_seg = (n_units + kRSeg - 1) / kRSeg;
-    auto seg_mass = [&](int i) -> float {
-        if (d.residual) return sm.mass[i];
-        const float ref = sm.ref[i];
-        return ref > -INFINITY ? sm.mass[i] * ex2((ref - d.M) * d.c) : 0.f;
-    };
     int seg = -1;
-    float base = 0.f, thr = 0.5f;
+    double base = 0.0, thr = 0.5;
     if (greedy) {  // the first segment holding the maximum; its first element equal to it
         for (int i0 = 0; i0 < n_seg && seg < 0; i0 += 32) {
             const int i = i0 + lane;
@@ -294,23 +341,15 @@ __device__ int draw(const Dist& d, const RowSmem& sm, int V, float u, bool greed
             if (hit) seg = i0 + __ffs(hit) - 1;
         }
     } else {
-        float tot = 0.f;
-        for (int i = lane; i < n_seg; i += 32) tot += seg_mass(i);
-        tot = warp_sum(tot);
-        thr = u * tot;
-        float run = 0.f, lbase = 0.f;
+        thr = (double)u * row_total(d, sm, n_seg, lane);
+        double run = 0.0, lbase = 0.0;
         int last_nz = -1;
         for (int i0 = 0; i0 < n_seg && seg < 0; i0 += 32) {
             const int i = i0 + lane;
-            const float v = i < n_seg ? seg_mass(i) : 0.f;
-            float incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
-            }
-            const unsigned cross = __ballot_sync(0xffffffffu, v > 0.f && run + incl > thr);
-            const unsigned nz = __ballot_sync(0xffffffffu, v > 0.f);
+            const double v = i < n_seg ? (double)seg_mass(d, sm, i) : 0.0;
+            const double incl = warp_scan_d(v, lane);
+            const unsigned cross = __ballot_sync(0xffffffffu, v > 0.0 && run + incl > thr);
+            const unsigned nz = __ballot_sync(0xffffffffu, v > 0.0);
             if (cross) {
                 const int l = __ffs(cross) - 1;
                 seg = i0 + l;
@@ -327,7 +366,7 @@ __device__ int draw(const Dist& d, const RowSmem& sm, int V, float u, bool greed
             base = lbase;
         }
     }
-    return seg >= 0 ? pick_in_segment<DT>(d, seg, n_units, V, thr - base, greedy, lane) : -1;
+    return seg >= 0 ? pick_in_segment<DT>(d, seg, n_units, V, (float)(thr - base), greedy, lane) : -1;
 }
 
 // The row maximum after a softmax pass (every thread); false if the row
@@ -594,22 +633,13 @@ __device__ void write_residual_row(const Problem& pb, int b, const Dist& d, cons
     const int n_units = (V + EPU - 1) / EPU;
     const int n_seg = (n_units + kRSeg - 1) / kRSeg;
     // the total, summed as the draw sums it (every warp for itself)
-    float tot = 0.f;
-    for (int i = lane; i < n_seg; i += 32) {
-        if (d.residual) {
-            tot += sm.mass[i];
-        } else {
-            const float ref = sm.ref[i];
-            tot += ref > -INFINITY ? sm.mass[i] * ex2((ref - d.M) * d.c) : 0.f;
-        }
-    }
-    tot = warp_sum(tot);
+    const double tot = row_total(d, sm, n_seg, lane);
     for (int ug = tid; ug < n_units; ug += (int)blockDim.x) {
         float v[EPU];
         unit_masses<DT>(d, ug, n_units, V, false, v);
 #pragma unroll
         for (int e = 0; e < EPU; ++e)
-            if (ug * EPU + e < V) row[ug * EPU + e] = v[e] / tot;
+            if (ug * EPU + e < V) row[ug * EPU + e] = (float)((double)v[e] / tot);
     }
 }
 
@@ -690,11 +720,9 @@ __global__ void __launch_bounds__(NT, 1024 / NT) finish_kernel(Problem pb, int g
         residual_pass<DT>(d, V, sm, lane, w);
         __syncthreads();
         if (sum_here) {
-            float tot = 0.f;  // summed as the draw sums it (every warp for itself)
-            for (int i = lane; i < n_seg; i += 32) tot += sm.mass[i];
-            tot = fmaxf(warp_sum(tot), 0.f);
-            if (tid == 0 && pb.residual_mass) pb.residual_mass[b] = tot;
-            d.residual = tot > 0.f;
+            const double tot = fmax(row_total(d, sm, n_seg, lane), 0.0);  // as the draw sums it
+            if (tid == 0 && pb.residual_mass) pb.residual_mass[b] = (float)tot;
+            d.residual = tot > 0.0;
         }
     }
     if (!d.residual) {

@@ -98,7 +98,9 @@ def make(workload, device="cpu", *, seed: Optional[int] = None, temperature: Opt
         if v is not None:
             cfg[k] = v
     B_, K_, L_, V_ = cfg["B"], cfg["K"], cfg["L"], cfg["V"]
-    T = cfg["T"] if temperature is None else float(temperature)
+    # the C interface takes the temperature as a float: the batch carries
+    # that float's value, so that every consumer is handed the same number
+    T = float(torch.tensor(cfg["T"] if temperature is None else float(temperature), dtype=torch.float32))
     seed = cfg["seed"] if seed is None else seed
     dt = torch.bfloat16 if cfg["dtype"] == "bf16" else torch.float32
     stride = _round8(V_) + stride_pad

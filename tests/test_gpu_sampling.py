@@ -44,6 +44,7 @@ def _uniforms(n, s, seed):
 
 
 def _check(logits, n_samples, u, T, V=None, what=""):
+    T = float(np.float32(T))  # the value the library's float argument holds
     tokens, status = sdv.sample_rows(logits, n_samples, u, T, V=V)
     torch.cuda.synchronize()
     got = tokens.cpu().numpy()
