@@ -633,13 +633,13 @@ __device__ void write_residual_row(const Problem& pb, int b, const Dist& d, cons
     const int n_units = (V + EPU - 1) / EPU;
     const int n_seg = (n_units + kRSeg - 1) / kRSeg;
     // the total, summed as the draw sums it (every warp for itself)
-    const double tot = row_total(d, sm, n_seg, lane);
+    const float tot = (float)row_total(d, sm, n_seg, lane);
     for (int ug = tid; ug < n_units; ug += (int)blockDim.x) {
         float v[EPU];
         unit_masses<DT>(d, ug, n_units, V, false, v);
 #pragma unroll
         for (int e = 0; e < EPU; ++e)
-            if (ug * EPU + e < V) row[ug * EPU + e] = (float)((double)v[e] / tot);
+            if (ug * EPU + e < V) row[ug * EPU + e] = v[e] / tot;
     }
 }
 
