@@ -253,16 +253,28 @@ def test_skipping_last_sweeps_keeps_every_output(name, kw, T):
         np.testing.assert_allclose(full["residual_mass"][at_root], lazy["residual_mass"][at_root], atol=1e-6, rtol=0)
 
 
-# The node kernel streams rows in chunks of 1024 16-byte units (8192 bf16 or
-# 4096 fp32 logits), 64 contiguous units per warp: vocabularies at and
-# around those boundaries, a tail chunk that only some warps reach, and a
-# tail unit that only part of a warp's lanes reach.
-@pytest.mark.parametrize("V,dtype", [(8191, "bf16"), (8192, "bf16"), (8193, "bf16"), (8192 + 64 * 8, "bf16"),
-                                     (8192 + 40 * 8 + 3, "bf16"), (16384, "bf16"), (4095, "f32"),
-                                     (4096, "f32"), (4096 + 64 * 4 + 1, "f32")])
+# The node kernel streams rows in chunks of 768 16-byte units (6144 bf16 or
+# 3072 fp32 logits: 12 consumer warps of 64 contiguous units each):
+# vocabularies at and around those boundaries, a tail chunk that only some
+# warps reach, and a tail unit that only part of a warp's lanes reach; and
+# the same around the 8192-logit boundary of 16-warp chunks, which now fall
+# inside a chunk.
+@pytest.mark.parametrize("V,dtype", [(6143, "bf16"), (6144, "bf16"), (6145, "bf16"), (6144 + 64 * 8, "bf16"),
+                                     (6144 + 40 * 8 + 3, "bf16"), (12288, "bf16"), (12288 + 11 * 64 * 8 + 5, "bf16"),
+                                     (3071, "f32"), (3072, "f32"), (3073, "f32"), (3072 + 64 * 4 + 1, "f32"),
+                                     (8191, "bf16"), (8192, "bf16"), (8193, "bf16"), (4096, "f32")])
 def test_chunk_boundaries(V, dtype):
     batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=4, K=4, L=3, V=V, dtype=dtype)
     for mode in ("token", "multidraft"):
+        _compare_both(mode, batch, P.oracle_run(mode, batch), f"V={V}/{dtype}/{mode}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [262143, 262144])
+def test_largest_vocabulary(dtype, V):
+    # the library's largest vocabulary (SDV_MAX_V) and a ragged one below it
+    batch = W.make("multidraft-B32-K4-L4-V32000-f32", DEV, B=3, K=3, L=2, V=V, dtype=dtype, temperature=0.8)
+    for mode in MODES_K + ["kseq"]:
         _compare_both(mode, batch, P.oracle_run(mode, batch), f"V={V}/{dtype}/{mode}")
 
 
