@@ -493,6 +493,22 @@ def first_drafts(batch, K):
                                tokens=cut(batch.tokens), accept_u=cut(batch.accept_u), sample_u=cut(batch.sample_u))
 
 
+def capture_graph(fn, stream):
+    """fn captured in a CUDA graph (after one call outside the capture):
+    a serving loop replays one graph per step instead of launching."""
+    side = torch.cuda.Stream(device=stream.device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
 def time_flushed(fn, reps, stream, flush, prof=False):
     """Mean ms of fn between CUDA events on `stream`, L2 flushed (a write
     larger than L2) before every call and outside the timed pair; with prof,
@@ -546,6 +562,16 @@ def config_lines(args, dev, stream, peak, rank):
         kms = time_flushed(call, reps, stream, flush, prof=True)
         if int(out.device_status.item()):
             raise RuntimeError(f"{name} {mode}: device status {int(out.device_status.item())}")
+        # the same call replayed from a CUDA graph (its launches and memsets
+        # captured once), on the same stream
+        graph = capture_graph(lambda: sdv.verify(mode, batch.target, batch.draft, batch.tokens, batch.lengths,
+                                                 batch.accept_u, batch.sample_u, batch.temperature, V=batch.V,
+                                                 out=out), stream)
+        with torch.cuda.stream(stream):
+            gms = time_flushed(graph.replay, reps, stream, flush)
+        if int(out.device_status.item()):
+            raise RuntimeError(f"{name} {mode} (graph): device status {int(out.device_status.item())}")
+        del graph
         nbytes = row_bytes_of(batch, inner, leaves, greedy=greedy,
                               ended_at_leaf=int((out.accept_len == batch.lengths).sum().item()))
         gbs = nbytes / (kms / 1000.0) / 1e9
@@ -555,7 +581,9 @@ def config_lines(args, dev, stream, peak, rank):
                  "algorithmic_bytes": nbytes, "achieved_gbs": gbs, "frac": gbs / peak,
                  "size_table_bytes": table_rows(batch.lengths, batch.K, greedy) * batch.V * (
                      2 if batch.dtype == "bf16" else 4),
-                 "gpu_launches_per_call": 3, "l2": "flushed before every call"}
+                 "gpu_launches_per_call": 3, "l2": "flushed before every call",
+                 "graph": {"ms_per_call": gms, "value": batch.positions / (gms / 1000.0), "unit": UNIT,
+                           "what": "the same call captured once in a CUDA graph and replayed"}}
         if rank == 0:
             p, dt = oracle_sample(batch, "greedy" if greedy else mode, list(range(batch.B)))
             entry["cpu_baseline"] = {"value": p / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -779,6 +807,22 @@ def run_ours(args, world, rank, local):
                                     "row_kernel_ms_per_step": r2 / args.steps,
                                     "algorithmic_bytes_per_step": ob, "achieved_gbs": og, "frac": og / peak}
             del out2
+        # the headline call captured once in a CUDA graph and replayed (a
+        # serving loop's form: no launch work on the host per step)
+        graph = capture_graph(lambda: sdv.verify(args.mode, batch.target, batch.draft, batch.tokens, batch.lengths,
+                                                 batch.accept_u, batch.sample_u, batch.temperature, V=batch.V,
+                                                 out=out), stream)
+        for _ in range(2):
+            graph.replay()
+        tg, _ = time_calls(graph.replay, args.steps, stream)
+        tg = max_over_ranks(tg, world)
+        if int(out.device_status.item()):
+            raise RuntimeError(f"graph replay: device status {int(out.device_status.item())}")
+        del graph
+        line["graph"] = {"value": all_positions / (tg / args.steps / 1000.0), "unit": UNIT,
+                         "ms_per_step": tg / args.steps,
+                         "what": "the same call captured once in a CUDA graph (its memsets and 3 launches) "
+                                 "and replayed each step"}
         # end to end through the C-ABI with host buffers: the host-to-device
         # copy of the inputs (of the logits, the rows verification reads,
         # sdv_copy_read_rows), the call, and the per-request results back
