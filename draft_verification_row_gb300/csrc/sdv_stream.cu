@@ -1,14 +1,15 @@
 // sdv_stream.cu -- the node kernel: every vocabulary-row computation of a
 // verification call, in one persistent launch.
 //
-// One CTA per SM verifies one draft-trie node at a time; the node's target
-// and draft rows stream through shared memory:
+// Two CTAs per SM, each verifying one draft-trie node at a time; the
+// node's target and draft rows stream through shared memory:
 //   pass 1 (from HBM): online maxima and softmax normalisers of both rows,
 //           in a warp-uniform reference, the row maxima counted apart so
 //           that 1 - P of a dominant token stays exact;
 //   pass 2 (from L2, once per draw): the residual sweep
-//           S_j = sum_x max(p P(x) - C_j Q(x), 0), and, on the last sweep,
-//           the mass per (chunk, warp) for the inverse-CDF sample.
+//           S_j = sum_x max(p P(x) - C_j Q(x), 0).  A node keeps its final
+//           residual's description for the correction draw, which the
+//           decision kernel takes (sdv_sample.cu) in a pass of its own.
 // Only inner nodes are visited: a leaf has no draws (its residual is p P,
 // of mass p), and its target row is read by the bonus draw alone, after
 // the decision and only if the decision ends there.
