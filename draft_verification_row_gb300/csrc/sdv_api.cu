@@ -24,7 +24,7 @@ bool sizes_ok(int B, int K, int L, int V)
 size_t workspace_size(int B, int K, int L)
 {
     const size_t n = slot_count(B, K, L);
-    return 6 * align_up(n * 4) + align_up(n * 6 * 4) + align_up(n) + 2 * align_up((size_t)B * 4) +
+    return 5 * align_up(n * 4) + align_up(n * 8) + align_up(n * 6 * 4) + align_up(n) + 2 * align_up((size_t)B * 4) +
            align_up((size_t)(L + 1) * B * K * 4) + align_up((size_t)(2 * L + 3) * 4);
 }
 
@@ -54,8 +54,8 @@ Workspace carve(void* base, int B, int K, int L)
     p += align_up(n * 4);
     w.S = reinterpret_cast<float*>(p);
     p += align_up(n * 4);
-    w.pbar = reinterpret_cast<float*>(p);
-    p += align_up(n * 4);
+    w.wt = reinterpret_cast<float2*>(p);
+    p += align_up(n * 8);
     w.prm = reinterpret_cast<float*>(p);
     p += align_up(n * 6 * 4);
     w.xs = reinterpret_cast<int*>(p);

@@ -20,8 +20,10 @@ struct Workspace {
     float* a;              // draw acceptance probability a (token / multidraft)
     float* h;              // node block acceptance probability h_v
     float* S;              // node residual mass S_n
-    float* pbar;           // node weight complement 1 - p_v, written by the parent's draw
-                           //   (below 0 until then: the child's flag)
+    float2* wt;            // node weight {1 - p_v, p_v}, written together (one 8-byte store)
+                           //   by the parent's draw; .x below 0 until then: the child's flag.
+                           //   Both are kept so that neither loses its digits: 1 - p_v when
+                           //   p_v is near 1, p_v when it is small
     float* prm;            // node residual for the correction draw: [slot][6] =
                            //   -(M_T c), -(M_D c), aT = p / Z_T, aD / aT, R_n(x*), floor
                            //   (the residual is aT max(e_T - (aD/aT) e_D, floor e_T))

@@ -95,7 +95,7 @@ __global__ void prep_kernel(Problem pb)
         const unsigned below = (1u << lane) - 1;
         if (node && draws > 1) pb.ws.nodes[j * BK + fb + __popc(mh & below)] = (int)slot;
         if (node && draws == 1) pb.ws.nodes[j * BK + BK - 1 - (bb + __popc(ml & below))] = (int)slot;
-        if (lane < K) pb.ws.pbar[slot] = j == 0 ? 0.f : -1.f;  // the root's weight is 1
+        if (lane < K) pb.ws.wt[slot] = j == 0 ? make_float2(0.f, 1.f) : make_float2(-1.f, 0.f);  // root: p = 1
         listed += __popc(mh) + __popc(ml);
     }
     if (lane == 0) pb.ws.left[b] = listed;

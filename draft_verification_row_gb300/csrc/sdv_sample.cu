@@ -476,7 +476,7 @@ __device__ void decide_request(const Problem& pb, int b, bool greedy, DecideSmem
         else if (token)
             v = pb.ws.a[s0 + i];
         else  // a leaf's block acceptance is its weight p (the node kernel skips leaves)
-            v = i >= Lb * K ? (Lb == 0 ? 1.f : 1.f - pb.ws.pbar[s0 + i]) : pb.ws.h[s0 + i];
+            v = i >= Lb * K ? (Lb == 0 ? 1.f : pb.ws.wt[s0 + i].y) : pb.ws.h[s0 + i];
         val[i] = v;
     }
     for (int i = lane; i < K * L; i += 32) {
@@ -594,7 +594,7 @@ __device__ void decide_request(const Problem& pb, int b, bool greedy, DecideSmem
     pb.accept_draft[b] = eo;
     s.endn = (int)(se | (leaf ? (1u << 30) : 0u));
     if (pb.residual_mass)
-        pb.residual_mass[b] = leaf ? (token || Lb == 0 ? 1.f : 1.f - pb.ws.pbar[se]) : pb.ws.S[se];
+        pb.residual_mass[b] = leaf ? (token || Lb == 0 ? 1.f : pb.ws.wt[se].y) : pb.ws.S[se];
 }
 
 // A request found invalid after its decision (one warp): the outputs an

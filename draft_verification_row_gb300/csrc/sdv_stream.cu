@@ -78,18 +78,21 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
         : "memory");
 }
 
-// A node's weight is its own flag: the parent's draw writes it (a value of
-// 0 or more) and the child reads nothing else, so relaxed accesses suffice.
-__device__ __forceinline__ float ld_relaxed(const float* p)
+// A node's weight is its own flag: the parent's draw writes the pair
+// {1 - p, p} (the first 0 or more) in one 8-byte access and the child
+// reads nothing else, so relaxed accesses suffice.
+__device__ __forceinline__ float2 ld_weight(const float2* p)
 {
-    float v;
-    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-    return v;
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return make_float2(__uint_as_float((unsigned)v), __uint_as_float((unsigned)(v >> 32)));
 }
 
-__device__ __forceinline__ void st_relaxed(float* p, float v)
+__device__ __forceinline__ void st_weight(float2* p, float pbar, float pw)
 {
-    asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+    const unsigned long long v = (unsigned long long)__float_as_uint(pbar) |
+                                 ((unsigned long long)__float_as_uint(pw) << 32);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // What the metadata warp prepares for each node, ahead of its rows.
@@ -115,7 +118,7 @@ struct StreamSmem {
     // scalar state (consumer thread 0)
     float MT, MD, gnegT, gnegD, zT, zD, zrestT, zrestD, emaxT, emaxD;
     int uT, uD;
-    float S, D, cbar, pbar, Pbs, Qbs, Rs, Ts, Rj, aT, aD, rD;
+    float S, D, cbar, pbar, pw, Pbs, Qbs, Rs, Ts, Rj, aT, aD, rD;  // pbar = 1 - p, pw = p
     int xs, bad;
     int skip_last, last_go;          // the node's last sweep: skipped here / issued by the copy warp
     // K-SEQ search (consumer thread 0): bracket [klo, khi] of rho, beta at
@@ -904,29 +907,31 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                 atomicOr(&pb.ws.req[b], SDV_REQ_NONFINITE);
                 if (pb.device_status) atomicOr(pb.device_status, SDV_REQ_NONFINITE);
             }
-            // the node weight, written by the parent (below 0 until then)
-            float pbar = 0.f;
+            // the node weight {1 - p, p}, written by the parent (.x below 0
+            // until then)
+            float2 wt = make_float2(0.f, 1.f);
             if (!KSEQ && j > 0 && pb.mode != SDV_MODE_TOKEN) {
-                const float* f = pb.ws.pbar + slot;
-                pbar = ld_relaxed(f);
-                if (!(pbar >= 0.f)) {
+                const float2* f = pb.ws.wt + slot;
+                wt = ld_weight(f);
+                if (!(wt.x >= 0.f)) {
                     const uint64_t t0 = globaltimer();
-                    while (!((pbar = ld_relaxed(f)) >= 0.f)) {
+                    while (!((wt = ld_weight(f)).x >= 0.f)) {
                         if (globaltimer() - t0 > lim) {
                             sm->abort = 1;
-                            pbar = 0.f;
+                            wt = make_float2(0.f, 1.f);
                             break;
                         }
                     }
                 }
             }
-            sm->pbar = pbar;
+            sm->pbar = wt.x;
+            sm->pw = wt.y;
             const int xs = (sm->uT >= 0 && sm->uT == sm->uD) ? sm->uT : -1;
             sm->xs = xs;
             sm->Pbs = xs >= 0 ? sm->zrestT / sm->zT : 0.f;
             sm->Qbs = xs >= 0 ? sm->zrestD / sm->zD : 0.f;
             sm->Rs = sm->Ts = 0.f;
-            sm->S = 1.f - pbar;
+            sm->S = wt.y;
             sm->D = 1.f;
             sm->cbar = 0.f;
             if constexpr (KSEQ) {
@@ -945,7 +950,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
             }
         }
         cbar_sync();
-        const float pbar = sm->pbar, p = 1.f - pbar;
+        const float pbar = sm->pbar, p = sm->pw;
         const float gnegT = sm->gnegT, gnegD = sm->gnegD;
         const int xs = sm->xs;
 
@@ -953,7 +958,10 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
         // R_0 = p P, R_j = max(R_{j-1} - D_{j-1} Q, 0), S_j = sum R_j,
         // D_j = (1 - p) + S_j.  Scalars are kept as complements (pbar =
         // 1 - p, cbar = C - 1, Pbs = 1 - P(x*), Qbs = 1 - Q(x*)) so that
-        // nothing cancels when p, P or Q is close to 1.  The shared
+        // nothing cancels when p, P or Q is close to 1; the weight p is
+        // kept as well, and the terms proportional to it (p P) take it, so
+        // that a small weight keeps its digits down a chain of nodes whose
+        // ratios P / Q can raise it again.  The shared
         // dominant token x* (the unique maximum of both rows) is left out
         // of the sweeps and carried in closed form:
         //   R_1(x*) = Qbs - Pbs - pbar + pbar Pbs,
@@ -974,14 +982,14 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                     float R, Qy, abar_num;
                     if (y == xs) {
                         Qy = 1.f - Qbs;
-                        R = first_draw ? (1.f - pbar) * (1.f - Pbs) : sm->Rs;
+                        R = first_draw ? p * (1.f - Pbs) : sm->Rs;
                         abar_num = fmaxf(-Rj, 0.f);
                     } else {
                         const ProbS Py = prob_s(sm, true, y, sm->cur.gT[di], c);
                         const ProbS Qp = prob_s(sm, false, y, sm->cur.gD[di], c);
                         Qy = Qp.P;
-                        R = first_draw ? p * Py.P : fmaxf((1.f - pbar) * Py.P - (1.f + sm->cbar) * Qp.P, 0.f);
-                        abar_num = fmaxf((1.f + cnew) * Qp.P - (1.f - pbar) * Py.P, 0.f);
+                        R = first_draw ? p * Py.P : fmaxf(p * Py.P - (1.f + sm->cbar) * Qp.P, 0.f);
+                        abar_num = fmaxf((1.f + cnew) * Qp.P - p * Py.P, 0.f);
                     }
                     float a, abar;
                     const float ratio = (D > 0.f && Qy > 0.f) ? (R / D) / Qy : INFINITY;
@@ -1003,7 +1011,7 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                         const size_t sc = sbase + K + k2;
                         // child first reached by this draw: its weight (never NaN:
                         // the child waits for a value of 0 or more)
-                        if (first_of_token) st_relaxed(&pb.ws.pbar[sc], fmaxf(abar, 0.f));
+                        if (first_of_token) st_weight(&pb.ws.wt[sc], fmaxf(abar, 0.f), a);
                     }
                     sm->aT = p / sm->zT;
                     sm->aD = (1.f + cnew) / sm->zD;
