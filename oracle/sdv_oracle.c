@@ -438,7 +438,7 @@ static int run_block(req_t* r, float* accept_prob, outcome_t* out, double* resid
         softmax(pb, row_of(pb, 1, r->b, 0, i), pb->temperature, r->P);
         softmax(pb, row_of(pb, 0, r->b, 0, i), pb->temperature, r->Q);
         for (int x = 0; x < V; ++x) S += fmax(p[i] * r->P[x] - r->Q[x], 0.0);
-        h[i] = (S + 1.0 - p[i]) > 0.0 ? S / (S + 1.0 - p[i]) : 1.0;
+        h[i] = S + (1.0 - p[i]) > 0.0 ? S / (S + (1.0 - p[i])) : 1.0;
     }
     if (Lb >= 1) h[Lb] = p[Lb];
     if (accept_prob)

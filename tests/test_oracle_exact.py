@@ -196,6 +196,26 @@ def test_rrs_two_draws_closed_form():
             assert np.max(np.abs(ex[0, 0] - want)) < TOL
 
 
+@pytest.mark.parametrize("mode", ["block", "multidraft"])
+def test_full_weight_with_tiny_residual_accepts(mode):
+    # GBV (and SpecTr-GBV at K = 1): h = S / (S + 1 - p).  With p = 1 the
+    # test accepts for any S > 0, however small: here the depth-0 ratio
+    # P(X)/Q(X) is 1, so p_1 = 1, and the depth-1 residual lives on one
+    # token whose target probability is about 1.5e-16 (below half an ulp
+    # of 1 in double) while the draft's is about 1e-35.
+    V, K, L = 2, 1, 2
+    tgt = np.zeros((1, K, L + 1, V), np.float32)
+    dft = np.zeros((1, K, L, V), np.float32)
+    tgt[0, 0, 1] = [0.0, np.log(1.5e-16)]
+    dft[0, 0, 1] = [0.0, -80.0]
+    tok = np.zeros((1, K, L), np.int32)
+    prob = oracle.Problem(tgt, dft, tok, None, np.zeros((1, K, L)), np.zeros((1, K, L + 1)), 1.0)
+    out = oracle.verify(mode, prob)
+    assert out["rc"] == 0
+    assert out["accept_prob"][0, 0, 0] == 1.0  # h at depth 1
+    assert 1e-16 < out["residual_mass"][0] < 1e-15 or out["accept_len"][0] == L
+
+
 @pytest.mark.parametrize("mode,K", [("token", 1), ("token", 3), ("block", 1), ("multidraft", 3)])
 def test_identical_models_accept_everything(mode, K):
     V, L = 4, 3
@@ -310,7 +330,7 @@ MUTANTS = {
     "residual_from_P_each_draw": ("r->R[x] = fmax(r->R[x] - D * r->Q[x], 0.0);",
                                   "r->R[x] = fmax(p * r->P[x] - D * r->Q[x], 0.0);"),
     "h_sign_flip": ("r->h[j][o] = D > 0.0 ? S / D : 1.0;", "r->h[j][o] = S / (1.0 + p + S);"),
-    "gbv_h_denominator": ("h[i] = (S + 1.0 - p[i]) > 0.0 ? S / (S + 1.0 - p[i]) : 1.0;",
+    "gbv_h_denominator": ("h[i] = S + (1.0 - p[i]) > 0.0 ? S / (S + (1.0 - p[i])) : 1.0;",
                           "h[i] = S / (S + 1.0);"),
     "gbv_residual_without_p": ("r->R[x] = fmax(p[tau] * r->P[x] - r->Q[x], 0.0);",
                                "r->R[x] = fmax(r->P[x] - r->Q[x], 0.0);"),
