@@ -991,16 +991,19 @@ __global__ void __launch_bounds__(kSThreads, kCtasPerSm) stream_kernel(Problem p
                         R = first_draw ? p * Py.P : fmaxf(p * Py.P - (1.f + sm->cbar) * Qp.P, 0.f);
                         abar_num = fmaxf((1.f + cnew) * Qp.P - p * Py.P, 0.f);
                     }
+                    // a = min(R / (D Q(y)), 1) and its complement, each in its
+                    // own right: a ratio within 6e-8 of 1 rounds to 1 in fp32,
+                    // while 1 - a = (D Q(y) - R) / (D Q(y)) keeps its digits
                     float a, abar;
-                    const float ratio = (D > 0.f && Qy > 0.f) ? (R / D) / Qy : INFINITY;
-                    if (ratio >= 1.f) {
+                    const bool dq = D > 0.f && Qy > 0.f;
+                    if (!dq) {
                         a = 1.f;
                         abar = 0.f;
                     } else if (!(R > 0.f)) {
                         a = 0.f;
                         abar = 1.f;
                     } else {
-                        a = ratio;
+                        a = fminf((R / D) / Qy, 1.f);
                         abar = fminf((abar_num / D) / Qy, 1.f);
                     }
                     sm->cbar = cnew;
