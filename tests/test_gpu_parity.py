@@ -269,6 +269,22 @@ def test_chunk_boundaries(V, dtype):
         _compare_both(mode, batch, P.oracle_run(mode, batch), f"V={V}/{dtype}/{mode}")
 
 
+# Seeds on which an earlier build drifted from the oracle beyond 1e-5:
+# a node weight below the complement's resolution raised again down the
+# chain (block seed 100, multi-draft seed 110 at T = 0.1), and a ratio
+# P(x)/Q(x) within 6e-8 of 1 whose complement was dropped (block seed 318
+# at T = 0.1).  Every request, with and without accept_prob.
+@pytest.mark.parametrize("name,seed,T,mode", [
+    ("block-B128-K1-L5-V128256-bf16", 100, 0.7, "block"),
+    ("block-B128-K1-L5-V128256-bf16", 318, 0.1, "block"),
+    ("multidraft-B32-K4-L4-V32000-f32", 110, 0.1, "multidraft"),
+])
+def test_numerically_hard_seeds(name, seed, T, mode):
+    batch = W.make(name, DEV, seed=seed, temperature=T)
+    _compare_both(mode, batch, P.oracle_run(mode, batch), f"{name}/seed {seed}/T={T}/{mode}",
+                  workload=f"{name} (hard seeds)")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("V", [262143, 262144])
 def test_largest_vocabulary(dtype, V):
