@@ -303,16 +303,19 @@ __device__ void residual_pass(const Dist& d, int V, RowSmem& sm, int lane, int w
 // factor between the two is 2 to the difference of those float offsets.
 // The difference of two floats is exact as a float plus a remainder
 // (TwoSum); the factor is exp2f of the first times a first-order term for
-// the second.
+// the second.  The operations are written with rounding intrinsics so
+// that the compiler cannot fuse the product into the first sum (an FMA
+// there would add the unrounded product, 2 to whose rounding error, up to
+// 5e-6 relative at 1/T = 10, would then scale the segment).
 __device__ __forceinline__ float seg_mass(const Dist& d, const RowSmem& sm, int i)
 {
     if (d.residual) return sm.mass[i];
     const float ref = sm.ref[i];
     if (!(ref > -INFINITY)) return 0.f;
-    const float a = d.negM, b = ref * d.c;  // delta = a + b, b = -negm
-    const float hi = a + b;
-    const float bb = hi - a;
-    const float lo = (a - (hi - bb)) + (b - bb);
+    const float a = d.negM, b = __fmul_rn(ref, d.c);  // delta = a + b, b = -negm
+    const float hi = __fadd_rn(a, b);
+    const float bb = __fsub_rn(hi, a);
+    const float lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
     return sm.mass[i] * (exp2f(hi) * fmaf(lo, 0.693147180559945309f, 1.f));
 }
 
