@@ -102,3 +102,27 @@ def test_sampler_flips_lie_within_fp32_resolution():
         del rows
         torch.cuda.empty_cache()
     print(f"\nsampler, 4 x 512 depth-0 draft rows of the mixed batch: {flips} flips in {draws} draws")
+
+
+@pytest.mark.parametrize("T", [0.1, 1.0])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_sampler_flips_on_peaked_and_flat_rows(dtype, T):
+    # rows of N(0, 9) logits: at T = 0.1 a few tokens hold nearly all the
+    # mass, so any error in how a segment is rescaled to the row maximum
+    # moves every later interval end by that much
+    V, n = 32000, 1024
+    g = torch.Generator(device=DEV)
+    g.manual_seed(V)
+    x = torch.randn((n, V), generator=g, device=DEV) * 3.0
+    x = x.to(torch.bfloat16 if dtype == "bf16" else torch.float32)
+    u = torch.rand((n, 4), generator=g, device=DEV)
+    Tf = float(np.float32(T))
+    tokens, status = sdv.sample_rows(x, 4, u, Tf, V=V)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.sample_rows(x.cpu(), 4, u.cpu(), Tf, V=V)
+    bad = tokens.cpu().numpy() != ref["tokens"]
+    if bad.any():
+        worst = float(ref["margin"][bad].max())
+        assert worst < DRAW_BOUND, f"{dtype} T={T}: a draw differs {worst:.3g} from its interval end"
+    print(f"\nrandom rows V={V} {dtype} T={T}: {int(bad.sum())} flips in {bad.size} draws")
