@@ -203,6 +203,31 @@ def test_leaf_rows_are_read_only_by_the_bonus_draw(name, K):
             assert gpu["residual_mass"][b] == 0.0 and (gpu["accept_prob"][b] == 0).all()
 
 
+def test_concurrent_calls_on_two_streams():
+    # two calls with their own outputs and workspaces, queued on two streams
+    # without a synchronisation between them, give what they give alone: a
+    # node kernel's CTAs take work only while running, so a parent is always
+    # held by a running CTA whatever share of the GPU the other call has
+    a = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=24, V=15197, seed=71)
+    b = W.make("block-B128-K1-L5-V128256-bf16", DEV, B=24, seed=72)
+    jobs = [(a, "multidraft"), (b, "block"), (a, "token"), (b, "token")]
+    alone = [P.gpu_run(m, x) for x, m in jobs]
+    outs = [binding.Outputs(m, x.B, x.K, x.L, x.V, x.target.device) for x, m in jobs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for i, (x, m) in enumerate(jobs):
+        with torch.cuda.stream(streams[i % 2]):
+            sdv.verify(m, x.target, x.draft, x.tokens, x.lengths, x.accept_u, x.sample_u, x.temperature, V=x.V,
+                       out=outs[i])
+    torch.cuda.synchronize()
+    for i, (x, m) in enumerate(jobs):
+        got = {k: (None if v is None else v.cpu().numpy()) for k, v in outs[i].as_dict().items()}
+        for k, v in alone[i].items():
+            if v is None:
+                continue
+            np.testing.assert_array_equal(got[k], v, err_msg=f"job {i} ({m}): {k}")
+
+
 def test_deterministic():
     batch = W.make("mixed-B256-K8-L8-V151936-bf16", DEV, B=8, V=30011)
     for mode, kw in (("token", {}), ("multidraft", {}), ("multidraft", dict(accept_prob=False))):
