@@ -231,8 +231,10 @@ const char *sdv_status_string(int status);
  *                if some row was unusable (other rows are unaffected).
  *   cuda_stream  the stream to run on (NULL: the default stream).
  * Asynchronous; allocates nothing.  Returns SDV_OK, SDV_ERR_INVALID or
- * SDV_ERR_CUDA.  Arithmetic is fp32; a draw whose uniform lies within
- * about 1e-6 of a CDF boundary may fall on the neighbouring token. */
+ * SDV_ERR_CUDA.  Element masses are fp32, the row total and the running
+ * sums over segments double; a draw whose uniform lies within about 1e-7
+ * of a CDF boundary (the fp32 error of the largest masses) may fall on the
+ * neighbouring token. */
 int sdv_sample_rows(int n_rows, int V, long long row_stride, int dtype, float temperature, const void *logits,
                     int n_samples, const float *u, int *tokens, int *device_status, void *cuda_stream);
 
