@@ -168,8 +168,10 @@ __device__ __forceinline__ float unit_max_masked(const uint4& u, int x0, int V)
 __device__ __forceinline__ void online_rebase(Online& s, float wm, float c)
 {
     if (wm > s.m || wm != wm) {
-        const float nneg = -(wm * c);
-        s.z = s.z * ex2(nneg - s.neg) + (s.cnt > 0 ? (float)s.cnt * ex2(fmaf(s.m, c, nneg)) : 0.f);
+        // the offset is the rounded product, as every exponent argument
+        // takes it: written so that it cannot fuse into the subtraction
+        const float nneg = -__fmul_rn(wm, c);
+        s.z = s.z * ex2(__fsub_rn(nneg, s.neg)) + (s.cnt > 0 ? (float)s.cnt * ex2(fmaf(s.m, c, nneg)) : 0.f);
         s.cnt = 0;
         s.first = 0x7fffffff;
         s.m = wm;
@@ -573,7 +575,9 @@ __device__ __forceinline__ void combine_rows(StreamSmem* sm, const Online& sT, c
         MT = max_nan(MT, sm->redf[0][i]);
         MD = max_nan(MD, sm->redf[1][i]);
     }
-    const float gnegT = -(MT * c), gnegD = -(MD * c);
+    // rounded products (no FMA into the rescale differences below): each
+    // partial sum was taken against -fl(m c), and moves to -fl(M c)
+    const float gnegT = -__fmul_rn(MT, c), gnegD = -__fmul_rn(MD, c);
     // a thread whose reference is the row's adds its sums as they are;
     // another rescales them (its maxima are then ordinary elements)
     float cT, cD;
@@ -583,7 +587,7 @@ __device__ __forceinline__ void combine_rows(StreamSmem* sm, const Online& sT, c
         nT = sT.cnt;
         if (nT > 0) atomicMin(&sm->firstT, sT.first);
     } else {
-        const float scl = (sT.cnt > 0 || sT.z > 0.f) ? ex2(gnegT - sT.neg) : 0.f;
+        const float scl = (sT.cnt > 0 || sT.z > 0.f) ? ex2(__fsub_rn(gnegT, sT.neg)) : 0.f;
         cT = sT.cnt > 0 ? scl * (sT.z + (float)sT.cnt * ex2(fmaf(sT.m, c, sT.neg))) : scl * sT.z;
     }
     if (sD.m == MD) {
@@ -591,7 +595,7 @@ __device__ __forceinline__ void combine_rows(StreamSmem* sm, const Online& sT, c
         nD = sD.cnt;
         if (nD > 0) atomicMin(&sm->firstD, sD.first);
     } else {
-        const float scl = (sD.cnt > 0 || sD.z > 0.f) ? ex2(gnegD - sD.neg) : 0.f;
+        const float scl = (sD.cnt > 0 || sD.z > 0.f) ? ex2(__fsub_rn(gnegD, sD.neg)) : 0.f;
         cD = sD.cnt > 0 ? scl * (sD.z + (float)sD.cnt * ex2(fmaf(sD.m, c, sD.neg))) : scl * sD.z;
     }
     cT = warp_sum(cT);
